@@ -1,0 +1,366 @@
+// C-ABI entry points of libfp4moe: argument checks, workspace layout and the
+// launch sequence of the forward.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace fp4moe {
+
+namespace {
+
+constexpr int64_t kAlign = 256;
+inline int64_t align_up(int64_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+fp4moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FP4MOE_OK : FP4MOE_ERR_CUDA; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The GEMMs use sm_103a instructions: refuse any other device up front.
+fp4moe_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FP4MOE_ERR_DEVICE;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return FP4MOE_ERR_DEVICE;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return FP4MOE_ERR_DEVICE;
+  return (major == 10 && minor == 3) ? FP4MOE_OK : FP4MOE_ERR_DEVICE;
+}
+
+bool dims_ok(const fp4moe_dims& d) {
+  if (d.T < 1 || d.T > 65536) return false;
+  if (d.H < 256 || d.H % 256 != 0 || d.H > 65536) return false;
+  if (d.I < 128 || d.I % 128 != 0 || d.I > 65536) return false;
+  if (d.E < 1 || d.E > 512) return false;
+  if (d.top_k < 1 || d.top_k > 16 || d.top_k > d.E) return false;
+  if (d.n_group < 1 || d.n_group > 32 || d.E % d.n_group != 0) return false;
+  if (d.topk_group < 1 || d.topk_group > d.n_group) return false;
+  if (d.n_group > 1 && (d.E / d.n_group > 64 || d.topk_group * (d.E / d.n_group) < d.top_k)) return false;
+  if (d.n_shared < 0 || d.n_shared > 1) return false;
+  if (d.fmt != FP4MOE_MXFP4 && d.fmt != FP4MOE_NVFP4) return false;
+  if (!(d.routed_scaling == d.routed_scaling)) return false;
+  return true;
+}
+
+int pick_n_tile(const fp4moe_dims& d) {
+  const double avg = (double)d.T * d.top_k / d.E;
+  if (avg <= 24.0) return 32;
+  if (avg <= 48.0) return 64;
+  return 128;
+}
+
+// Router split-K factor: a divisor of H / 256 that gives the logits kernel
+// enough CTAs (or warps) to cover the GPU.
+int pick_splits(const fp4moe_dims& d) {
+  const int kt = d.H / 256;
+  int64_t units, want;
+  if (d.T <= 16) {
+    units = d.E;             // warps
+    want = 8 * 152;
+  } else {
+    units = (int64_t)((d.T + 127) / 128) * ((d.E + 63) / 64);  // CTAs
+    want = 2 * 152;
+  }
+  for (int s = 1; s <= kt; ++s)
+    if (kt % s == 0 && units * s >= want) return s;
+  return kt;
+}
+
+}  // namespace
+
+bool make_layout(const fp4moe_dims& d, Layout* L) {
+  if (!dims_ok(d)) return false;
+  memset(L, 0, sizeof(*L));
+  const bool nv = d.fmt == FP4MOE_NVFP4;
+  L->n_exp = d.E + d.n_shared;
+  L->n_chunks = (d.T + kChunkTokens - 1) / kChunkTokens;
+  L->n_route_per_tok = d.top_k + d.n_shared;
+  const int64_t R = (int64_t)d.T * L->n_route_per_tok;
+  fp4moe_ws_layout& w = L->ws;
+  w.n_tile = pick_n_tile(d);
+  w.n_splits = pick_splits(d);
+  const int64_t slots_cap = R / w.n_tile + L->n_exp + 1;
+  if (slots_cap * kSlotRows > INT32_MAX / 2) return false;
+  w.rows_cap = (int32_t)(slots_cap * kSlotRows);
+  int64_t off = 0;
+  auto take = [&](int64_t bytes) {
+    const int64_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  w.status = take(kStatusInts * 4);
+  w.logits = take((int64_t)w.n_splits * d.T * d.E * 4);
+  w.topk_idx = take((int64_t)d.T * d.top_k * 4);
+  w.topk_w = take((int64_t)d.T * d.top_k * 4);
+  L->chunk_counts = take((int64_t)L->n_chunks * L->n_exp * 4);
+  L->plan = take(sizeof(Plan));
+  w.expert_count = take((int64_t)L->n_exp * 4);
+  w.expert_slot = take((int64_t)L->n_exp * 4);
+  L->gu_start = take((int64_t)(L->n_exp + 1) * 4);
+  L->dn_start = take((int64_t)(L->n_exp + 1) * 4);
+  w.route_row = take(R * 4);
+  w.row_tok = take((int64_t)w.rows_cap * 4);
+  w.row_w = take((int64_t)w.rows_cap * 4);
+  L->row_e = take((int64_t)w.rows_cap * 4);
+  w.xq = take((int64_t)w.rows_cap * (d.H / 2));
+  w.xsf = take((int64_t)slots_cap * katoms_padded(d.H, nv) * 512);
+  w.hq = take((int64_t)w.rows_cap * (d.I / 2));
+  w.hsf = take((int64_t)slots_cap * katoms_padded(d.I, nv) * 512);
+  w.h32 = nv ? take((int64_t)w.rows_cap * d.I * 4) : take(0);
+  w.gscale = take((int64_t)(2 + L->n_exp) * 4);
+  L->amax = take((int64_t)(2 + L->n_exp) * 4);
+  w.out_acc = take((int64_t)d.T * d.H * 4);
+  w.total_bytes = off;
+  return true;
+}
+
+}  // namespace fp4moe
+
+using namespace fp4moe;
+
+extern "C" {
+
+int32_t fp4moe_version(void) { return 100; }
+
+const char* fp4moe_status_string(int32_t s) {
+  switch (s) {
+    case FP4MOE_OK: return "ok";
+    case FP4MOE_ERR_INVALID_ARG: return "invalid argument";
+    case FP4MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case FP4MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case FP4MOE_ERR_CUDA: return "CUDA error";
+    case FP4MOE_ERR_TIMEOUT: return "device wait timed out";
+    case FP4MOE_ERR_NAN_SCALE: return "NaN scale byte";
+    case FP4MOE_ERR_INEXACT: return "conversion row below the exponent floor";
+    case FP4MOE_ERR_DEVICE: return "no sm_103 device";
+    default: return "unknown status";
+  }
+}
+
+size_t fp4moe_workspace_size(const fp4moe_dims* dims) {
+  if (!dims) return 0;
+  Layout L;
+  if (!make_layout(*dims, &L)) return 0;
+  return (size_t)L.ws.total_bytes;
+}
+
+fp4moe_status fp4moe_workspace_layout(const fp4moe_dims* dims, fp4moe_ws_layout* out) {
+  if (!dims || !out) return FP4MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(*dims, &L)) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  *out = L.ws;
+  return FP4MOE_OK;
+}
+
+size_t fp4moe_packed_scales_bytes(int64_t n_mat, int32_t rows, int32_t kblocks, int32_t fmt) {
+  if (n_mat < 0 || rows <= 0 || rows % 128 != 0 || kblocks <= 0 || kblocks % 4 != 0) return 0;
+  if (fmt != FP4MOE_MXFP4 && fmt != FP4MOE_NVFP4) return 0;
+  const bool nv = fmt == FP4MOE_NVFP4;
+  const int64_t katoms = katoms_padded((int64_t)kblocks * (nv ? 16 : 32), nv);
+  return (size_t)(n_mat * (rows / 128) * katoms * 512);
+}
+
+fp4moe_status fp4moe_pack_scales(const uint8_t* src, uint8_t* dst, int64_t n_mat, int32_t rows, int32_t kblocks,
+                                 int32_t fmt, void* stream) {
+  if (!src || !dst) return FP4MOE_ERR_INVALID_ARG;
+  if (fp4moe_packed_scales_bytes(n_mat, rows, kblocks, fmt) == 0 && n_mat != 0) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  if (fmt != FP4MOE_MXFP4 && fmt != FP4MOE_NVFP4) return FP4MOE_ERR_INVALID_ARG;
+  if (fp4moe_status st = check_device()) return st;
+  return cuda_status(launch_pack_scales(src, dst, n_mat, rows, kblocks, fmt == FP4MOE_NVFP4,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+fp4moe_status fp4moe_route(const fp4moe_dims* dims, const uint16_t* x, const uint16_t* w_router, const float* bias,
+                           int32_t* topk_idx, float* topk_w, float* logits_out, void* ws, size_t ws_bytes,
+                           void* stream) {
+  if (!dims || !x || !w_router || !bias || !topk_idx || !topk_w || !ws) return FP4MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(*dims, &L)) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  if (ws_bytes < (size_t)L.ws.total_bytes) return FP4MOE_ERR_WORKSPACE;
+  if (!aligned16(x) || !aligned16(w_router)) return FP4MOE_ERR_INVALID_ARG;
+  if (fp4moe_status st = check_device()) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const fp4moe_dims& d = *dims;
+  float* partial = reinterpret_cast<float*>(base + L.ws.logits);
+  int32_t* cc = reinterpret_cast<int32_t*>(base + L.chunk_counts);
+  cudaError_t e = cudaMemsetAsync(cc, 0, (size_t)L.n_chunks * L.n_exp * 4, s);
+  if (e == cudaSuccess) e = launch_router_logits(x, w_router, partial, d.T, d.H, d.E, L.ws.n_splits, s);
+  if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, bias, topk_idx, topk_w, logits_out, cc, L.n_exp, s);
+  return cuda_status(e);
+}
+
+fp4moe_status fp4moe_quantize_act(const void* x, int32_t x_is_fp32, int64_t rows, int32_t cols, int32_t fmt,
+                                  const float* global_in, uint8_t* codes, uint8_t* scales, float* global_out,
+                                  void* ws, size_t ws_bytes, void* stream) {
+  if (!x || !codes || !scales || !ws) return FP4MOE_ERR_INVALID_ARG;
+  if (rows < 0 || cols <= 0 || cols % 32 != 0) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  if (fmt != FP4MOE_MXFP4 && fmt != FP4MOE_NVFP4) return FP4MOE_ERR_INVALID_ARG;
+  if (ws_bytes < 256) return FP4MOE_ERR_WORKSPACE;
+  if (!aligned16(x) || !aligned16(codes)) return FP4MOE_ERR_INVALID_ARG;
+  if (fp4moe_status st = check_device()) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t* amax = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + 64);
+  const bool nv = fmt == FP4MOE_NVFP4;
+  cudaError_t e = cudaSuccess;
+  if (nv && !global_in) e = launch_amax(x, x_is_fp32 ? 1 : 0, rows * (int64_t)cols, amax, s);
+  if (e == cudaSuccess)
+    e = launch_quantize_rows(x, x_is_fp32 ? 1 : 0, rows, cols, nv, global_in, amax, codes, scales, global_out, s);
+  return cuda_status(e);
+}
+
+fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, const uint16_t* x, uint16_t* out,
+                             const fp4moe_debug* dbg, void* ws, size_t ws_bytes, void* stream) {
+  if (!dims || !w || !x || !out || !ws) return FP4MOE_ERR_INVALID_ARG;
+  const fp4moe_dims& d = *dims;
+  Layout L;
+  if (!make_layout(d, &L)) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  if (ws_bytes < (size_t)L.ws.total_bytes) return FP4MOE_ERR_WORKSPACE;
+  const bool nv = d.fmt == FP4MOE_NVFP4;
+  if (!w->w13 || !w->w13_scale || !w->w2 || !w->w2_scale || !w->w_router || !w->bias) return FP4MOE_ERR_INVALID_ARG;
+  if (nv && (!w->g13 || !w->g2)) return FP4MOE_ERR_INVALID_ARG;
+  if (d.n_shared && (!w->sh13 || !w->sh13_scale || !w->sh2 || !w->sh2_scale)) return FP4MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w->w13) || !aligned16(w->w2) || !aligned16(w->w13_scale) ||
+      !aligned16(w->w2_scale) || !aligned16(w->w_router) || !aligned16(ws) || !aligned16(out))
+    return FP4MOE_ERR_INVALID_ARG;
+  if (d.n_shared && (!aligned16(w->sh13) || !aligned16(w->sh2) || !aligned16(w->sh13_scale) ||
+                     !aligned16(w->sh2_scale)))
+    return FP4MOE_ERR_INVALID_ARG;
+  if (fp4moe_status st = check_device()) return st;
+  const int num_sms = device_sm_count();
+  if (num_sms <= 0) return FP4MOE_ERR_DEVICE;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  auto P = [&](int64_t off) { return base + off; };
+  int32_t* status = reinterpret_cast<int32_t*>(P(L.ws.status));
+  float* partial = reinterpret_cast<float*>(P(L.ws.logits));
+  int32_t* idx = reinterpret_cast<int32_t*>(P(L.ws.topk_idx));
+  float* tw = reinterpret_cast<float*>(P(L.ws.topk_w));
+  int32_t* cc = reinterpret_cast<int32_t*>(P(L.chunk_counts));
+  Plan* plan = reinterpret_cast<Plan*>(P(L.plan));
+  int32_t* ecount = reinterpret_cast<int32_t*>(P(L.ws.expert_count));
+  int32_t* eslot = reinterpret_cast<int32_t*>(P(L.ws.expert_slot));
+  int32_t* gu_start = reinterpret_cast<int32_t*>(P(L.gu_start));
+  int32_t* dn_start = reinterpret_cast<int32_t*>(P(L.dn_start));
+  int32_t* route_row = reinterpret_cast<int32_t*>(P(L.ws.route_row));
+  int32_t* row_tok = reinterpret_cast<int32_t*>(P(L.ws.row_tok));
+  float* row_w = reinterpret_cast<float*>(P(L.ws.row_w));
+  int32_t* row_e = reinterpret_cast<int32_t*>(P(L.row_e));
+  uint8_t* xq = P(L.ws.xq);
+  uint8_t* xsf = P(L.ws.xsf);
+  uint8_t* hq = P(L.ws.hq);
+  uint8_t* hsf = P(L.ws.hsf);
+  float* h32 = nv ? reinterpret_cast<float*>(P(L.ws.h32)) : nullptr;
+  float* gscale = reinterpret_cast<float*>(P(L.ws.gscale));
+  uint32_t* amax = reinterpret_cast<uint32_t*>(P(L.amax));
+  float* acc = reinterpret_cast<float*>(P(L.ws.out_acc));
+  const int n_tile = L.ws.n_tile;
+
+  auto rec = [&](int i) -> cudaError_t {
+    if (dbg && dbg->events[i]) return cudaEventRecord(static_cast<cudaEvent_t>(dbg->events[i]), s);
+    return cudaSuccess;
+  };
+
+  cudaError_t e = rec(0);
+  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, kStatusInts * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(cc, 0, (size_t)L.n_chunks * L.n_exp * 4, s);
+  if (e == cudaSuccess && nv) e = cudaMemsetAsync(amax, 0, (size_t)(2 + L.n_exp) * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(acc, 0, (size_t)d.T * d.H * 4, s);
+  if (e == cudaSuccess) e = launch_router_logits(x, w->w_router, partial, d.T, d.H, d.E, L.ws.n_splits, s);
+  if (e == cudaSuccess) e = rec(1);
+  if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, nullptr, cc, L.n_exp, s);
+  if (e == cudaSuccess) e = rec(2);
+  if (e == cudaSuccess)
+    e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, ecount, eslot, gu_start, dn_start, plan, s);
+  if (e == cudaSuccess)
+    e = launch_scatter(d, idx, tw, cc, L.n_chunks, L.n_exp, n_tile, eslot, route_row, row_tok, row_w, row_e, s);
+  if (e == cudaSuccess) e = rec(3);
+  if (e == cudaSuccess && nv) e = launch_amax(x, 0, (int64_t)d.T * d.H, amax, s);
+  if (e == cudaSuccess) e = launch_gather_quant(d, x, route_row, xq, xsf, amax, gscale, s);
+  if (e == cudaSuccess) e = rec(4);
+
+  GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  a.d = &d;
+  a.nv = nv;
+  a.n_tile = n_tile;
+  a.num_sms = num_sms;
+  a.rows_cap = L.ws.rows_cap;
+  a.expert_count = ecount;
+  a.expert_slot = eslot;
+  a.plan = plan;
+  a.row_tok = row_tok;
+  a.row_w = row_w;
+  a.status = status;
+  if (e == cudaSuccess) {
+    GemmArgs g = a;
+    g.w = w->w13;
+    g.wsf = w->w13_scale;
+    g.sh = d.n_shared ? w->sh13 : nullptr;
+    g.shsf = d.n_shared ? w->sh13_scale : nullptr;
+    g.gw = w->g13;
+    g.b = xq;
+    g.bsf = xsf;
+    g.unit_start = gu_start;
+    g.g_b = gscale;  // g_x
+    g.hq = hq;
+    g.hsf = hsf;
+    g.h32 = h32;
+    g.amax_h = amax + 2;
+    g.h_dbg = dbg ? dbg->h_pre : nullptr;
+    e = launch_gateup(g, s);
+  }
+  if (e == cudaSuccess && nv) e = launch_h_quant_nv_routes(d, h32, route_row, row_e, amax + 2, gscale + 2, hq, hsf, s);
+  if (e == cudaSuccess) e = rec(5);
+  if (e == cudaSuccess) {
+    GemmArgs g = a;
+    g.w = w->w2;
+    g.wsf = w->w2_scale;
+    g.sh = d.n_shared ? w->sh2 : nullptr;
+    g.shsf = d.n_shared ? w->sh2_scale : nullptr;
+    g.gw = w->g2;
+    g.b = hq;
+    g.bsf = hsf;
+    g.unit_start = dn_start;
+    g.g_b = gscale + 2;  // g_h per expert
+    g.out_acc = acc;
+    e = launch_down(g, s);
+  }
+  if (e == cudaSuccess) e = rec(6);
+  if (e == cudaSuccess) e = launch_finalize(acc, out, (int64_t)d.T * d.H, s);
+  if (e == cudaSuccess) e = rec(7);
+  return cuda_status(e);
+}
+
+fp4moe_status fp4moe_mxfp4_to_fp8_rowscale(const uint8_t* codes, const uint8_t* scales_e8m0, int64_t rows, int32_t K,
+                                           uint8_t* fp8_out, float* row_scale, uint8_t* row_status, void* ws,
+                                           size_t ws_bytes, void* stream) {
+  if (!codes || !scales_e8m0 || !fp8_out || !row_scale || !ws) return FP4MOE_ERR_INVALID_ARG;
+  if (rows < 0 || K <= 0 || K % 32 != 0) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  if (ws_bytes < 256) return FP4MOE_ERR_WORKSPACE;
+  if (!aligned16(codes) || !aligned16(fp8_out)) return FP4MOE_ERR_INVALID_ARG;
+  if (fp4moe_status st = check_device()) return st;
+  return cuda_status(launch_convert(codes, scales_e8m0, rows, K, fp8_out, row_scale, row_status,
+                                    static_cast<int32_t*>(ws), static_cast<cudaStream_t>(stream)));
+}
+
+fp4moe_status fp4moe_clear_status(void* ws, void* stream) {
+  if (!ws) return FP4MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, kStatusInts * 4, static_cast<cudaStream_t>(stream)));
+}
+
+fp4moe_status fp4moe_get_status(void* ws, void* stream, fp4moe_status* st, int64_t* count) {
+  if (!ws) return FP4MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t h[kStatusInts];
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FP4MOE_ERR_CUDA;
+  if (cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FP4MOE_ERR_CUDA;
+  if (st) *st = static_cast<fp4moe_status>(h[ST_FIRST]);
+  if (count) *count = h[ST_COUNT];
+  return FP4MOE_OK;
+}
+
+}  // extern "C"

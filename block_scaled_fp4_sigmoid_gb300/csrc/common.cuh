@@ -1,0 +1,328 @@
+// Shared device helpers of the fp4moe library: status word, bounded waits,
+// PTX wrappers for mbarrier / TMA / tcgen05, and the FP4 / FP8 encoders.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/fp4moe.h"
+
+namespace fp4moe {
+
+// ---------------------------------------------------------------- status word
+// int32[16] at the start of every workspace: [0] first status code recorded,
+// [1] number of records, [2] NaN-scale rows, [3] below-floor rows,
+// [4] timeouts, [5] where the last timeout happened.
+enum { ST_FIRST = 0, ST_COUNT = 1, ST_NAN = 2, ST_INEXACT = 3, ST_TIMEOUT = 4, ST_WHERE = 5 };
+constexpr int kStatusInts = 16;
+
+__device__ __forceinline__ void record_status(int32_t* st, int code, int which, int n = 1) {
+  if (st == nullptr) return;
+  atomicCAS(st + ST_FIRST, 0, code);
+  atomicAdd(st + ST_COUNT, n);
+  atomicAdd(st + which, n);
+}
+
+// Wall-clock limit of every device-side wait, in nanoseconds.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- shared memory / mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits until the phase with the given parity has completed.  Gives up after
+// kWaitLimitNs and returns false; the caller records the timeout and unwinds.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ---------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar, int32_t c0,
+                                            int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(tmap), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int32_t c0,
+                                            int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// Plain (untiled) bulk copy global -> shared; both addresses 16-byte aligned,
+// size a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols));
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// Scale factors: 32 lanes x 128 bits from shared memory, replicated into the
+// four lane quadrants.
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+template <bool kNV>
+__device__ __forceinline__ void tc_mma_fp4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                           uint32_t sfb, uint32_t accumulate) {
+  if constexpr (kNV) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+  }
+}
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor (sm_100 family): start address, leading and
+// stride byte offsets (in 16-byte units), fixed version bits 46..47 = 1,
+// layout type in bits 61..63 (0 none, 2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                              uint32_t layout) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)(layout & 7u) << 61;
+  return d;
+}
+
+// Instruction descriptor of a block-scaled FP4 MMA: E2M1 x E2M1, K-major A and
+// B, M = 128, N = n, scale type E8M0 (MXFP4) or E4M3 (NVFP4), scale-factor
+// byte ids for A and B.
+__host__ __device__ constexpr uint32_t idesc_fp4(uint32_t n, bool nv, uint32_t sfa_id, uint32_t sfb_id) {
+  return (sfb_id & 3u) << 4        // B scale-factor id
+         | 1u << 7                 // A format: E2M1
+         | 1u << 10                // B format: E2M1
+         | (n >> 3) << 17          // N / 8
+         | (nv ? 0u : 1u) << 23    // scale format: 0 = UE4M3, 1 = UE8M0
+         | (128u >> 4) << 24       // M / 16
+         | (sfa_id & 3u) << 29;    // A scale-factor id
+}
+
+// ---------------------------------------------------------------- FP4 / FP8 encoders
+// Round-to-nearest-even magnitude code of E2M1 for a non-negative value:
+// grid 0, .5, 1, 1.5, 2, 3, 4, 6; ties to the even code; saturating.
+__device__ __forceinline__ uint32_t e2m1_mag(float m) {
+  return (uint32_t)(m > 0.25f) + (uint32_t)(m >= 0.75f) + (uint32_t)(m > 1.25f) + (uint32_t)(m >= 1.75f) +
+         (uint32_t)(m > 2.5f) + (uint32_t)(m >= 3.5f) + (uint32_t)(m > 5.0f);
+}
+
+// Full E2M1 code; the sign bit follows the sign bit of v (zero included).
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+  return e2m1_mag(fabsf(v)) | ((__float_as_uint(v) >> 28) & 8u);
+}
+
+// Round-to-nearest-even E4M3 (OCP FN) byte of a non-negative finite value,
+// saturating at 448.
+__device__ __forceinline__ uint32_t e4m3_pos(float x) {
+  if (!(x > 0.f)) return 0u;
+  if (x >= 448.f) return 0x7Eu;
+  if (x < 0.015625f) {  // below 2^-6: subnormal step 2^-9
+    return (uint32_t)__float2int_rn(x * 512.f);  // 8 means 2^-6, i.e. code 0x08
+  }
+  const uint32_t b = __float_as_uint(x);
+  const int e = (int)((b >> 23) & 0xFF) - 127 + 7;  // 1..15
+  const uint32_t mant = b & 0x7FFFFFu;
+  uint32_t r = (mant + 0x7FFFFu + ((mant >> 20) & 1u)) >> 20;
+  uint32_t code = ((uint32_t)e << 3) + r;  // a carry out of r bumps the exponent
+  return code > 0x7Eu ? 0x7Eu : code;
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t s) {
+  const uint32_t e = (s >> 3) & 15u, m = s & 7u;
+  if (e == 0) return (float)m * 0.001953125f;  // m * 2^-9
+  return __uint_as_float(((e - 7u + 127u) << 23) | (m << 20));
+}
+
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  const float mag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+  const float v = mag[c & 7u];
+  return (c & 8u) ? -v : v;
+}
+
+// 2^n as a float for n in [-127, 127] (2^-127 is the subnormal 0x00400000).
+__device__ __forceinline__ float exp2i(int n) {
+  return n >= -126 ? __uint_as_float((uint32_t)(n + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// MXFP4 block exponent e = floor(log2 amax) - 2, clamped to [-127, 127];
+// amax = 0 gives -127.
+__device__ __forceinline__ int floor_log2_pos(float x) {  // x finite, > 0
+  const uint32_t b = __float_as_uint(x);
+  const int ef = (int)((b >> 23) & 0xFF);
+  return ef ? ef - 127 : -118 - __clz(b & 0x7FFFFFu);  // subnormal: mant * 2^-149
+}
+
+__device__ __forceinline__ int mx_block_exp(float amax) {
+  if (!(amax > 0.f)) return -127;
+  int e = floor_log2_pos(amax) - 2;
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// Quantises 32 values of one MXFP4 block: 16 packed code bytes and the scale byte.
+__device__ __forceinline__ void mx_quant32(const float* v, uint32_t* packed4, uint32_t* scale_byte) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int e = mx_block_exp(amax);
+  const float inv = exp2i(-e);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) word |= e2m1_code(v[8 * w + j] * inv) << (4 * j);
+    packed4[w] = word;
+  }
+  *scale_byte = (uint32_t)(e + 127);
+}
+
+// NVFP4: tensor scale g = amax / 2688 (correctly rounded fp32 division).
+__device__ __forceinline__ float nv_global(float amax) { return __fdiv_rn(amax, 2688.0f); }
+
+// Quantises 16 values of one NVFP4 block with tensor scale g: 8 packed code
+// bytes (two words) and the E4M3 scale byte.  Every step is one correctly
+// rounded fp32 operation: s = E4M3(amax / (6 g)), d = s * g, code = E2M1(v / d).
+__device__ __forceinline__ void nv_quant16(const float* v, float g, uint32_t* packed2, uint32_t* scale_byte) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const float six_g = __fmul_rn(6.0f, g);
+  const uint32_t s = six_g > 0.f ? e4m3_pos(__fdiv_rn(amax, six_g)) : 0u;
+  const float d = __fmul_rn(e4m3_value(s), g);
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float x = v[8 * w + j];
+      const float q = d > 0.f ? __fdiv_rn(x, d) : x * 0.f;
+      word |= e2m1_code(q) << (4 * j);
+    }
+    packed2[w] = word;
+  }
+  *scale_byte = s;
+}
+
+// ---------------------------------------------------------------- tiled scale layout
+// For a matrix of `rows` rows and `katoms` groups of four scale blocks
+// (padded to whole K tiles), the byte of (row r, block kb) sits at
+//   ((r / 128) * katoms + kb / 4) * 512 + 16 * (r % 32) + 4 * ((r / 32) % 4) + kb % 4.
+__host__ __device__ __forceinline__ int64_t sf_tiled_offset(int64_t r, int64_t kb, int64_t katoms) {
+  return ((r >> 7) * katoms + (kb >> 2)) * 512 + 16 * (r & 31) + 4 * ((r >> 5) & 3) + (kb & 3);
+}
+
+// Scale-block groups per 256-value K tile: MXFP4 8 blocks = 2 groups,
+// NVFP4 16 blocks = 4 groups.
+__host__ __device__ constexpr int atoms_per_ktile(bool nv) { return nv ? 4 : 2; }
+
+__host__ __device__ inline int64_t katoms_padded(int64_t K, bool nv) {
+  const int64_t ktiles = (K + 255) / 256;
+  return ktiles * atoms_per_ktile(nv);
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0;  // NaN
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+}  // namespace fp4moe

@@ -1,0 +1,352 @@
+// Persistent grouped GEMM on block-scaled FP4 tensor cores (tcgen05) for the
+// two expert projections of the MoE layer.
+//
+// The block-scaled product follows "Serve Kimi-K2.5-MXFP4 on MI355X with
+// ATOM" (Figure 1 and section "When Is the Scale Applied?"): payloads and
+// per-block scales of both operands go into the matrix instruction, which
+// applies the scales inside the product.  On sm_103a that instruction is
+// tcgen05.mma .kind::mxf4 (E8M0 per 32) or .kind::mxf4nvf4 (E4M3 per 16),
+// with fp32 accumulators in tensor memory.
+//
+// Operand roles ("swap AB"): A = 128 weight rows (M = 128), B = up to N
+// tokens of one expert (N = 32 / 64 / 128), both K-major.  A work unit is
+// (expert, 128-row weight tile, token tile); units of one expert are laid
+// out weight-tile-major so concurrent CTAs share each weight tile through L2.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over units):
+//   warp 0     TMA producer: weight tiles (3-D tensor map over [E, rows,
+//              K/2]), token tiles (2-D map over the padded permuted rows),
+//              scale groups (bulk copies of the tiled scale layout);
+//   warp 1     tensor-memory owner and single-thread MMA issuer: copies the
+//              stage's scale factors to tensor memory (tcgen05.cp), issues
+//              four K=64 MMAs per 256-wide K tile and per A operand, commits
+//              the stage back to the producer;
+//   warps 2-5  epilogue, one per tensor-memory lane quadrant:
+//              gate/up: SwiGLU, then MXFP4 requantisation of h across the
+//              32 lanes of a warp (= one 32-block along I), or (NVFP4) fp32
+//              h plus a per-expert amax;
+//              down: routing weight times y, added into the fp32 combine
+//              buffer (red.global.add).
+// Every wait is bounded; a timeout sets a CTA-wide abort flag, records
+// FP4MOE_ERR_TIMEOUT in the status word, drains in-flight copies and MMAs,
+// frees tensor memory and returns.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace fp4moe {
+
+struct KParams {
+  CUtensorMap tmA;     // routed weights, uint8 [E, rows_per_expert, K/2]
+  CUtensorMap tmA_sh;  // shared expert weights, uint8 [1, rows_per_expert, K/2]
+  CUtensorMap tmB;     // activations, uint8 [rows_cap, K/2]
+  const uint8_t *wsf, *shsf, *bsf;
+  const float *gw, *gb;
+  const int32_t *expert_count, *expert_slot, *unit_start, *total_units;
+  const int32_t* row_tok;
+  const float* row_w;
+  uint8_t *hq, *hsf;
+  float *h32, *h_dbg, *out_acc;
+  uint32_t* amax_h;
+  int32_t* status;
+  int E, n_exp, H, I, K, rows_per_expert, m_tiles, katoms_a, katoms_b, katoms_h, has_shared;
+};
+
+template <int N, bool GATEUP, bool NV>
+struct GemmCfg {
+  static constexpr int kA = GATEUP ? 2 : 1;          // A operands per unit (gate and up)
+  static constexpr int kAtoms = NV ? 4 : 2;          // scale groups per 256-wide K tile
+  static constexpr int kABytes = 128 * 128;          // 128 rows x 128 bytes
+  static constexpr int kBBytes = N * 128;
+  static constexpr int kSFBytes = kAtoms * 512;      // per 128-row operand and K tile
+  static constexpr int kOffA1 = kABytes;
+  static constexpr int kOffB = kA * kABytes;
+  static constexpr int kOffSFA0 = kOffB + kBBytes;
+  static constexpr int kOffSFA1 = kOffSFA0 + kSFBytes;
+  static constexpr int kOffSFB = kOffSFA0 + kA * kSFBytes;
+  static constexpr int kStage = kOffSFB + kSFBytes;
+  static constexpr int kBudget = 229376;
+  static constexpr int kStages = (kBudget / kStage) > 8 ? 8 : (kBudget / kStage);
+  static constexpr int kSmem = kStages * kStage + 1024;
+  static constexpr int kAccCols = kA * N;
+  static constexpr int kSfaCol = kAccCols;
+  static constexpr int kSfbCol = kAccCols + kA * kAtoms * 4;
+  static constexpr int kCols = kSfbCol + kAtoms * 4;
+  static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
+  static_assert(kCols <= 512, "tensor memory");
+  static_assert(kStage % 1024 == 0, "stage alignment");
+  static_assert(kStages >= 2, "pipeline depth");
+};
+
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) { return smem_desc(saddr, 16, 1024, 2); }
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) { return smem_desc(saddr, 0, 128, 0); }
+
+template <int N>
+__device__ __forceinline__ void decode_unit(const KParams& p, int u, int& e, int& mt, int& slot, int& cnt) {
+  int lo = 0, hi = p.n_exp;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(p.unit_start + mid) <= u) lo = mid;
+    else hi = mid;
+  }
+  e = lo;
+  const int local = u - __ldg(p.unit_start + e);
+  const int count = __ldg(p.expert_count + e);
+  const int nt = (count + N - 1) / N;
+  mt = local / nt;
+  const int ti = local - mt * nt;
+  slot = __ldg(p.expert_slot + e) + ti;
+  cnt = min(N, count - ti * N);
+}
+
+template <int N, bool GATEUP, bool NV>
+__global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant__ KParams p) {
+  using C = GemmCfg<N, GATEUP, NV>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full[C::kStages];
+  __shared__ __align__(8) uint64_t bar_empty[C::kStages];
+  __shared__ __align__(8) uint64_t bar_tfull, bar_tempty, bar_done;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = __ldg(p.total_units);
+  const int KT = (p.K + 255) / 256;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&bar_full[s]), 1);
+      mbar_init(smem_u32(&bar_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bar_tfull), 1);
+    mbar_init(smem_u32(&bar_tempty), 4);
+    mbar_init(smem_u32(&bar_done), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.tmA);
+    prefetch_tmap(&p.tmB);
+    if (p.has_shared) prefetch_tmap(&p.tmA_sh);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort_v = &abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_par = 0;
+      for (int u = blockIdx.x; u < total && !*abort_v; u += gridDim.x) {
+        int e, mt, slot, cnt;
+        decode_unit<N>(p, u, e, mt, slot, cnt);
+        const bool sh = e >= p.E;
+        const CUtensorMap* tmA = sh ? &p.tmA_sh : &p.tmA;
+        const int ec = sh ? e - p.E : e;
+        const uint8_t* sfw = sh ? p.shsf : p.wsf;
+        const int rt_per_e = p.rows_per_expert >> 7;
+        const int row0 = mt * 128;
+        const int row1 = p.I + mt * 128;  // up rows (gate/up only)
+        const uint8_t* sfa0 = sfw + ((int64_t)(ec * rt_per_e + (row0 >> 7)) * p.katoms_a) * 512;
+        const uint8_t* sfa1 = sfw + ((int64_t)(ec * rt_per_e + (row1 >> 7)) * p.katoms_a) * 512;
+        const uint8_t* sfb = p.bsf + ((int64_t)slot * p.katoms_b) * 512;
+        bool ok = true;
+        for (int kt = 0; kt < KT; ++kt) {
+          const uint32_t fb = smem_u32(&bar_full[stage]);
+          if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u)) { ok = false; break; }
+          const uint32_t base = sbase + stage * C::kStage;
+          mbar_arrive_expect_tx(fb, C::kStage);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          tma_load_3d(base, tmA, fb, kt * 128, row0, ec);
+          if constexpr (GATEUP) tma_load_3d(base + C::kOffA1, tmA, fb, kt * 128, row1, ec);
+          tma_load_2d(base + C::kOffB, &p.tmB, fb, kt * 128, slot * kSlotRows);
+          bulk_load(base + C::kOffSFA0, sfa0 + kt * C::kSFBytes, C::kSFBytes, fb);
+          if constexpr (GATEUP) bulk_load(base + C::kOffSFA1, sfa1 + kt * C::kSFBytes, C::kSFBytes, fb);
+          bulk_load(base + C::kOffSFB, sfb + kt * C::kSFBytes, C::kSFBytes, fb);
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) {
+          *abort_v = 1;
+          record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
+          break;
+        }
+      }
+      // every armed stage must have landed before the CTA exits
+      for (int s = 0; s < C::kStages; ++s)
+        if ((armed >> s) & 1u) (void)mbar_wait(smem_u32(&bar_full[s]), (armed_par >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t t_acc0 = tmem;
+      const uint32_t t_acc1 = tmem + N;
+      const uint32_t t_sfa0 = tmem + C::kSfaCol;
+      const uint32_t t_sfa1 = t_sfa0 + C::kAtoms * 4;
+      const uint32_t t_sfb = tmem + C::kSfbCol;
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      for (int u = blockIdx.x; u < total && !*abort_v; u += gridDim.x) {
+        bool ok = mbar_wait(smem_u32(&bar_tempty), acc_phase ^ 1u);
+        tc_fence_after();
+        for (int kt = 0; ok && kt < KT; ++kt) {
+          if (!mbar_wait(smem_u32(&bar_full[stage]), phase)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t base = sbase + stage * C::kStage;
+#pragma unroll
+          for (int a = 0; a < C::kAtoms; ++a) {
+            tc_cp_sf(t_sfa0 + 4 * a, desc_sf(base + C::kOffSFA0 + 512 * a));
+            if constexpr (GATEUP) tc_cp_sf(t_sfa1 + 4 * a, desc_sf(base + C::kOffSFA1 + 512 * a));
+            tc_cp_sf(t_sfb + 4 * a, desc_sf(base + C::kOffSFB + 512 * a));
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int atom = NV ? j : (j >> 1);
+            const uint32_t sfid = NV ? 0u : (uint32_t)(j & 1) * 2u;
+            const uint32_t idesc = idesc_fp4(N, NV, sfid, sfid);
+            const uint64_t bdesc = desc_sw128(base + C::kOffB + 32 * j);
+            const uint32_t accum = (kt | j) ? 1u : 0u;
+            tc_mma_fp4<NV>(t_acc0, desc_sw128(base + 32 * j), bdesc, idesc, t_sfa0 + 4 * atom, t_sfb + 4 * atom,
+                           accum);
+            if constexpr (GATEUP)
+              tc_mma_fp4<NV>(t_acc1, desc_sw128(base + C::kOffA1 + 32 * j), bdesc, idesc, t_sfa1 + 4 * atom,
+                             t_sfb + 4 * atom, accum);
+          }
+          tc_commit(smem_u32(&bar_empty[stage]));
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) {
+          *abort_v = 1;
+          record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
+          break;
+        }
+        tc_commit(smem_u32(&bar_tfull));
+        acc_phase ^= 1u;
+      }
+      // all issued MMAs must finish before tensor memory is released
+      tc_commit(smem_u32(&bar_done));
+      (void)mbar_wait(smem_u32(&bar_done), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // tensor-memory lane quadrant of this warp
+    const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < total && !*abort_v; u += gridDim.x) {
+      int e, mt, slot, cnt;
+      decode_unit<N>(p, u, e, mt, slot, cnt);
+      if (!mbar_wait(smem_u32(&bar_tfull), acc_phase)) {
+        *abort_v = 1;
+        if (lane == 0) record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const int64_t row0 = (int64_t)slot * kSlotRows;
+      if constexpr (GATEUP) {
+        const int i = mt * 128 + 32 * q + lane;  // intermediate index of this lane
+        float sc = 1.f;
+        if constexpr (NV) sc = __fmul_rn(__ldg(p.gb), __ldg(p.gw + e));
+        float amax = 0.f;
+        for (int c0 = 0; c0 < cnt; c0 += 32) {
+          float g[32], uu[32];
+          tc_ld32(tq + c0, g);
+          tc_ld32(tq + N + c0, uu);
+          tc_wait_ld();
+          const int jn = min(32, cnt - c0);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j >= jn) break;
+            float gv = g[j], uv = uu[j];
+            if constexpr (NV) {
+              gv = gv * sc;
+              uv = uv * sc;
+            }
+            const float h = gv / (1.0f + expf(-gv)) * uv;
+            const int64_t row = row0 + c0 + j;
+            if (p.h_dbg) p.h_dbg[row * p.I + i] = h;
+            if constexpr (NV) {
+              p.h32[row * p.I + i] = h;
+              amax = fmaxf(amax, fabsf(h));
+            } else {
+              float a = fabsf(h);
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+              const int ex = mx_block_exp(a);
+              const uint32_t code = e2m1_code(h * exp2i(-ex));
+              const uint32_t nb = code | (__shfl_down_sync(0xffffffffu, code, 1) << 4);
+              const uint32_t w8 = nb | (__shfl_down_sync(0xffffffffu, nb, 2) << 8);
+              const uint32_t w16 = w8 | (__shfl_down_sync(0xffffffffu, w8, 4) << 16);
+              const uint32_t x1 = __shfl_sync(0xffffffffu, w16, 8);
+              const uint32_t x2 = __shfl_sync(0xffffffffu, w16, 16);
+              const uint32_t x3 = __shfl_sync(0xffffffffu, w16, 24);
+              if (lane == 0) {
+                *reinterpret_cast<uint4*>(p.hq + row * (p.I >> 1) + ((mt * 128 + 32 * q) >> 1)) =
+                    make_uint4(w16, x1, x2, x3);
+                p.hsf[sf_tiled_offset(row, 4 * mt + q, p.katoms_h)] = (uint8_t)(ex + 127);
+                if (mt == p.m_tiles - 1 && p.katoms_h > p.m_tiles)  // pad group up to the K tile: scale 1.0
+                  p.hsf[sf_tiled_offset(row, 4 * p.m_tiles + q, p.katoms_h)] = 127;
+              }
+            }
+          }
+        }
+        if constexpr (NV) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          if (lane == 0) atomicMax(p.amax_h + e, __float_as_uint(amax));
+        }
+      } else {
+        const int h_idx = mt * 128 + 32 * q + lane;
+        float sc = 1.f;
+        if constexpr (NV) sc = __fmul_rn(__ldg(p.gb + e), __ldg(p.gw + e));
+        for (int c0 = 0; c0 < cnt; c0 += 32) {
+          float y[32];
+          tc_ld32(tq + c0, y);
+          tc_wait_ld();
+          const int jn = min(32, cnt - c0);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j >= jn) break;
+            const int64_t row = row0 + c0 + j;
+            const int t = __ldg(p.row_tok + row);
+            const float w = __ldg(p.row_w + row) * sc;
+            atomicAdd(p.out_acc + (int64_t)t * p.H + h_idx, y[j] * w);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_tempty));
+      acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int N, bool GATEUP, bool NV>
+cudaError_t launch_gemm_t(const KParams& p, int grid, cudaStream_t s) {
+  using C = GemmCfg<N, GATEUP, NV>;
+  auto k = moe_gemm_kernel<N, GATEUP, NV>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  k<<<grid, 192, C::kSmem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fp4moe

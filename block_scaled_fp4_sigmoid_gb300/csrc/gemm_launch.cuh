@@ -1,0 +1,75 @@
+// Host side of the grouped GEMMs: tensor maps, parameter block and the
+// choice of template instance.
+#pragma once
+
+#include "gemm.cuh"
+
+namespace fp4moe {
+
+template <bool GATEUP>
+cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
+  const fp4moe_dims& d = *a.d;
+  KParams p;
+  memset(&p, 0, sizeof(p));
+  const int K = GATEUP ? d.H : d.I;
+  const int rows = GATEUP ? 2 * d.I : d.H;
+  {
+    const uint64_t dims[3] = {(uint64_t)K / 2, (uint64_t)rows, (uint64_t)d.E};
+    const uint64_t strides[2] = {(uint64_t)K / 2, (uint64_t)rows * (K / 2)};
+    const uint32_t box[3] = {128, 128, 1};
+    if (!encode_tmap_u8(&p.tmA, a.w, 3, dims, strides, box, true)) return cudaErrorInvalidValue;
+  }
+  if (a.sh) {
+    const uint64_t dims[3] = {(uint64_t)K / 2, (uint64_t)rows, 1};
+    const uint64_t strides[2] = {(uint64_t)K / 2, (uint64_t)rows * (K / 2)};
+    const uint32_t box[3] = {128, 128, 1};
+    if (!encode_tmap_u8(&p.tmA_sh, a.sh, 3, dims, strides, box, true)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)K / 2, (uint64_t)a.rows_cap};
+    const uint64_t strides[1] = {(uint64_t)K / 2};
+    const uint32_t box[2] = {128, (uint32_t)a.n_tile};
+    if (!encode_tmap_u8(&p.tmB, a.b, 2, dims, strides, box, true)) return cudaErrorInvalidValue;
+  }
+  p.wsf = a.wsf;
+  p.shsf = a.shsf;
+  p.bsf = a.bsf;
+  p.gw = a.gw;
+  p.gb = a.g_b;
+  p.expert_count = a.expert_count;
+  p.expert_slot = a.expert_slot;
+  p.unit_start = a.unit_start;
+  p.total_units = GATEUP ? &a.plan->gu_units : &a.plan->dn_units;
+  p.row_tok = a.row_tok;
+  p.row_w = a.row_w;
+  p.hq = a.hq;
+  p.hsf = a.hsf;
+  p.h32 = a.h32;
+  p.h_dbg = a.h_dbg;
+  p.out_acc = a.out_acc;
+  p.amax_h = a.amax_h;
+  p.status = a.status;
+  p.E = d.E;
+  p.n_exp = d.E + d.n_shared;
+  p.H = d.H;
+  p.I = d.I;
+  p.K = K;
+  p.rows_per_expert = rows;
+  p.m_tiles = GATEUP ? d.I / 128 : d.H / 128;
+  p.katoms_a = (int)katoms_padded(K, a.nv);
+  p.katoms_b = (int)katoms_padded(K, a.nv);
+  p.katoms_h = (int)katoms_padded(d.I, a.nv);
+  p.has_shared = a.sh != nullptr;
+  const int grid = a.num_sms > 0 ? a.num_sms : 1;
+  switch (a.n_tile * 2 + (a.nv ? 1 : 0)) {
+    case 64: return launch_gemm_t<32, GATEUP, false>(p, grid, s);
+    case 65: return launch_gemm_t<32, GATEUP, true>(p, grid, s);
+    case 128: return launch_gemm_t<64, GATEUP, false>(p, grid, s);
+    case 129: return launch_gemm_t<64, GATEUP, true>(p, grid, s);
+    case 256: return launch_gemm_t<128, GATEUP, false>(p, grid, s);
+    case 257: return launch_gemm_t<128, GATEUP, true>(p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fp4moe

@@ -1,0 +1,103 @@
+// Host-side interfaces between the translation units of libfp4moe.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fp4moe.h"
+
+namespace fp4moe {
+
+constexpr int kSlotRows = 128;    // rows of one slot of the permuted layout
+constexpr int kChunkTokens = 256;  // tokens per chunk of the stable scatter
+
+// Device-side plan of one forward call, written by the plan kernel.
+struct Plan {
+  int32_t n_exp;         // E + n_shared
+  int32_t gu_units;      // gate/up work units
+  int32_t dn_units;      // down work units
+  int32_t slots;         // 128-row slots in use
+};
+
+// Everything the kernels of one forward call need to know about the workspace.
+struct Layout {
+  fp4moe_ws_layout ws;
+  int64_t chunk_counts;  // int32 [n_chunks, n_exp]
+  int64_t plan;          // Plan
+  int64_t gu_start;      // int32 [n_exp + 1] prefix of gate/up units
+  int64_t dn_start;      // int32 [n_exp + 1] prefix of down units
+  int64_t row_e;         // int32 [rows_cap] expert of each row
+  int64_t amax;          // uint32 [2 + n_exp] amax bits (x, spare, h per expert)
+  int n_exp, n_chunks, n_route_per_tok;
+};
+
+bool make_layout(const fp4moe_dims& d, Layout* L);
+
+// ------------------------------------------------------------- launchers
+cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* wr, float* partial, int T, int H, int E,
+                                 int n_splits, cudaStream_t s);
+cudaError_t launch_topk(const fp4moe_dims& d, const float* partial, int n_splits, const float* bias,
+                        int32_t* idx, float* w, float* logits_out, int32_t* chunk_counts, int n_exp,
+                        cudaStream_t s);
+cudaError_t launch_plan(const fp4moe_dims& d, int32_t* chunk_counts, int n_chunks, int n_exp, int n_tile,
+                        int32_t* expert_count, int32_t* expert_slot, int32_t* gu_start, int32_t* dn_start,
+                        Plan* plan, cudaStream_t s);
+cudaError_t launch_scatter(const fp4moe_dims& d, const int32_t* idx, const float* w, const int32_t* chunk_counts,
+                           int n_chunks, int n_exp, int n_tile, const int32_t* expert_slot, int32_t* route_row,
+                           int32_t* row_tok, float* row_w, int32_t* row_e, cudaStream_t s);
+cudaError_t launch_amax(const void* x, int x_is_fp32, int64_t n, uint32_t* amax_bits, cudaStream_t s);
+cudaError_t launch_gather_quant(const fp4moe_dims& d, const uint16_t* x, const int32_t* route_row, uint8_t* xq,
+                                uint8_t* xsf, const uint32_t* amax_x, float* g_out, cudaStream_t s);
+cudaError_t launch_h_quant_nv_routes(const fp4moe_dims& d, const float* h32, const int32_t* route_row,
+                                     const int32_t* row_e, const uint32_t* amax_h, float* gh_out, uint8_t* hq,
+                                     uint8_t* hsf, cudaStream_t s);
+cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, cudaStream_t s);
+cudaError_t launch_quantize_rows(const void* x, int x_is_fp32, int64_t rows, int cols, bool nv,
+                                 const float* global_in, const uint32_t* amax_bits, uint8_t* codes,
+                                 uint8_t* scales, float* global_out, cudaStream_t s);
+cudaError_t launch_pack_scales(const uint8_t* src, uint8_t* dst, int64_t n_mat, int rows, int kblocks, bool nv,
+                               cudaStream_t s);
+cudaError_t launch_convert(const uint8_t* codes, const uint8_t* scales, int64_t rows, int K, uint8_t* out,
+                           float* row_scale, uint8_t* row_status, int32_t* status, cudaStream_t s);
+
+// ------------------------------------------------------------- grouped GEMMs
+struct GemmArgs {
+  const fp4moe_dims* d;
+  bool nv;
+  int n_tile;
+  int num_sms;
+  // weights
+  const uint8_t *w, *wsf;          // routed experts
+  const uint8_t *sh, *shsf;        // shared expert (nullable)
+  const float *gw;                 // NVFP4 tensor scales [E + n_shared]
+  // activations (B operand)
+  const uint8_t *b, *bsf;
+  int rows_cap;
+  // plan
+  const int32_t *expert_count, *expert_slot, *unit_start;
+  const Plan* plan;
+  const int32_t *row_tok;
+  const float *row_w;
+  const float *g_b;                // NVFP4: tensor scale of B (x: one; h: per expert)
+  // outputs
+  uint8_t *hq, *hsf;               // gate/up, MXFP4
+  float *h32;                      // gate/up, NVFP4 (pre-quantisation h)
+  uint32_t *amax_h;                // gate/up, NVFP4
+  float *h_dbg;                    // optional copy of h
+  float *out_acc;                  // down
+  int32_t *status;
+};
+
+cudaError_t launch_gateup(const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_down(const GemmArgs& a, cudaStream_t s);
+
+int device_sm_count();
+
+// Encodes a uint8 tensor map: dims[0] innermost (bytes), strides[i] the byte
+// stride of dimension i + 1, box in elements, optional 128-byte swizzle.
+bool encode_tmap_u8(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides, const uint32_t* box, bool swizzle128);
+
+}  // namespace fp4moe

@@ -1,0 +1,403 @@
+// Router (logits, sigmoid + bias grouped top-k) and the token permutation
+// (expert histogram, prefix sum over experts, stable scatter into the padded
+// slot layout).
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace fp4moe {
+
+namespace {
+
+// ---------------------------------------------------------------- router logits, few tokens
+// One warp per (expert, K split): streams the expert's router row once and
+// forms the dot products with all T <= 16 token rows.
+template <int TMAX>
+__global__ void router_gemv_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
+                                   float* __restrict__ partial, int T, int H, int E, int n_splits) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= E * n_splits) return;
+  const int e = warp % E, sp = warp / E;
+  const int kc = H / n_splits;  // multiple of 256
+  const int k0 = sp * kc;
+  float acc[TMAX];
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
+  const uint16_t* wrow = wr + (int64_t)e * H;
+  for (int k = k0 + lane * 8; k < k0 + kc; k += 256) {
+    const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wrow + k));
+    const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
+    float wf[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      wf[2 * j] = __uint_as_float(wu[j] << 16);
+      wf[2 * j + 1] = __uint_as_float(wu[j] & 0xFFFF0000u);
+    }
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+      if (t < T) {
+        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + (int64_t)t * H + k));
+        const uint32_t xu[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[t] = fmaf(__uint_as_float(xu[j] << 16), wf[2 * j], acc[t]);
+          acc[t] = fmaf(__uint_as_float(xu[j] & 0xFFFF0000u), wf[2 * j + 1], acc[t]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t) {
+    float v = acc[t];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0 && t < T) partial[((int64_t)sp * T + t) * E + e] = v;
+  }
+}
+
+// ---------------------------------------------------------------- router logits, many tokens
+// bf16 tensor-core GEMM (mma.sync m16n8k16, fp32 accumulation) with a
+// three-stage cp.async pipeline.  CTA tile 128 tokens x 64 experts x 32 K,
+// four warps of 32 x 64.  Split-K partials go to partial[split].
+constexpr int RBM = 128, RBN = 64, RBK = 32, RST = 3, RPAD = 8;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__global__ void __launch_bounds__(128) router_mma_kernel(const uint16_t* __restrict__ x,
+                                                         const uint16_t* __restrict__ wr,
+                                                         float* __restrict__ partial, int T, int H, int E,
+                                                         int kc) {
+  __shared__ __align__(16) uint16_t sA[RST][RBM][RBK + RPAD];
+  __shared__ __align__(16) uint16_t sB[RST][RBN][RBK + RPAD];
+  const int tm = blockIdx.x * RBM, tn = blockIdx.y * RBN, sp = blockIdx.z;
+  const int k0 = sp * kc;
+  const int nk = kc / RBK;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  auto load_stage = [&](int st, int kt) {
+    const int kb = k0 + kt * RBK;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // A: 128 rows x 4 chunks of 16 bytes
+      const int c = tid + i * 128;
+      const int r = c >> 2, q = c & 3;
+      const int gr = tm + r;
+      const bool ok = gr < T;
+      cp_async16(smem_u32(&sA[st][r][q * 8]), x + (int64_t)(ok ? gr : 0) * H + kb + q * 8, ok);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {  // B: 64 rows x 4 chunks
+      const int c = tid + i * 128;
+      const int r = c >> 2, q = c & 3;
+      const int gr = tn + r;
+      const bool ok = gr < E;
+      cp_async16(smem_u32(&sB[st][r][q * 8]), wr + (int64_t)(ok ? gr : 0) * H + kb + q * 8, ok);
+    }
+  };
+
+  float acc[2][8][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[i][j][q] = 0.f;
+
+#pragma unroll
+  for (int st = 0; st < RST - 1; ++st) {
+    if (st < nk) load_stage(st, st);
+    cp_commit();
+  }
+  for (int kt = 0; kt < nk; ++kt) {
+    cp_wait<RST - 2>();
+    __syncthreads();
+    const int nxt = kt + RST - 1;
+    if (nxt < nk) load_stage(nxt % RST, nxt);
+    cp_commit();
+    const int st = kt % RST;
+#pragma unroll
+    for (int kk = 0; kk < RBK; kk += 16) {
+      uint32_t af[2][4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int r = warp * 32 + i * 16 + (lane & 15);
+        const int c = kk + ((lane >> 4) << 3);
+        ldsm_x4(smem_u32(&sA[st][r][c]), af[i][0], af[i][1], af[i][2], af[i][3]);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // pairs of n8 tiles
+        const int n = j * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int c = kk + (((lane >> 3) & 1) << 3);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(smem_u32(&sB[st][n][c]), b0, b1, b2, b3);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          mma_bf16(acc[i][2 * j], af[i], b0, b1);
+          mma_bf16(acc[i][2 * j + 1], af[i], b2, b3);
+        }
+      }
+    }
+  }
+  cp_wait<0>();
+  float* dst = partial + (int64_t)sp * T * E;
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r0 = tm + warp * 32 + i * 16 + (lane >> 2);
+      const int c0 = tn + j * 8 + (lane & 3) * 2;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = r0 + 8 * h;
+        if (r < T) {
+          if (c0 < E) dst[(int64_t)r * E + c0] = acc[i][j][2 * h];
+          if (c0 + 1 < E) dst[(int64_t)r * E + c0 + 1] = acc[i][j][2 * h + 1];
+        }
+      }
+    }
+}
+
+// ---------------------------------------------------------------- sigmoid + bias grouped top-k
+// One warp per token.  Scores live in shared memory (E <= 512).
+constexpr int kTopkWarps = 4;
+
+__global__ void topk_kernel(const float* __restrict__ partial, int n_splits, const float* __restrict__ bias,
+                            int T, int E, int k, int n_group, int topk_group, float scaling, int renorm,
+                            int32_t* __restrict__ idx_out, float* __restrict__ w_out, float* __restrict__ logits_out,
+                            int32_t* __restrict__ chunk_counts, int n_exp) {
+  __shared__ float s_s[kTopkWarps][512];
+  __shared__ float s_c[kTopkWarps][512];
+  __shared__ float s_g[kTopkWarps][32];
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kTopkWarps + wib;
+  if (t >= T) return;
+  float* sv = s_s[wib];
+  float* cv = s_c[wib];
+  for (int e = lane; e < E; e += 32) {
+    float l = 0.f;
+    for (int sp = 0; sp < n_splits; ++sp) l += partial[((int64_t)sp * T + t) * E + e];
+    if (logits_out) logits_out[(int64_t)t * E + e] = l;
+    const float s = 1.0f / (1.0f + expf(-l));
+    sv[e] = s;
+    cv[e] = s + bias[e];
+  }
+  __syncwarp();
+  // group selection: group score = sum of the two largest corrected scores
+  uint32_t group_ok = 0xffffffffu;
+  if (n_group > 1) {
+    const int gsz = E / n_group;
+    float gs = -INFINITY;
+    if (lane < n_group) {
+      float a = -INFINITY, b = -INFINITY;
+      for (int i = 0; i < gsz; ++i) {
+        const float v = cv[lane * gsz + i];
+        if (v > a) { b = a; a = v; } else if (v > b) { b = v; }
+      }
+      gs = a + b;
+    }
+    group_ok = 0;
+    for (int r = 0; r < topk_group; ++r) {
+      float bv = (lane < n_group && !((group_ok >> lane) & 1u)) ? gs : -INFINITY;
+      int bi = lane;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      group_ok |= 1u << bi;
+    }
+    for (int e = lane; e < E; e += 32)
+      if (!((group_ok >> (e / gsz)) & 1u)) cv[e] = -INFINITY;
+    __syncwarp();
+  }
+  // top-k over corrected scores, ties to the lower expert index
+  int my_idx = -1;
+  float my_s = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int e = lane; e < E; e += 32) {
+      const float v = cv[e];
+      if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    }
+    if (lane == j) { my_idx = bi; my_s = sv[bi]; }
+    __syncwarp();
+    if (lane == 0) cv[bi] = -INFINITY;
+    __syncwarp();
+  }
+  float tot = 0.f;
+  for (int j = 0; j < k; ++j) tot += __shfl_sync(0xffffffffu, my_s, j);
+  if (lane < k) {
+    const float w = renorm ? my_s / tot * scaling : my_s * scaling;
+    idx_out[(int64_t)t * k + lane] = my_idx;
+    w_out[(int64_t)t * k + lane] = w;
+    atomicAdd(&chunk_counts[(t / kChunkTokens) * n_exp + my_idx], 1);
+  }
+}
+
+// ---------------------------------------------------------------- plan
+// One CTA.  Turns per-chunk counts into per-chunk bases (in place), totals,
+// tiles, slots and the unit prefixes of both GEMMs.
+__global__ void plan_kernel(int32_t* chunk_counts, int n_chunks, int n_exp, int E, int T, int n_tile,
+                            int gu_mtiles, int dn_mtiles, int32_t* expert_count, int32_t* expert_slot,
+                            int32_t* gu_start, int32_t* dn_start, Plan* plan) {
+  __shared__ int32_t s_tiles[1024];
+  for (int e = threadIdx.x; e < n_exp; e += blockDim.x) {
+    int run = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      int32_t* p = chunk_counts + (int64_t)c * n_exp + e;
+      int v;
+      if (e >= E) v = min(kChunkTokens, T - c * kChunkTokens);  // shared expert: every token
+      else v = *p;
+      *p = run;
+      run += v;
+    }
+    expert_count[e] = run;
+    s_tiles[e] = (run + n_tile - 1) / n_tile;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int slot = 0, gu = 0, dn = 0;
+    for (int e = 0; e < n_exp; ++e) {
+      expert_slot[e] = slot;
+      gu_start[e] = gu;
+      dn_start[e] = dn;
+      slot += s_tiles[e];
+      gu += s_tiles[e] * gu_mtiles;
+      dn += s_tiles[e] * dn_mtiles;
+    }
+    gu_start[n_exp] = gu;
+    dn_start[n_exp] = dn;
+    plan->n_exp = n_exp;
+    plan->gu_units = gu;
+    plan->dn_units = dn;
+    plan->slots = slot;
+  }
+}
+
+// ---------------------------------------------------------------- stable scatter
+// One warp per chunk of 256 tokens.  Routes are visited in (token, slot)
+// order; __match_any_sync groups the routes of one expert inside each 32-route
+// step, so the position of a route is the chunk base + earlier routes of the
+// same expert in this chunk.
+constexpr int kScatterWarps = 2;
+
+__global__ void scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w,
+                               const int32_t* __restrict__ chunk_base, int T, int k, int E, int n_exp, int n_chunks,
+                               int n_tile, const int32_t* __restrict__ expert_slot, int32_t* __restrict__ route_row,
+                               int32_t* __restrict__ row_tok, float* __restrict__ row_w, int32_t* __restrict__ row_e) {
+  __shared__ int32_t s_cnt[kScatterWarps][520];
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * kScatterWarps + wib;
+  if (c >= n_chunks) return;
+  int32_t* cnt = s_cnt[wib];
+  for (int e = lane; e < n_exp; e += 32) cnt[e] = 0;
+  __syncwarp();
+  const int rpt = k + (n_exp - E);
+  const int t0 = c * kChunkTokens, t1 = min(T, t0 + kChunkTokens);
+  const int64_t r0 = (int64_t)t0 * k, r1 = (int64_t)t1 * k;
+  for (int64_t base = r0; base < r1; base += 32) {
+    const int64_t r = base + lane;
+    const bool valid = r < r1;
+    const int e = valid ? idx[r] : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int prior = valid ? cnt[e] : 0;
+    __syncwarp();
+    if (valid && rank == 0) cnt[e] = prior + __popc(peers);
+    __syncwarp();
+    if (valid) {
+      const int pos = chunk_base[(int64_t)c * n_exp + e] + prior + rank;
+      const int64_t row = (int64_t)(expert_slot[e] + pos / n_tile) * kSlotRows + pos % n_tile;
+      const int64_t t = r / k;
+      const int j = (int)(r - t * k);
+      route_row[t * rpt + j] = (int32_t)row;
+      row_tok[row] = (int32_t)t;
+      row_w[row] = w[r];
+      row_e[row] = e;
+    }
+  }
+  for (int s = E; s < n_exp; ++s) {  // shared experts: every token, in order
+    for (int t = t0 + lane; t < t1; t += 32) {
+      const int pos = t;
+      const int64_t row = (int64_t)(expert_slot[s] + pos / n_tile) * kSlotRows + pos % n_tile;
+      route_row[(int64_t)t * rpt + k + (s - E)] = (int32_t)row;
+      row_tok[row] = t;
+      row_w[row] = 1.0f;
+      row_e[row] = s;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* wr, float* partial, int T, int H, int E,
+                                 int n_splits, cudaStream_t s) {
+  if (T <= 16) {
+    const int warps = E * n_splits;
+    const int threads = 256;
+    const unsigned blocks = (unsigned)((warps * 32 + threads - 1) / threads);
+    if (T <= 8) router_gemv_kernel<8><<<blocks, threads, 0, s>>>(x, wr, partial, T, H, E, n_splits);
+    else router_gemv_kernel<16><<<blocks, threads, 0, s>>>(x, wr, partial, T, H, E, n_splits);
+  } else {
+    dim3 grid((T + RBM - 1) / RBM, (E + RBN - 1) / RBN, n_splits);
+    router_mma_kernel<<<grid, 128, 0, s>>>(x, wr, partial, T, H, E, H / n_splits);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const fp4moe_dims& d, const float* partial, int n_splits, const float* bias, int32_t* idx,
+                        float* w, float* logits_out, int32_t* chunk_counts, int n_exp, cudaStream_t s) {
+  const unsigned blocks = (unsigned)((d.T + kTopkWarps - 1) / kTopkWarps);
+  topk_kernel<<<blocks, 32 * kTopkWarps, 0, s>>>(partial, n_splits, bias, d.T, d.E, d.top_k, d.n_group,
+                                                 d.topk_group, d.routed_scaling, d.renormalize, idx, w, logits_out,
+                                                 chunk_counts, n_exp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const fp4moe_dims& d, int32_t* chunk_counts, int n_chunks, int n_exp, int n_tile,
+                        int32_t* expert_count, int32_t* expert_slot, int32_t* gu_start, int32_t* dn_start,
+                        Plan* plan, cudaStream_t s) {
+  plan_kernel<<<1, 1024, 0, s>>>(chunk_counts, n_chunks, n_exp, d.E, d.T, n_tile, d.I / 128, d.H / 128,
+                                 expert_count, expert_slot, gu_start, dn_start, plan);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const fp4moe_dims& d, const int32_t* idx, const float* w, const int32_t* chunk_counts,
+                           int n_chunks, int n_exp, int n_tile, const int32_t* expert_slot, int32_t* route_row,
+                           int32_t* row_tok, float* row_w, int32_t* row_e, cudaStream_t s) {
+  const unsigned blocks = (unsigned)((n_chunks + kScatterWarps - 1) / kScatterWarps);
+  scatter_kernel<<<blocks, 32 * kScatterWarps, 0, s>>>(idx, w, chunk_counts, d.T, d.top_k, d.E, n_exp, n_chunks,
+                                                        n_tile, expert_slot, route_row, row_tok, row_w, row_e);
+  return cudaGetLastError();
+}
+
+}  // namespace fp4moe

@@ -1,0 +1,137 @@
+"""A routed block-scaled FP4 MoE layer held in device memory.
+
+``MoELayer`` owns the expert weights (packed FP4 codes, repacked block
+scales, NVFP4 tensor scales), the router weights and bias, and a workspace;
+``forward`` calls fp4moe_forward.  PyTorch only allocates device memory and
+supplies the stream.  ``MoELayer.synthetic`` draws a layer from the seeded
+generator in ``synth`` directly on the GPU (weights of the NVFP4
+configuration are quantised from bf16 by fp4moe_quantize_act, one tensor scale
+per expert and weight tensor).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import (MXFP4, NVFP4, Debug, Weights, forward, make_dims, pack_scales, packed_scales_bytes,
+               quantize_act, workspace_layout, workspace_size)
+
+
+def _ptr(t):
+    return t.data_ptr() if t is not None else None
+
+
+class MoELayer:
+    def __init__(self, dims, w13, w13_scale, w2, w2_scale, w_router, bias, g13=None, g2=None,
+                 sh13=None, sh13_scale=None, sh2=None, sh2_scale=None):
+        """Tensors on one CUDA device.  Scales are the raw row-major block
+        scales ([E, rows, K/32] E8M0 or [E, rows, K/16] E4M3); they are
+        repacked here into the layout the GEMMs load."""
+        self.dims = dims
+        self.fmt = dims.fmt
+        self.device = w13.device
+        blk = 16 if dims.fmt == NVFP4 else 32
+        self.w13, self.w2 = w13.contiguous(), w2.contiguous()
+        self.w13_scale = self._pack(w13_scale, dims.E, 2 * dims.I, dims.H // blk)
+        self.w2_scale = self._pack(w2_scale, dims.E, dims.H, dims.I // blk)
+        self.w_router, self.bias = w_router.contiguous(), bias.contiguous()
+        self.g13, self.g2 = g13, g2
+        self.sh13, self.sh2 = sh13, sh2
+        self.sh13_scale = self._pack(sh13_scale, 1, 2 * dims.I, dims.H // blk) if sh13 is not None else None
+        self.sh2_scale = self._pack(sh2_scale, 1, dims.H, dims.I // blk) if sh2 is not None else None
+        self.ws_bytes = workspace_size(dims)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        self.layout = workspace_layout(dims)
+        self.weights = Weights(_ptr(self.w13), _ptr(self.w13_scale), _ptr(self.w2), _ptr(self.w2_scale),
+                               _ptr(self.g13), _ptr(self.g2), _ptr(self.sh13), _ptr(self.sh13_scale),
+                               _ptr(self.sh2), _ptr(self.sh2_scale), _ptr(self.w_router), _ptr(self.bias))
+
+    def _pack(self, raw, n_mat, rows, kblocks):
+        dst = torch.empty(packed_scales_bytes(n_mat, rows, kblocks, self.fmt), dtype=torch.uint8,
+                          device=raw.device)
+        pack_scales(raw.data_ptr(), dst.data_ptr(), n_mat, rows, kblocks, self.fmt,
+                    torch.cuda.current_stream(raw.device).cuda_stream)
+        return dst
+
+    def weight_bytes_per_expert(self) -> int:
+        """Packed FP4 codes plus scales of one routed expert (w13 and w2)."""
+        d = self.dims
+        blk = 16 if d.fmt == NVFP4 else 32
+        elems = 3 * d.H * d.I
+        return elems // 2 + elems // blk
+
+    def forward(self, x, out=None, debug: Debug | None = None, stream=None):
+        d = self.dims
+        if out is None:
+            out = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=self.device)
+        s = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
+        forward(d, self.weights, x.data_ptr(), out.data_ptr(), self.ws.data_ptr(), self.ws_bytes, s, debug)
+        return out
+
+    # ------------------------------------------------------------ workspace views
+    def ws_view(self, name: str, dtype, count: int):
+        off = getattr(self.layout, name)
+        nbytes = count * torch.empty((), dtype=dtype).element_size()
+        return self.ws[off:off + nbytes].view(dtype)
+
+    # ------------------------------------------------------------ synthetic layers
+    @classmethod
+    def synthetic(cls, cfg, device="cuda"):
+        import synth
+        fmt = NVFP4 if cfg.fmt == "nvfp4" else MXFP4
+        dims = make_dims(cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k, cfg.n_group, cfg.topk_group, cfg.n_shared,
+                         cfg.routed_scaling, cfg.renormalize, fmt)
+        dev = torch.device(device)
+        wr = torch.from_numpy(synth.gen_router_bf16(cfg).view("int16")).to(dev)
+        bias = torch.from_numpy(synth.gen_bias_f32(cfg)).to(dev)
+        ws_small = torch.zeros(256, dtype=torch.uint8, device=dev)
+
+        def mx_weight(which, n_exp):
+            rows, K = synth.weight_shape(cfg, which)
+            codes_s, scale_s = synth._mx_streams(which)
+            codes = torch.empty((n_exp, rows, K // 2), dtype=torch.uint8, device=dev)
+            synth.dev_uniform_bytes(cfg.seed, codes_s, 0, codes)
+            scales = torch.empty((n_exp, rows, K // 32), dtype=torch.uint8, device=dev)
+            synth.dev_e8m0_scales(cfg.seed, scale_s, 0, n_exp * rows, K // 32, scales)
+            return codes, scales, None
+
+        def nv_weight(which, n_exp):
+            rows, K = synth.weight_shape(cfg, which)
+            st = {"w13": synth.S_W13_BF16, "w2": synth.S_W2_BF16,
+                  "sh13": synth.S_SH13_BF16, "sh2": synth.S_SH2_BF16}[which]
+            codes = torch.empty((n_exp, rows, K // 2), dtype=torch.uint8, device=dev)
+            scales = torch.empty((n_exp, rows, K // 16), dtype=torch.uint8, device=dev)
+            g = torch.empty(n_exp, dtype=torch.float32, device=dev)
+            tmp = torch.empty((rows, K), dtype=torch.int16, device=dev)
+            s = torch.cuda.current_stream(dev).cuda_stream
+            for e in range(n_exp):
+                synth.dev_normal_bf16(cfg.seed, st, e * rows * K, tmp, cfg.w_std, s)
+                quantize_act(tmp.data_ptr(), False, rows, K, NVFP4, None, codes[e].data_ptr(), scales[e].data_ptr(),
+                             g[e:e + 1].data_ptr(), ws_small.data_ptr(), 256, s)
+            return codes, scales, g
+
+        make = nv_weight if fmt == NVFP4 else mx_weight
+        w13, w13s, g13 = make("w13", cfg.E)
+        w2, w2s, g2 = make("w2", cfg.E)
+        sh = {}
+        if cfg.n_shared:
+            s13, s13s, sg13 = make("sh13", 1)
+            s2, s2s, sg2 = make("sh2", 1)
+            sh = dict(sh13=s13, sh13_scale=s13s, sh2=s2, sh2_scale=s2s)
+            if fmt == NVFP4:
+                g13 = torch.cat([g13, sg13])
+                g2 = torch.cat([g2, sg2])
+        layer = cls(dims, w13, w13s, w2, w2s, wr, bias, g13=g13, g2=g2, **sh)
+        layer.cfg = cfg
+        layer.raw_scales = (w13s, w2s)
+        return layer
+
+    def synthetic_x(self, t0: int = 0, t1: int | None = None):
+        """Activations of the synthetic configuration, drawn on the device."""
+        import synth
+        cfg = self.cfg
+        t1 = cfg.T if t1 is None else t1
+        x = torch.empty((t1 - t0, cfg.H), dtype=torch.int16, device=self.device)
+        synth.dev_normal_bf16(cfg.seed, synth.S_X, t0 * cfg.H, x, cfg.x_std)
+        return x.view(torch.bfloat16)

@@ -1,0 +1,226 @@
+/*
+ * fp4moe - routed mixture-of-experts layer over block-scaled FP4 weights,
+ * for NVIDIA GB300 (sm_103a).  C ABI.
+ *
+ * The layer (one call of fp4moe_forward) computes, for T tokens x[T, H]:
+ *   1. router logits l = x . Wr^T (bf16 inputs, fp32 accumulation), sigmoid
+ *      scores s, corrected scores c = s + bias, grouped top-k on c, routing
+ *      weights from s                      ("Kimi-K2.7-Code on Gaudi 2",
+ *      section "What was built": grouped top-k router, sigmoid scoring with
+ *      correction bias);
+ *   2. an expert histogram, prefix sum and stable permutation of the routes;
+ *   3. on-the-fly MXFP4 or NVFP4 quantisation of x ("Serve Kimi-K2.5-MXFP4 on
+ *      MI355X with ATOM", section "Stage B: Dynamic Activation Quantization";
+ *      "Serving NVFP4 models on AMD Instinct MI355 accelerators", section
+ *      "Weight Dequantization and Activation QDQ");
+ *   4. the gate/up grouped GEMM on block-scaled FP4 tensor cores, SwiGLU and
+ *      requantisation of the intermediate (A4W4);
+ *   5. the down grouped GEMM whose epilogue adds w * y into the output
+ *      (section "Stage D: MXFP4 Fused MoE": two-stage fused MoE, atomic
+ *      combine variant).
+ * fp4moe_mxfp4_to_fp8_rowscale is the exact per-channel MXFP4 -> FP8
+ * conversion of "Kimi-K2.7-Code on Gaudi 2", section "Exact MXFP4 to FP8
+ * per-channel conversion".
+ *
+ * Conventions for every entry point:
+ *   - Pointers are CUDA device pointers owned by the caller unless stated.
+ *     The library allocates no device memory; scratch lives in a caller
+ *     workspace (fp4moe_workspace_size).
+ *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream.  Every call is asynchronous on it; none synchronises the host.
+ *   - Argument and shape errors are returned synchronously and launch nothing.
+ *     Data-dependent conditions (NaN scale bytes, conversion rows outside the
+ *     exactness contract, a device wait that timed out) are recorded in a
+ *     status word in the workspace; fp4moe_get_status reads it.
+ *   - bf16 values are passed as uint16_t bit patterns.
+ *   - Packed FP4: element 2j of a row in the low nibble of byte j, element
+ *     2j+1 in the high nibble.  E2M1 code: sign bit 3, exponent bits 2..1
+ *     (bias 1), mantissa bit 0.
+ *   - MXFP4 scales: one E8M0 byte per 32 consecutive K values (2^(b-127)).
+ *     NVFP4 scales: one E4M3 byte per 16 K values, plus one fp32 tensor scale.
+ */
+#ifndef FP4MOE_H
+#define FP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FP4MOE_OK = 0,
+  FP4MOE_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad enum   */
+  FP4MOE_ERR_UNSUPPORTED_SHAPE = 2, /* a size outside the supported set        */
+  FP4MOE_ERR_WORKSPACE = 3,         /* workspace missing or too small          */
+  FP4MOE_ERR_CUDA = 4,              /* a CUDA runtime/driver call failed       */
+  FP4MOE_ERR_TIMEOUT = 5,           /* a device-side wait ran out (status word) */
+  FP4MOE_ERR_NAN_SCALE = 6,         /* an E8M0 scale byte 255 was seen          */
+  FP4MOE_ERR_INEXACT = 7,           /* conversion row below the exponent floor */
+  FP4MOE_ERR_DEVICE = 8             /* no sm_103 device is current             */
+} fp4moe_status;
+
+typedef enum { FP4MOE_MXFP4 = 0, FP4MOE_NVFP4 = 1 } fp4moe_format;
+
+/* Layer shape and routing parameters.
+ *   T tokens, H hidden size, I expert intermediate size, E routed experts,
+ *   top_k experts per token, n_group / topk_group grouped routing
+ *   (n_group = 1: plain top-k), n_shared always-on shared experts (0 or 1),
+ *   routed_scaling multiplies the routing weights, renormalize != 0 divides
+ *   the chosen sigmoid scores by their sum first, fmt an fp4moe_format.
+ * Supported: 1 <= T <= 65536; H % 256 == 0; I % 128 == 0; 1 <= E <= 512;
+ *   1 <= top_k <= 16 and top_k <= E; E % n_group == 0; E / n_group <= 64 when
+ *   n_group > 1; 1 <= topk_group <= n_group <= 32; n_shared in {0, 1}. */
+typedef struct {
+  int32_t T, H, I, E, top_k, n_group, topk_group, n_shared;
+  float routed_scaling;
+  int32_t renormalize;
+  int32_t fmt;
+} fp4moe_dims;
+
+/* Expert and router weights.
+ *   w13       packed FP4 [E, 2I, H/2]: rows 0..I-1 gate, I..2I-1 up.
+ *   w2        packed FP4 [E, H, I/2].
+ *   w13_scale / w2_scale: block scales already repacked by fp4moe_pack_scales
+ *             (E8M0 for MXFP4, E4M3 for NVFP4).
+ *   g13, g2   NVFP4 only: fp32 tensor scales [E + n_shared] (shared expert
+ *             last); NULL for MXFP4.
+ *   sh13, sh13_scale, sh2, sh2_scale: the shared expert, same layouts with
+ *             E = 1; NULL when n_shared == 0.
+ *   w_router  bf16 [E, H].   bias  fp32 [E] correction bias. */
+typedef struct {
+  const uint8_t *w13, *w13_scale, *w2, *w2_scale;
+  const float *g13, *g2;
+  const uint8_t *sh13, *sh13_scale, *sh2, *sh2_scale;
+  const uint16_t *w_router;
+  const float *bias;
+} fp4moe_weights;
+
+/* Byte offsets of the forward's intermediates inside the workspace, for
+ * inspection after a call (all relative to the workspace base).  Row indices
+ * refer to the padded permuted layout: routes of one expert occupy tiles of
+ * n_tile rows, each tile at the start of its own 128-row slot. */
+typedef struct {
+  int64_t status;       /* int32[16] status word                            */
+  int64_t logits;       /* fp32 [n_splits, T, E] partial router logits      */
+  int64_t topk_idx;     /* int32 [T, top_k], in descending corrected score  */
+  int64_t topk_w;       /* fp32 [T, top_k]                                  */
+  int64_t expert_count; /* int32 [E + n_shared] routes per expert           */
+  int64_t expert_slot;  /* int32 [E + n_shared] first 128-row slot          */
+  int64_t route_row;    /* int32 [T, top_k + n_shared] padded row of route  */
+  int64_t row_tok;      /* int32 [rows_cap] token of each padded row        */
+  int64_t row_w;        /* fp32  [rows_cap] routing weight of each row      */
+  int64_t xq;           /* u8 [rows_cap, H/2] quantised activations         */
+  int64_t xsf;          /* u8 tiled scales of xq (fp4moe_pack_scales layout) */
+  int64_t hq;           /* u8 [rows_cap, I/2] quantised intermediate        */
+  int64_t hsf;          /* u8 tiled scales of hq                            */
+  int64_t h32;          /* fp32 [rows_cap, I] pre-quantisation h (NVFP4)    */
+  int64_t gscale;       /* fp32 [2 + E + n_shared]: g_x, spare, g_h[e]       */
+  int64_t out_acc;      /* fp32 [T, H] combine accumulator                  */
+  int64_t total_bytes;
+  int32_t n_splits;     /* router split-K factor                            */
+  int32_t n_tile;       /* tokens per GEMM tile                             */
+  int32_t rows_cap;     /* rows of the padded permuted layout               */
+  int32_t reserved;
+} fp4moe_ws_layout;
+
+/* Optional instrumentation for fp4moe_forward.
+ *   events[i] (cudaEvent_t as void*, nullable) is recorded on the stream
+ *     before stage i: 0 router, 1 top-k, 2 permutation, 3 activation
+ *     quantisation, 4 gate/up GEMM, 5 down GEMM, 6 finalise, 7 end.
+ *   h_pre (nullable): fp32 [rows_cap, I]; when set the gate/up epilogue also
+ *     writes each h value there before quantising it. */
+typedef struct {
+  void *events[8];
+  float *h_pre;
+} fp4moe_debug;
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t fp4moe_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char *fp4moe_status_string(int32_t status);
+
+/* Workspace bytes fp4moe_forward needs for these dims (0 on invalid dims). */
+size_t fp4moe_workspace_size(const fp4moe_dims *dims);
+
+/* Fills *out with the workspace layout of these dims. */
+fp4moe_status fp4moe_workspace_layout(const fp4moe_dims *dims, fp4moe_ws_layout *out);
+
+/* Bytes of the tiled scale layout for n_mat matrices of `rows` rows and
+ * `kblocks` scale blocks per row (rows % 128 == 0, kblocks % 4 == 0). */
+size_t fp4moe_packed_scales_bytes(int64_t n_mat, int32_t rows, int32_t kblocks, int32_t fmt);
+
+/* Repacks row-major block scales src[n_mat, rows, kblocks] into the tiled
+ * layout the GEMMs load: for each matrix, 128-row tile and group of four
+ * blocks, 512 bytes where row r = 32*m1 + m0 and block k1 sit at byte
+ * 16*m0 + 4*m1 + k1.  Groups are padded to whole 256-value K tiles with the
+ * scale 1.0.  This is the one-time weight preparation step, the counterpart
+ * of the pre-shuffled weight operand of "Serve Kimi-K2.5-MXFP4 on MI355X with
+ * ATOM", section "Stage C: MXFP4 Linear GEMM".  dst holds
+ * fp4moe_packed_scales_bytes bytes. */
+fp4moe_status fp4moe_pack_scales(const uint8_t *src, uint8_t *dst, int64_t n_mat, int32_t rows,
+                                 int32_t kblocks, int32_t fmt, void *stream);
+
+/* Router: logits, sigmoid + bias, grouped top-k and routing weights
+ * ("Kimi-K2.7-Code on Gaudi 2", section "What was built").
+ *   x [T, H] bf16, w_router [E, H] bf16, bias [E] fp32 ->
+ *   topk_idx [T, top_k] int32 (descending corrected score, ties to the lower
+ *   expert index), topk_w [T, top_k] fp32, logits_out [T, E] fp32 (nullable).
+ * ws: a workspace of fp4moe_workspace_size(dims) bytes. */
+fp4moe_status fp4moe_route(const fp4moe_dims *dims, const uint16_t *x, const uint16_t *w_router,
+                           const float *bias, int32_t *topk_idx, float *topk_w, float *logits_out,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/* Activation quantisation ("Serve Kimi-K2.5-MXFP4 on MI355X with ATOM",
+ * section "Stage B: Dynamic Activation Quantization"; "Serving NVFP4 models on
+ * AMD Instinct MI355 accelerators", section "Weight Dequantization and
+ * Activation QDQ").
+ *   x [rows, cols] bf16 (x_is_fp32 = 0) or fp32 (x_is_fp32 = 1), row-major.
+ *   codes [rows, cols/2] packed E2M1.  scales row-major: MXFP4 [rows, cols/32]
+ *   E8M0 bytes, e = floor(log2 amax) - 2; NVFP4 [rows, cols/16] E4M3 bytes.
+ *   NVFP4 tensor scale: global_in (nullable, fp32 device scalar) is used when
+ *   given, else g = amax(x) / 2688 is computed over the whole tensor; the g
+ *   used is written to global_out (nullable).
+ *   cols % 32 == 0.  ws must hold >= 256 bytes (amax scratch + status). */
+fp4moe_status fp4moe_quantize_act(const void *x, int32_t x_is_fp32, int64_t rows, int32_t cols,
+                                  int32_t fmt, const float *global_in, uint8_t *codes,
+                                  uint8_t *scales, float *global_out, void *ws, size_t ws_bytes,
+                                  void *stream);
+
+/* The whole MoE layer: out[T, H] (bf16) for x[T, H] (bf16).  All weights as
+ * in fp4moe_weights.  dbg is nullable.  ws: fp4moe_workspace_size(dims) bytes;
+ * its intermediates stay readable after the call (fp4moe_workspace_layout). */
+fp4moe_status fp4moe_forward(const fp4moe_dims *dims, const fp4moe_weights *w, const uint16_t *x,
+                             uint16_t *out, const fp4moe_debug *dbg, void *ws, size_t ws_bytes,
+                             void *stream);
+
+/* Exact MXFP4 -> FP8 (E4M3) per-channel conversion ("Kimi-K2.7-Code on
+ * Gaudi 2", section "Exact MXFP4 to FP8 per-channel conversion").
+ *   codes [rows, K/2] packed E2M1, scales [rows, K/32] E8M0 row-major ->
+ *   fp8_out [rows, K] E4M3 bytes, row_scale [rows] fp32 = 2^k with
+ *   k = floor(log2 max|v|) - 7, row_status [rows] (nullable): 0 exact and
+ *   every element exponent in [-5, 7]; 1 some element below the -5 floor
+ *   (written round-to-nearest-even, possibly inexact); 2 a scale byte 255
+ *   (bytes 0, scale NaN).  All-zero rows: scale 1.0.  K % 32 == 0.
+ *   Rows with status 1 or 2 are counted in the workspace status word
+ *   (FP4MOE_ERR_INEXACT / FP4MOE_ERR_NAN_SCALE); ws >= 256 bytes. */
+fp4moe_status fp4moe_mxfp4_to_fp8_rowscale(const uint8_t *codes, const uint8_t *scales_e8m0,
+                                           int64_t rows, int32_t K, uint8_t *fp8_out,
+                                           float *row_scale, uint8_t *row_status, void *ws,
+                                           size_t ws_bytes, void *stream);
+
+/* Clears the workspace status word (asynchronous). */
+fp4moe_status fp4moe_clear_status(void *ws, void *stream);
+
+/* Synchronises `stream` and reads the workspace status word: *st the first
+ * recorded condition (FP4MOE_OK if none), *count how many were recorded.
+ * Either output may be NULL. */
+fp4moe_status fp4moe_get_status(void *ws, void *stream, fp4moe_status *st, int64_t *count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP4MOE_H */

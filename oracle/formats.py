@@ -54,18 +54,24 @@ _E4M3_POS = E4M3_TABLE[:127]
 
 def _rne_grid(mag: np.ndarray, grid: np.ndarray) -> np.ndarray:
     """Index of the grid point nearest to each non-negative magnitude; a tie
-    goes to the even index; magnitudes beyond the last point saturate."""
+    goes to the even index; magnitudes beyond the last point saturate.
+
+    With mids[i] the midpoint of grid[i] and grid[i+1], the nearest point of
+    a magnitude is the number of midpoints strictly below it; a magnitude on
+    a midpoint lies between an odd and an even index and takes the even one."""
     mag = np.asarray(mag, dtype=np.float64)
-    hi = np.searchsorted(grid, mag, side="left")          # grid[hi-1] < mag <= grid[hi]
-    hi = np.minimum(hi, len(grid) - 1)
-    lo = np.maximum(hi - 1, 0)
-    dlo = mag - grid[lo]
-    dhi = grid[hi] - mag
-    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
-    idx = np.where(pick_hi, hi, lo)
-    idx = np.where(mag >= grid[-1], len(grid) - 1, idx)
-    idx = np.where(mag <= 0, 0, idx)
-    return idx.astype(np.int64)
+    mids = (grid[1:] + grid[:-1]) / 2
+    if len(mids) <= 16:  # short grid: count the midpoints one by one
+        idx = np.zeros(mag.shape, dtype=np.int64)
+        on_mid = np.zeros(mag.shape, dtype=bool)
+        for m in mids:
+            idx += mag > m
+            on_mid |= mag == m
+    else:
+        idx = np.searchsorted(mids, mag, side="left")
+        on_mid = np.take(mids, np.minimum(idx, len(mids) - 1)) == mag
+    idx += on_mid & ((idx & 1) == 1)
+    return idx
 
 
 def e2m1_encode(v: np.ndarray) -> np.ndarray:

@@ -152,15 +152,64 @@ class WeightSource:
         self._cache.pop((which, e), None)
 
 
+def expert_rows(cfg, e: int, a: np.ndarray, wts: np.ndarray, weights: WeightSource,
+                gamma: float = GAMMA, with_ambiguity: bool = True) -> dict:
+    """The MLP of expert e (ids >= E are shared experts) for the dequantised
+    activation rows a [n, H] routed to it with weights wts [n].  Returns the
+    intermediates and y, the S term and the ambiguity term per row."""
+    E, I, fmt = cfg.E, cfg.I, cfg.fmt
+    if e < E:
+        w13, w2 = weights.get("w13", e), weights.get("w2", e)
+    else:
+        w13, w2 = weights.get("sh13", e - E), weights.get("sh2", e - E)
+    W13 = Q.dequant(w13[0], w13[1], fmt, w13[2])
+    gu = a @ W13.T
+    gu_abs = np.abs(a) @ np.abs(W13).T
+    del W13
+    g, u = gu[:, :I], gu[:, I:]
+    h = silu(g) * u
+    h32 = h.astype(np.float32).astype(np.float64)
+    if fmt == "mxfp4":
+        hq, hs = Q.mx_quantize(h32)
+        g_h = None
+    else:
+        hq, hs, g_h = Q.nv_quantize(h32)
+    hd = Q.dequant(hq, hs, fmt, g_h)
+    W2 = Q.dequant(w2[0], w2[1], fmt, w2[2])
+    W2a = np.abs(W2)
+    y = hd @ W2.T
+    Sy = np.abs(hd) @ W2a.T
+    info = {"wt": wts, "h": h, "h32": h32, "hq": hq, "hs": hs, "g_h": g_h, "y": y, "Sy": Sy,
+            "gu_abs": gu_abs}
+    if with_ambiguity:
+        dg = gamma * gu_abs[:, :I] + 2.0 ** -22 * np.abs(g)
+        du = gamma * gu_abs[:, I:] + 2.0 ** -22 * np.abs(u)
+        sg = silu(g)
+        dh = (SILU_LIP * dg * (np.abs(u) + du) + np.abs(sg) * du
+              + EPS_SWIGLU * np.abs(h) + 2.0 ** -140)
+        if fmt == "mxfp4":
+            dmax, srange = _h_candidates_mx(h32, dh, hq, hs)
+        else:
+            dmax, srange = _h_candidates_nv(h32, dh, hq, hs, g_h)
+        info.update({"dh": dh, "dmax": dmax, "scale_range": srange, "Ay": dmax @ W2a.T,
+                     "n_ambiguous": int(np.count_nonzero(dmax))})
+    else:
+        info["Ay"] = np.zeros_like(y)
+    return info
+
+
 def layer_forward(cfg, x_bits_f64: np.ndarray, wr_f64: np.ndarray, bias_f32: np.ndarray,
                   weights: WeightSource, tokens=None, gamma: float = GAMMA,
                   with_ambiguity: bool = True):
-    """The whole layer for the tokens in ``tokens`` (default: all).
+    """The whole layer with routing over all T tokens; outputs for the tokens
+    in ``tokens`` (default: all).  Every expert a chosen token uses is
+    evaluated on all of its routed rows (NVFP4's per-expert tensor scale of h
+    depends on all of them).
 
     x_bits_f64 / wr_f64 hold the exact values of the bf16 inputs.  Returns a
     dict with routing, quantised activations, permutation, per-expert
     intermediates, and for the chosen tokens ref / S / A [len(tokens), H]."""
-    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k
+    T, H, E, k = cfg.T, cfg.H, cfg.E, cfg.top_k
     ns = cfg.n_shared
     fmt = cfg.fmt
     tokens = np.arange(T) if tokens is None else np.asarray(tokens)
@@ -180,57 +229,17 @@ def layer_forward(cfg, x_bits_f64: np.ndarray, wr_f64: np.ndarray, bias_f32: np.
         rows = np.arange(offsets[e], offsets[e + 1])
         toks = ptok[rows]
         slots = pslot[rows]
-        if e < E:
-            wts = w[toks, np.minimum(slots, k - 1)]
-            w13 = weights.get("w13", e)
-            w2 = weights.get("w2", e)
-        else:
-            wts = np.ones(len(rows))
-            w13 = weights.get("sh13", e - E)
-            w2 = weights.get("sh2", e - E)
+        wts = w[toks, np.minimum(slots, k - 1)] if e < E else np.ones(len(rows))
         a = Q.dequant(xc[toks], xs[toks], fmt, gx)
-        W13 = Q.dequant(w13[0], w13[1], fmt, w13[2])
-        gu = a @ W13.T
-        gu_abs = np.abs(a) @ np.abs(W13).T
-        del W13
-        g, u = gu[:, :I], gu[:, I:]
-        h = silu(g) * u
-        h32 = h.astype(np.float32).astype(np.float64)
-        if fmt == "mxfp4":
-            hq, hs = Q.mx_quantize(h32)
-            g_h = None
-        else:
-            hq, hs, g_h = Q.nv_quantize(h32)
-        hd = Q.dequant(hq, hs, fmt, g_h)
-        W2 = Q.dequant(w2[0], w2[1], fmt, w2[2])
-        W2a = np.abs(W2)
-        y = hd @ W2.T
-        Sy = np.abs(hd) @ W2a.T
-        info = {"rows": rows, "tok": toks, "slot": slots, "wt": wts, "h": h, "h32": h32,
-                "hq": hq, "hs": hs, "g_h": g_h}
-        if with_ambiguity:
-            dg = gamma * gu_abs[:, :I] + 2.0 ** -22 * np.abs(g)
-            du = gamma * gu_abs[:, I:] + 2.0 ** -22 * np.abs(u)
-            sg = silu(g)
-            dh = (SILU_LIP * dg * (np.abs(u) + du) + np.abs(sg) * du
-                  + EPS_SWIGLU * np.abs(h) + 2.0 ** -140)
-            if fmt == "mxfp4":
-                dmax, srange = _h_candidates_mx(h32, dh, hq, hs)
-            else:
-                dmax, srange = _h_candidates_nv(h32, dh, hq, hs, g_h)
-            Ay = dmax @ W2a.T
-            info.update({"dh": dh, "dmax": dmax, "scale_range": srange,
-                         "n_ambiguous": int(np.count_nonzero(dmax))})
-        else:
-            Ay = np.zeros_like(y)
-        del W2, W2a
+        info = expert_rows(cfg, e, a, wts, weights, gamma, with_ambiguity)
+        info.update({"rows": rows, "tok": toks, "slot": slots})
         for r in range(len(rows)):
             t = int(toks[r])
             if t in tok_pos:
                 i = tok_pos[t]
-                ref[i] += wts[r] * y[r]
-                S[i] += abs(wts[r]) * Sy[r]
-                A[i] += abs(wts[r]) * Ay[r]
+                ref[i] += wts[r] * info["y"][r]
+                S[i] += abs(wts[r]) * info["Sy"][r]
+                A[i] += abs(wts[r]) * info["Ay"][r]
         experts[e] = info
     margins = [decision_margins(logits[t], bias_f32, k, cfg.n_group, cfg.topk_group)
                for t in range(T)]
@@ -238,6 +247,38 @@ def layer_forward(cfg, x_bits_f64: np.ndarray, wr_f64: np.ndarray, bias_f32: np.
             "xc": xc, "xs": xs, "gx": gx, "counts": counts, "offsets": offsets,
             "perm_tok": ptok, "perm_slot": pslot, "experts": experts,
             "tokens": tokens, "ref": ref, "S": S, "A": A}
+
+
+def token_forward(cfg, x_rows_f64: np.ndarray, wr_f64: np.ndarray, bias_f32: np.ndarray,
+                  weights: WeightSource, gamma: float = GAMMA, with_ambiguity: bool = True):
+    """MXFP4 only: the layer output of individual tokens x_rows [n, H].  With
+    MXFP4 both quantisations (x and h) act row by row, so one token's output
+    depends on its own routes alone.  Returns per-token routing, the routes'
+    intermediates and ref / S / A [n, H]."""
+    assert cfg.fmt == "mxfp4", "NVFP4 tensor scales couple tokens; use layer_forward"
+    E, k, ns = cfg.E, cfg.top_k, cfg.n_shared
+    logits, lsum = router_logits(x_rows_f64, wr_f64)
+    idx, w = route(logits, bias_f32, k, cfg.n_group, cfg.topk_group, cfg.routed_scaling,
+                   cfg.renormalize)
+    xc, xs = Q.mx_quantize(x_rows_f64)
+    n, H = x_rows_f64.shape
+    ref, S, A = np.zeros((n, H)), np.zeros((n, H)), np.zeros((n, H))
+    routes = []
+    for i in range(n):
+        a = Q.mx_dequant(xc[i:i + 1], xs[i:i + 1])
+        per = []
+        for j, e in enumerate(list(idx[i]) + list(range(E, E + ns))):
+            wt = w[i, j] if j < k else 1.0
+            info = expert_rows(cfg, int(e), a, np.array([wt]), weights, gamma, with_ambiguity)
+            ref[i] += wt * info["y"][0]
+            S[i] += abs(wt) * info["Sy"][0]
+            A[i] += abs(wt) * info["Ay"][0]
+            info["expert"] = int(e)
+            per.append(info)
+        routes.append(per)
+    margins = [decision_margins(logits[i], bias_f32, k, cfg.n_group, cfg.topk_group) for i in range(n)]
+    return {"logits": logits, "lsum": lsum, "idx": idx, "w": w, "margins": margins, "xc": xc, "xs": xs,
+            "routes": routes, "ref": ref, "S": S, "A": A}
 
 
 def tolerance(ref: np.ndarray, S: np.ndarray, A: np.ndarray) -> np.ndarray:

@@ -58,17 +58,24 @@ def stream_key(seed: int, stream: int) -> int:
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
-    z = (z ^ (z >> np.uint64(30))) * np.uint64(MIX1)
-    z = (z ^ (z >> np.uint64(27))) * np.uint64(MIX2)
-    return z ^ (z >> np.uint64(31))
+    """SplitMix64 finaliser, in place."""
+    with np.errstate(over="ignore"):
+        z ^= z >> np.uint64(30)
+        z *= np.uint64(MIX1)
+        z ^= z >> np.uint64(27)
+        z *= np.uint64(MIX2)
+        z ^= z >> np.uint64(31)
+    return z
 
 
 def words(seed: int, stream: int, start: int, count: int) -> np.ndarray:
     """Words ``start .. start+count-1`` of one stream, as uint64."""
     key = np.uint64(stream_key(seed, stream))
     with np.errstate(over="ignore"):
-        idx = np.arange(start, start + count, dtype=np.uint64)
-        return _mix(key + idx * np.uint64(GOLDEN))
+        z = np.arange(start, start + count, dtype=np.uint64)
+        z *= np.uint64(GOLDEN)
+        z += key
+    return _mix(z)
 
 
 def uniform_bytes(seed: int, stream: int, start: int, count: int) -> np.ndarray:
@@ -97,18 +104,25 @@ def e8m0_scales(seed: int, stream: int, row0: int, rows: int, nblk: int,
 def normal(seed: int, stream: int, start: int, count: int, std: float) -> np.ndarray:
     """Approximately normal float64 values with the given standard deviation."""
     w = words(seed, stream, start, count)
-    s = np.zeros(count, dtype=np.int64)
-    for lane in range(4):
-        s += ((w >> np.uint64(16 * lane)) & np.uint64(0xFFFF)).astype(np.int64)
-    c = float(std) / IH4_SIGMA
-    return (s - IH4_MEAN).astype(np.float64) * c
+    s = w & np.uint64(0xFFFF)
+    for lane in range(1, 4):
+        w >>= np.uint64(16)
+        s += w & np.uint64(0xFFFF)
+    out = s.view(np.int64).astype(np.float64)
+    out -= IH4_MEAN
+    out *= float(std) / IH4_SIGMA
+    return out
 
 
 def to_bf16_bits(v: np.ndarray) -> np.ndarray:
     """float64 -> float32 (RNE) -> bfloat16 (RNE); returns uint16 bit patterns."""
     f = np.asarray(v, dtype=np.float64).astype(np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    u = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    u = f.view(np.uint32).copy()
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    with np.errstate(over="ignore"):
+        u += np.uint32(0x7FFF)
+        u += lsb
+    u >>= np.uint32(16)
     return u.astype(np.uint16)
 
 
@@ -277,3 +291,66 @@ def adversarial_conversion_rows(K: int = 256) -> tuple[np.ndarray, np.ndarray, l
     rows_s.append(np.asarray([127 - (b % 4) for b in range(nb)], dtype=np.uint8))
     names.append("mixed_codes")
     return np.stack(rows_c), np.stack(rows_s), names
+
+
+# --------------------------------------------------------------------------
+# Device-side draws (same definitions), through synth/libfp4moe_synth.so.
+
+_DEV = None
+
+
+def _device_lib():
+    global _DEV
+    if _DEV is None:
+        import ctypes
+        from pathlib import Path
+        so = Path(__file__).resolve().parent / "libfp4moe_synth.so"
+        if not so.exists():
+            build_device_lib()
+        lib = ctypes.CDLL(str(so))
+        u64, vp, i32, f64 = ctypes.c_uint64, ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+        lib.synth_words.argtypes = [u64, u64, u64, vp, vp]
+        lib.synth_e8m0.argtypes = [u64, u64, u64, u64, i32, i32, i32, vp, vp]
+        lib.synth_normal_bf16.argtypes = [u64, u64, u64, f64, vp, vp]
+        for f in (lib.synth_words, lib.synth_e8m0, lib.synth_normal_bf16):
+            f.restype = i32
+        _DEV = lib
+    return _DEV
+
+
+def build_device_lib(force: bool = False):
+    """Compiles synth_gen.cu into synth/libfp4moe_synth.so (sm_103a)."""
+    import subprocess
+    from pathlib import Path
+    here = Path(__file__).resolve().parent
+    src, out = here / "synth_gen.cu", here / "libfp4moe_synth.so"
+    if out.exists() and not force and out.stat().st_mtime >= src.stat().st_mtime:
+        return out
+    cmd = ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-Xcompiler", "-fPIC", "-shared",
+           str(src), "-o", str(out)]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def _check(rc):
+    if rc != 0:
+        raise RuntimeError(f"synth device kernel failed: cuda error {rc}")
+
+
+def dev_uniform_bytes(seed, stream, start_byte, out_tensor, cuda_stream=0):
+    """Fills a uint8 CUDA tensor (size multiple of 8, start_byte % 8 == 0) with
+    bytes start_byte.. of the stream."""
+    n = out_tensor.numel()
+    assert n % 8 == 0 and start_byte % 8 == 0
+    _check(_device_lib().synth_words(stream_key(seed, stream), start_byte // 8, n // 8,
+                                     out_tensor.data_ptr(), cuda_stream))
+
+
+def dev_e8m0_scales(seed, stream, row0, rows, nblk, out_tensor, lo=-10, hi=-6, cuda_stream=0):
+    _check(_device_lib().synth_e8m0(stream_key(seed, stream), stream_key(seed, stream + 1), row0, rows, nblk,
+                                    lo, hi, out_tensor.data_ptr(), cuda_stream))
+
+
+def dev_normal_bf16(seed, stream, start, out_tensor, std, cuda_stream=0):
+    _check(_device_lib().synth_normal_bf16(stream_key(seed, stream), start, out_tensor.numel(),
+                                           float(std) / IH4_SIGMA, out_tensor.data_ptr(), cuda_stream))

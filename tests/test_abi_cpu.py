@@ -1,0 +1,80 @@
+"""The C-ABI library builds, loads and exports every function the header
+declares; host-side entry points (workspace sizing, layout) answer without a
+GPU.  No compute entry point is called here."""
+import ctypes
+
+import pytest
+
+import block_scaled_fp4_sigmoid_gb300 as fm
+from block_scaled_fp4_sigmoid_gb300 import build
+import synth
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_library()
+    return fm.lib()
+
+
+def test_exports_every_header_function(lib):
+    names = fm.header_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version(lib):
+    assert fm.version() >= 100
+
+
+@pytest.mark.parametrize("name", list(synth.configs()))
+def test_workspace_sizes(lib, name):
+    cfg = synth.configs()[name]
+    fmt = fm.NVFP4 if cfg.fmt == "nvfp4" else fm.MXFP4
+    d = fm.make_dims(cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k, cfg.n_group, cfg.topk_group, cfg.n_shared,
+                     cfg.routed_scaling, 1, fmt)
+    n = fm.workspace_size(d)
+    L = fm.workspace_layout(d)
+    assert n == L.total_bytes > 0
+    offs = [L.status, L.logits, L.topk_idx, L.topk_w, L.expert_count, L.expert_slot, L.route_row, L.row_tok,
+            L.row_w, L.xq, L.xsf, L.hq, L.hsf, L.gscale, L.out_acc]
+    assert all(o % 256 == 0 for o in offs)
+    assert offs == sorted(offs) and offs[-1] + cfg.T * cfg.H * 4 <= n
+    R = cfg.T * (cfg.top_k + cfg.n_shared)
+    assert L.rows_cap >= 128 * (R // L.n_tile + 1)
+    assert cfg.H // 256 % L.n_splits == 0
+
+
+@pytest.mark.parametrize("bad", [dict(T=0), dict(H=200), dict(I=100), dict(E=0), dict(top_k=0), dict(n_shared=2),
+                                 dict(n_group=3), dict(fmt=5), dict(top_k=9, E=8)])
+def test_invalid_dims_rejected(lib, bad):
+    kw = dict(T=4, H=256, I=128, E=8, top_k=2)
+    kw.update(bad)
+    fmt = kw.pop("fmt", fm.MXFP4)
+    d = fm.make_dims(**kw, fmt=fmt)
+    assert lib.fp4moe_workspace_size(ctypes.byref(d)) == 0
+    with pytest.raises(fm.Fp4MoeError):
+        fm.workspace_layout(d)
+
+
+def test_packed_scale_sizes(lib):
+    assert fm.packed_scales_bytes(384, 4096, 224, fm.MXFP4) == 384 * 32 * 56 * 512
+    assert fm.packed_scales_bytes(1, 128, 4, fm.MXFP4) == 2 * 512   # padded to a whole K tile
+    assert fm.packed_scales_bytes(1, 128, 8, fm.NVFP4) == 4 * 512
+    assert fm.packed_scales_bytes(1, 100, 8, fm.MXFP4) == 0
+
+
+def test_argument_errors_need_no_gpu(lib):
+    d = fm.make_dims(4, 256, 128, 8, 2)
+    # null pointers are refused before any device work
+    assert lib.fp4moe_forward(ctypes.byref(d), None, None, None, None, None, 0, None) == 1
+    assert lib.fp4moe_quantize_act(None, 0, 4, 64, 0, None, None, None, None, None, 0, None) == 1
+    assert lib.fp4moe_mxfp4_to_fp8_rowscale(None, None, 1, 32, None, None, None, None, 0, None) == 1
+    assert lib.fp4moe_status_string(5) == b"device wait timed out"
+
+
+def test_synth_device_library_builds():
+    so = synth.build_device_lib()
+    lib = ctypes.CDLL(str(so))
+    for n in ("synth_words", "synth_e8m0", "synth_normal_bf16"):
+        assert hasattr(lib, n)

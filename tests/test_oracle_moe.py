@@ -133,3 +133,15 @@ def test_shared_expert_gets_every_token_with_weight_one():
     W2 = Q.mx_dequant(*ws.get("sh2", 0)[:2])
     y = Q.mx_dequant(sh["hq"], sh["hs"]) @ W2.T
     np.testing.assert_allclose(out["ref"], base + y, rtol=1e-13, atol=1e-16)
+
+
+def test_token_forward_matches_layer_forward():
+    cfg = replace(synth.configs()["tiny"], n_shared=1)
+    x, wr, b = OI.layer_inputs(cfg)
+    ws = OI.oracle_weights(cfg)
+    full = M.layer_forward(cfg, x, wr, b, ws)
+    for t in range(cfg.T):
+        one = M.token_forward(cfg, x[t:t + 1], wr, b, ws)
+        assert np.array_equal(one["idx"][0], full["idx"][t])
+        np.testing.assert_allclose(one["ref"][0], full["ref"][t], rtol=1e-13, atol=1e-16)
+        np.testing.assert_allclose(one["S"][0], full["S"][t], rtol=1e-13, atol=1e-16)
