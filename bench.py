@@ -1,0 +1,409 @@
+"""Benchmark of the routed block-scaled FP4 MoE layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+One step is one fp4moe_forward over one batch: routing, permutation,
+activation quantisation, gate/up GEMM + SwiGLU + requantisation, down GEMM +
+combine.  The default workload is the Kimi-shaped decode layer (T=8, H=7168,
+I=2048, E=384, top-8, MXFP4 A4W4).  Weights (~9 GB) are drawn on the device
+from the seeded generator; inputs are resident in HBM when timing starts.
+Between timed steps a 256 MiB buffer is written to flush L2 (untimed).  Each
+step is timed with CUDA events on the launching stream; the dominant kernel
+(gate/up GEMM) is timed by events recorded around its launch.
+
+With torchrun (N > 1) each rank runs an independent replica on its own batch
+(no collective on the data path); the line reports the max over ranks.
+
+--impl reference times the FP64 CPU oracle (the only other implementation of
+this layer) on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "MoE-layer tokens/s; FP4 TFLOP/s (prefill), weight-stream HBM GB/s (decode)"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def measured_peaks() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def source_sha(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        h.update((ROOT / p).read_bytes())
+    return h.hexdigest()[:16]
+
+
+GEMM_SOURCES = ["block_scaled_fp4_sigmoid_gb300/csrc/gemm.cuh", "block_scaled_fp4_sigmoid_gb300/csrc/common.cuh",
+                "block_scaled_fp4_sigmoid_gb300/csrc/gemm_launch.cuh"]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the gate/up kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    f = ROOT / "profiles" / f"ncu_gateup_{workload}.md"
+    if not f.exists():
+        return None
+    text = f.read_text()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != source_sha(GEMM_SOURCES):
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self) -> dict:
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def oracle_route_sample(cfg_name: str, n_routes: int, frac: float = 1.0, start_token: int = 0):
+    """Times the FP64 oracle on n_routes (token, expert) routes of the
+    workload: each token's routing and x quantisation, then its expert MLPs.
+    frac < 1 evaluates each MLP on the first frac * I intermediate channels
+    only (a sub-problem of the same form: whole 32-blocks of h).  Weight
+    generation is input preparation and stays outside the timing.
+    Returns (seconds, tokens processed)."""
+    from dataclasses import replace
+    import numpy as np
+    import synth
+    from oracle import inputs as OI
+    from oracle import moe as M
+    from oracle import quant as Q
+    from oracle.router import route, router_logits
+    cfg = synth.configs()[cfg_name]
+    Ip = cfg.I if frac >= 1 else max(32, int(cfg.I * frac) // 32 * 32)
+    sub = replace(cfg, I=Ip)
+    ws = OI.oracle_weights(cfg)
+    wr = synth.bf16_bits_to_f64(synth.gen_router_bf16(cfg))
+    bias = synth.gen_bias_f32(cfg)
+    done, t_total, t = 0, 0.0, start_token
+    while done < n_routes:
+        x = synth.bf16_bits_to_f64(synth.gen_x_bf16(cfg, t % cfg.T, t % cfg.T + 1))
+        t0 = time.perf_counter()
+        logits, _ = router_logits(x, wr)
+        idx, w = route(logits, bias, cfg.top_k, cfg.n_group, cfg.topk_group, cfg.routed_scaling, cfg.renormalize)
+        xc, xs, gx = Q.quantize(x, cfg.fmt)
+        a = Q.dequant(xc, xs, cfg.fmt, gx)
+        t_total += time.perf_counter() - t0
+        experts = [int(e) for e in idx[0]] + list(range(cfg.E, cfg.E + cfg.n_shared))
+        for j, e in enumerate(experts):
+            if done >= n_routes:
+                break
+            wt = w[0, j] if j < cfg.top_k else 1.0
+            names = ("w13", "w2") if e < cfg.E else ("sh13", "sh2")
+            ee = e if e < cfg.E else e - cfg.E
+            w13 = ws.get(names[0], ee)
+            w2 = ws.get(names[1], ee)
+            blk = 16 if cfg.fmt == "nvfp4" else 32
+            keep = np.r_[0:Ip, cfg.I:cfg.I + Ip]
+            s13 = (w13[0][keep], w13[1][keep], w13[2])
+            s2 = (np.ascontiguousarray(w2[0][:, :Ip]), np.ascontiguousarray(w2[1][:, :Ip // blk]), w2[2])
+            sub_ws = M.WeightSource(lambda which, _e, _a=s13, _b=s2: _a if which in ("w13", "sh13") else _b)
+            t0 = time.perf_counter()
+            M.expert_rows(sub, e, a, np.array([wt]), sub_ws, with_ambiguity=False)
+            t_total += time.perf_counter() - t0
+            ws.drop(names[0], ee)
+            ws.drop(names[1], ee)
+            done += 1
+        t += 1
+    rpt = cfg.top_k + cfg.n_shared
+    return t_total, n_routes / rpt * (Ip / cfg.I)
+
+
+def reference_arm(args, cfg, rank, world):
+    if rank != 0:
+        return
+    # size each step so that warm-up + steps take about two minutes
+    t_one, _ = oracle_route_sample(args.config, 1)
+    budget = 120.0 / (args.steps + args.warmup)
+    frac = min(1.0, budget / max(t_one, 1e-3))
+    secs, toks = [], 0.0
+    for i in range(args.warmup + args.steps):
+        sec, n = oracle_route_sample(args.config, 1, frac, start_token=i)
+        if i >= args.warmup:
+            secs.append(sec)
+            toks += n
+    total = sum(secs)
+    value = toks / total
+    cores = cpu_cores()
+    Ip = cfg.I if frac >= 1 else max(32, int(cfg.I * frac) // 32 * 32)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(secs),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": cfg_label(cfg),
+                                            "step": f"one (token, expert) route on {Ip} of {cfg.I} channels"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} routes of the {cfg.name} workload, {Ip}/{cfg.I} "
+                                       f"intermediate channels each"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cfg_label(cfg) -> str:
+    return (f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.top_k}"
+            f"{f' groups {cfg.n_group}/{cfg.topk_group}' if cfg.n_group > 1 else ''}"
+            f"{' +1 shared' if cfg.n_shared else ''} {cfg.fmt.upper()} A4W4")
+
+
+# ------------------------------------------------------------------ GPU arm
+def gpu_arm(args, cfg, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import block_scaled_fp4_sigmoid_gb300 as fm
+    from block_scaled_fp4_sigmoid_gb300.layer import MoELayer
+    import __graft_entry__
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+    layer = MoELayer.synthetic(cfg, device=dev)
+    # each rank runs its own batch: tokens rank*T .. (rank+1)*T of the stream
+    x = layer.synthetic_x(rank * cfg.T, (rank + 1) * cfg.T)
+    out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+
+    def make_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)
+        return evs
+
+    def dbg_for(evs):
+        d = fm.Debug()
+        for i, e in enumerate(evs):
+            d.events[i] = e.cuda_event
+        return d
+
+    # warm-up (also compiles nothing: the library is prebuilt)
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        layer.forward(x, out)
+    torch.cuda.synchronize()
+    st, n_st = fm.get_status(layer.ws.data_ptr(), s)
+    if st != 0:
+        raise RuntimeError(f"device status {fm.STATUS.get(st, st)}")
+
+    steps = args.steps
+    ev = [make_events(8) for _ in range(steps)]
+    dbgs = [dbg_for(e) for e in ev]
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        time.sleep(0.3)
+        wall0 = time.perf_counter()
+        for i in range(steps):
+            flush.fill_(float(i))
+            layer.forward(x, out, debug=dbgs[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ms = [e[0].elapsed_time(e[7]) for e in ev]
+    stage_ms = {fm.STAGES[j]: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j in range(7)}
+    gu_ms = [e[4].elapsed_time(e[5]) for e in ev]
+    dn_ms = [e[5].elapsed_time(e[6]) for e in ev]
+    ms = statistics.mean(step_ms)
+
+    # end to end through the public API with host buffers
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+    e2e_steps = max(10, min(steps, 200))
+    for _ in range(3):
+        x_dev.copy_(x_host, non_blocking=True)
+        layer.forward(x_dev, out)
+        out_host.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_ev = [make_events(2) for _ in range(e2e_steps)]
+    torch.cuda.synchronize()
+    for i in range(e2e_steps):
+        flush.fill_(float(i))
+        e2e_ev[i][0].record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        layer.forward(x_dev, out)
+        out_host.copy_(out, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
+
+    # work actually done: touched experts and routes
+    ne = cfg.E + cfg.n_shared
+    count = layer.ws_view("expert_count", torch.int32, ne).cpu().numpy()
+    touched = int(np.count_nonzero(count))
+    routes = int(count.sum())
+    wpe = layer.weight_bytes_per_expert()
+    d = layer.dims
+    blk = 16 if cfg.fmt == "nvfp4" else 32
+    act = 0.5 + 1.0 / blk                              # bytes per FP4 value incl. scale
+    gu_bytes = touched * (2 * d.I * d.H * act) + routes * d.H * act + routes * d.I * act
+    dn_bytes = touched * (d.H * d.I * act) + routes * d.I * act + routes * d.H * 4
+    flops = 2.0 * 3 * d.I * d.H * routes
+
+    # max over ranks
+    vals = torch.tensor([ms, e2e_ms, statistics.mean(gu_ms)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    ms_max, e2e_max, gu_max = vals.tolist()
+    if rank != 0:
+        return
+    peaks = measured_peaks()
+    achieved = gu_bytes / (gu_max * 1e-3) / 1e9
+    traffic = profiled_traffic(cfg.name)
+    clocks = clk.summary()
+    launches_per_step = 8 + (2 if cfg.fmt == "nvfp4" else 0)
+    # CPU baseline: the oracle on a bounded sample of this workload
+    n_routes = 16 if args.cpu_routes is None else args.cpu_routes
+    cpu_s, cpu_tok = oracle_route_sample(args.config, n_routes) if n_routes > 0 else (float("nan"), 0.0)
+    line = {
+        "metric": METRIC,
+        "value": cfg.T * world / (ms_max * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "mxfp4" if cfg.fmt == "mxfp4" else "nvfp4",
+        "data": "synthetic (seeded; weights drawn on the device)",
+        "config": {"workload": cfg_label(cfg), "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "l2": "flushed between steps (256 MiB write, untimed)", "touched_experts": touched,
+                   "routes": routes},
+        "clocks": clocks,
+        "e2e": {"value": cfg.T * world / (e2e_max * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(x.numel() * 2), "d2h_bytes_per_step": int(out.numel() * 2)},
+        "gpu_launches": launches_per_step * steps,
+        "roofline": {"bound": "hbm", "kernel": "gate/up grouped GEMM", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": traffic, "algorithmic_bytes": gu_bytes, "peak_source": peaks["source"]},
+        "step": {"weight_stream_gbs": (touched * wpe) / (ms_max * 1e-3) / 1e9,
+                 "weight_stream_frac": (touched * wpe) / (ms_max * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                 "tflops": flops / (ms_max * 1e-3) / 1e12, "stages_ms": stage_ms,
+                 "down_gemm_gbs": dn_bytes / (statistics.mean(dn_ms) * 1e-3) / 1e9,
+                 "wall_s": wall},
+        "cpu_baseline": {"value": cpu_tok / cpu_s, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{n_routes} routes ({cpu_tok:g} tokens) of the same workload, FP64 numpy"},
+        "context": "pages: 1.43 ms per MoE layer call at T=8 on one Gaudi 2 card holding 48 of 384 experts",
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="kimi_decode")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-routes", type=int, default=None)
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override E (smaller device footprint for profiler captures)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    import synth
+    from dataclasses import replace
+    cfg = synth.configs()[args.config]
+    if args.experts:
+        cfg = replace(cfg, E=args.experts, name=f"{cfg.name}_e{args.experts}")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, cfg, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        gpu_arm(args, cfg, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

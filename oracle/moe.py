@@ -164,7 +164,7 @@ def expert_rows(cfg, e: int, a: np.ndarray, wts: np.ndarray, weights: WeightSour
         w13, w2 = weights.get("sh13", e - E), weights.get("sh2", e - E)
     W13 = Q.dequant(w13[0], w13[1], fmt, w13[2])
     gu = a @ W13.T
-    gu_abs = np.abs(a) @ np.abs(W13).T
+    gu_abs = np.abs(a) @ np.abs(W13).T if with_ambiguity else None
     del W13
     g, u = gu[:, :I], gu[:, I:]
     h = silu(g) * u
@@ -176,9 +176,9 @@ def expert_rows(cfg, e: int, a: np.ndarray, wts: np.ndarray, weights: WeightSour
         hq, hs, g_h = Q.nv_quantize(h32)
     hd = Q.dequant(hq, hs, fmt, g_h)
     W2 = Q.dequant(w2[0], w2[1], fmt, w2[2])
-    W2a = np.abs(W2)
     y = hd @ W2.T
-    Sy = np.abs(hd) @ W2a.T
+    W2a = np.abs(W2) if with_ambiguity else None
+    Sy = np.abs(hd) @ W2a.T if with_ambiguity else None
     info = {"wt": wts, "h": h, "h32": h32, "hq": hq, "hs": hs, "g_h": g_h, "y": y, "Sy": Sy,
             "gu_abs": gu_abs}
     if with_ambiguity:
