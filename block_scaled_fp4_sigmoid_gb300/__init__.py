@@ -167,3 +167,13 @@ def get_status(ws: int, stream: int = 0) -> tuple[int, int]:
     st, n = ctypes.c_int32(0), ctypes.c_int64(0)
     _ok(lib().fp4moe_get_status(ws, stream, ctypes.byref(st), ctypes.byref(n)), "fp4moe_get_status")
     return st.value, n.value
+
+
+def route_noalloc(dims: Dims, x: int, w_router: int, bias: int, topk_idx: int, topk_w: int,
+                  logits_out: int | None, stream: int = 0) -> None:
+    """fp4moe_route without a workspace: the library's fixed scratch array is used."""
+    L = lib()
+    f = L.fp4moe_route_noalloc
+    f.argtypes = [ctypes.POINTER(Dims)] + [ctypes.c_void_p] * 7
+    f.restype = ctypes.c_int32
+    _ok(f(ctypes.byref(dims), x, w_router, bias, topk_idx, topk_w, logits_out, stream), "fp4moe_route_noalloc")

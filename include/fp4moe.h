@@ -173,6 +173,30 @@ fp4moe_status fp4moe_route(const fp4moe_dims *dims, const uint16_t *x, const uin
                            const float *bias, int32_t *topk_idx, float *topk_w, float *logits_out,
                            void *ws, size_t ws_bytes, void *stream);
 
+/* Size of the fixed device scratch array used by fp4moe_route_noalloc. */
+#define FP4MOE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/* Router for callers that cannot allocate device memory (no counterpart on the
+ * pages: it is fp4moe_route with its scratch moved into the library).
+ * Engines that plan all device memory ahead and forbid later allocations, or
+ * code that must not call cudaMalloc because it may synchronise the device,
+ * cannot hand fp4moe_route a workspace.  This entry point keeps the scratch
+ * (split-K partial logits, per-chunk expert counts) in one file-scope device
+ * array of FP4MOE_NOALLOC_SCRATCH_BYTES that every GPU loading the library
+ * holds until process exit, and allocates nothing itself.
+ *   Arguments and outputs as fp4moe_route, without the workspace.
+ *   Returns FP4MOE_ERR_WORKSPACE when the dims need more scratch than the
+ *   array holds (n_splits*T*E*4 bytes of partials, 256-byte aligned, plus
+ *   ceil(T/256)*(E+n_shared)*4 bytes of counts).
+ *   The first call on a device looks up the array's device address with that
+ *   device current; make that first call before any stream capture.
+ *   All calls share the array: calls that overlap on the GPU race, so
+ *   serialise them (one stream, or host-side ordering).  Each call clears the
+ *   counts it accumulates; the array otherwise keeps the last call's data. */
+fp4moe_status fp4moe_route_noalloc(const fp4moe_dims *dims, const uint16_t *x, const uint16_t *w_router,
+                                   const float *bias, int32_t *topk_idx, float *topk_w, float *logits_out,
+                                   void *stream);
+
 /* Activation quantisation ("Serve Kimi-K2.5-MXFP4 on MI355X with ATOM",
  * section "Stage B: Dynamic Activation Quantization"; "Serving NVFP4 models on
  * AMD Instinct MI355 accelerators", section "Weight Dequantization and
