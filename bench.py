@@ -260,8 +260,28 @@ def gpu_arm(args, cfg, rank, world, local_rank):
         raise RuntimeError(f"device status {fm.STATUS.get(st, st)}")
 
     steps = args.steps
-    ev = [make_events(8) for _ in range(steps)]
-    dbgs = [dbg_for(e) for e in ev]
+    # eager calls (host launch overhead included), for context
+    eager_n = min(steps, 100)
+    eager_ev = [make_events(2) for _ in range(eager_n)]
+    torch.cuda.synchronize()
+    for i in range(eager_n):
+        flush.fill_(float(i))
+        eager_ev[i][0].record(stream)
+        layer.forward(x, out)
+        eager_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    eager_ms = statistics.mean(a.elapsed_time(b) for a, b in eager_ev)
+
+    # the timed step: one forward captured once into a CUDA graph and replayed
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        layer.forward(x, out)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    ev = [make_events(2) for _ in range(steps)]
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -271,18 +291,31 @@ def gpu_arm(args, cfg, rank, world, local_rank):
         wall0 = time.perf_counter()
         for i in range(steps):
             flush.fill_(float(i))
-            layer.forward(x, out, debug=dbgs[i])
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
         time.sleep(0.3)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    step_ms = [e[0].elapsed_time(e[7]) for e in ev]
-    stage_ms = {fm.STAGES[j]: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j in range(7)}
-    gu_ms = [e[4].elapsed_time(e[5]) for e in ev]
-    dn_ms = [e[5].elapsed_time(e[6]) for e in ev]
+    step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = statistics.mean(step_ms)
+    # per-stage times: eager forwards with events between the stages, one at a
+    # time (the host enqueues a whole forward before the GPU finishes it)
+    gev = make_events(8)
+    gdbg = dbg_for(gev)
+    stage_runs, gu_ms, dn_ms = [], [], []
+    for i in range(min(steps, 50)):
+        flush.fill_(float(i))
+        torch.cuda.synchronize()
+        layer.forward(x, out, debug=gdbg)
+        torch.cuda.synchronize()
+        stage_runs.append([gev[j].elapsed_time(gev[j + 1]) for j in range(7)])
+        gu_ms.append(gev[4].elapsed_time(gev[5]))
+        dn_ms.append(gev[5].elapsed_time(gev[6]))
+    stage_ms = {fm.STAGES[j]: statistics.mean(r[j] for r in stage_runs) for j in range(7)}
 
     # end to end through the public API with host buffers
     x_host = x.cpu().pin_memory()
@@ -330,7 +363,8 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     achieved = gu_bytes / (gu_max * 1e-3) / 1e9
     traffic = profiled_traffic(cfg.name)
     clocks = clk.summary()
-    launches_per_step = 8 + (2 if cfg.fmt == "nvfp4" else 0)
+    fused_front = cfg.fmt == "mxfp4" and cfg.T <= 16
+    launches_per_step = 4 if fused_front else 8 + (2 if cfg.fmt == "nvfp4" else 0)
     # CPU baseline: the oracle on a bounded sample of this workload
     n_routes = 16 if args.cpu_routes is None else args.cpu_routes
     cpu_s, cpu_tok = oracle_route_sample(args.config, n_routes) if n_routes > 0 else (float("nan"), 0.0)
@@ -348,6 +382,7 @@ def gpu_arm(args, cfg, rank, world, local_rank):
         "dtype": "mxfp4" if cfg.fmt == "mxfp4" else "nvfp4",
         "data": "synthetic (seeded; weights drawn on the device)",
         "config": {"workload": cfg_label(cfg), "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "launch": "one fp4moe_forward captured in a CUDA graph, replayed per step",
                    "l2": "flushed between steps (256 MiB write, untimed)", "touched_experts": touched,
                    "routes": routes},
         "clocks": clocks,
@@ -361,7 +396,7 @@ def gpu_arm(args, cfg, rank, world, local_rank):
                  "weight_stream_frac": (touched * wpe) / (ms_max * 1e-3) / 1e9 / peaks["hbm_gbs"],
                  "tflops": flops / (ms_max * 1e-3) / 1e12, "stages_ms": stage_ms,
                  "down_gemm_gbs": dn_bytes / (statistics.mean(dn_ms) * 1e-3) / 1e9,
-                 "wall_s": wall},
+                 "wall_s": wall, "eager_ms_per_step": eager_ms},
         "cpu_baseline": {"value": cpu_tok / cpu_s, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                          "sample": f"{n_routes} routes ({cpu_tok:g} tokens) of the same workload, FP64 numpy"},
         "context": "pages: 1.43 ms per MoE layer call at T=8 on one Gaudi 2 card holding 48 of 384 experts",
@@ -379,6 +414,7 @@ def main():
     ap.add_argument("--cpu-routes", type=int, default=None)
     ap.add_argument("--experts", type=int, default=None,
                     help="override E (smaller device footprint for profiler captures)")
+    ap.add_argument("--tokens", type=int, default=None, help="override T")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     import synth
@@ -386,6 +422,8 @@ def main():
     cfg = synth.configs()[args.config]
     if args.experts:
         cfg = replace(cfg, E=args.experts, name=f"{cfg.name}_e{args.experts}")
+    if args.tokens:
+        cfg = replace(cfg, T=args.tokens, name=f"{cfg.name}_t{args.tokens}")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

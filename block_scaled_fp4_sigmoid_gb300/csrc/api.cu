@@ -46,9 +46,10 @@ bool dims_ok(const fp4moe_dims& d) {
 
 int pick_n_tile(const fp4moe_dims& d) {
   const double avg = (double)d.T * d.top_k / d.E;
+  // 32 and 64 keep two accumulator sets in tensor memory (epilogue overlaps
+  // the next unit's MMAs); 128 fits only one for the gate/up pair
   if (avg <= 24.0) return 32;
-  if (avg <= 48.0) return 64;
-  return 128;
+  return 64;
 }
 
 // Router split-K factor: a divisor of H / 256 that gives the logits kernel
@@ -57,8 +58,8 @@ int pick_splits(const fp4moe_dims& d) {
   const int kt = d.H / 256;
   int64_t units, want;
   if (d.T <= 16) {
-    units = d.E;             // warps
-    want = 8 * 152;
+    units = d.E;             // warps; each should issue all its weight loads in one batch
+    want = 16 * 152;
   } else {
     units = (int64_t)((d.T + 127) / 128) * ((d.E + 63) / 64);  // CTAs
     want = 2 * 152;
@@ -112,6 +113,7 @@ bool make_layout(const fp4moe_dims& d, Layout* L) {
   w.gscale = take((int64_t)(2 + L->n_exp) * 4);
   L->amax = take((int64_t)(2 + L->n_exp) * 4);
   w.out_acc = take((int64_t)d.T * d.H * 4);
+  L->front = !nv && d.T <= kFrontMaxT;
   w.total_bytes = off;
   return true;
 }
@@ -265,22 +267,53 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
   };
 
   cudaError_t e = rec(0);
-  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, kStatusInts * 4, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(cc, 0, (size_t)L.n_chunks * L.n_exp * 4, s);
-  if (e == cudaSuccess && nv) e = cudaMemsetAsync(amax, 0, (size_t)(2 + L.n_exp) * 4, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(acc, 0, (size_t)d.T * d.H * 4, s);
-  if (e == cudaSuccess) e = launch_router_logits(x, w->w_router, partial, d.T, d.H, d.E, L.ws.n_splits, s);
-  if (e == cudaSuccess) e = rec(1);
-  if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, nullptr, cc, L.n_exp, s);
-  if (e == cudaSuccess) e = rec(2);
-  if (e == cudaSuccess)
-    e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, ecount, eslot, gu_start, dn_start, plan, s);
-  if (e == cudaSuccess)
-    e = launch_scatter(d, idx, tw, cc, L.n_chunks, L.n_exp, n_tile, eslot, route_row, row_tok, row_w, row_e, s);
-  if (e == cudaSuccess) e = rec(3);
-  if (e == cudaSuccess && nv) e = launch_amax(x, 0, (int64_t)d.T * d.H, amax, s);
-  if (e == cudaSuccess) e = launch_gather_quant(d, x, route_row, xq, xsf, amax, gscale, s);
-  if (e == cudaSuccess) e = rec(4);
+  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, kStatusInts * 4, s);  // also clears the tickets
+  if (L.front) {
+    // few tokens: router, top-k, plan, scatter and x quantisation in one launch
+    FrontArgs f;
+    memset(&f, 0, sizeof(f));
+    f.d = d;
+    f.x = x;
+    f.wr = w->w_router;
+    f.bias = w->bias;
+    f.partial = partial;
+    f.n_splits = L.ws.n_splits;
+    f.n_tile = n_tile;
+    f.n_exp = L.n_exp;
+    f.out_acc = acc;
+    f.idx = idx;
+    f.w = tw;
+    f.expert_count = ecount;
+    f.expert_slot = eslot;
+    f.gu_start = gu_start;
+    f.dn_start = dn_start;
+    f.plan = plan;
+    f.route_row = route_row;
+    f.row_tok = row_tok;
+    f.row_e = row_e;
+    f.row_w = row_w;
+    f.ticket = status + ST_TICKET_FRONT;
+    if (e == cudaSuccess) e = launch_decode_front(f, s);
+    for (int i = 1; i <= 3 && e == cudaSuccess; ++i) e = rec(i);
+    if (e == cudaSuccess) e = launch_gather_quant(d, x, route_row, xq, xsf, amax, gscale, s);
+    if (e == cudaSuccess) e = rec(4);
+  } else {
+    if (e == cudaSuccess) e = cudaMemsetAsync(cc, 0, (size_t)L.n_chunks * L.n_exp * 4, s);
+    if (e == cudaSuccess && nv) e = cudaMemsetAsync(amax, 0, (size_t)(2 + L.n_exp) * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(acc, 0, (size_t)d.T * d.H * 4, s);
+    if (e == cudaSuccess) e = launch_router_logits(x, w->w_router, partial, d.T, d.H, d.E, L.ws.n_splits, s);
+    if (e == cudaSuccess) e = rec(1);
+    if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, nullptr, cc, L.n_exp, s);
+    if (e == cudaSuccess) e = rec(2);
+    if (e == cudaSuccess)
+      e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, ecount, eslot, gu_start, dn_start, plan, s);
+    if (e == cudaSuccess)
+      e = launch_scatter(d, idx, tw, cc, L.n_chunks, L.n_exp, n_tile, eslot, route_row, row_tok, row_w, row_e, s);
+    if (e == cudaSuccess) e = rec(3);
+    if (e == cudaSuccess && nv) e = launch_amax(x, 0, (int64_t)d.T * d.H, amax, s);
+    if (e == cudaSuccess) e = launch_gather_quant(d, x, route_row, xq, xsf, amax, gscale, s);
+    if (e == cudaSuccess) e = rec(4);
+  }
 
   GemmArgs a;
   memset(&a, 0, sizeof(a));

@@ -12,8 +12,10 @@ namespace fp4moe {
 // ---------------------------------------------------------------- status word
 // int32[16] at the start of every workspace: [0] first status code recorded,
 // [1] number of records, [2] NaN-scale rows, [3] below-floor rows,
-// [4] timeouts, [5] where the last timeout happened.
-enum { ST_FIRST = 0, ST_COUNT = 1, ST_NAN = 2, ST_INEXACT = 3, ST_TIMEOUT = 4, ST_WHERE = 5 };
+// [4] timeouts, [5] where the last timeout happened, [8..9] tickets of the
+// kernels whose last CTA finishes a step.
+enum { ST_FIRST = 0, ST_COUNT = 1, ST_NAN = 2, ST_INEXACT = 3, ST_TIMEOUT = 4, ST_WHERE = 5,
+       ST_TICKET_FRONT = 8, ST_TICKET_DOWN = 9 };  // [8], [9]: last-CTA tickets, cleared per call
 constexpr int kStatusInts = 16;
 
 __device__ __forceinline__ void record_status(int32_t* st, int code, int which, int n = 1) {
@@ -31,6 +33,13 @@ __device__ __forceinline__ uint64_t globaltimer() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start before
+// its predecessor finishes; it must call pdl_wait() before touching anything
+// the predecessor writes.  pdl_trigger() lets the successor launch early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ---------------------------------------------------------------- shared memory / mbarrier
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

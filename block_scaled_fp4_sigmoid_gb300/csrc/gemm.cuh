@@ -68,37 +68,50 @@ struct GemmCfg {
   static constexpr int kOffSFA1 = kOffSFA0 + kSFBytes;
   static constexpr int kOffSFB = kOffSFA0 + kA * kSFBytes;
   static constexpr int kStage = kOffSFB + kSFBytes;
-  static constexpr int kBudget = 229376;
+  // 227 KB per CTA = pipeline stages + 1 KB alignment slack + static shared
+  // memory (epilogue transpose tiles 16.5 KB, plan cache 6 KB, barriers)
+  static constexpr int kBudget = 232448 - 1024 - 24576;
   static constexpr int kStages = (kBudget / kStage) > 8 ? 8 : (kBudget / kStage);
   static constexpr int kSmem = kStages * kStage + 1024;
-  static constexpr int kAccCols = kA * N;
-  static constexpr int kSfaCol = kAccCols;
-  static constexpr int kSfbCol = kAccCols + kA * kAtoms * 4;
+  static constexpr int kAccCols = kA * N;                           // one accumulator set
+  static constexpr int kSfCols = (kA + 1) * kAtoms * 4;             // scale factors of one K tile
+  // two accumulator sets when they fit: the epilogue of one unit then
+  // overlaps the MMAs of the next
+  static constexpr int kAccStages = (2 * kAccCols + kSfCols <= 512) ? 2 : 1;
+  static constexpr int kSfaCol = kAccStages * kAccCols;
+  static constexpr int kSfbCol = kSfaCol + kA * kAtoms * 4;
   static constexpr int kCols = kSfbCol + kAtoms * 4;
   static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
   static_assert(kCols <= 512, "tensor memory");
   static_assert(kStage % 1024 == 0, "stage alignment");
   static_assert(kStages >= 2, "pipeline depth");
+  static_assert(kStages * kStage + 1024 + 24576 <= 232448, "shared memory per CTA");
 };
 
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) { return smem_desc(saddr, 16, 1024, 2); }
 __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) { return smem_desc(saddr, 0, 128, 0); }
 
+constexpr int kMaxExperts = 520;  // plan arrays cached in shared memory (E + n_shared <= 513)
+
+// Unit u -> (expert, weight tile, token-tile slot, tokens in the tile), from
+// the plan cached in shared memory: the expert is the last one whose first
+// unit is <= u.
 template <int N>
-__device__ __forceinline__ void decode_unit(const KParams& p, int u, int& e, int& mt, int& slot, int& cnt) {
-  int lo = 0, hi = p.n_exp;
+__device__ __forceinline__ void decode_unit(const int32_t* s_start, const int32_t* s_count, const int32_t* s_slot,
+                                            int n_exp, int u, int& e, int& mt, int& slot, int& cnt) {
+  int lo = 0, hi = n_exp;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (__ldg(p.unit_start + mid) <= u) lo = mid;
+    if (s_start[mid] <= u) lo = mid;
     else hi = mid;
   }
   e = lo;
-  const int local = u - __ldg(p.unit_start + e);
-  const int count = __ldg(p.expert_count + e);
+  const int local = u - s_start[e];
+  const int count = s_count[e];
   const int nt = (count + N - 1) / N;
   mt = local / nt;
   const int ti = local - mt * nt;
-  slot = __ldg(p.expert_slot + e) + ti;
+  slot = s_slot[e] + ti;
   cnt = min(N, count - ti * N);
 }
 
@@ -108,13 +121,15 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[C::kStages];
   __shared__ __align__(8) uint64_t bar_empty[C::kStages];
-  __shared__ __align__(8) uint64_t bar_tfull, bar_tempty, bar_done;
+  __shared__ __align__(8) uint64_t bar_tfull[2], bar_tempty[2], bar_done;
+  __shared__ float epi_tile[4][32][33];  // per epilogue warp: 32 lanes x 32 columns, transposed
+  __shared__ int32_t s_start[kMaxExperts], s_count[kMaxExperts], s_slot[kMaxExperts];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int total = __ldg(p.total_units);
+
   const int KT = (p.K + 255) / 256;
 
   if (threadIdx.x == 0) {
@@ -122,8 +137,10 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
       mbar_init(smem_u32(&bar_full[s]), 1);
       mbar_init(smem_u32(&bar_empty[s]), 1);
     }
-    mbar_init(smem_u32(&bar_tfull), 1);
-    mbar_init(smem_u32(&bar_tempty), 4);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&bar_tfull[a]), 1);
+      mbar_init(smem_u32(&bar_tempty[a]), 4);
+    }
     mbar_init(smem_u32(&bar_done), 1);
     abort_flag = 0;
     fence_barrier_init();
@@ -136,6 +153,17 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
     prefetch_tmap(&p.tmA);
     prefetch_tmap(&p.tmB);
     if (p.has_shared) prefetch_tmap(&p.tmA_sh);
+  }
+  // everything above overlaps the previous kernel; the plan and the
+  // activations it wrote are read only after this point
+  pdl_wait();
+  const int total = *p.total_units;
+  for (int i = threadIdx.x; i <= p.n_exp; i += blockDim.x) {
+    s_start[i] = p.unit_start[i];
+    if (i < p.n_exp) {
+      s_count[i] = p.expert_count[i];
+      s_slot[i] = p.expert_slot[i];
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -150,7 +178,7 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
       uint32_t phase = 0, armed = 0, armed_par = 0;
       for (int u = blockIdx.x; u < total && !*abort_v; u += gridDim.x) {
         int e, mt, slot, cnt;
-        decode_unit<N>(p, u, e, mt, slot, cnt);
+        decode_unit<N>(s_start, s_count, s_slot, p.n_exp, u, e, mt, slot, cnt);
         const bool sh = e >= p.E;
         const CUtensorMap* tmA = sh ? &p.tmA_sh : &p.tmA;
         const int ec = sh ? e - p.E : e;
@@ -190,16 +218,17 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t t_acc0 = tmem;
-      const uint32_t t_acc1 = tmem + N;
       const uint32_t t_sfa0 = tmem + C::kSfaCol;
       const uint32_t t_sfa1 = t_sfa0 + C::kAtoms * 4;
       const uint32_t t_sfb = tmem + C::kSfbCol;
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
+      int as = 0;  // accumulator set of this unit
       for (int u = blockIdx.x; u < total && !*abort_v; u += gridDim.x) {
-        bool ok = mbar_wait(smem_u32(&bar_tempty), acc_phase ^ 1u);
+        bool ok = mbar_wait(smem_u32(&bar_tempty[as]), acc_phase ^ 1u);
         tc_fence_after();
+        const uint32_t t_acc0 = tmem + as * C::kAccCols;
+        const uint32_t t_acc1 = t_acc0 + N;
         for (int kt = 0; ok && kt < KT; ++kt) {
           if (!mbar_wait(smem_u32(&bar_full[stage]), phase)) { ok = false; break; }
           tc_fence_after();
@@ -231,8 +260,8 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
           record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
           break;
         }
-        tc_commit(smem_u32(&bar_tfull));
-        acc_phase ^= 1u;
+        tc_commit(smem_u32(&bar_tfull[as]));
+        if (++as == C::kAccStages) { as = 0; acc_phase ^= 1u; }
       }
       // all issued MMAs must finish before tensor memory is released
       tc_commit(smem_u32(&bar_done));
@@ -242,63 +271,69 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // tensor-memory lane quadrant of this warp
     const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+    float(*tile)[33] = epi_tile[warp - 2];
     uint32_t acc_phase = 0;
+    int as = 0;
     for (int u = blockIdx.x; u < total && !*abort_v; u += gridDim.x) {
       int e, mt, slot, cnt;
-      decode_unit<N>(p, u, e, mt, slot, cnt);
-      if (!mbar_wait(smem_u32(&bar_tfull), acc_phase)) {
+      decode_unit<N>(s_start, s_count, s_slot, p.n_exp, u, e, mt, slot, cnt);
+      if (!mbar_wait(smem_u32(&bar_tfull[as]), acc_phase)) {
         *abort_v = 1;
         if (lane == 0) record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
         break;
       }
       tc_fence_after();
+      const uint32_t ta = tq + as * C::kAccCols;
       const int64_t row0 = (int64_t)slot * kSlotRows;
       if constexpr (GATEUP) {
-        const int i = mt * 128 + 32 * q + lane;  // intermediate index of this lane
+        const int i0 = mt * 128 + 32 * q;  // first intermediate index of this warp's lanes
         float sc = 1.f;
         if constexpr (NV) sc = __fmul_rn(__ldg(p.gb), __ldg(p.gw + e));
         float amax = 0.f;
         for (int c0 = 0; c0 < cnt; c0 += 32) {
           float g[32], uu[32];
-          tc_ld32(tq + c0, g);
-          tc_ld32(tq + N + c0, uu);
+          tc_ld32(ta + c0, g);
+          tc_ld32(ta + N + c0, uu);
           tc_wait_ld();
-          const int jn = min(32, cnt - c0);
+          // lane l holds h(i0 + l, token c0 + j); transpose through shared memory
+          // so that lane j then holds the 32 values of token c0 + j, one block
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            if (j >= jn) break;
             float gv = g[j], uv = uu[j];
             if constexpr (NV) {
               gv = gv * sc;
               uv = uv * sc;
             }
-            const float h = gv / (1.0f + expf(-gv)) * uv;
-            const int64_t row = row0 + c0 + j;
-            if (p.h_dbg) p.h_dbg[row * p.I + i] = h;
-            if constexpr (NV) {
-              p.h32[row * p.I + i] = h;
-              amax = fmaxf(amax, fabsf(h));
-            } else {
-              float a = fabsf(h);
+            tile[j][lane] = gv / (1.0f + expf(-gv)) * uv;
+          }
+          __syncwarp();
+          const int n = c0 + lane;
+          if (n < cnt) {
+            const int64_t row = row0 + n;
+            float v[32];
 #pragma unroll
-              for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-              const int ex = mx_block_exp(a);
-              const uint32_t code = e2m1_code(h * exp2i(-ex));
-              const uint32_t nb = code | (__shfl_down_sync(0xffffffffu, code, 1) << 4);
-              const uint32_t w8 = nb | (__shfl_down_sync(0xffffffffu, nb, 2) << 8);
-              const uint32_t w16 = w8 | (__shfl_down_sync(0xffffffffu, w8, 4) << 16);
-              const uint32_t x1 = __shfl_sync(0xffffffffu, w16, 8);
-              const uint32_t x2 = __shfl_sync(0xffffffffu, w16, 16);
-              const uint32_t x3 = __shfl_sync(0xffffffffu, w16, 24);
-              if (lane == 0) {
-                *reinterpret_cast<uint4*>(p.hq + row * (p.I >> 1) + ((mt * 128 + 32 * q) >> 1)) =
-                    make_uint4(w16, x1, x2, x3);
-                p.hsf[sf_tiled_offset(row, 4 * mt + q, p.katoms_h)] = (uint8_t)(ex + 127);
-                if (mt == p.m_tiles - 1 && p.katoms_h > p.m_tiles)  // pad group up to the K tile: scale 1.0
-                  p.hsf[sf_tiled_offset(row, 4 * p.m_tiles + q, p.katoms_h)] = 127;
-              }
+            for (int r = 0; r < 32; ++r) v[r] = tile[lane][r];
+            if (p.h_dbg) {
+              float4* dst = reinterpret_cast<float4*>(p.h_dbg + row * p.I + i0);
+#pragma unroll
+              for (int r = 0; r < 8; ++r) dst[r] = make_float4(v[4 * r], v[4 * r + 1], v[4 * r + 2], v[4 * r + 3]);
+            }
+            if constexpr (NV) {
+              float4* dst = reinterpret_cast<float4*>(p.h32 + row * p.I + i0);
+#pragma unroll
+              for (int r = 0; r < 8; ++r) dst[r] = make_float4(v[4 * r], v[4 * r + 1], v[4 * r + 2], v[4 * r + 3]);
+#pragma unroll
+              for (int r = 0; r < 32; ++r) amax = fmaxf(amax, fabsf(v[r]));
+            } else {
+              uint32_t pk[4], sb;
+              mx_quant32(v, pk, &sb);
+              *reinterpret_cast<uint4*>(p.hq + row * (p.I >> 1) + (i0 >> 1)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              p.hsf[sf_tiled_offset(row, i0 >> 5, p.katoms_h)] = (uint8_t)sb;
+              if (mt == p.m_tiles - 1 && p.katoms_h > p.m_tiles)  // pad group up to the K tile: scale 1.0
+                p.hsf[sf_tiled_offset(row, 4 * p.m_tiles + q, p.katoms_h)] = 127;
             }
           }
+          __syncwarp();
         }
         if constexpr (NV) {
 #pragma unroll
@@ -311,26 +346,32 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
         if constexpr (NV) sc = __fmul_rn(__ldg(p.gb + e), __ldg(p.gw + e));
         for (int c0 = 0; c0 < cnt; c0 += 32) {
           float y[32];
-          tc_ld32(tq + c0, y);
+          tc_ld32(ta + c0, y);
           tc_wait_ld();
           const int jn = min(32, cnt - c0);
+          int tk = 0;
+          float wk = 0.f;
+          if (lane < jn) {  // lane j fetches token and weight of column c0 + j
+            tk = __ldg(p.row_tok + row0 + c0 + lane);
+            wk = __ldg(p.row_w + row0 + c0 + lane) * sc;
+          }
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             if (j >= jn) break;
-            const int64_t row = row0 + c0 + j;
-            const int t = __ldg(p.row_tok + row);
-            const float w = __ldg(p.row_w + row) * sc;
+            const int t = __shfl_sync(0xffffffffu, tk, j);
+            const float w = __shfl_sync(0xffffffffu, wk, j);
             atomicAdd(p.out_acc + (int64_t)t * p.H + h_idx, y[j] * w);
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bar_tempty));
-      acc_phase ^= 1u;
+      if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[as]));
+      if (++as == C::kAccStages) { as = 0; acc_phase ^= 1u; }
     }
   }
 
+  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -343,10 +384,16 @@ template <int N, bool GATEUP, bool NV>
 cudaError_t launch_gemm_t(const KParams& p, int grid, cudaStream_t s) {
   using C = GemmCfg<N, GATEUP, NV>;
   auto k = moe_gemm_kernel<N, GATEUP, NV>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  static bool attr_set[64] = {};  // once per device and template instance
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  k<<<grid, 192, C::kSmem, s>>>(p);
-  return cudaGetLastError();
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  return launch_pdl(k, dim3(grid), dim3(192), C::kSmem, s, p);
 }
 
 }  // namespace fp4moe

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -30,6 +31,7 @@ struct Layout {
   int64_t dn_start;      // int32 [n_exp + 1] prefix of down units
   int64_t row_e;         // int32 [rows_cap] expert of each row
   int64_t amax;          // uint32 [2 + n_exp] amax bits (x, spare, h per expert)
+  bool front;            // few-token MXFP4 forward uses the fused front end
   int n_exp, n_chunks, n_route_per_tok;
 };
 
@@ -47,6 +49,26 @@ cudaError_t launch_plan(const fp4moe_dims& d, int32_t* chunk_counts, int n_chunk
 cudaError_t launch_scatter(const fp4moe_dims& d, const int32_t* idx, const float* w, const int32_t* chunk_counts,
                            int n_chunks, int n_exp, int n_tile, const int32_t* expert_slot, int32_t* route_row,
                            int32_t* row_tok, float* row_w, int32_t* row_e, cudaStream_t s);
+// Fused router + top-k + plan + scatter for few tokens (MXFP4, T <= 16):
+// one launch instead of four.
+struct FrontArgs {
+  fp4moe_dims d;  // by value: the kernel reads it
+  const uint16_t *x, *wr;
+  const float* bias;
+  float* partial;
+  int n_splits, n_tile, n_exp;
+  float* out_acc;            // zeroed here
+  int32_t* idx;
+  float* w;
+  int32_t *expert_count, *expert_slot, *gu_start, *dn_start;
+  Plan* plan;
+  int32_t *route_row, *row_tok, *row_e;
+  float* row_w;
+  int32_t* ticket;  // zero on entry
+};
+constexpr int kFrontMaxT = 16;
+cudaError_t launch_decode_front(const FrontArgs& a, cudaStream_t s);
+
 cudaError_t launch_amax(const void* x, int x_is_fp32, int64_t n, uint32_t* amax_bits, cudaStream_t s);
 cudaError_t launch_gather_quant(const fp4moe_dims& d, const uint16_t* x, const int32_t* route_row, uint8_t* xq,
                                 uint8_t* xsf, const uint32_t* amax_x, float* g_out, cudaStream_t s);
@@ -94,6 +116,25 @@ cudaError_t launch_gateup(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_down(const GemmArgs& a, cudaStream_t s);
 
 int device_sm_count();
+
+// Launches kernel<<<grid, block, smem, s>>>(args...) with programmatic stream
+// serialisation: it may begin while the previous kernel on s drains; the
+// kernel waits (griddepcontrol.wait) before reading that kernel's outputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Encodes a uint8 tensor map: dims[0] innermost (bytes), strides[i] the byte
 // stride of dimension i + 1, box in elements, optional 128-byte swizzle.

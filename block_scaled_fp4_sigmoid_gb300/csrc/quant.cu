@@ -95,6 +95,8 @@ __global__ void quantize_rows_kernel(const void* x, int x_is_fp32, int64_t rows,
 __global__ void gather_quant_kernel(const uint16_t* x, int T, int H, int routes_per_tok,
                                     const int32_t* route_row, uint8_t* xq, uint8_t* xsf, int nv,
                                     const uint32_t* amax_x, float* g_out) {
+  pdl_wait();  // route_row (and the NVFP4 amax) come from the previous kernels
+  pdl_trigger();
   const int per_row = H >> 5;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t n_routes = (int64_t)T * routes_per_tok;
@@ -179,6 +181,7 @@ __global__ void pack_scales_kernel(const uint8_t* src, uint8_t* dst, int64_t n_m
 
 // ---------------------------------------------------------------- combine finaliser
 __global__ void finalize_kernel(const float* acc, uint16_t* out, int64_t n) {
+  pdl_wait();
   const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (i + 3 < n) {
     const float4 v = *reinterpret_cast<const float4*>(acc + i);
@@ -313,9 +316,8 @@ cudaError_t launch_gather_quant(const fp4moe_dims& d, const uint16_t* x, const i
   const int rpt = d.top_k + d.n_shared;
   const int64_t n = (int64_t)d.T * rpt * (d.H >> 5);
   if (n == 0) return cudaSuccess;
-  gather_quant_kernel<<<blocks_for(n, 256), 256, 0, s>>>(x, d.T, d.H, rpt, route_row, xq, xsf,
-                                                          d.fmt == FP4MOE_NVFP4, amax_x, g_out);
-  return cudaGetLastError();
+  return launch_pdl(gather_quant_kernel, dim3(blocks_for(n, 256)), dim3(256), 0, s, x, d.T, d.H, rpt, route_row,
+                    xq, xsf, (int)(d.fmt == FP4MOE_NVFP4), amax_x, g_out);
 }
 
 cudaError_t launch_h_quant_nv_routes(const fp4moe_dims& d, const float* h32, const int32_t* route_row,
@@ -331,8 +333,7 @@ cudaError_t launch_h_quant_nv_routes(const fp4moe_dims& d, const float* h32, con
 
 cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  finalize_kernel<<<blocks_for((n + 3) / 4, 256), 256, 0, s>>>(acc, out, n);
-  return cudaGetLastError();
+  return launch_pdl(finalize_kernel, dim3(blocks_for((n + 3) / 4, 256)), dim3(256), 0, s, acc, out, n);
 }
 
 cudaError_t launch_pack_scales(const uint8_t* src, uint8_t* dst, int64_t n_mat, int rows, int kblocks, bool nv,

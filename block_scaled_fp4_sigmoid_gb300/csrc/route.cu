@@ -14,11 +14,9 @@ namespace {
 // One warp per (expert, K split): streams the expert's router row once and
 // forms the dot products with all T <= 16 token rows.
 template <int TMAX>
-__global__ void router_gemv_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
-                                   float* __restrict__ partial, int T, int H, int E, int n_splits) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= E * n_splits) return;
+__device__ __forceinline__ void gemv_warp(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
+                                          float* __restrict__ partial, int T, int H, int E, int n_splits, int warp,
+                                          int lane) {
   const int e = warp % E, sp = warp / E;
   const int kc = H / n_splits;  // multiple of 256
   const int k0 = sp * kc;
@@ -26,6 +24,7 @@ __global__ void router_gemv_kernel(const uint16_t* __restrict__ x, const uint16_
 #pragma unroll
   for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
   const uint16_t* wrow = wr + (int64_t)e * H;
+#pragma unroll 4
   for (int k = k0 + lane * 8; k < k0 + kc; k += 256) {
     const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wrow + k));
     const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
@@ -55,6 +54,14 @@ __global__ void router_gemv_kernel(const uint16_t* __restrict__ x, const uint16_
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     if (lane == 0 && t < T) partial[((int64_t)sp * T + t) * E + e] = v;
   }
+}
+
+template <int TMAX>
+__global__ void router_gemv_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
+                                   float* __restrict__ partial, int T, int H, int E, int n_splits) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (warp >= E * n_splits) return;
+  gemv_warp<TMAX>(x, wr, partial, T, H, E, n_splits, warp, threadIdx.x & 31);
 }
 
 // ---------------------------------------------------------------- router logits, many tokens
@@ -180,27 +187,38 @@ __global__ void __launch_bounds__(128) router_mma_kernel(const uint16_t* __restr
 
 // ---------------------------------------------------------------- sigmoid + bias grouped top-k
 // One warp per token.  Scores live in shared memory (E <= 512).
-constexpr int kTopkWarps = 4;
-
-__global__ void topk_kernel(const float* __restrict__ partial, int n_splits, const float* __restrict__ bias,
-                            int T, int E, int k, int n_group, int topk_group, float scaling, int renorm,
-                            int32_t* __restrict__ idx_out, float* __restrict__ w_out, float* __restrict__ logits_out,
-                            int32_t* __restrict__ chunk_counts, int n_exp) {
-  __shared__ float s_s[kTopkWarps][512];
-  __shared__ float s_c[kTopkWarps][512];
-  __shared__ float s_g[kTopkWarps][32];
-  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kTopkWarps + wib;
-  if (t >= T) return;
-  float* sv = s_s[wib];
-  float* cv = s_c[wib];
-  for (int e = lane; e < E; e += 32) {
-    float l = 0.f;
-    for (int sp = 0; sp < n_splits; ++sp) l += partial[((int64_t)sp * T + t) * E + e];
-    if (logits_out) logits_out[(int64_t)t * E + e] = l;
-    const float s = 1.0f / (1.0f + expf(-l));
-    sv[e] = s;
-    cv[e] = s + bias[e];
+// Routes token t with one warp: sums the split-K partial logits, sigmoid,
+// bias, group selection, top-k.  sv / cv: E floats of shared memory for this
+// warp.  Lane j < k returns the j-th chosen expert in *idx and its routing
+// weight in *w (ties to the lower group and expert index).
+__device__ __forceinline__ void topk_token(const float* __restrict__ partial, int n_splits,
+                                           const float* __restrict__ bias, int T, int t, int E, int k,
+                                           int n_group, int topk_group, float scaling, int renorm,
+                                           float* __restrict__ logits_out, float* sv, float* cv, int lane,
+                                           int* idx, float* w) {
+  // E <= 512: at most 16 logits per lane; issue each split's loads together
+  float lv[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) lv[q] = 0.f;
+#pragma unroll 4
+  for (int sp = 0; sp < n_splits; ++sp) {  // unrolled: several splits' loads in flight
+    const float* src = partial + ((int64_t)sp * T + t) * E;
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      if (lane + 32 * q < E) lv[q] += src[lane + 32 * q];
+  }
+  float bv16[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) bv16[q] = lane + 32 * q < E ? bias[lane + 32 * q] : 0.f;
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int e = lane + 32 * q;
+    if (e < E) {
+      if (logits_out) logits_out[(int64_t)t * E + e] = lv[q];
+      const float s = 1.0f / (1.0f + expf(-lv[q]));
+      sv[e] = s;
+      cv[e] = s + bv16[q];
+    }
   }
   __syncwarp();
   // group selection: group score = sum of the two largest corrected scores
@@ -232,33 +250,58 @@ __global__ void topk_kernel(const float* __restrict__ partial, int n_splits, con
       if (!((group_ok >> (e / gsz)) & 1u)) cv[e] = -INFINITY;
     __syncwarp();
   }
-  // top-k over corrected scores, ties to the lower expert index
+  // top-k over corrected scores, ties to the lower expert index; each lane
+  // keeps its (at most 16) candidates in registers
+  float cr[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) cr[q] = lane + 32 * q < E ? cv[lane + 32 * q] : -INFINITY;
   int my_idx = -1;
   float my_s = 0.f;
   for (int j = 0; j < k; ++j) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int e = lane; e < E; e += 32) {
-      const float v = cv[e];
-      if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
-    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q)  // ascending expert index within the lane: '>' keeps the lower on ties
+      if (cr[q] > bv) { bv = cr[q]; bi = lane + 32 * q; }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
       const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
       if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
     }
-    if (lane == j) { my_idx = bi; my_s = sv[bi]; }
-    __syncwarp();
-    if (lane == 0) cv[bi] = -INFINITY;
-    __syncwarp();
+    if (bi >= E) bi = 0;  // only reachable with NaN scores (out of contract): keep the index in range
+    if (lane == j) my_idx = bi;
+    if ((bi & 31) == lane) {  // the owner drops the winner from its candidates
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        if (lane + 32 * q == bi) cr[q] = -INFINITY;
+    }
   }
+  if (lane < k) my_s = sv[my_idx];
   float tot = 0.f;
   for (int j = 0; j < k; ++j) tot += __shfl_sync(0xffffffffu, my_s, j);
+  *idx = my_idx;
+  *w = renorm ? my_s / tot * scaling : my_s * scaling;
+}
+
+constexpr int kTopkWarps = 4;
+
+__global__ void topk_kernel(const float* __restrict__ partial, int n_splits, const float* __restrict__ bias,
+                            int T, int E, int k, int n_group, int topk_group, float scaling, int renorm,
+                            int32_t* __restrict__ idx_out, float* __restrict__ w_out, float* __restrict__ logits_out,
+                            int32_t* __restrict__ chunk_counts, int n_exp) {
+  __shared__ float s_s[kTopkWarps][512];
+  __shared__ float s_c[kTopkWarps][512];
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kTopkWarps + wib;
+  if (t >= T) return;
+  int my_idx;
+  float my_w;
+  topk_token(partial, n_splits, bias, T, t, E, k, n_group, topk_group, scaling, renorm, logits_out, s_s[wib],
+             s_c[wib], lane, &my_idx, &my_w);
   if (lane < k) {
-    const float w = renorm ? my_s / tot * scaling : my_s * scaling;
     idx_out[(int64_t)t * k + lane] = my_idx;
-    w_out[(int64_t)t * k + lane] = w;
+    w_out[(int64_t)t * k + lane] = my_w;
     atomicAdd(&chunk_counts[(t / kChunkTokens) * n_exp + my_idx], 1);
   }
 }
@@ -357,6 +400,131 @@ __global__ void scatter_kernel(const int32_t* __restrict__ idx, const float* __r
   }
 }
 
+// ---------------------------------------------------------------- fused front end for few tokens
+// Phase A (every CTA): one warp per (expert, K split) of the router GEMV and
+// grid-stride zeroing of the combine buffer.  The CTA that finishes last (a
+// ticket counter; no CTA ever waits for another) runs phase B: top-k per
+// token, expert counts and stable positions (each token routes to an expert
+// at most once, so a route's position is the number of earlier tokens routed
+// to the same expert), the plan, and the route -> row map.  The quantised
+// rows are then written by gather_quant_kernel.
+constexpr int kFrontThreads = 256;
+constexpr int kFrontWarps = kFrontThreads / 32;
+
+__global__ void __launch_bounds__(kFrontThreads, 3) decode_front_kernel(FrontArgs a) {
+  __shared__ float s_sc[kFrontWarps][2][512];  // scores of the token a warp routes
+  __shared__ int s_last;
+  __shared__ int32_t s_idx[kFrontMaxT][16];
+  __shared__ float s_w[kFrontMaxT][16];
+  __shared__ int32_t s_count[520];
+  __shared__ int32_t s_slot[520];
+  __shared__ int32_t s_wsum[kFrontWarps];
+  const fp4moe_dims& d = a.d;
+  const int T = d.T, H = d.H, E = d.E, k = d.top_k;
+  const int tid = threadIdx.x, lane = tid & 31, wib = tid >> 5;
+  const int warp = (blockIdx.x * blockDim.x + tid) >> 5;
+  const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + tid;
+  const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
+
+  pdl_trigger();  // the next kernel may launch and wait for this one
+  // ---- phase A
+  if (warp < E * a.n_splits) {
+    if (T <= 8) gemv_warp<8>(a.x, a.wr, a.partial, T, H, E, a.n_splits, warp, lane);
+    else gemv_warp<kFrontMaxT>(a.x, a.wr, a.partial, T, H, E, a.n_splits, warp, lane);
+  }
+  for (int64_t i = gtid; i < (int64_t)T * H / 4; i += nthr)
+    reinterpret_cast<float4*>(a.out_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(a.ticket, 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // ---- phase B (one CTA)
+  const int n_exp = a.n_exp, rpt = k + d.n_shared;
+  for (int t = wib; t < T; t += kFrontWarps) {
+    int id;
+    float wt;
+    topk_token(a.partial, a.n_splits, a.bias, T, t, E, k, d.n_group, d.topk_group, d.routed_scaling,
+               d.renormalize, nullptr, s_sc[wib][0], s_sc[wib][1], lane, &id, &wt);
+    if (lane < k) {
+      s_idx[t][lane] = id;
+      s_w[t][lane] = wt;
+      a.idx[t * k + lane] = id;
+      a.w[t * k + lane] = wt;
+    }
+    __syncwarp();
+  }
+  for (int e = tid; e < n_exp; e += blockDim.x) s_count[e] = e >= E ? T : 0;
+  __syncthreads();
+  for (int r = tid; r < T * k; r += blockDim.x) atomicAdd(&s_count[s_idx[r / k][r % k]], 1);
+  __syncthreads();
+  // plan: exclusive scan of tiles over experts; thread j owns experts 3j..3j+2
+  const int gm = d.I / 128, dm = H / 128;
+  int tl[3], my = 0;
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    const int e = 3 * tid + q;
+    tl[q] = e < n_exp ? (s_count[e] + a.n_tile - 1) / a.n_tile : 0;
+    my += tl[q];
+  }
+  int incl = my;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_wsum[wib] = incl;
+  __syncthreads();
+  int base = incl - my;
+  for (int w2 = 0; w2 < wib; ++w2) base += s_wsum[w2];
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    const int e = 3 * tid + q;
+    if (e < n_exp) {
+      s_slot[e] = base;
+      a.expert_count[e] = s_count[e];
+      a.expert_slot[e] = base;
+      a.gu_start[e] = base * gm;
+      a.dn_start[e] = base * dm;
+    }
+    base += tl[q];
+  }
+  if (tid == 0) {
+    int total = 0;
+    for (int w2 = 0; w2 < kFrontWarps; ++w2) total += s_wsum[w2];
+    a.gu_start[n_exp] = total * gm;
+    a.dn_start[n_exp] = total * dm;
+    a.plan->n_exp = n_exp;
+    a.plan->gu_units = total * gm;
+    a.plan->dn_units = total * dm;
+    a.plan->slots = total;
+  }
+  __syncthreads();
+  for (int r = tid; r < T * rpt; r += blockDim.x) {
+    const int t = r / rpt, j = r - t * rpt;
+    int e, pos;
+    float wt;
+    if (j < k) {
+      e = s_idx[t][j];
+      wt = s_w[t][j];
+      pos = 0;
+      for (int t2 = 0; t2 < t; ++t2)
+        for (int j2 = 0; j2 < k; ++j2) pos += s_idx[t2][j2] == e;
+    } else {
+      e = E + (j - k);
+      wt = 1.0f;
+      pos = t;
+    }
+    const int row = (s_slot[e] + pos / a.n_tile) * kSlotRows + pos % a.n_tile;
+    a.route_row[r] = row;
+    a.row_tok[row] = t;
+    a.row_w[row] = wt;
+    a.row_e[row] = e;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* wr, float* partial, int T, int H, int E,
@@ -397,6 +565,13 @@ cudaError_t launch_scatter(const fp4moe_dims& d, const int32_t* idx, const float
   const unsigned blocks = (unsigned)((n_chunks + kScatterWarps - 1) / kScatterWarps);
   scatter_kernel<<<blocks, 32 * kScatterWarps, 0, s>>>(idx, w, chunk_counts, d.T, d.top_k, d.E, n_exp, n_chunks,
                                                         n_tile, expert_slot, route_row, row_tok, row_w, row_e);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_front(const FrontArgs& a, cudaStream_t s) {
+  const int warps = a.d.E * a.n_splits;
+  const unsigned blocks = (unsigned)((warps * 32 + kFrontThreads - 1) / kFrontThreads);
+  decode_front_kernel<<<blocks, kFrontThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
