@@ -61,6 +61,8 @@ def source_sha(paths) -> str:
 
 GEMM_SOURCES = ["block_scaled_fp4_sigmoid_gb300/csrc/gemm.cuh", "block_scaled_fp4_sigmoid_gb300/csrc/common.cuh",
                 "block_scaled_fp4_sigmoid_gb300/csrc/gemm_launch.cuh"]
+# the committed ncu summary names the kernel it measured
+PROFILED_KERNEL = "moe_gemm_kernel"
 
 
 def profiled_traffic(workload: str):
@@ -216,6 +218,43 @@ def cfg_label(cfg) -> str:
             f"{' +1 shared' if cfg.n_shared else ''} {cfg.fmt.upper()} A4W4")
 
 
+# ------------------------------------------------------------------ MXFP4 -> FP8 conversion
+def time_conversion(layer, peaks, stream, reps: int = 5):
+    """fp4moe_mxfp4_to_fp8_rowscale over every routed expert row of the layer
+    (w13 rows of K = H, then w2 rows of K = I), timed with CUDA events.
+    Algorithmic bytes: codes + scales in, E4M3 bytes + row scale + status out."""
+    import torch
+    import block_scaled_fp4_sigmoid_gb300 as fm
+    d = layer.dims
+    s = stream.cuda_stream
+    ws = torch.zeros(256, dtype=torch.uint8, device=layer.device)
+    w13s, w2s = layer.raw_scales
+    parts = [(layer.w13, w13s, d.E * 2 * d.I, d.H), (layer.w2, w2s, d.E * d.H, d.I)]
+    total_ms, total_bytes, rows_all = 0.0, 0, 0
+    for codes, scales, rows, K in parts:
+        out = torch.empty((rows, K), dtype=torch.uint8, device=layer.device)
+        rs = torch.empty(rows, dtype=torch.float32, device=layer.device)
+        st = torch.empty(rows, dtype=torch.uint8, device=layer.device)
+        args = (codes.data_ptr(), scales.data_ptr(), rows, K, out.data_ptr(), rs.data_ptr(), st.data_ptr(),
+                ws.data_ptr(), 256, s)
+        fm.mxfp4_to_fp8_rowscale(*args)  # warm-up
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+        for i in range(reps):
+            ev[2 * i].record(stream)
+            fm.mxfp4_to_fp8_rowscale(*args)
+            ev[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        total_ms += statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(reps))
+        total_bytes += rows * (K // 2 + K // 32 + K + 4 + 1)
+        rows_all += rows
+        del out, rs, st
+    st_code, n_bad = fm.get_status(ws.data_ptr(), s)
+    gbs = total_bytes / (total_ms * 1e-3) / 1e9
+    return {"rows": rows_all, "ms": total_ms, "achieved": gbs, "unit": "GB/s", "peak": peaks["hbm_gbs"],
+            "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": total_bytes, "rows_flagged": n_bad,
+            "bound": "hbm", "l2": "inputs and outputs (25.9 GB) far exceed L2"}
+
+
 # ------------------------------------------------------------------ GPU arm
 def gpu_arm(args, cfg, rank, world, local_rank):
     import numpy as np
@@ -363,8 +402,12 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     achieved = gu_bytes / (gu_max * 1e-3) / 1e9
     traffic = profiled_traffic(cfg.name)
     clocks = clk.summary()
-    fused_front = cfg.fmt == "mxfp4" and cfg.T <= 16
-    launches_per_step = 4 if fused_front else 8 + (2 if cfg.fmt == "nvfp4" else 0)
+    # front (or router, top-k, plan, scatter), gather, gate/up, down, finalise
+    if cfg.fmt == "mxfp4":
+        launches_per_step = 5 if cfg.T <= 16 else 8
+    else:
+        launches_per_step = 10
+    conversion = time_conversion(layer, peaks, stream) if args.conversion else None
     # CPU baseline: the oracle on a bounded sample of this workload
     n_routes = 16 if args.cpu_routes is None else args.cpu_routes
     cpu_s, cpu_tok = oracle_route_sample(args.config, n_routes) if n_routes > 0 else (float("nan"), 0.0)
@@ -400,6 +443,7 @@ def gpu_arm(args, cfg, rank, world, local_rank):
         "cpu_baseline": {"value": cpu_tok / cpu_s, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                          "sample": f"{n_routes} routes ({cpu_tok:g} tokens) of the same workload, FP64 numpy"},
         "context": "pages: 1.43 ms per MoE layer call at T=8 on one Gaudi 2 card holding 48 of 384 experts",
+        "conversion": conversion,
     }
     print(json.dumps(line), flush=True)
 
@@ -415,6 +459,8 @@ def main():
     ap.add_argument("--experts", type=int, default=None,
                     help="override E (smaller device footprint for profiler captures)")
     ap.add_argument("--tokens", type=int, default=None, help="override T")
+    ap.add_argument("--conversion", action="store_true",
+                    help="also time the MXFP4 -> FP8 conversion of all routed expert rows")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     import synth

@@ -2,6 +2,8 @@
 // gather-and-quantise step of the forward, NVFP4 requantisation of the
 // intermediate, the combine finaliser, and the exact MXFP4 -> FP8 conversion.
 #include <algorithm>
+#include <array>
+#include <utility>
 
 #include "common.cuh"
 #include "internal.h"
@@ -195,15 +197,6 @@ __global__ void finalize_kernel(const float* acc, uint16_t* out, int64_t n) {
 }
 
 // ---------------------------------------------------------------- MXFP4 -> FP8 conversion
-// Exponent of the largest magnitude code among 8 nibbles of a word: codes
-// 1..7 have exponents -1, 0, 0, 1, 1, 2, 2 (code >> 1) - 1; -100 if all zero.
-__device__ __forceinline__ uint32_t max_mag_nibble(uint32_t w) {
-  uint32_t m = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) m = max(m, (w >> (4 * j)) & 7u);
-  return m;
-}
-
 // E4M3 byte of one E2M1 code with block exponent sb (scale byte - 127) under
 // channel shift k.  *low is set when a non-zero element lands below 2^-5.
 __device__ __forceinline__ uint32_t conv_nibble(uint32_t c, int sb, int k, bool* low) {
@@ -227,65 +220,255 @@ __device__ __forceinline__ uint32_t conv_nibble(uint32_t c, int sb, int k, bool*
   return sign | r;
 }
 
-// One warp per row.  Lane l handles 32-element blocks l, l + 32, ...
-__global__ void convert_kernel(const uint8_t* codes, const uint8_t* scales, int64_t rows, int K, uint8_t* out,
-                               float* row_scale, uint8_t* row_status, int32_t* status) {
-  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const int nblk = K >> 5;
-  const uint4* crow = reinterpret_cast<const uint4*>(codes + row * (K >> 1));
-  const uint8_t* srow = scales + row * nblk;
-  int emax = -1000;
-  bool nan = false;
-  for (int b = lane; b < nblk; b += 32) {
-    const uint4 w = __ldg(crow + b);
-    const uint32_t s = __ldg(srow + b);
-    nan |= (s == 255u);
-    const uint32_t m = max(max(max_mag_nibble(w.x), max_mag_nibble(w.y)), max(max_mag_nibble(w.z), max_mag_nibble(w.w)));
-    if (m) emax = max(emax, (int)(m >> 1) - 1 + (int)s - 127);
+// Exponent class of the largest magnitude among 16 codes (two words): 0 when
+// every magnitude is zero, else 1, 2, 3, 4 for a largest magnitude of 1,
+// 2-3, 4-5, 6-7, whose element exponents floor(log2 v) are -1, 0, 1, 2.
+__device__ __forceinline__ int half_class(uint32_t x, uint32_t y) {
+  const uint32_t om = (x | y) & 0x77777777u;
+  const uint32_t b21 = ((x & (x << 1)) | (y & (y << 1))) & 0x44444444u;  // a magnitude 6 or 7
+  return (om != 0u) + ((om & 0x66666666u) != 0u) + ((om & 0x44444444u) != 0u) + (b21 != 0u);
+}
+
+// Eight codes -> eight E4M3 bytes (two words).  Magnitude by table lookup:
+// each code's low three bits select a byte of the block table (tlo, thi).
+// Sign: bit 3 of even codes moves to bit 7 of a byte after a 4-bit shift,
+// bit 3 of odd codes already sits at bit 7 of a byte; a byte permute
+// interleaves them into code order.
+__device__ __forceinline__ void conv8(uint32_t w, uint32_t tlo, uint32_t thi, uint32_t& o0, uint32_t& o1) {
+  const uint32_t m = w & 0x77777777u, e = w << 4;
+  o0 = __byte_perm(tlo, thi, m) | (__byte_perm(e, w, 0x5140) & 0x80808080u);
+  o1 = __byte_perm(tlo, thi, m >> 16) | (__byte_perm(e, w, 0x7362) & 0x80808080u);
+}
+
+// Nonzero when some code of w has magnitude in [1, j], where c = (7 - j) in
+// every nibble: adding 7 to a 3-bit magnitude carries into the nibble's top
+// bit iff it is at least 1, adding 7 - j iff it exceeds j.  c = 0x77777777
+// (j = 0) gives zero.
+__device__ __forceinline__ uint32_t small_codes(uint32_t w, uint32_t c) {
+  const uint32_t m = w & 0x77777777u;
+  return (m + 0x77777777u) & ~(m + c) & 0x88888888u;
+}
+
+// The E4M3 byte of magnitude m under a block depends only on the block's
+// exponent relative to the row shift, delta = (scale - 127) - k.  A block
+// holding a nonzero code has delta <= 8 (its largest element is at most the
+// row's largest, exponent k + 7); at delta <= -13 every nonzero magnitude is
+// below half the smallest E4M3 subnormal, so all deltas under the table's
+// range give the same bytes as its first entry, and deltas above it only
+// occur for blocks whose codes are all zero.  The magnitudes that land below
+// the normal range are always 1..j for some j (the exponent grows with the
+// magnitude); the table keeps (7 - j) in every nibble.
+constexpr int kDeltaLo = -16, kDeltaN = 32;
+
+// Rows are spread over a persistent grid, one warp per row at a time.  Lane
+// l handles the 16-code halves l, l + 32, ... of the row (NPER of them).
+// Each warp double-buffers code rows in shared memory with cp.async: the
+// next row's codes (and, into registers, its scale bytes) are in flight while
+// the current row is encoded.  Rows longer than 8192 codes go to a plain
+// two-pass kernel over global memory.
+constexpr int kConvWarps = 8;
+constexpr int kConvRowBytes = 4096;
+constexpr int kConvSmem = kConvWarps * 2 * kConvRowBytes;
+constexpr int kConvMaxPer = kConvRowBytes / (8 * 32);  // 16 halves per lane
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+struct ConvTables {
+  uint2 mag[kDeltaN];      // E4M3 bytes of magnitudes 0..3 (x) and 4..7 (y)
+  uint32_t small[kDeltaN];  // (7 - j) per nibble, magnitudes 1..j below the normal range
+};
+
+__device__ __forceinline__ void build_tables(ConvTables& t) {
+  if (threadIdx.x < kDeltaN) {
+    uint32_t l = 0, h = 0, j = 0;
+    const int delta = kDeltaLo + (int)threadIdx.x;
+    for (uint32_t m = 0; m < 8; ++m) {
+      bool f = false;
+      const uint32_t byte = conv_nibble(m, delta, 0, &f);
+      if (m < 4) l |= byte << (8 * m);
+      else h |= byte << (8 * (m - 4));
+      if (f) j = m;
+    }
+    t.mag[threadIdx.x] = make_uint2(l, h);
+    t.small[threadIdx.x] = (7u - j) * 0x11111111u;
   }
+  __syncthreads();
+}
+
+// Row results: per-row status byte, power-of-two scale, global status word.
+__device__ __forceinline__ void finish_row(int64_t row, bool nan, bool low, int k, float* row_scale,
+                                           uint8_t* row_status, int32_t* status) {
+  const uint32_t st = nan ? 2u : (low ? 1u : 0u);
+  if (row_status) row_status[row] = (uint8_t)st;
+  float sc;
+  if (nan) sc = __uint_as_float(0x7FC00000u);
+  else if (k >= -126) sc = __uint_as_float((uint32_t)(k + 127) << 23);
+  else sc = __uint_as_float(1u << (k + 149));  // fp32 subnormal, exact
+  row_scale[row] = sc;
+  if (st == 2u) record_status(status, FP4MOE_ERR_NAN_SCALE, ST_NAN);
+  if (st == 1u) record_status(status, FP4MOE_ERR_INEXACT, ST_INEXACT);
+}
+
+// Row-wide reductions of pass 1.  top = max over halves of (class + scale)
+// for nonzero halves (0 when the row is all zero): the row's largest element
+// exponent is top - 129.  smin = least scale of a nonzero half (255 if none),
+// smax = largest scale byte (255 marks a NaN scale).
+struct RowStats {
+  uint32_t top = 0, smin = 255, smax = 0;
+  __device__ __forceinline__ void add(uint2 w, uint32_t sc) {
+    const uint32_t c = (uint32_t)half_class(w.x, w.y);
+    top = max(top, c ? c + sc : 0u);
+    smin = min(smin, c ? sc : 255u);
+    smax = max(smax, sc);
+  }
+  __device__ __forceinline__ void reduce() {
+    top = __reduce_max_sync(0xffffffffu, top);
+    smin = __reduce_min_sync(0xffffffffu, smin);
+    smax = __reduce_max_sync(0xffffffffu, smax);
+  }
+  // shift k = (largest element exponent) - 7
+  __device__ __forceinline__ int shift() const { return top ? (int)top - 136 : 0; }
+  // A nonzero code lands below the normal range only if its element exponent
+  // (at least smin - 128) is under k - 5.
+  __device__ __forceinline__ bool maybe_low() const { return top && (int)smin - 128 < shift() - 5; }
+};
+
+template <int NPER>
+__global__ void __launch_bounds__(32 * kConvWarps, 3) convert_kernel(const uint8_t* codes, const uint8_t* scales,
+                                                                     int64_t rows, int K, uint8_t* out,
+                                                                     float* row_scale, uint8_t* row_status,
+                                                                     int32_t* status) {
+  extern __shared__ __align__(16) uint8_t conv_smem[];
+  __shared__ ConvTables tab;
+  build_tables(tab);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * kConvWarps;
+  const int nhalf = K >> 4, nchunk = K >> 5;  // 8-byte halves and 16-byte chunks of a code row
+  const bool last_ok = lane + 32 * (NPER - 1) < nhalf;  // only the last half per lane can be past the row
+  int64_t row = (int64_t)blockIdx.x * kConvWarps + warp;
+
+  uint8_t* wbuf = conv_smem + warp * 2 * kConvRowBytes;
+  uint32_t cs[NPER], ns[NPER];
+  auto stage = [&](int64_t r, int b, uint32_t* sdst) {
+    const uint8_t* src = codes + r * (K >> 1);
+    const uint32_t dst = smem_u32(wbuf + b * kConvRowBytes);
+    for (int c = lane; c < nchunk; c += 32) cp_async16(dst + 16 * c, src + 16 * c);
+    const uint8_t* srow = scales + r * (K >> 5) + (lane >> 1);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
-  nan = __any_sync(0xffffffffu, nan);
-  const int k = emax == -1000 ? 0 : emax - 7;
-  uint4* orow = reinterpret_cast<uint4*>(out + row * K);
-  bool low = false;
-  for (int b = lane; b < nblk; b += 32) {
-    uint32_t o[8];
+    for (int i = 0; i < NPER; ++i)
+      if (i < NPER - 1 || last_ok) sdst[i] = __ldg(srow + 16 * i);
+  };
+  if (row < rows) stage(row, 0, cs);
+  cp_async_commit();
+  int buf = 0;
+  for (; row < rows; row += nwarps) {
+    const int64_t next = row + nwarps;
+    if (next < rows) stage(next, buf ^ 1, ns);
+    cp_async_commit();
+    cp_async_wait<1>();  // this row's group has landed (the next row's may still fly)
+    __syncwarp();
+    const uint2* cur = reinterpret_cast<const uint2*>(wbuf + buf * kConvRowBytes) + lane;
+    RowStats rs;
+#pragma unroll
+    for (int i = 0; i < NPER; ++i)
+      if (i < NPER - 1 || last_ok) rs.add(cur[32 * i], cs[i]);
+    rs.reduce();
+    const bool nan = rs.smax == 255u;
+    const int k = rs.shift();
+    uint4* orow = reinterpret_cast<uint4*>(out + row * K) + lane;
+    const int base = 127 + k + kDeltaLo;
+    uint32_t lowacc = 0;
     if (nan) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = 0;
+      for (int i = 0; i < NPER; ++i)
+        if (i < NPER - 1 || last_ok) orow[32 * i] = make_uint4(0u, 0u, 0u, 0u);
+    } else if (!rs.maybe_low()) {
+#pragma unroll
+      for (int i = 0; i < NPER; ++i)
+        if (i < NPER - 1 || last_ok) {
+          const uint2 w = cur[32 * i];
+          const uint2 t = tab.mag[min(max((int)cs[i] - base, 0), kDeltaN - 1)];
+          uint4 o;
+          conv8(w.x, t.x, t.y, o.x, o.y);
+          conv8(w.y, t.x, t.y, o.z, o.w);
+          orow[32 * i] = o;
+        }
     } else {
-      const uint4 w = __ldg(crow + b);
-      const int sb = (int)__ldg(srow + b) - 127;
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t lo = 0, hi = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) lo |= conv_nibble((ws[q] >> (4 * j)) & 15u, sb, k, &low) << (8 * j);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) hi |= conv_nibble((ws[q] >> (16 + 4 * j)) & 15u, sb, k, &low) << (8 * j);
-        o[2 * q] = lo;
-        o[2 * q + 1] = hi;
-      }
+      for (int i = 0; i < NPER; ++i)
+        if (i < NPER - 1 || last_ok) {
+          const uint2 w = cur[32 * i];
+          const int idx = min(max((int)cs[i] - base, 0), kDeltaN - 1);
+          const uint2 t = tab.mag[idx];
+          const uint32_t c = tab.small[idx];
+          lowacc |= small_codes(w.x, c) | small_codes(w.y, c);
+          uint4 o;
+          conv8(w.x, t.x, t.y, o.x, o.y);
+          conv8(w.y, t.x, t.y, o.z, o.w);
+          orow[32 * i] = o;
+        }
     }
-    orow[2 * b] = make_uint4(o[0], o[1], o[2], o[3]);
-    orow[2 * b + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    const bool low = __any_sync(0xffffffffu, lowacc != 0u);
+    if (lane == 0) finish_row(row, nan, low, k, row_scale, row_status, status);
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) cs[i] = ns[i];
+    buf ^= 1;
+    __syncwarp();  // every lane is done with this buffer before it is refilled
   }
-  low = __any_sync(0xffffffffu, low);
-  if (lane == 0) {
-    const uint32_t st = nan ? 2u : (low ? 1u : 0u);
-    if (row_status) row_status[row] = (uint8_t)st;
-    float sc;
-    if (nan) sc = __uint_as_float(0x7FC00000u);
-    else if (k >= -126) sc = __uint_as_float((uint32_t)(k + 127) << 23);
-    else sc = __uint_as_float(1u << (k + 149));  // fp32 subnormal, exact
-    row_scale[row] = sc;
-    if (st == 2u) record_status(status, FP4MOE_ERR_NAN_SCALE, ST_NAN);
-    if (st == 1u) record_status(status, FP4MOE_ERR_INEXACT, ST_INEXACT);
+  cp_async_wait<0>();
+}
+
+// Rows longer than the staging buffer: pass 1 and pass 2 both read global
+// memory.
+__global__ void __launch_bounds__(32 * kConvWarps) convert_long_kernel(const uint8_t* codes, const uint8_t* scales,
+                                                                       int64_t rows, int K, uint8_t* out,
+                                                                       float* row_scale, uint8_t* row_status,
+                                                                       int32_t* status) {
+  __shared__ ConvTables tab;
+  build_tables(tab);
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * kConvWarps;
+  const int nhalf = K >> 4;
+  for (int64_t row = (int64_t)blockIdx.x * kConvWarps + (threadIdx.x >> 5); row < rows; row += nwarps) {
+    const uint2* crow = reinterpret_cast<const uint2*>(codes + row * (K >> 1));
+    const uint8_t* srow = scales + row * (K >> 5);
+    RowStats rs;
+    for (int h = lane; h < nhalf; h += 32) rs.add(__ldg(crow + h), __ldg(srow + (h >> 1)));
+    rs.reduce();
+    const bool nan = rs.smax == 255u;
+    const int k = rs.shift();
+    const int base = 127 + k + kDeltaLo;
+    uint4* orow = reinterpret_cast<uint4*>(out + row * K);
+    uint32_t lowacc = 0;
+    for (int h = lane; h < nhalf; h += 32) {
+      uint4 o = make_uint4(0u, 0u, 0u, 0u);
+      if (!nan) {
+        const uint2 w = __ldg(crow + h);
+        const int idx = min(max((int)__ldg(srow + (h >> 1)) - base, 0), kDeltaN - 1);
+        const uint2 t = tab.mag[idx];
+        lowacc |= small_codes(w.x, tab.small[idx]) | small_codes(w.y, tab.small[idx]);
+        conv8(w.x, t.x, t.y, o.x, o.y);
+        conv8(w.y, t.x, t.y, o.z, o.w);
+      }
+      orow[h] = o;
+    }
+    const bool low = __any_sync(0xffffffffu, lowacc != 0u);
+    if (lane == 0) finish_row(row, nan, low, k, row_scale, row_status, status);
   }
+}
+
+using ConvKernel = void (*)(const uint8_t*, const uint8_t*, int64_t, int, uint8_t*, float*, uint8_t*, int32_t*);
+
+template <int... P>
+constexpr std::array<ConvKernel, sizeof...(P)> conv_kernels(std::integer_sequence<int, P...>) {
+  return {convert_kernel<P + 1>...};
 }
 
 inline unsigned blocks_for(int64_t n, int threads) { return (unsigned)((n + threads - 1) / threads); }
@@ -349,9 +532,27 @@ cudaError_t launch_pack_scales(const uint8_t* src, uint8_t* dst, int64_t n_mat, 
 cudaError_t launch_convert(const uint8_t* codes, const uint8_t* scales, int64_t rows, int K, uint8_t* out,
                            float* row_scale, uint8_t* row_status, int32_t* status, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  const int warps = 8;
-  convert_kernel<<<blocks_for(rows, warps), 32 * warps, 0, s>>>(codes, scales, rows, K, out, row_scale, row_status,
-                                                                status);
+  static const auto kernels = conv_kernels(std::make_integer_sequence<int, kConvMaxPer>{});
+  static int resident[64][kConvMaxPer + 1] = {};  // CTAs per SM, per device and kernel
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const int nper = ((K >> 4) + 31) / 32;
+  const bool staged = nper <= kConvMaxPer;
+  const ConvKernel kern = staged ? kernels[nper - 1] : convert_long_kernel;
+  const int slot = staged ? nper : 0;
+  const int smem = staged ? kConvSmem : 0;
+  if (!resident[dev][slot]) {
+    int n = 0;
+    cudaError_t e = staged ? cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                           : cudaSuccess;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32 * kConvWarps, smem);
+    if (e != cudaSuccess) return e;
+    resident[dev][slot] = n > 0 ? n : 1;
+  }
+  const int64_t grid =
+      std::min<int64_t>(blocks_for(rows, kConvWarps), (int64_t)device_sm_count() * resident[dev][slot]);
+  kern<<<(unsigned)grid, 32 * kConvWarps, smem, s>>>(codes, scales, rows, K, out, row_scale, row_status, status);
   return cudaGetLastError();
 }
 

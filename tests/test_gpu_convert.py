@@ -62,6 +62,23 @@ def test_random_rows(span):
         assert np.all(st == 0) and count == 0
 
 
+@pytest.mark.parametrize("K,n", [(32, 37), (96, 300), (480, 1001), (8192, 150), (8224, 90), (16384, 70)])
+def test_row_lengths(K, n):
+    """Row lengths from one block (odd scale-row widths, rows not a multiple
+    of the warps per CTA) to past the 8192 codes a warp stages in shared
+    memory, where the kernel switches to two passes over global memory."""
+    torch = torch_cuda()
+    ensure_built()
+    rng = np.random.default_rng(K + n)
+    codes, scales = _rows_with_span(rng, n, K, 12)
+    out, rs, st, code, count = _run(torch, codes, scales)
+    ro, rrs, rst = C.mxfp4_to_fp8_rowscale(codes, scales)
+    assert np.array_equal(st, rst)
+    assert np.array_equal(rs.view(np.uint32), rrs.view(np.uint32))
+    assert np.array_equal(out, ro)
+    assert count == int((rst != 0).sum())
+
+
 def test_full_size_skewed_workload():
     """All routed expert rows of the skewed workload: 384 experts x (4096 gate/up
     rows of K=7168 + 7168 down rows of K=2048) = 4,325,376 rows."""
