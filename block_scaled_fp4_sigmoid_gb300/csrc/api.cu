@@ -82,6 +82,17 @@ bool make_layout(const fp4moe_dims& d, Layout* L) {
   fp4moe_ws_layout& w = L->ws;
   w.n_tile = pick_n_tile(d);
   w.n_splits = pick_splits(d);
+  // the fused front end: K splits of at most 1024 router columns when that
+  // takes no more than 8 (one cluster per expert group), else of at most
+  // kFrontMaxKc; rows too long for 8 splits use the separate kernels
+  L->front_splits = 0;
+  for (int cap : {1024, kFrontMaxKc}) {
+    for (int s = 1; s <= 8 && !L->front_splits; ++s)
+      if ((d.H / 256) % s == 0 && d.H / s <= cap) L->front_splits = s;
+    if (L->front_splits) break;
+  }
+  L->front = !nv && d.T <= kFrontMaxT && L->front_splits > 0;
+  const int planes = w.n_splits;  // the front end keeps one plane of scores
   const int64_t slots_cap = R / w.n_tile + L->n_exp + 1;
   if (slots_cap * kSlotRows > INT32_MAX / 2) return false;
   w.rows_cap = (int32_t)(slots_cap * kSlotRows);
@@ -91,11 +102,12 @@ bool make_layout(const fp4moe_dims& d, Layout* L) {
     off = align_up(off + bytes);
     return o;
   };
+  // status and the per-chunk counters are adjacent: one memset clears both
   w.status = take(kStatusInts * 4);
-  w.logits = take((int64_t)w.n_splits * d.T * d.E * 4);
+  L->chunk_counts = take((int64_t)L->n_chunks * L->n_exp * 4);
+  w.logits = take((int64_t)planes * d.T * d.E * 4);
   w.topk_idx = take((int64_t)d.T * d.top_k * 4);
   w.topk_w = take((int64_t)d.T * d.top_k * 4);
-  L->chunk_counts = take((int64_t)L->n_chunks * L->n_exp * 4);
   L->plan = take(sizeof(Plan));
   w.expert_count = take((int64_t)L->n_exp * 4);
   w.expert_slot = take((int64_t)L->n_exp * 4);
@@ -113,7 +125,6 @@ bool make_layout(const fp4moe_dims& d, Layout* L) {
   w.gscale = take((int64_t)(2 + L->n_exp) * 4);
   L->amax = take((int64_t)(2 + L->n_exp) * 4);
   w.out_acc = take((int64_t)d.T * d.H * 4);
-  L->front = !nv && d.T <= kFrontMaxT;
   w.total_bytes = off;
   return true;
 }
@@ -267,7 +278,9 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
   };
 
   cudaError_t e = rec(0);
-  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, kStatusInts * 4, s);  // also clears the tickets
+  // status word (with the last-CTA tickets) and the per-chunk expert counters
+  const size_t clear_bytes = (size_t)(L.chunk_counts - L.ws.status) + (size_t)L.n_chunks * L.n_exp * 4;
+  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, clear_bytes, s);
   if (L.front) {
     // few tokens: router, top-k, plan, scatter and x quantisation in one launch
     FrontArgs f;
@@ -277,7 +290,7 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
     f.wr = w->w_router;
     f.bias = w->bias;
     f.partial = partial;
-    f.n_splits = L.ws.n_splits;
+    f.n_splits = L.front_splits;
     f.n_tile = n_tile;
     f.n_exp = L.n_exp;
     f.out_acc = acc;
@@ -298,7 +311,6 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
     if (e == cudaSuccess) e = launch_gather_quant(d, x, route_row, xq, xsf, amax, gscale, s);
     if (e == cudaSuccess) e = rec(4);
   } else {
-    if (e == cudaSuccess) e = cudaMemsetAsync(cc, 0, (size_t)L.n_chunks * L.n_exp * 4, s);
     if (e == cudaSuccess && nv) e = cudaMemsetAsync(amax, 0, (size_t)(2 + L.n_exp) * 4, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(acc, 0, (size_t)d.T * d.H * 4, s);
     if (e == cudaSuccess) e = launch_router_logits(x, w->w_router, partial, d.T, d.H, d.E, L.ws.n_splits, s);

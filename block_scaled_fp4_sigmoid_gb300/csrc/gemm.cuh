@@ -154,9 +154,10 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
     prefetch_tmap(&p.tmB);
     if (p.has_shared) prefetch_tmap(&p.tmA_sh);
   }
-  // everything above overlaps the previous kernel; the plan and the
-  // activations it wrote are read only after this point
-  pdl_wait();
+  // The plan (unit table, expert counts and slots) was written at least two
+  // kernels back: the previous kernel signals its dependents only after its
+  // own dependency wait, so the plan is complete here.  The activations of
+  // the previous kernel are read only after pdl_wait() below.
   const int total = *p.total_units;
   for (int i = threadIdx.x; i <= p.n_exp; i += blockDim.x) {
     s_start[i] = p.unit_start[i];
@@ -171,44 +172,97 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
   const uint32_t tmem = tmem_slot;
   volatile int* abort_v = &abort_flag;
 
+  // Weight side of one pipeline step (A tiles and their scale groups): it
+  // depends on nothing the previous kernel writes.
+  struct Step {
+    const CUtensorMap* tmA;
+    int ec, row0, row1, slot;
+    const uint8_t *sfa0, *sfa1, *sfb;
+  };
+  auto unit_step = [&](int u) {
+    int e, mt, slot, cnt;
+    decode_unit<N>(s_start, s_count, s_slot, p.n_exp, u, e, mt, slot, cnt);
+    const bool sh = e >= p.E;
+    Step st;
+    st.tmA = sh ? &p.tmA_sh : &p.tmA;
+    st.ec = sh ? e - p.E : e;
+    const uint8_t* sfw = sh ? p.shsf : p.wsf;
+    const int rt_per_e = p.rows_per_expert >> 7;
+    st.row0 = mt * 128;
+    st.row1 = p.I + mt * 128;  // up rows (gate/up only)
+    st.slot = slot;
+    st.sfa0 = sfw + ((int64_t)(st.ec * rt_per_e + (st.row0 >> 7)) * p.katoms_a) * 512;
+    st.sfa1 = sfw + ((int64_t)(st.ec * rt_per_e + (st.row1 >> 7)) * p.katoms_a) * 512;
+    st.sfb = p.bsf + ((int64_t)slot * p.katoms_b) * 512;
+    return st;
+  };
+  auto load_weights = [&](const Step& st, int kt, uint32_t base, uint32_t fb) {
+    tma_load_3d(base, st.tmA, fb, kt * 128, st.row0, st.ec);
+    if constexpr (GATEUP) tma_load_3d(base + C::kOffA1, st.tmA, fb, kt * 128, st.row1, st.ec);
+    bulk_load(base + C::kOffSFA0, st.sfa0 + kt * C::kSFBytes, C::kSFBytes, fb);
+    if constexpr (GATEUP) bulk_load(base + C::kOffSFA1, st.sfa1 + kt * C::kSFBytes, C::kSFBytes, fb);
+  };
+  auto load_acts = [&](const Step& st, int kt, uint32_t base, uint32_t fb) {
+    tma_load_2d(base + C::kOffB, &p.tmB, fb, kt * 128, st.slot * kSlotRows);
+    bulk_load(base + C::kOffSFB, st.sfb + kt * C::kSFBytes, C::kSFBytes, fb);
+  };
+
+  // The first pipeline stages start streaming weights before the wait, so
+  // they overlap the tail of the previous kernel.
+  int pre = 0;
+  if (warp == 0 && lane == 0) {
+    for (int u = blockIdx.x; u < total && pre < C::kStages; u += gridDim.x) {
+      const Step st = unit_step(u);
+      for (int kt = 0; kt < KT && pre < C::kStages; ++kt, ++pre) {
+        const uint32_t fb = smem_u32(&bar_full[pre]);
+        mbar_arrive_expect_tx(fb, C::kStage);  // stage is empty: first use
+        load_weights(st, kt, sbase + pre * C::kStage, fb);
+      }
+    }
+  }
+  pdl_wait();
+  pdl_trigger();  // the plan is complete, so the next kernel may launch now
+
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int stage = 0;
+      int stage = 0, step = 0;
       uint32_t phase = 0, armed = 0, armed_par = 0;
       for (int u = blockIdx.x; u < total && !*abort_v; u += gridDim.x) {
-        int e, mt, slot, cnt;
-        decode_unit<N>(s_start, s_count, s_slot, p.n_exp, u, e, mt, slot, cnt);
-        const bool sh = e >= p.E;
-        const CUtensorMap* tmA = sh ? &p.tmA_sh : &p.tmA;
-        const int ec = sh ? e - p.E : e;
-        const uint8_t* sfw = sh ? p.shsf : p.wsf;
-        const int rt_per_e = p.rows_per_expert >> 7;
-        const int row0 = mt * 128;
-        const int row1 = p.I + mt * 128;  // up rows (gate/up only)
-        const uint8_t* sfa0 = sfw + ((int64_t)(ec * rt_per_e + (row0 >> 7)) * p.katoms_a) * 512;
-        const uint8_t* sfa1 = sfw + ((int64_t)(ec * rt_per_e + (row1 >> 7)) * p.katoms_a) * 512;
-        const uint8_t* sfb = p.bsf + ((int64_t)slot * p.katoms_b) * 512;
+        const Step st = unit_step(u);
         bool ok = true;
-        for (int kt = 0; kt < KT; ++kt) {
+        for (int kt = 0; kt < KT; ++kt, ++step) {
           const uint32_t fb = smem_u32(&bar_full[stage]);
-          if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u)) { ok = false; break; }
           const uint32_t base = sbase + stage * C::kStage;
-          mbar_arrive_expect_tx(fb, C::kStage);
+          if (step >= pre) {
+            if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u)) { ok = false; break; }
+            mbar_arrive_expect_tx(fb, C::kStage);
+            load_weights(st, kt, base, fb);
+          }
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-          tma_load_3d(base, tmA, fb, kt * 128, row0, ec);
-          if constexpr (GATEUP) tma_load_3d(base + C::kOffA1, tmA, fb, kt * 128, row1, ec);
-          tma_load_2d(base + C::kOffB, &p.tmB, fb, kt * 128, slot * kSlotRows);
-          bulk_load(base + C::kOffSFA0, sfa0 + kt * C::kSFBytes, C::kSFBytes, fb);
-          if constexpr (GATEUP) bulk_load(base + C::kOffSFA1, sfa1 + kt * C::kSFBytes, C::kSFBytes, fb);
-          bulk_load(base + C::kOffSFB, sfb + kt * C::kSFBytes, C::kSFBytes, fb);
+          load_acts(st, kt, base, fb);
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) {
           *abort_v = 1;
           record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
           break;
+        }
+      }
+      // stages whose weights were requested before the wait but whose unit
+      // was not reached (abort) get their activation copies too, so that
+      // their barriers complete
+      if (step < pre) {
+        int s2 = 0;
+        for (int u = blockIdx.x; u < total && s2 < pre; u += gridDim.x) {
+          const Step st = unit_step(u);
+          for (int kt = 0; kt < KT && s2 < pre; ++kt, ++s2)
+            if (s2 >= step) {
+              load_acts(st, kt, sbase + s2 * C::kStage, smem_u32(&bar_full[s2]));
+              armed |= 1u << s2;
+              armed_par &= ~(1u << s2);  // first use: phase 0
+            }
         }
       }
       // every armed stage must have landed before the CTA exits
@@ -371,7 +425,6 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
     }
   }
 
-  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

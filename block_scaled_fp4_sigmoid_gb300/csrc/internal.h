@@ -32,6 +32,7 @@ struct Layout {
   int64_t row_e;         // int32 [rows_cap] expert of each row
   int64_t amax;          // uint32 [2 + n_exp] amax bits (x, spare, h per expert)
   bool front;            // few-token MXFP4 forward uses the fused front end
+  int front_splits;      // K splits of the front end's router GEMV (cluster size)
   int n_exp, n_chunks, n_route_per_tok;
 };
 
@@ -56,8 +57,8 @@ struct FrontArgs {
   const uint16_t *x, *wr;
   const float* bias;
   float* partial;
-  int n_splits, n_tile, n_exp;
-  float* out_acc;            // zeroed here
+  int n_splits, n_tile, n_exp;  // n_splits: K splits (cluster size, <= 8), H / n_splits <= kFrontMaxKc
+  float* out_acc;                // zeroed here
   int32_t* idx;
   float* w;
   int32_t *expert_count, *expert_slot, *gu_start, *dn_start;
@@ -67,6 +68,7 @@ struct FrontArgs {
   int32_t* ticket;  // zero on entry
 };
 constexpr int kFrontMaxT = 16;
+constexpr int kFrontMaxKc = 2048;  // router columns per split of the front end
 cudaError_t launch_decode_front(const FrontArgs& a, cudaStream_t s);
 
 cudaError_t launch_amax(const void* x, int x_is_fp32, int64_t n, uint32_t* amax_bits, cudaStream_t s);

@@ -187,10 +187,16 @@ __global__ void __launch_bounds__(128) router_mma_kernel(const uint16_t* __restr
 
 // ---------------------------------------------------------------- sigmoid + bias grouped top-k
 // One warp per token.  Scores live in shared memory (E <= 512).
+// Selection for one token from its scores in shared memory: sv = sigmoid
+// scores, cv = scores + bias (overwritten: unselected groups become -inf).
+// Group selection, then top-k over the corrected scores.  Lane j < k returns
+// the j-th chosen expert in *idx and its routing weight in *w (ties to the
+// lower group and expert index).
+__device__ __forceinline__ void topk_select(const float* sv, float* cv, int E, int k, int n_group, int topk_group,
+                                            float scaling, int renorm, int lane, int* idx, float* w);
+
 // Routes token t with one warp: sums the split-K partial logits, sigmoid,
-// bias, group selection, top-k.  sv / cv: E floats of shared memory for this
-// warp.  Lane j < k returns the j-th chosen expert in *idx and its routing
-// weight in *w (ties to the lower group and expert index).
+// bias, then topk_select.  sv / cv: E floats of shared memory for this warp.
 __device__ __forceinline__ void topk_token(const float* __restrict__ partial, int n_splits,
                                            const float* __restrict__ bias, int T, int t, int E, int k,
                                            int n_group, int topk_group, float scaling, int renorm,
@@ -221,6 +227,11 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ partial, in
     }
   }
   __syncwarp();
+  topk_select(sv, cv, E, k, n_group, topk_group, scaling, renorm, lane, idx, w);
+}
+
+__device__ __forceinline__ void topk_select(const float* sv, float* cv, int E, int k, int n_group, int topk_group,
+                                            float scaling, int renorm, int lane, int* idx, float* w) {
   // group selection: group score = sum of the two largest corrected scores
   uint32_t group_ok = 0xffffffffu;
   if (n_group > 1) {
@@ -251,25 +262,48 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ partial, in
     __syncwarp();
   }
   // top-k over corrected scores, ties to the lower expert index; each lane
-  // keeps its (at most 16) candidates in registers
+  // keeps its (at most 16) candidates in registers (absent or NaN: -inf,
+  // never chosen).  Per round: the lane's best by a pairwise tournament (ties
+  // keep the lower index), then the warp's largest score (order-preserving
+  // integer key, one warp reduction) and the lowest index holding it (a
+  // second reduction).
   float cr[16];
 #pragma unroll
-  for (int q = 0; q < 16; ++q) cr[q] = lane + 32 * q < E ? cv[lane + 32 * q] : -INFINITY;
+  for (int q = 0; q < 16; ++q) {
+    const float v = lane + 32 * q < E ? cv[lane + 32 * q] : -INFINITY;
+    cr[q] = v > -INFINITY ? v : -INFINITY;
+  }
   int my_idx = -1;
   float my_s = 0.f;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
+    float v8[8], v4[4], v2[2];
+    int q8[8], q4[4], q2[2];
 #pragma unroll
-    for (int q = 0; q < 16; ++q)  // ascending expert index within the lane: '>' keeps the lower on ties
-      if (cr[q] > bv) { bv = cr[q]; bi = lane + 32 * q; }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    for (int i = 0; i < 8; ++i) {
+      const bool r = cr[2 * i + 1] > cr[2 * i];
+      v8[i] = r ? cr[2 * i + 1] : cr[2 * i];
+      q8[i] = r ? 2 * i + 1 : 2 * i;
     }
-    if (bi >= E) bi = 0;  // only reachable with NaN scores (out of contract): keep the index in range
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const bool r = v8[2 * i + 1] > v8[2 * i];
+      v4[i] = r ? v8[2 * i + 1] : v8[2 * i];
+      q4[i] = r ? q8[2 * i + 1] : q8[2 * i];
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const bool r = v4[2 * i + 1] > v4[2 * i];
+      v2[i] = r ? v4[2 * i + 1] : v4[2 * i];
+      q2[i] = r ? q4[2 * i + 1] : q4[2 * i];
+    }
+    const bool r = v2[1] > v2[0];
+    const float bv = r ? v2[1] : v2[0];
+    const int li = bv > -INFINITY ? lane + 32 * (r ? q2[1] : q2[0]) : 0x7fffffff;
+    const uint32_t bits = __float_as_uint(bv);
+    const uint32_t key = li != 0x7fffffff ? ((bits & 0x80000000u) ? ~bits : (bits | 0x80000000u)) : 0u;
+    const uint32_t m = __reduce_max_sync(0xffffffffu, key);
+    int bi = __reduce_min_sync(0xffffffffu, key == m ? li : 0x7fffffff);
+    if (bi >= E) bi = 0;  // only reachable without k valid candidates (out of contract): keep the index in range
     if (lane == j) my_idx = bi;
     if ((bi & 31) == lane) {  // the owner drops the winner from its candidates
 #pragma unroll
@@ -401,18 +435,112 @@ __global__ void scatter_kernel(const int32_t* __restrict__ idx, const float* __r
 }
 
 // ---------------------------------------------------------------- fused front end for few tokens
-// Phase A (every CTA): one warp per (expert, K split) of the router GEMV and
-// grid-stride zeroing of the combine buffer.  The CTA that finishes last (a
-// ticket counter; no CTA ever waits for another) runs phase B: top-k per
-// token, expert counts and stable positions (each token routes to an expert
-// at most once, so a route's position is the number of earlier tokens routed
-// to the same expert), the plan, and the route -> row map.  The quantised
-// rows are then written by gather_quant_kernel.
+// Phase A: CTA (group of 16 experts, K split sp) stages the tokens' x
+// columns of its split in shared memory, and each warp forms the split's
+// partial logits of two experts (every lane issues all its router-weight
+// loads in one batch).  The n_splits CTAs of a group form one thread-block cluster; after
+// a cluster barrier the rank-0 CTA reads the others' partials from their
+// shared memory, sums them in split order, and stores the sigmoid scores.
+// All CTAs zero the combine buffer.  The rank-0 CTA that finishes last (a
+// ticket counter; no CTA ever waits for another outside its cluster) runs
+// phase B: top-k per token, expert counts and stable positions (each token
+// routes to an expert at most once, so a route's position is the number of
+// earlier tokens routed to the same expert), the plan, and the route -> row
+// map.  The quantised rows are then written by gather_quant_kernel.
 constexpr int kFrontThreads = 256;
 constexpr int kFrontWarps = kFrontThreads / 32;
+constexpr int kFrontExperts = 2 * kFrontWarps;  // experts per CTA: two per warp
+static_assert(kFrontExperts * kFrontMaxT == kFrontThreads, "one rank-0 thread per (expert, token)");
 
-__global__ void __launch_bounds__(kFrontThreads, 3) decode_front_kernel(FrontArgs a) {
-  __shared__ float s_sc[kFrontWarps][2][512];  // scores of the token a warp routes
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// fp32 at a shared-memory address of CTA `rank` of this cluster
+__device__ __forceinline__ float ld_dsmem(const float* p, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// Partial logits of experts e0 and e0 + 1 over this CTA's K split (nk <= NK
+// pieces of 256 columns, x staged in xs).  Lane t returns token t's sums.
+template <int TMAX, int NK>
+__device__ __forceinline__ float2 front_gemv(const FrontArgs& a, uint16_t* xs, int sp, int e0, int lane) {
+  const int T = a.d.T, H = a.d.H, E = a.d.E;
+  const int kc = H / a.n_splits, k0 = sp * kc, nk = kc / 256;
+  float acc0[TMAX], acc1[TMAX];
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t) acc0[t] = acc1[t] = 0.f;
+  // rows past E load a valid row and are never stored
+  const uint16_t* w0 = a.wr + (int64_t)min(e0, E - 1) * H + k0 + 8 * lane;
+  const uint16_t* w1 = a.wr + (int64_t)min(e0 + 1, E - 1) * H + k0 + 8 * lane;
+  uint4 wv0[NK], wv1[NK];
+#pragma unroll
+  for (int i = 0; i < NK; ++i)
+    if (i < nk) {
+      wv0[i] = __ldg(reinterpret_cast<const uint4*>(w0 + 256 * i));
+      wv1[i] = __ldg(reinterpret_cast<const uint4*>(w1 + 256 * i));
+    }
+  const int per_row = kc / 8;  // 16-byte pieces of one token's columns
+  for (int v = threadIdx.x; v < T * per_row; v += kFrontThreads) {
+    const int t = v / per_row, c = v - t * per_row;
+    reinterpret_cast<uint4*>(xs + (int64_t)t * kc)[c] = __ldg(reinterpret_cast<const uint4*>(a.x + (int64_t)t * H + k0) + c);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < NK; ++i) {
+    if (i >= nk) break;
+    const uint32_t u0[4] = {wv0[i].x, wv0[i].y, wv0[i].z, wv0[i].w};
+    const uint32_t u1[4] = {wv1[i].x, wv1[i].y, wv1[i].z, wv1[i].w};
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+      if (t < T) {
+        const uint4 xv = reinterpret_cast<const uint4*>(xs + (int64_t)t * kc + 256 * i)[lane];
+        const uint32_t xu[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float xa = __uint_as_float(xu[j] << 16), xb = __uint_as_float(xu[j] & 0xFFFF0000u);
+          acc0[t] = fmaf(xa, __uint_as_float(u0[j] << 16), acc0[t]);
+          acc0[t] = fmaf(xb, __uint_as_float(u0[j] & 0xFFFF0000u), acc0[t]);
+          acc1[t] = fmaf(xa, __uint_as_float(u1[j] << 16), acc1[t]);
+          acc1[t] = fmaf(xb, __uint_as_float(u1[j] & 0xFFFF0000u), acc1[t]);
+        }
+      }
+    }
+  }
+  float2 mine = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t) {
+    float v0 = acc0[t], v1 = acc1[t];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      v0 += __shfl_xor_sync(0xffffffffu, v0, o);
+      v1 += __shfl_xor_sync(0xffffffffu, v1, o);
+    }
+    if (lane == t) mine = make_float2(v0, v1);
+  }
+  return mine;
+}
+
+template <int TMAX>
+__device__ __forceinline__ float2 front_gemv_any(const FrontArgs& a, uint16_t* xs, int sp, int e0, int lane) {
+  const int nk = a.d.H / a.n_splits / 256;
+  if (nk <= 2) return front_gemv<TMAX, 2>(a, xs, sp, e0, lane) ;
+  if (nk <= 4) return front_gemv<TMAX, 4>(a, xs, sp, e0, lane);
+  return front_gemv<TMAX, kFrontMaxKc / 256>(a, xs, sp, e0, lane);
+}
+
+__global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArgs a) {
+  extern __shared__ __align__(16) uint16_t front_xs[];  // [T][kc] bf16 of this CTA's split
+  __shared__ __align__(16) float s_sc[kFrontWarps][2][512];  // scores of the token a warp routes
+  __shared__ float s_part[kFrontExperts][kFrontMaxT];        // this split's partial logits
   __shared__ int s_last;
   __shared__ int32_t s_idx[kFrontMaxT][16];
   __shared__ float s_w[kFrontMaxT][16];
@@ -422,21 +550,35 @@ __global__ void __launch_bounds__(kFrontThreads, 3) decode_front_kernel(FrontArg
   const fp4moe_dims& d = a.d;
   const int T = d.T, H = d.H, E = d.E, k = d.top_k;
   const int tid = threadIdx.x, lane = tid & 31, wib = tid >> 5;
-  const int warp = (blockIdx.x * blockDim.x + tid) >> 5;
   const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + tid;
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
 
   pdl_trigger();  // the next kernel may launch and wait for this one
   // ---- phase A
-  if (warp < E * a.n_splits) {
-    if (T <= 8) gemv_warp<8>(a.x, a.wr, a.partial, T, H, E, a.n_splits, warp, lane);
-    else gemv_warp<kFrontMaxT>(a.x, a.wr, a.partial, T, H, E, a.n_splits, warp, lane);
+  const int sp = (int)cluster_rank();  // the cluster is one expert group, rank = K split
+  const int e0 = (blockIdx.x / a.n_splits) * kFrontExperts + 2 * wib;  // this warp: experts e0, e0 + 1
+  const float2 part = T <= 8 ? front_gemv_any<8>(a, front_xs, sp, e0, lane)
+                             : front_gemv_any<kFrontMaxT>(a, front_xs, sp, e0, lane);
+  if (lane < T) {
+    s_part[2 * wib][lane] = part.x;
+    s_part[2 * wib + 1][lane] = part.y;
   }
   for (int64_t i = gtid; i < (int64_t)T * H / 4; i += nthr)
     reinterpret_cast<float4*>(a.out_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  cluster_sync();  // every split's partials are in its CTA's shared memory
+  if (sp == 0) {  // thread (expert slot, token)
+    const int j = tid / kFrontMaxT, t = tid % kFrontMaxT, e = (blockIdx.x / a.n_splits) * kFrontExperts + j;
+    if (e < E && t < T) {
+      float l = 0.f;
+      for (int r = 0; r < a.n_splits; ++r) l += ld_dsmem(&s_part[j][t], (uint32_t)r);
+      a.partial[(int64_t)t * E + e] = 1.0f / (1.0f + expf(-l));  // sigmoid scores [T, E]
+    }
+  }
+  cluster_sync();  // the other CTAs' shared memory stays valid until rank 0 has read it
+  if (sp != 0) return;
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(a.ticket, 1) == (int)gridDim.x - 1;
+  if (tid == 0) s_last = atomicAdd(a.ticket, 1) == (int)(gridDim.x / a.n_splits) - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
@@ -444,10 +586,27 @@ __global__ void __launch_bounds__(kFrontThreads, 3) decode_front_kernel(FrontArg
   // ---- phase B (one CTA)
   const int n_exp = a.n_exp, rpt = k + d.n_shared;
   for (int t = wib; t < T; t += kFrontWarps) {
+    float* sv = s_sc[wib][0];
+    float* cv = s_sc[wib][1];
+    float sg[16], bv[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int ee = lane + 32 * q;
+      sg[q] = ee < E ? __ldcg(a.partial + (int64_t)t * E + ee) : 0.f;
+      bv[q] = ee < E ? __ldg(a.bias + ee) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int ee = lane + 32 * q;
+      if (ee < E) {
+        sv[ee] = sg[q];
+        cv[ee] = sg[q] + bv[q];
+      }
+    }
+    __syncwarp();
     int id;
     float wt;
-    topk_token(a.partial, a.n_splits, a.bias, T, t, E, k, d.n_group, d.topk_group, d.routed_scaling,
-               d.renormalize, nullptr, s_sc[wib][0], s_sc[wib][1], lane, &id, &wt);
+    topk_select(sv, cv, E, k, d.n_group, d.topk_group, d.routed_scaling, d.renormalize, lane, &id, &wt);
     if (lane < k) {
       s_idx[t][lane] = id;
       s_w[t][lane] = wt;
@@ -569,10 +728,31 @@ cudaError_t launch_scatter(const fp4moe_dims& d, const int32_t* idx, const float
 }
 
 cudaError_t launch_decode_front(const FrontArgs& a, cudaStream_t s) {
-  const int warps = a.d.E * a.n_splits;
-  const unsigned blocks = (unsigned)((warps * 32 + kFrontThreads - 1) / kFrontThreads);
-  decode_front_kernel<<<blocks, kFrontThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  const int kc = a.d.H / a.n_splits;
+  if (a.d.T > kFrontMaxT || kc > kFrontMaxKc || kc % 256 != 0 || a.n_splits > 8) return cudaErrorInvalidValue;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(decode_front_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kFrontMaxT * kFrontMaxKc * 2);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(((a.d.E + kFrontExperts - 1) / kFrontExperts) * a.n_splits));
+  cfg.blockDim = dim3(kFrontThreads);
+  cfg.dynamicSmemBytes = (size_t)a.d.T * kc * 2;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;  // one cluster per expert group: its K splits
+  attr[0].val.clusterDim.x = (unsigned)a.n_splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_front_kernel, a);
 }
 
 }  // namespace fp4moe

@@ -103,7 +103,9 @@ typedef struct {
  * n_tile rows, each tile at the start of its own 128-row slot. */
 typedef struct {
   int64_t status;       /* int32[16] status word                            */
-  int64_t logits;       /* fp32 [n_splits, T, E] partial router logits      */
+  int64_t logits;       /* fp32 [n_splits, T, E] partial router logits (the
+                         * few-token MXFP4 path may use fewer or more
+                         * splits; the region holds them)                  */
   int64_t topk_idx;     /* int32 [T, top_k], in descending corrected score  */
   int64_t topk_w;       /* fp32 [T, top_k]                                  */
   int64_t expert_count; /* int32 [E + n_shared] routes per expert           */

@@ -40,6 +40,10 @@ SMALL = {
     "tiny": _cfg("tiny"),
     "tiny_T1": _cfg("tiny", T=1),
     "ragged_shared": _cfg("tiny", name="ragged_shared", T=37, H=512, I=256, E=16, top_k=4, n_shared=1),
+    # few-token fused front end: a ragged expert group (24 = 16 + 8), three
+    # 256-column pieces per split, a shared expert; then a 3-CTA cluster
+    "front_T16_shared": _cfg("tiny", name="front_T16_shared", T=16, H=768, I=256, E=24, top_k=4, n_shared=1),
+    "front_cluster3": _cfg("tiny", name="front_cluster3", T=9, H=2304, I=256, E=40, top_k=3),
     "wide_padK": _cfg("tiny", name="wide_padK", T=300, H=1024, I=384, E=8, top_k=2, routed_scaling=2.827),
     "nv_grouped": _cfg("deepseek_nvfp4", name="nv_grouped", T=64, H=512, I=256, E=32, top_k=4, n_group=4,
                        topk_group=2),
