@@ -92,8 +92,9 @@ __global__ void quantize_rows_kernel(const void* x, int x_is_fp32, int64_t rows,
 }
 
 // ---------------------------------------------------------------- forward: gather + quantise x
-// One thread per (route, 32 values of H): quantises x[token] into the route's
-// padded row of xq, with the scales in the tiled layout.
+// One thread per (token, 32 values of H): quantises the block once and
+// stores it into the padded row of each of the token's routes, with the
+// scales in the tiled layout.
 __global__ void gather_quant_kernel(const uint16_t* x, int T, int H, int routes_per_tok,
                                     const int32_t* route_row, uint8_t* xq, uint8_t* xsf, int nv,
                                     const uint32_t* amax_x, float* g_out) {
@@ -101,31 +102,31 @@ __global__ void gather_quant_kernel(const uint16_t* x, int T, int H, int routes_
   pdl_trigger();
   const int per_row = H >> 5;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t n_routes = (int64_t)T * routes_per_tok;
-  if (tid >= n_routes * per_row) return;
-  const int64_t rt = tid / per_row;
-  const int b = (int)(tid - rt * per_row);
-  const int64_t t = rt / routes_per_tok;
-  const int64_t row = route_row[rt];
+  if (tid >= (int64_t)T * per_row) return;
+  const int64_t t = tid / per_row;
+  const int b = (int)(tid - t * per_row);
   float v[32];
   load32(x, 0, t * H + 32 * b, v);
-  uint32_t p[4];
-  uint4* dst = reinterpret_cast<uint4*>(xq + row * (H >> 1) + 16 * b);
+  uint32_t p[4], s0, s1 = 0;
   const int64_t katoms = katoms_padded(H, nv != 0);
   if (!nv) {
-    uint32_t s;
-    mx_quant32(v, p, &s);
-    *dst = make_uint4(p[0], p[1], p[2], p[3]);
-    xsf[sf_tiled_offset(row, b, katoms)] = (uint8_t)s;
+    mx_quant32(v, p, &s0);
   } else {
     const float g = nv_global(__uint_as_float(*amax_x));
     if (tid == 0 && g_out) *g_out = g;
-    uint32_t s0, s1;
     nv_quant16(v, g, p, &s0);
     nv_quant16(v + 16, g, p + 2, &s1);
-    *dst = make_uint4(p[0], p[1], p[2], p[3]);
-    xsf[sf_tiled_offset(row, 2 * b, katoms)] = (uint8_t)s0;
-    xsf[sf_tiled_offset(row, 2 * b + 1, katoms)] = (uint8_t)s1;
+  }
+  const uint4 q = make_uint4(p[0], p[1], p[2], p[3]);
+  for (int j = 0; j < routes_per_tok; ++j) {
+    const int64_t row = route_row[t * routes_per_tok + j];
+    *reinterpret_cast<uint4*>(xq + row * (H >> 1) + 16 * b) = q;
+    if (!nv) {
+      xsf[sf_tiled_offset(row, b, katoms)] = (uint8_t)s0;
+    } else {
+      xsf[sf_tiled_offset(row, 2 * b, katoms)] = (uint8_t)s0;
+      xsf[sf_tiled_offset(row, 2 * b + 1, katoms)] = (uint8_t)s1;
+    }
   }
 }
 
@@ -497,7 +498,7 @@ cudaError_t launch_quantize_rows(const void* x, int x_is_fp32, int64_t rows, int
 cudaError_t launch_gather_quant(const fp4moe_dims& d, const uint16_t* x, const int32_t* route_row, uint8_t* xq,
                                 uint8_t* xsf, const uint32_t* amax_x, float* g_out, cudaStream_t s) {
   const int rpt = d.top_k + d.n_shared;
-  const int64_t n = (int64_t)d.T * rpt * (d.H >> 5);
+  const int64_t n = (int64_t)d.T * (d.H >> 5);
   if (n == 0) return cudaSuccess;
   return launch_pdl(gather_quant_kernel, dim3(blocks_for(n, 256)), dim3(256), 0, s, x, d.T, d.H, rpt, route_row,
                     xq, xsf, (int)(d.fmt == FP4MOE_NVFP4), amax_x, g_out);
