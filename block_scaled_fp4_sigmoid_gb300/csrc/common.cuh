@@ -38,6 +38,12 @@ __device__ __forceinline__ uint64_t globaltimer() {
 // A kernel launched with programmatic stream serialisation may start before
 // its predecessor finishes; it must call pdl_wait() before touching anything
 // the predecessor writes.  pdl_trigger() lets the successor launch early.
+// Adds four floats to four consecutive fp32 words (16-byte aligned) as one
+// reduction.
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

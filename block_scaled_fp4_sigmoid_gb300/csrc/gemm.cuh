@@ -395,7 +395,11 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
           if (lane == 0) atomicMax(p.amax_h + e, __float_as_uint(amax));
         }
       } else {
-        const int h_idx = mt * 128 + 32 * q + lane;
+        // routing weight times y added into the fp32 combine buffer: the
+        // warp's 32 rows x 32 token columns go through shared memory so that
+        // each lane adds 4 consecutive outputs of one token per 16-byte
+        // reduction (lane l: rows 4 (l % 8) .. + 3 of columns l / 8 + 4 k)
+        const int h0 = mt * 128 + 32 * q + 4 * (lane & 7);
         float sc = 1.f;
         if constexpr (NV) sc = __fmul_rn(__ldg(p.gb + e), __ldg(p.gw + e));
         for (int c0 = 0; c0 < cnt; c0 += 32) {
@@ -410,12 +414,19 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
             wk = __ldg(p.row_w + row0 + c0 + lane) * sc;
           }
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (j >= jn) break;
+          for (int j = 0; j < 32; ++j) tile[j][lane] = y[j];
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int j = (lane >> 3) + 4 * k;
             const int t = __shfl_sync(0xffffffffu, tk, j);
             const float w = __shfl_sync(0xffffffffu, wk, j);
-            atomicAdd(p.out_acc + (int64_t)t * p.H + h_idx, y[j] * w);
+            if (j < jn) {
+              const float* src = &tile[j][4 * (lane & 7)];
+              red_add_v4(p.out_acc + (int64_t)t * p.H + h0, src[0] * w, src[1] * w, src[2] * w, src[3] * w);
+            }
           }
+          __syncwarp();
         }
       }
       tc_fence_before();
