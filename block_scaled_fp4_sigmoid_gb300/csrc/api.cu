@@ -46,13 +46,14 @@ bool dims_ok(const fp4moe_dims& d) {
 
 int pick_n_tile(const fp4moe_dims& d) {
   const double avg = (double)d.T * d.top_k / d.E;
-  // 32 and 64 keep two accumulator sets in tensor memory (epilogue overlaps
-  // the next unit's MMAs); 128 fits only one for the gate/up pair, but each
-  // MMA does twice the work of a 64-token one, which wins once experts see
-  // 64 tokens on average
+  // Every size keeps two accumulator sets in tensor memory (the epilogue of
+  // one unit overlaps the next unit's MMAs): 2 x (gate + up) x 112 columns
+  // plus one K tile's scale factors is the most that fits in 512.  Wider
+  // tiles do more work per MMA, which wins once experts see 64 tokens on
+  // average.
   if (avg <= 24.0) return 32;
   if (avg < 64.0) return 64;
-  return 128;
+  return 112;
 }
 
 // Router split-K factor: a divisor of H / 256 that gives the logits kernel

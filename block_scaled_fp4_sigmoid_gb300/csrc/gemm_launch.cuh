@@ -66,8 +66,8 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
     case 65: return launch_gemm_t<32, GATEUP, true>(p, grid, s);
     case 128: return launch_gemm_t<64, GATEUP, false>(p, grid, s);
     case 129: return launch_gemm_t<64, GATEUP, true>(p, grid, s);
-    case 256: return launch_gemm_t<128, GATEUP, false>(p, grid, s);
-    case 257: return launch_gemm_t<128, GATEUP, true>(p, grid, s);
+    case 224: return launch_gemm_t<112, GATEUP, false>(p, grid, s);
+    case 225: return launch_gemm_t<112, GATEUP, true>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
