@@ -402,9 +402,10 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     achieved = gu_bytes / (gu_max * 1e-3) / 1e9
     traffic = profiled_traffic(cfg.name)
     clocks = clk.summary()
-    # front (or router, top-k, plan, scatter), gather, gate/up, down, finalise
+    # few tokens: front end (routing, plan, x quantisation), gate/up, down,
+    # finalise; else router, top-k, plan, scatter, gather, gate/up, down, finalise
     if cfg.fmt == "mxfp4":
-        launches_per_step = 5 if cfg.T <= 16 else 8
+        launches_per_step = 4 if cfg.T <= 16 else 8
     else:
         launches_per_step = 10
     conversion = time_conversion(layer, peaks, stream) if args.conversion else None

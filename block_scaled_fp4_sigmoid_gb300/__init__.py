@@ -50,7 +50,7 @@ class WsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in
                 ("status", "logits", "topk_idx", "topk_w", "expert_count", "expert_slot", "route_row",
                  "row_tok", "row_w", "xq", "xsf", "hq", "hsf", "h32", "gscale", "out_acc", "total_bytes")] + \
-               [(n, ctypes.c_int32) for n in ("n_splits", "n_tile", "rows_cap", "reserved")]
+               [(n, ctypes.c_int32) for n in ("n_splits", "n_tile", "rows_cap", "x_by_token")]
 
 
 class Debug(ctypes.Structure):

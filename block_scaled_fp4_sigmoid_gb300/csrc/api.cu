@@ -96,6 +96,7 @@ bool make_layout(const fp4moe_dims& d, Layout* L) {
     if (L->front_splits) break;
   }
   L->front = !nv && d.T <= kFrontMaxT && L->front_splits > 0;
+  w.x_by_token = L->front ? 1 : 0;
   const int planes = w.n_splits;  // the front end keeps one plane of scores
   const int64_t slots_cap = R / w.n_tile + L->n_exp + 1;
   if (slots_cap * kSlotRows > INT32_MAX / 2) return false;
@@ -310,10 +311,11 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
     f.row_e = row_e;
     f.row_w = row_w;
     f.ticket = status + ST_TICKET_FRONT;
+    f.xq = xq;
+    f.xsf = xsf;
+    f.tok_mask = reinterpret_cast<uint32_t*>(cc);  // the per-chunk counters are not used here
     if (e == cudaSuccess) e = launch_decode_front(f, s);
-    for (int i = 1; i <= 3 && e == cudaSuccess; ++i) e = rec(i);
-    if (e == cudaSuccess) e = launch_gather_quant(d, x, route_row, xq, xsf, amax, gscale, s);
-    if (e == cudaSuccess) e = rec(4);
+    for (int i = 1; i <= 4 && e == cudaSuccess; ++i) e = rec(i);
   } else {
     if (e == cudaSuccess && nv) e = cudaMemsetAsync(amax, 0, (size_t)(2 + L.n_exp) * 4, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(acc, 0, (size_t)d.T * d.H * 4, s);
@@ -360,6 +362,8 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
     g.h32 = h32;
     g.amax_h = amax + 2;
     g.h_dbg = dbg ? dbg->h_pre : nullptr;
+    g.tok_mask = L.front ? reinterpret_cast<const uint32_t*>(cc) : nullptr;
+    g.plan_from_prev = L.front;  // the front end, launched just before, wrote the plan
     e = launch_gateup(g, s);
   }
   if (e == cudaSuccess && nv) e = launch_h_quant_nv_routes(d, h32, route_row, row_e, amax + 2, gscale + 2, hq, hsf, s);

@@ -48,11 +48,16 @@ struct KParams {
   const int32_t *expert_count, *expert_slot, *unit_start, *total_units;
   const int32_t* row_tok;
   const float* row_w;
+  // gate/up with few tokens: B is the token rows 0..T-1 for every unit (x
+  // quantised once per token) and column t is kept when bit t of
+  // tok_mask[expert] is set; null: B is the unit's token tile
+  const uint32_t* tok_mask;
   uint8_t *hq, *hsf;
   float *h32, *h_dbg, *out_acc;
   uint32_t* amax_h;
   int32_t* status;
-  int E, n_exp, H, I, K, rows_per_expert, m_tiles, katoms_a, katoms_b, katoms_h, has_shared;
+  int E, n_exp, H, I, K, rows_per_expert, m_tiles, katoms_a, katoms_b, katoms_h, has_shared, T;
+  int plan_early;  // the plan was written at least two kernels back (see the kernel)
 };
 
 template <int N, bool GATEUP, bool NV>
@@ -124,6 +129,7 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
   __shared__ __align__(8) uint64_t bar_tfull[2], bar_tempty[2], bar_done;
   __shared__ float epi_tile[4][32][33];  // per epilogue warp: 32 lanes x 32 columns, transposed
   __shared__ int32_t s_start[kMaxExperts], s_count[kMaxExperts], s_slot[kMaxExperts];
+  __shared__ uint32_t s_mask[kMaxExperts];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -154,16 +160,19 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
     prefetch_tmap(&p.tmB);
     if (p.has_shared) prefetch_tmap(&p.tmA_sh);
   }
-  // The plan (unit table, expert counts and slots) was written at least two
-  // kernels back: the previous kernel signals its dependents only after its
-  // own dependency wait, so the plan is complete here.  The activations of
-  // the previous kernel are read only after pdl_wait() below.
+  // The plan (unit table, expert counts, slots, token masks): when it was
+  // written at least two kernels back (plan_early) it is complete here, as
+  // the previous kernel signals its dependents only after its own dependency
+  // wait; when the previous kernel wrote it, it is read after the wait.  The
+  // previous kernel's activations are always read after the wait.
+  if (!p.plan_early) pdl_wait();
   const int total = *p.total_units;
   for (int i = threadIdx.x; i <= p.n_exp; i += blockDim.x) {
     s_start[i] = p.unit_start[i];
     if (i < p.n_exp) {
       s_count[i] = p.expert_count[i];
       s_slot[i] = p.expert_slot[i];
+      if (p.tok_mask) s_mask[i] = p.tok_mask[i];
     }
   }
   tc_fence_before();
@@ -190,10 +199,10 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
     const int rt_per_e = p.rows_per_expert >> 7;
     st.row0 = mt * 128;
     st.row1 = p.I + mt * 128;  // up rows (gate/up only)
-    st.slot = slot;
+    st.slot = p.tok_mask ? 0 : slot;  // slot of the B rows
     st.sfa0 = sfw + ((int64_t)(st.ec * rt_per_e + (st.row0 >> 7)) * p.katoms_a) * 512;
     st.sfa1 = sfw + ((int64_t)(st.ec * rt_per_e + (st.row1 >> 7)) * p.katoms_a) * 512;
-    st.sfb = p.bsf + ((int64_t)slot * p.katoms_b) * 512;
+    st.sfb = p.bsf + ((int64_t)st.slot * p.katoms_b) * 512;
     return st;
   };
   auto load_weights = [&](const Step& st, int kt, uint32_t base, uint32_t fb) {
@@ -220,7 +229,7 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
       }
     }
   }
-  pdl_wait();
+  if (p.plan_early) pdl_wait();
   pdl_trigger();  // the plan is complete, so the next kernel may launch now
 
   if (warp == 0) {
@@ -344,7 +353,9 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
         float sc = 1.f;
         if constexpr (NV) sc = __fmul_rn(__ldg(p.gb), __ldg(p.gw + e));
         float amax = 0.f;
-        for (int c0 = 0; c0 < cnt; c0 += 32) {
+        const uint32_t mask = p.tok_mask ? s_mask[e] : 0u;
+        const int ncol = p.tok_mask ? p.T : cnt;  // accumulator columns holding tokens
+        for (int c0 = 0; c0 < ncol; c0 += 32) {
           float g[32], uu[32];
           tc_ld32(ta + c0, g);
           tc_ld32(ta + N + c0, uu);
@@ -362,8 +373,11 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
           }
           __syncwarp();
           const int n = c0 + lane;
-          if (n < cnt) {
-            const int64_t row = row0 + n;
+          // column n -> row of the unit's tile: n itself, or (token columns)
+          // the token's rank among the expert's tokens
+          const bool keep = p.tok_mask ? (n < ncol && ((mask >> n) & 1u)) : n < cnt;
+          if (keep) {
+            const int64_t row = row0 + (p.tok_mask ? __popc(mask & ((1u << n) - 1u)) : n);
             float v[32];
 #pragma unroll
             for (int r = 0; r < 32; ++r) v[r] = tile[lane][r];

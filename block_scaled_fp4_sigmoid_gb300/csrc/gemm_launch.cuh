@@ -41,6 +41,9 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   p.unit_start = a.unit_start;
   p.total_units = GATEUP ? &a.plan->gu_units : &a.plan->dn_units;
   p.row_tok = a.row_tok;
+  p.tok_mask = GATEUP ? a.tok_mask : nullptr;
+  p.plan_early = a.plan_from_prev ? 0 : 1;
+  p.T = d.T;
   p.row_w = a.row_w;
   p.hq = a.hq;
   p.hsf = a.hsf;

@@ -66,6 +66,8 @@ struct FrontArgs {
   int32_t *route_row, *row_tok, *row_e;
   float* row_w;
   int32_t* ticket;  // zero on entry
+  uint8_t *xq, *xsf;     // quantised x: token rows (slot 0 of the permuted layout)
+  uint32_t* tok_mask;    // [n_exp] bit t: token t routes to the expert
 };
 constexpr int kFrontMaxT = 16;
 constexpr int kFrontMaxKc = 2048;  // router columns per split of the front end
@@ -104,6 +106,8 @@ struct GemmArgs {
   const Plan* plan;
   const int32_t *row_tok;
   const float *row_w;
+  const uint32_t *tok_mask;        // gate/up, few tokens: B = token rows, column t kept per mask bit
+  bool plan_from_prev;             // the kernel launched just before wrote the plan
   const float *g_b;                // NVFP4: tensor scale of B (x: one; h: per expert)
   // outputs
   uint8_t *hq, *hsf;               // gate/up, MXFP4

@@ -438,15 +438,17 @@ __global__ void scatter_kernel(const int32_t* __restrict__ idx, const float* __r
 // Phase A: CTA (group of 16 experts, K split sp) stages the tokens' x
 // columns of its split in shared memory, and each warp forms the split's
 // partial logits of two experts (every lane issues all its router-weight
-// loads in one batch).  The n_splits CTAs of a group form one thread-block cluster; after
-// a cluster barrier the rank-0 CTA reads the others' partials from their
-// shared memory, sums them in split order, and stores the sigmoid scores.
-// All CTAs zero the combine buffer.  The rank-0 CTA that finishes last (a
-// ticket counter; no CTA ever waits for another outside its cluster) runs
-// phase B: top-k per token, expert counts and stable positions (each token
-// routes to an expert at most once, so a route's position is the number of
-// earlier tokens routed to the same expert), the plan, and the route -> row
-// map.  The quantised rows are then written by gather_quant_kernel.
+// loads in one batch).  The n_splits CTAs of a group form one thread-block
+// cluster; after a cluster barrier the rank-0 CTA reads the others' partials
+// from their shared memory, sums them in split order, and stores the sigmoid
+// scores.  All CTAs zero the combine buffer and quantise x to MXFP4 once per
+// token (token t is row t of the layout; the gate/up GEMM reads every token
+// and keeps the routed ones).  The rank-0 CTA that finishes last (a ticket
+// counter; no CTA ever waits for another outside its cluster) runs phase B:
+// top-k per token, expert counts, token masks and stable positions (each
+// token routes to an expert at most once, so a route's position is the
+// number of earlier tokens routed to the same expert), the plan, and the
+// route -> row map.
 constexpr int kFrontThreads = 256;
 constexpr int kFrontWarps = kFrontThreads / 32;
 constexpr int kFrontExperts = 2 * kFrontWarps;  // experts per CTA: two per warp
@@ -546,12 +548,11 @@ __global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArg
   __shared__ float s_w[kFrontMaxT][16];
   __shared__ int32_t s_count[520];
   __shared__ int32_t s_slot[520];
+  __shared__ uint32_t s_mask[520];
   __shared__ int32_t s_wsum[kFrontWarps];
   const fp4moe_dims& d = a.d;
   const int T = d.T, H = d.H, E = d.E, k = d.top_k;
   const int tid = threadIdx.x, lane = tid & 31, wib = tid >> 5;
-  const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + tid;
-  const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
 
   pdl_trigger();  // the next kernel may launch and wait for this one
   // ---- phase A
@@ -563,8 +564,6 @@ __global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArg
     s_part[2 * wib][lane] = part.x;
     s_part[2 * wib + 1][lane] = part.y;
   }
-  for (int64_t i = gtid; i < (int64_t)T * H / 4; i += nthr)
-    reinterpret_cast<float4*>(a.out_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   cluster_sync();  // every split's partials are in its CTA's shared memory
   if (sp == 0) {  // thread (expert slot, token)
     const int j = tid / kFrontMaxT, t = tid % kFrontMaxT, e = (blockIdx.x / a.n_splits) * kFrontExperts + j;
@@ -575,7 +574,39 @@ __global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArg
     }
   }
   cluster_sync();  // the other CTAs' shared memory stays valid until rank 0 has read it
-  if (sp != 0) return;
+  // Off the critical path (the ranks other than 0 are done; with one split
+  // the rank-0 CTAs do it): zero the combine buffer and quantise x to MXFP4
+  // once per token, token t in row t of the layout.  The next kernel reads
+  // both only after this grid has completed.
+  if (sp != 0 || a.n_splits == 1) {
+    const int64_t helpers = a.n_splits == 1 ? gridDim.x : gridDim.x - gridDim.x / a.n_splits;
+    const int64_t hid = a.n_splits == 1 ? blockIdx.x : blockIdx.x - blockIdx.x / a.n_splits - 1;
+    const int64_t hthr = hid * kFrontThreads + tid, hn = helpers * kFrontThreads;
+    for (int64_t i = hthr; i < (int64_t)T * H / 4; i += hn)
+      reinterpret_cast<float4*>(a.out_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int per_row = H >> 5;
+    const int64_t katoms = katoms_padded(H, false);
+    for (int64_t i = hthr; i < (int64_t)T * per_row; i += hn) {
+      const int t = (int)(i / per_row), b = (int)(i - (int64_t)t * per_row);
+      const uint4* src = reinterpret_cast<const uint4*>(a.x + (int64_t)t * H + 32 * b);
+      float v[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w = __ldg(src + q);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          v[8 * q + 2 * r] = __uint_as_float(ws[r] << 16);
+          v[8 * q + 2 * r + 1] = __uint_as_float(ws[r] & 0xFFFF0000u);
+        }
+      }
+      uint32_t pk[4], sb;
+      mx_quant32(v, pk, &sb);
+      *reinterpret_cast<uint4*>(a.xq + (int64_t)t * (H >> 1) + 16 * b) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      a.xsf[sf_tiled_offset(t, b, katoms)] = (uint8_t)sb;
+    }
+    if (sp != 0) return;
+  }
   __threadfence();
   __syncthreads();
   if (tid == 0) s_last = atomicAdd(a.ticket, 1) == (int)(gridDim.x / a.n_splits) - 1;
@@ -615,10 +646,18 @@ __global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArg
     }
     __syncwarp();
   }
-  for (int e = tid; e < n_exp; e += blockDim.x) s_count[e] = e >= E ? T : 0;
+  for (int e = tid; e < n_exp; e += blockDim.x) {
+    s_count[e] = e >= E ? T : 0;
+    s_mask[e] = e >= E ? (1u << T) - 1u : 0u;  // T <= 16
+  }
   __syncthreads();
-  for (int r = tid; r < T * k; r += blockDim.x) atomicAdd(&s_count[s_idx[r / k][r % k]], 1);
+  for (int r = tid; r < T * k; r += blockDim.x) {
+    const int e = s_idx[r / k][r % k];
+    atomicAdd(&s_count[e], 1);
+    atomicOr(&s_mask[e], 1u << (r / k));  // token mask of the expert
+  }
   __syncthreads();
+  for (int e = tid; e < n_exp; e += blockDim.x) a.tok_mask[e] = s_mask[e];
   // plan: exclusive scan of tiles over experts; thread j owns experts 3j..3j+2
   const int gm = d.I / 128, dm = H / 128;
   int tl[3], my = 0;

@@ -124,7 +124,10 @@ typedef struct {
   int32_t n_splits;     /* router split-K factor                            */
   int32_t n_tile;       /* tokens per GEMM tile                             */
   int32_t rows_cap;     /* rows of the padded permuted layout               */
-  int32_t reserved;
+  int32_t x_by_token;   /* 1: xq / xsf rows are token rows (few-token MXFP4
+                         * path: x quantised once, the gate/up GEMM reads
+                         * every token and keeps the routed ones); 0: route
+                         * rows of the padded permuted layout               */
 } fp4moe_ws_layout;
 
 /* Optional instrumentation for fp4moe_forward.

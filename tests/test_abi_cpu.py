@@ -43,6 +43,8 @@ def test_workspace_sizes(lib, name):
     R = cfg.T * (cfg.top_k + cfg.n_shared)
     assert L.rows_cap >= 128 * (R // L.n_tile + 1)
     assert cfg.H // 256 % L.n_splits == 0
+    # few-token MXFP4 forwards quantise x once per token (token rows)
+    assert L.x_by_token == int(cfg.fmt == "mxfp4" and cfg.T <= 16)
 
 
 @pytest.mark.parametrize("bad", [dict(T=0), dict(H=200), dict(I=100), dict(E=0), dict(top_k=0), dict(n_shared=2),

@@ -90,12 +90,14 @@ class GpuRun:
         self.rows = self.route_row.reshape(-1)
         nv = cfg.fmt == "nvfp4"
         self.nv = nv
+        # quantised x sits in the route rows, or (few-token path) in token rows
+        xrows = np.repeat(np.arange(T), rpt) if L.x_by_token else self.rows
         xq = ws[L.xq:L.xq + L.rows_cap * cfg.H // 2].view(L.rows_cap, cfg.H // 2)
-        self.xq = xq[torch.from_numpy(self.rows).long().cuda()].cpu().numpy().reshape(T, rpt, cfg.H // 2)
+        self.xq = xq[torch.from_numpy(xrows).long().cuda()].cpu().numpy().reshape(T, rpt, cfg.H // 2)
         blk = 16 if nv else 32
         slots = L.rows_cap // 128
         xsf = ws[L.xsf:L.xsf + slots * katoms_padded(cfg.H, nv) * 512].cpu().numpy()
-        self.xs = read_tiled_scales(xsf, self.rows, cfg.H // blk, katoms_padded(cfg.H, nv)).reshape(T, rpt, -1)
+        self.xs = read_tiled_scales(xsf, xrows, cfg.H // blk, katoms_padded(cfg.H, nv)).reshape(T, rpt, -1)
         hq = ws[L.hq:L.hq + L.rows_cap * cfg.I // 2].view(L.rows_cap, cfg.I // 2)
         self.hq = hq[torch.from_numpy(self.rows).long().cuda()].cpu().numpy().reshape(T, rpt, cfg.I // 2)
         hsf = ws[L.hsf:L.hsf + slots * katoms_padded(cfg.I, nv) * 512].cpu().numpy()
