@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
   struct Step {
     const CUtensorMap* tmA;
     int ec, row0, row1, slot;
+    bool once;  // the expert has one token tile: no other unit reads these weight tiles
     const uint8_t *sfa0, *sfa1, *sfb;
   };
   auto unit_step = [&](int u) {
@@ -200,16 +201,29 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
     st.row0 = mt * 128;
     st.row1 = p.I + mt * 128;  // up rows (gate/up only)
     st.slot = p.tok_mask ? 0 : slot;  // slot of the B rows
+    st.once = s_count[e] <= N;
     st.sfa0 = sfw + ((int64_t)(st.ec * rt_per_e + (st.row0 >> 7)) * p.katoms_a) * 512;
     st.sfa1 = sfw + ((int64_t)(st.ec * rt_per_e + (st.row1 >> 7)) * p.katoms_a) * 512;
     st.sfb = p.bsf + ((int64_t)st.slot * p.katoms_b) * 512;
     return st;
   };
+  // Weight tiles read by one unit only stream with an evict-first L2 policy
+  // (measured: a 128-row-box weight stream goes from 5.0 to 5.7 TB/s); tiles
+  // shared by the units of several token tiles keep the default policy so
+  // that those units find them in L2.
+  const uint64_t pol_once = l2_evict_first();
   auto load_weights = [&](const Step& st, int kt, uint32_t base, uint32_t fb) {
-    tma_load_3d(base, st.tmA, fb, kt * 128, st.row0, st.ec);
-    if constexpr (GATEUP) tma_load_3d(base + C::kOffA1, st.tmA, fb, kt * 128, st.row1, st.ec);
-    bulk_load(base + C::kOffSFA0, st.sfa0 + kt * C::kSFBytes, C::kSFBytes, fb);
-    if constexpr (GATEUP) bulk_load(base + C::kOffSFA1, st.sfa1 + kt * C::kSFBytes, C::kSFBytes, fb);
+    if (st.once) {
+      tma_load_3d_hint(base, st.tmA, fb, kt * 128, st.row0, st.ec, pol_once);
+      if constexpr (GATEUP) tma_load_3d_hint(base + C::kOffA1, st.tmA, fb, kt * 128, st.row1, st.ec, pol_once);
+      bulk_load_hint(base + C::kOffSFA0, st.sfa0 + kt * C::kSFBytes, C::kSFBytes, fb, pol_once);
+      if constexpr (GATEUP) bulk_load_hint(base + C::kOffSFA1, st.sfa1 + kt * C::kSFBytes, C::kSFBytes, fb, pol_once);
+    } else {
+      tma_load_3d(base, st.tmA, fb, kt * 128, st.row0, st.ec);
+      if constexpr (GATEUP) tma_load_3d(base + C::kOffA1, st.tmA, fb, kt * 128, st.row1, st.ec);
+      bulk_load(base + C::kOffSFA0, st.sfa0 + kt * C::kSFBytes, C::kSFBytes, fb);
+      if constexpr (GATEUP) bulk_load(base + C::kOffSFA1, st.sfa1 + kt * C::kSFBytes, C::kSFBytes, fb);
+    }
   };
   auto load_acts = [&](const Step& st, int kt, uint32_t base, uint32_t fb) {
     tma_load_2d(base + C::kOffB, &p.tmB, fb, kt * 128, st.slot * kSlotRows);
