@@ -64,9 +64,16 @@ int pick_splits(const fp4moe_dims& d) {
   if (d.T <= 16) {
     units = d.E;             // warps; each should issue all its weight loads in one batch
     want = 16 * 152;
-  } else {
-    units = (int64_t)((d.T + 127) / 128) * ((d.E + 63) / 64);  // CTAs
-    want = 2 * 152;
+  } else {  // tensor-core router: one CTA per (128 tokens, expert tile, split), at most 8 splits
+    units = (int64_t)((d.T + 127) / 128) * ((d.E + 255) / 256);
+    want = 152;
+    int best = 1;
+    for (int s = 1; s <= kt && s <= 8; ++s)
+      if (kt % s == 0) {
+        best = s;
+        if (units * s >= want) return s;
+      }
+    return best;
   }
   for (int s = 1; s <= kt; ++s)
     if (kt % s == 0 && units * s >= want) return s;
@@ -205,7 +212,9 @@ fp4moe_status fp4moe_route(const fp4moe_dims* dims, const uint16_t* x, const uin
   float* partial = reinterpret_cast<float*>(base + L.ws.logits);
   int32_t* cc = reinterpret_cast<int32_t*>(base + L.chunk_counts);
   cudaError_t e = cudaMemsetAsync(cc, 0, (size_t)L.n_chunks * L.n_exp * 4, s);
-  if (e == cudaSuccess) e = launch_router_logits(x, w_router, partial, d.T, d.H, d.E, L.ws.n_splits, s);
+  if (e == cudaSuccess)
+    e = launch_router_logits(x, w_router, partial, d.T, d.H, d.E, L.ws.n_splits,
+                             reinterpret_cast<int32_t*>(base + L.ws.status), s);
   if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, bias, topk_idx, topk_w, logits_out, cc, L.n_exp, s);
   return cuda_status(e);
 }
@@ -319,7 +328,7 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
   } else {
     if (e == cudaSuccess && nv) e = cudaMemsetAsync(amax, 0, (size_t)(2 + L.n_exp) * 4, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(acc, 0, (size_t)d.T * d.H * 4, s);
-    if (e == cudaSuccess) e = launch_router_logits(x, w->w_router, partial, d.T, d.H, d.E, L.ws.n_splits, s);
+    if (e == cudaSuccess) e = launch_router_logits(x, w->w_router, partial, d.T, d.H, d.E, L.ws.n_splits, status, s);
     if (e == cudaSuccess) e = rec(1);
     if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, nullptr, cc, L.n_exp, s);
     if (e == cudaSuccess) e = rec(2);

@@ -40,7 +40,11 @@ bool make_layout(const fp4moe_dims& d, Layout* L);
 
 // ------------------------------------------------------------- launchers
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* wr, float* partial, int T, int H, int E,
-                                 int n_splits, cudaStream_t s);
+                                 int n_splits, int32_t* status, cudaStream_t s);
+// tcgen05 bf16 router GEMM (T > 16): tiles of 128 tokens x router_tc_n(E) experts
+cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* wr, float* partial, int T, int H, int E, int n_splits,
+                             int32_t* status, cudaStream_t s);
+int router_tc_n(int E);
 cudaError_t launch_topk(const fp4moe_dims& d, const float* partial, int n_splits, const float* bias,
                         int32_t* idx, float* w, float* logits_out, int32_t* chunk_counts, int n_exp,
                         cudaStream_t s);

@@ -77,7 +77,7 @@ extern "C" fp4moe_status fp4moe_route_noalloc(const fp4moe_dims* dims, const uin
   float* partial = static_cast<float*>(base);
   int32_t* cc = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(base) + counts_off);
   cudaError_t e = cudaMemsetAsync(cc, 0, counts_bytes, s);  // counts accumulate atomically
-  if (e == cudaSuccess) e = launch_router_logits(x, w_router, partial, d.T, d.H, d.E, L.ws.n_splits, s);
+  if (e == cudaSuccess) e = launch_router_logits(x, w_router, partial, d.T, d.H, d.E, L.ws.n_splits, nullptr, s);
   if (e == cudaSuccess)
     e = launch_topk(d, partial, L.ws.n_splits, bias, topk_idx, topk_w, logits_out, cc, L.n_exp, s);
   return e == cudaSuccess ? FP4MOE_OK : FP4MOE_ERR_CUDA;

@@ -64,127 +64,6 @@ __global__ void router_gemv_kernel(const uint16_t* __restrict__ x, const uint16_
   gemv_warp<TMAX>(x, wr, partial, T, H, E, n_splits, warp, threadIdx.x & 31);
 }
 
-// ---------------------------------------------------------------- router logits, many tokens
-// bf16 tensor-core GEMM (mma.sync m16n8k16, fp32 accumulation) with a
-// three-stage cp.async pipeline.  CTA tile 128 tokens x 64 experts x 32 K,
-// four warps of 32 x 64.  Split-K partials go to partial[split].
-constexpr int RBM = 128, RBN = 64, RBK = 32, RST = 3, RPAD = 8;
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__global__ void __launch_bounds__(128) router_mma_kernel(const uint16_t* __restrict__ x,
-                                                         const uint16_t* __restrict__ wr,
-                                                         float* __restrict__ partial, int T, int H, int E,
-                                                         int kc) {
-  __shared__ __align__(16) uint16_t sA[RST][RBM][RBK + RPAD];
-  __shared__ __align__(16) uint16_t sB[RST][RBN][RBK + RPAD];
-  const int tm = blockIdx.x * RBM, tn = blockIdx.y * RBN, sp = blockIdx.z;
-  const int k0 = sp * kc;
-  const int nk = kc / RBK;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  auto load_stage = [&](int st, int kt) {
-    const int kb = k0 + kt * RBK;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {  // A: 128 rows x 4 chunks of 16 bytes
-      const int c = tid + i * 128;
-      const int r = c >> 2, q = c & 3;
-      const int gr = tm + r;
-      const bool ok = gr < T;
-      cp_async16(smem_u32(&sA[st][r][q * 8]), x + (int64_t)(ok ? gr : 0) * H + kb + q * 8, ok);
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {  // B: 64 rows x 4 chunks
-      const int c = tid + i * 128;
-      const int r = c >> 2, q = c & 3;
-      const int gr = tn + r;
-      const bool ok = gr < E;
-      cp_async16(smem_u32(&sB[st][r][q * 8]), wr + (int64_t)(ok ? gr : 0) * H + kb + q * 8, ok);
-    }
-  };
-
-  float acc[2][8][4];
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) acc[i][j][q] = 0.f;
-
-#pragma unroll
-  for (int st = 0; st < RST - 1; ++st) {
-    if (st < nk) load_stage(st, st);
-    cp_commit();
-  }
-  for (int kt = 0; kt < nk; ++kt) {
-    cp_wait<RST - 2>();
-    __syncthreads();
-    const int nxt = kt + RST - 1;
-    if (nxt < nk) load_stage(nxt % RST, nxt);
-    cp_commit();
-    const int st = kt % RST;
-#pragma unroll
-    for (int kk = 0; kk < RBK; kk += 16) {
-      uint32_t af[2][4];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int r = warp * 32 + i * 16 + (lane & 15);
-        const int c = kk + ((lane >> 4) << 3);
-        ldsm_x4(smem_u32(&sA[st][r][c]), af[i][0], af[i][1], af[i][2], af[i][3]);
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {  // pairs of n8 tiles
-        const int n = j * 16 + (lane & 7) + ((lane >> 4) << 3);
-        const int c = kk + (((lane >> 3) & 1) << 3);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(smem_u32(&sB[st][n][c]), b0, b1, b2, b3);
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          mma_bf16(acc[i][2 * j], af[i], b0, b1);
-          mma_bf16(acc[i][2 * j + 1], af[i], b2, b3);
-        }
-      }
-    }
-  }
-  cp_wait<0>();
-  float* dst = partial + (int64_t)sp * T * E;
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int r0 = tm + warp * 32 + i * 16 + (lane >> 2);
-      const int c0 = tn + j * 8 + (lane & 3) * 2;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = r0 + 8 * h;
-        if (r < T) {
-          if (c0 < E) dst[(int64_t)r * E + c0] = acc[i][j][2 * h];
-          if (c0 + 1 < E) dst[(int64_t)r * E + c0 + 1] = acc[i][j][2 * h + 1];
-        }
-      }
-    }
-}
-
 // ---------------------------------------------------------------- sigmoid + bias grouped top-k
 // One warp per token.  Scores live in shared memory (E <= 512).
 // Selection for one token from its scores in shared memory: sv = sigmoid
@@ -726,18 +605,16 @@ __global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArg
 }  // namespace
 
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* wr, float* partial, int T, int H, int E,
-                                 int n_splits, cudaStream_t s) {
+                                 int n_splits, int32_t* status, cudaStream_t s) {
   if (T <= 16) {
     const int warps = E * n_splits;
     const int threads = 256;
     const unsigned blocks = (unsigned)((warps * 32 + threads - 1) / threads);
     if (T <= 8) router_gemv_kernel<8><<<blocks, threads, 0, s>>>(x, wr, partial, T, H, E, n_splits);
     else router_gemv_kernel<16><<<blocks, threads, 0, s>>>(x, wr, partial, T, H, E, n_splits);
-  } else {
-    dim3 grid((T + RBM - 1) / RBM, (E + RBN - 1) / RBN, n_splits);
-    router_mma_kernel<<<grid, 128, 0, s>>>(x, wr, partial, T, H, E, H / n_splits);
+    return cudaGetLastError();
   }
-  return cudaGetLastError();
+  return launch_router_tc(x, wr, partial, T, H, E, n_splits, status, s);
 }
 
 cudaError_t launch_topk(const fp4moe_dims& d, const float* partial, int n_splits, const float* bias, int32_t* idx,
