@@ -586,9 +586,7 @@ __global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArg
     if (j < k) {
       e = s_idx[t][j];
       wt = s_w[t][j];
-      pos = 0;
-      for (int t2 = 0; t2 < t; ++t2)
-        for (int j2 = 0; j2 < k; ++j2) pos += s_idx[t2][j2] == e;
+      pos = __popc(s_mask[e] & ((1u << t) - 1u));  // earlier tokens routed to e
     } else {
       e = E + (j - k);
       wt = 1.0f;
