@@ -104,6 +104,9 @@ bool make_layout(const fp4moe_dims& d, Layout* L) {
   }
   L->front = !nv && d.T <= kFrontMaxT && L->front_splits > 0;
   w.x_by_token = L->front ? 1 : 0;
+  // few tokens: one 16-token tile holds every token (the gate/up B operand)
+  // and every expert's routes; half the B bytes and MMA columns of 32
+  if (L->front) w.n_tile = 16;
   const int planes = w.n_splits;  // the front end keeps one plane of scores
   const int64_t slots_cap = R / w.n_tile + L->n_exp + 1;
   if (slots_cap * kSlotRows > INT32_MAX / 2) return false;

@@ -9,7 +9,7 @@
 // with fp32 accumulators in tensor memory.
 //
 // Operand roles ("swap AB"): A = 128 weight rows (M = 128), B = up to N
-// tokens of one expert (N = 32 / 64 / 112), both K-major.  A work unit is
+// tokens of one expert (N = 16 / 32 / 64 / 112), both K-major.  A work unit is
 // (expert, 128-row weight tile, token tile); units of one expert are laid
 // out weight-tile-major so concurrent CTAs share each weight tile through L2.
 //

@@ -65,6 +65,7 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   p.has_shared = a.sh != nullptr;
   const int grid = a.num_sms > 0 ? a.num_sms : 1;
   switch (a.n_tile * 2 + (a.nv ? 1 : 0)) {
+    case 32: return launch_gemm_t<16, GATEUP, false>(p, grid, s);  // few-token path (MXFP4)
     case 64: return launch_gemm_t<32, GATEUP, false>(p, grid, s);
     case 65: return launch_gemm_t<32, GATEUP, true>(p, grid, s);
     case 128: return launch_gemm_t<64, GATEUP, false>(p, grid, s);
