@@ -79,13 +79,19 @@ struct GemmCfg {
   static constexpr int kStages = (kBudget / kStage) > 8 ? 8 : (kBudget / kStage);
   static constexpr int kSmem = kStages * kStage + 1024;
   static constexpr int kAccCols = kA * N;                           // one accumulator set
-  static constexpr int kSfCols = (kA + 1) * kAtoms * 4;             // scale factors of one K tile
+  // One MMA-issuing thread per A operand (gate/up: two, in warps 1 and 6):
+  // a thread issues a tcgen05 instruction only every ~50 cycles, so one
+  // thread cannot keep the tensor pipe busy with 112-token MMAs.  Each issuer
+  // copies its own B scale factors.
+  static constexpr int kIssuers = kA;
+  static constexpr int kThreads = 192 + 32 * (kIssuers - 1);
+  static constexpr int kSfCols = (kA + kIssuers) * kAtoms * 4;      // scale factors of one K tile
   // two accumulator sets when they fit: the epilogue of one unit then
   // overlaps the MMAs of the next
   static constexpr int kAccStages = (2 * kAccCols + kSfCols <= 512) ? 2 : 1;
   static constexpr int kSfaCol = kAccStages * kAccCols;
-  static constexpr int kSfbCol = kSfaCol + kA * kAtoms * 4;
-  static constexpr int kCols = kSfbCol + kAtoms * 4;
+  static constexpr int kSfbCol = kSfaCol + kA * kAtoms * 4;         // issuer i's B scales at + i * kAtoms * 4
+  static constexpr int kCols = kSfaCol + kSfCols;
   static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
   static_assert(kCols <= 512, "tensor memory");
   static_assert(kStage % 1024 == 0, "stage alignment");
@@ -121,7 +127,7 @@ __device__ __forceinline__ void decode_unit(const int32_t* s_start, const int32_
 }
 
 template <int N, bool GATEUP, bool NV>
-__global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant__ KParams p) {
+__global__ void __launch_bounds__(GATEUP ? 224 : 192, 1) moe_gemm_kernel(const __grid_constant__ KParams p) {
   using C = GemmCfg<N, GATEUP, NV>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[C::kStages];
@@ -138,16 +144,17 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
 
   const int KT = (p.K + 255) / 256;
 
+  static_assert(C::kThreads == (GATEUP ? 224 : 192), "launch bounds");
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
-      mbar_init(smem_u32(&bar_empty[s]), 1);
+      mbar_init(smem_u32(&bar_empty[s]), C::kIssuers);  // every issuer releases the stage
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(smem_u32(&bar_tfull[a]), 1);
+      mbar_init(smem_u32(&bar_tfull[a]), C::kIssuers);
       mbar_init(smem_u32(&bar_tempty[a]), 4);
     }
-    mbar_init(smem_u32(&bar_done), 1);
+    mbar_init(smem_u32(&bar_done), C::kIssuers);
     abort_flag = 0;
     fence_barrier_init();
   }
@@ -292,28 +299,29 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
       for (int s = 0; s < C::kStages; ++s)
         if ((armed >> s) & 1u) (void)mbar_wait(smem_u32(&bar_full[s]), (armed_par >> s) & 1u);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 6) {
+    // ------------------------------------------------------------ MMA issuers
+    // issuer mi (warp 1: gate or the only operand; warp 6: up) drives the
+    // MMAs of A operand mi into its own accumulator
     if (lane == 0) {
-      const uint32_t t_sfa0 = tmem + C::kSfaCol;
-      const uint32_t t_sfa1 = t_sfa0 + C::kAtoms * 4;
-      const uint32_t t_sfb = tmem + C::kSfbCol;
+      const int mi = warp == 1 ? 0 : 1;
+      const uint32_t t_sfa = tmem + C::kSfaCol + mi * C::kAtoms * 4;
+      const uint32_t t_sfb = tmem + C::kSfbCol + mi * C::kAtoms * 4;
+      const uint32_t off_a = mi ? C::kOffA1 : 0u, off_sfa = mi ? C::kOffSFA1 : C::kOffSFA0;
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       int as = 0;  // accumulator set of this unit
       for (int u = blockIdx.x; u < total && !*abort_v; u += gridDim.x) {
         bool ok = mbar_wait(smem_u32(&bar_tempty[as]), acc_phase ^ 1u);
         tc_fence_after();
-        const uint32_t t_acc0 = tmem + as * C::kAccCols;
-        const uint32_t t_acc1 = t_acc0 + N;
+        const uint32_t t_acc = tmem + as * C::kAccCols + mi * N;
         for (int kt = 0; ok && kt < KT; ++kt) {
           if (!mbar_wait(smem_u32(&bar_full[stage]), phase)) { ok = false; break; }
           tc_fence_after();
           const uint32_t base = sbase + stage * C::kStage;
 #pragma unroll
           for (int a = 0; a < C::kAtoms; ++a) {
-            tc_cp_sf(t_sfa0 + 4 * a, desc_sf(base + C::kOffSFA0 + 512 * a));
-            if constexpr (GATEUP) tc_cp_sf(t_sfa1 + 4 * a, desc_sf(base + C::kOffSFA1 + 512 * a));
+            tc_cp_sf(t_sfa + 4 * a, desc_sf(base + off_sfa + 512 * a));
             tc_cp_sf(t_sfb + 4 * a, desc_sf(base + C::kOffSFB + 512 * a));
           }
 #pragma unroll
@@ -321,13 +329,9 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
             const int atom = NV ? j : (j >> 1);
             const uint32_t sfid = NV ? 0u : (uint32_t)(j & 1) * 2u;
             const uint32_t idesc = idesc_fp4(N, NV, sfid, sfid);
-            const uint64_t bdesc = desc_sw128(base + C::kOffB + 32 * j);
             const uint32_t accum = (kt | j) ? 1u : 0u;
-            tc_mma_fp4<NV>(t_acc0, desc_sw128(base + 32 * j), bdesc, idesc, t_sfa0 + 4 * atom, t_sfb + 4 * atom,
-                           accum);
-            if constexpr (GATEUP)
-              tc_mma_fp4<NV>(t_acc1, desc_sw128(base + C::kOffA1 + 32 * j), bdesc, idesc, t_sfa1 + 4 * atom,
-                             t_sfb + 4 * atom, accum);
+            tc_mma_fp4<NV>(t_acc, desc_sw128(base + off_a + 32 * j), desc_sw128(base + C::kOffB + 32 * j), idesc,
+                           t_sfa + 4 * atom, t_sfb + 4 * atom, accum);
           }
           tc_commit(smem_u32(&bar_empty[stage]));
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -485,7 +489,7 @@ cudaError_t launch_gemm_t(const KParams& p, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  return launch_pdl(k, dim3(grid), dim3(192), C::kSmem, s, p);
+  return launch_pdl(k, dim3(grid), dim3(C::kThreads), C::kSmem, s, p);
 }
 
 }  // namespace fp4moe
