@@ -78,19 +78,22 @@ struct GemmCfg {
   static constexpr int kBudget = 232448 - 1024 - 24576;
   static constexpr int kStages = (kBudget / kStage) > 8 ? 8 : (kBudget / kStage);
   static constexpr int kSmem = kStages * kStage + 1024;
-  static constexpr int kAccCols = kA * N;                           // one accumulator set
-  // One MMA-issuing thread per A operand (gate/up: two, in warps 1 and 6):
-  // a thread issues a tcgen05 instruction only every ~50 cycles, so one
-  // thread cannot keep the tensor pipe busy with 112-token MMAs.  Each issuer
-  // copies its own B scale factors.
-  static constexpr int kIssuers = kA;
-  static constexpr int kThreads = 192 + 32 * (kIssuers - 1);
-  static constexpr int kSfCols = (kA + kIssuers) * kAtoms * 4;      // scale factors of one K tile
+  // Two MMA-issuing threads (warps 1 and 6): a thread issues a tcgen05
+  // instruction only every ~50 cycles, so one thread cannot keep the tensor
+  // pipe busy with 112-token MMAs.  Gate/up: issuer i drives A operand i
+  // (gate, up).  Down (one A operand): issuer i takes the K tiles kt with
+  // kt % 2 == i into its own accumulator; the epilogue adds the two.  Each
+  // issuer copies its own A and B scale factors.
+  static constexpr int kIssuers = 2;
+  static constexpr bool kKSplit = !GATEUP;
+  static constexpr int kThreads = 224;
+  static constexpr int kAccCols = 2 * N;                            // one accumulator set: two N-column blocks
+  static constexpr int kSfCols = kIssuers * 2 * kAtoms * 4;         // scale factors of one K tile
   // two accumulator sets when they fit: the epilogue of one unit then
   // overlaps the MMAs of the next
   static constexpr int kAccStages = (2 * kAccCols + kSfCols <= 512) ? 2 : 1;
   static constexpr int kSfaCol = kAccStages * kAccCols;
-  static constexpr int kSfbCol = kSfaCol + kA * kAtoms * 4;         // issuer i's B scales at + i * kAtoms * 4
+  static constexpr int kSfbCol = kSfaCol + kIssuers * kAtoms * 4;   // issuer i's A scales at kSfaCol + i * kAtoms * 4, B at kSfbCol + i * kAtoms * 4
   static constexpr int kCols = kSfaCol + kSfCols;
   static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
   static_assert(kCols <= 512, "tensor memory");
@@ -127,7 +130,7 @@ __device__ __forceinline__ void decode_unit(const int32_t* s_start, const int32_
 }
 
 template <int N, bool GATEUP, bool NV>
-__global__ void __launch_bounds__(GATEUP ? 224 : 192, 1) moe_gemm_kernel(const __grid_constant__ KParams p) {
+__global__ void __launch_bounds__(224, 1) moe_gemm_kernel(const __grid_constant__ KParams p) {
   using C = GemmCfg<N, GATEUP, NV>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[C::kStages];
@@ -144,11 +147,11 @@ __global__ void __launch_bounds__(GATEUP ? 224 : 192, 1) moe_gemm_kernel(const _
 
   const int KT = (p.K + 255) / 256;
 
-  static_assert(C::kThreads == (GATEUP ? 224 : 192), "launch bounds");
+  static_assert(C::kThreads == 224, "launch bounds");
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
-      mbar_init(smem_u32(&bar_empty[s]), C::kIssuers);  // every issuer releases the stage
+      mbar_init(smem_u32(&bar_empty[s]), C::kKSplit ? 1 : C::kIssuers);  // the issuers that read the stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&bar_tfull[a]), C::kIssuers);
@@ -301,13 +304,13 @@ __global__ void __launch_bounds__(GATEUP ? 224 : 192, 1) moe_gemm_kernel(const _
     }
   } else if (warp == 1 || warp == 6) {
     // ------------------------------------------------------------ MMA issuers
-    // issuer mi (warp 1: gate or the only operand; warp 6: up) drives the
-    // MMAs of A operand mi into its own accumulator
+    // issuer mi (warp 1 or 6) drives its MMAs into accumulator block mi
     if (lane == 0) {
       const int mi = warp == 1 ? 0 : 1;
       const uint32_t t_sfa = tmem + C::kSfaCol + mi * C::kAtoms * 4;
       const uint32_t t_sfb = tmem + C::kSfbCol + mi * C::kAtoms * 4;
-      const uint32_t off_a = mi ? C::kOffA1 : 0u, off_sfa = mi ? C::kOffSFA1 : C::kOffSFA0;
+      const uint32_t off_a = (!C::kKSplit && mi) ? C::kOffA1 : 0u;
+      const uint32_t off_sfa = (!C::kKSplit && mi) ? C::kOffSFA1 : C::kOffSFA0;
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       int as = 0;  // accumulator set of this unit
@@ -316,9 +319,14 @@ __global__ void __launch_bounds__(GATEUP ? 224 : 192, 1) moe_gemm_kernel(const _
         tc_fence_after();
         const uint32_t t_acc = tmem + as * C::kAccCols + mi * N;
         for (int kt = 0; ok && kt < KT; ++kt) {
+          if (C::kKSplit && (kt & 1) != mi) {  // the other issuer's K tile
+            if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+            continue;
+          }
           if (!mbar_wait(smem_u32(&bar_full[stage]), phase)) { ok = false; break; }
           tc_fence_after();
           const uint32_t base = sbase + stage * C::kStage;
+          const bool first = C::kKSplit ? kt == mi : kt == 0;  // first K tile of this accumulator
 #pragma unroll
           for (int a = 0; a < C::kAtoms; ++a) {
             tc_cp_sf(t_sfa + 4 * a, desc_sf(base + off_sfa + 512 * a));
@@ -329,7 +337,7 @@ __global__ void __launch_bounds__(GATEUP ? 224 : 192, 1) moe_gemm_kernel(const _
             const int atom = NV ? j : (j >> 1);
             const uint32_t sfid = NV ? 0u : (uint32_t)(j & 1) * 2u;
             const uint32_t idesc = idesc_fp4(N, NV, sfid, sfid);
-            const uint32_t accum = (kt | j) ? 1u : 0u;
+            const uint32_t accum = (!first || j) ? 1u : 0u;
             tc_mma_fp4<NV>(t_acc, desc_sw128(base + off_a + 32 * j), desc_sw128(base + C::kOffB + 32 * j), idesc,
                            t_sfa + 4 * atom, t_sfb + 4 * atom, accum);
           }
@@ -436,7 +444,14 @@ __global__ void __launch_bounds__(GATEUP ? 224 : 192, 1) moe_gemm_kernel(const _
         if constexpr (NV) sc = __fmul_rn(__ldg(p.gb + e), __ldg(p.gw + e));
         for (int c0 = 0; c0 < cnt; c0 += 32) {
           float y[32];
-          tc_ld32(ta + c0, y);
+          tc_ld32(ta + c0, y);  // even K tiles
+          if (KT > 1) {         // odd K tiles (the second issuer's accumulator)
+            float y1[32];
+            tc_ld32(ta + N + c0, y1);
+            tc_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) y[j] += y1[j];
+          }
           tc_wait_ld();
           const int jn = min(32, cnt - c0);
           int tk = 0;
