@@ -395,7 +395,9 @@ __global__ void __launch_bounds__(224, 1) moe_gemm_kernel(const __grid_constant_
               gv = gv * sc;
               uv = uv * sc;
             }
-            tile[j][lane] = gv / (1.0f + expf(-gv)) * uv;
+            // silu(g) u with the hardware exponential and a correctly rounded
+            // reciprocal (e^-g = inf for g < -88 gives -0, the limit)
+            tile[j][lane] = gv * __frcp_rn(1.0f + __expf(-gv)) * uv;
           }
           __syncwarp();
           const int n = c0 + lane;

@@ -48,8 +48,13 @@ from .router import decision_margins, route, router_logits
 # Relative accumulation-error bound of an fp32 GEMM output:
 # |acc_gpu - acc_exact| <= GAMMA * sum_k |a_k * w_k|.
 GAMMA = 2.0 ** -16
-# Relative error allowed for the fp32 SwiGLU arithmetic.
+# Relative error allowed for the fp32 SwiGLU arithmetic: a few roundings
+# (EPS_SWIGLU) plus, for an exponential evaluated with the hardware unit, an
+# error that grows with the argument: at most 2 + 1.173 |g| units in the last
+# place of e^-g (the documented bound of CUDA's fast exponential), which the
+# sigmoid passes on at most once.  The pages fix no precision for this step.
 EPS_SWIGLU = 2.0 ** -20
+EPS_EXP_PER_G = 2.5 * 2.0 ** -24
 SILU_LIP = 1.1  # max |silu'|
 
 
@@ -186,7 +191,7 @@ def expert_rows(cfg, e: int, a: np.ndarray, wts: np.ndarray, weights: WeightSour
         du = gamma * gu_abs[:, I:] + 2.0 ** -22 * np.abs(u)
         sg = silu(g)
         dh = (SILU_LIP * dg * (np.abs(u) + du) + np.abs(sg) * du
-              + EPS_SWIGLU * np.abs(h) + 2.0 ** -140)
+              + (EPS_SWIGLU + EPS_EXP_PER_G * np.abs(g)) * np.abs(h) + 2.0 ** -140)
         if fmt == "mxfp4":
             dmax, srange = _h_candidates_mx(h32, dh, hq, hs)
         else:
