@@ -336,7 +336,8 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
     if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, nullptr, cc, L.n_exp, s);
     if (e == cudaSuccess) e = rec(2);
     if (e == cudaSuccess)
-      e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, ecount, eslot, gu_start, dn_start, plan, s);
+      e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, ecount, eslot, gu_start, dn_start, plan,
+                      status + ST_TICKET_PLAN, s);
     if (e == cudaSuccess)
       e = launch_scatter(d, idx, tw, cc, L.n_chunks, L.n_exp, n_tile, eslot, route_row, row_tok, row_w, row_e, s);
     if (e == cudaSuccess) e = rec(3);

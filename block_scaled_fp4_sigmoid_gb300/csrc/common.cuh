@@ -15,7 +15,7 @@ namespace fp4moe {
 // [4] timeouts, [5] where the last timeout happened, [8..9] tickets of the
 // kernels whose last CTA finishes a step.
 enum { ST_FIRST = 0, ST_COUNT = 1, ST_NAN = 2, ST_INEXACT = 3, ST_TIMEOUT = 4, ST_WHERE = 5,
-       ST_TICKET_FRONT = 8, ST_TICKET_DOWN = 9 };  // [8], [9]: last-CTA tickets, cleared per call
+       ST_TICKET_FRONT = 8, ST_TICKET_DOWN = 9, ST_TICKET_PLAN = 10 };  // [8]-[10]: last-CTA tickets, cleared per call
 constexpr int kStatusInts = 16;
 
 __device__ __forceinline__ void record_status(int32_t* st, int code, int which, int n = 1) {

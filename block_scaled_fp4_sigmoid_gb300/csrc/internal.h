@@ -12,7 +12,7 @@
 namespace fp4moe {
 
 constexpr int kSlotRows = 128;    // rows of one slot of the permuted layout
-constexpr int kChunkTokens = 256;  // tokens per chunk of the stable scatter
+constexpr int kChunkTokens = 32;  // tokens per chunk of the stable scatter (one warp each)
 
 // Device-side plan of one forward call, written by the plan kernel.
 struct Plan {
@@ -50,7 +50,7 @@ cudaError_t launch_topk(const fp4moe_dims& d, const float* partial, int n_splits
                         cudaStream_t s);
 cudaError_t launch_plan(const fp4moe_dims& d, int32_t* chunk_counts, int n_chunks, int n_exp, int n_tile,
                         int32_t* expert_count, int32_t* expert_slot, int32_t* gu_start, int32_t* dn_start,
-                        Plan* plan, cudaStream_t s);
+                        Plan* plan, int32_t* ticket, cudaStream_t s);
 cudaError_t launch_scatter(const fp4moe_dims& d, const int32_t* idx, const float* w, const int32_t* chunk_counts,
                            int n_chunks, int n_exp, int n_tile, const int32_t* expert_slot, int32_t* route_row,
                            int32_t* row_tok, float* row_w, int32_t* row_e, cudaStream_t s);

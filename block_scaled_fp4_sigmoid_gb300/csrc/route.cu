@@ -220,42 +220,90 @@ __global__ void topk_kernel(const float* __restrict__ partial, int n_splits, con
 }
 
 // ---------------------------------------------------------------- plan
-// One CTA.  Turns per-chunk counts into per-chunk bases (in place), totals,
-// tiles, slots and the unit prefixes of both GEMMs.
-__global__ void plan_kernel(int32_t* chunk_counts, int n_chunks, int n_exp, int E, int T, int n_tile,
-                            int gu_mtiles, int dn_mtiles, int32_t* expert_count, int32_t* expert_slot,
-                            int32_t* gu_start, int32_t* dn_start, Plan* plan) {
-  __shared__ int32_t s_tiles[1024];
-  for (int e = threadIdx.x; e < n_exp; e += blockDim.x) {
-    int run = 0;
-    for (int c = 0; c < n_chunks; ++c) {
-      int32_t* p = chunk_counts + (int64_t)c * n_exp + e;
-      int v;
-      if (e >= E) v = min(kChunkTokens, T - c * kChunkTokens);  // shared expert: every token
-      else v = *p;
-      *p = run;
+// One warp per expert: exclusive prefix of the expert's per-chunk counts (in
+// place: they become the chunk bases of the stable scatter), the expert's
+// total.  Lane l takes a contiguous run of chunks, so one warp scan orders
+// them.  The CTA that finishes last (a ticket; no CTA waits for another)
+// turns the totals into tiles, 128-row slots and the unit prefixes of both
+// GEMMs by a block scan.
+constexpr int kPlanWarps = 8;
+
+__global__ void __launch_bounds__(32 * kPlanWarps) plan_kernel(int32_t* chunk_counts, int n_chunks, int n_exp, int E,
+                                                                int T, int n_tile, int gu_mtiles, int dn_mtiles,
+                                                                int32_t* expert_count, int32_t* expert_slot,
+                                                                int32_t* gu_start, int32_t* dn_start, Plan* plan,
+                                                                int32_t* ticket) {
+  __shared__ int s_last;
+  __shared__ int32_t s_wsum[kPlanWarps];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int e = blockIdx.x * kPlanWarps + wib;
+  if (e < n_exp) {
+    const int per = (n_chunks + 31) / 32;
+    const int c0 = lane * per, c1 = min(n_chunks, c0 + per);
+    auto count = [&](int c) {  // the shared expert takes every token of the chunk
+      return e >= E ? min(kChunkTokens, T - c * kChunkTokens) : chunk_counts[(int64_t)c * n_exp + e];
+    };
+    int sum = 0;
+#pragma unroll 8
+    for (int c = c0; c < c1; ++c) sum += count(c);
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int c = c0; c < c1; ++c) {
+      const int v = count(c);
+      chunk_counts[(int64_t)c * n_exp + e] = run;
       run += v;
     }
-    expert_count[e] = run;
-    s_tiles[e] = (run + n_tile - 1) / n_tile;
+    if (lane == 31) expert_count[e] = incl;
   }
+  __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int slot = 0, gu = 0, dn = 0;
-    for (int e = 0; e < n_exp; ++e) {
-      expert_slot[e] = slot;
-      gu_start[e] = gu;
-      dn_start[e] = dn;
-      slot += s_tiles[e];
-      gu += s_tiles[e] * gu_mtiles;
-      dn += s_tiles[e] * dn_mtiles;
+  if (threadIdx.x == 0) s_last = atomicAdd(ticket, 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // last CTA: exclusive scan of tiles over the experts (thread j owns experts
+  // 3j .. 3j + 2; n_exp <= 520 < 3 * 256)
+  constexpr int kT = 32 * kPlanWarps;
+  int tl[3], my = 0;
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    const int ee = threadIdx.x * 3 + q;
+    tl[q] = ee < n_exp ? (__ldcg(expert_count + ee) + n_tile - 1) / n_tile : 0;
+    my += tl[q];
+  }
+  int incl = my;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_wsum[wib] = incl;
+  __syncthreads();
+  int base = incl - my;
+  for (int w2 = 0; w2 < wib; ++w2) base += s_wsum[w2];
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    const int ee = threadIdx.x * 3 + q;
+    if (ee < n_exp) {
+      expert_slot[ee] = base;
+      gu_start[ee] = base * gu_mtiles;
+      dn_start[ee] = base * dn_mtiles;
     }
-    gu_start[n_exp] = gu;
-    dn_start[n_exp] = dn;
+    base += tl[q];
+  }
+  if (threadIdx.x == kT - 1) {
+    const int total = base;  // the last thread's running sum covers every expert
+    gu_start[n_exp] = total * gu_mtiles;
+    dn_start[n_exp] = total * dn_mtiles;
     plan->n_exp = n_exp;
-    plan->gu_units = gu;
-    plan->dn_units = dn;
-    plan->slots = slot;
+    plan->gu_units = total * gu_mtiles;
+    plan->dn_units = total * dn_mtiles;
+    plan->slots = total;
   }
 }
 
@@ -626,9 +674,11 @@ cudaError_t launch_topk(const fp4moe_dims& d, const float* partial, int n_splits
 
 cudaError_t launch_plan(const fp4moe_dims& d, int32_t* chunk_counts, int n_chunks, int n_exp, int n_tile,
                         int32_t* expert_count, int32_t* expert_slot, int32_t* gu_start, int32_t* dn_start,
-                        Plan* plan, cudaStream_t s) {
-  plan_kernel<<<1, 1024, 0, s>>>(chunk_counts, n_chunks, n_exp, d.E, d.T, n_tile, d.I / 128, d.H / 128,
-                                 expert_count, expert_slot, gu_start, dn_start, plan);
+                        Plan* plan, int32_t* ticket, cudaStream_t s) {
+  const unsigned blocks = (unsigned)((n_exp + kPlanWarps - 1) / kPlanWarps);
+  plan_kernel<<<blocks, 32 * kPlanWarps, 0, s>>>(chunk_counts, n_chunks, n_exp, d.E, d.T, n_tile, d.I / 128,
+                                                 d.H / 128, expert_count, expert_slot, gu_start, dn_start, plan,
+                                                 ticket);
   return cudaGetLastError();
 }
 
