@@ -330,7 +330,6 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
     for (int i = 1; i <= 4 && e == cudaSuccess; ++i) e = rec(i);
   } else {
     if (e == cudaSuccess && nv) e = cudaMemsetAsync(amax, 0, (size_t)(2 + L.n_exp) * 4, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(acc, 0, (size_t)d.T * d.H * 4, s);
     if (e == cudaSuccess) e = launch_router_logits(x, w->w_router, partial, d.T, d.H, d.E, L.ws.n_splits, status, s);
     if (e == cudaSuccess) e = rec(1);
     if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, nullptr, cc, L.n_exp, s);
@@ -377,6 +376,8 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
     g.h_dbg = dbg ? dbg->h_pre : nullptr;
     g.tok_mask = L.front ? reinterpret_cast<const uint32_t*>(cc) : nullptr;
     g.plan_from_prev = L.front;  // the front end, launched just before, wrote the plan
+    g.out_acc = acc;
+    g.zero_acc = !L.front;  // the front end zeroes it itself
     e = launch_gateup(g, s);
   }
   if (e == cudaSuccess && nv) e = launch_h_quant_nv_routes(d, h32, route_row, row_e, amax + 2, gscale + 2, hq, hsf, s);

@@ -54,6 +54,8 @@ struct KParams {
   const uint32_t* tok_mask;
   uint8_t *hq, *hsf;
   float *h32, *h_dbg, *out_acc;
+  float4* zero_buf;  // gate/up: fp32 buffer warp 7 zeroes (the down GEMM's combine buffer), nullable
+  int64_t zero_n4;   // its size in float4
   uint32_t* amax_h;
   int32_t* status;
   int E, n_exp, H, I, K, rows_per_expert, m_tiles, katoms_a, katoms_b, katoms_h, has_shared, T;
@@ -86,7 +88,7 @@ struct GemmCfg {
   // issuer copies its own A and B scale factors.
   static constexpr int kIssuers = 2;
   static constexpr bool kKSplit = !GATEUP;
-  static constexpr int kThreads = 224;
+  static constexpr int kThreads = 256;  // + warp 7: zeroes the combine buffer (gate/up, when asked)
   static constexpr int kAccCols = 2 * N;                            // one accumulator set: two N-column blocks
   static constexpr int kSfCols = kIssuers * 2 * kAtoms * 4;         // scale factors of one K tile
   // two accumulator sets when they fit: the epilogue of one unit then
@@ -130,7 +132,7 @@ __device__ __forceinline__ void decode_unit(const int32_t* s_start, const int32_
 }
 
 template <int N, bool GATEUP, bool NV>
-__global__ void __launch_bounds__(224, 1) moe_gemm_kernel(const __grid_constant__ KParams p) {
+__global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant__ KParams p) {
   using C = GemmCfg<N, GATEUP, NV>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[C::kStages];
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(224, 1) moe_gemm_kernel(const __grid_constant_
 
   const int KT = (p.K + 255) / 256;
 
-  static_assert(C::kThreads == 224, "launch bounds");
+  static_assert(C::kThreads == 256, "launch bounds");
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
@@ -301,6 +303,14 @@ __global__ void __launch_bounds__(224, 1) moe_gemm_kernel(const __grid_constant_
       // every armed stage must have landed before the CTA exits
       for (int s = 0; s < C::kStages; ++s)
         if ((armed >> s) & 1u) (void)mbar_wait(smem_u32(&bar_full[s]), (armed_par >> s) & 1u);
+    }
+  } else if (warp == 7) {
+    // ------------------------------------------------------------ zeroing
+    // The combine buffer is read by the down GEMM, which starts after this
+    // grid has completed; the writes overlap this kernel's MMAs.
+    if (p.zero_buf) {
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int64_t i = (int64_t)blockIdx.x * 32 + lane; i < p.zero_n4; i += (int64_t)gridDim.x * 32) p.zero_buf[i] = z;
     }
   } else if (warp == 1 || warp == 6) {
     // ------------------------------------------------------------ MMA issuers

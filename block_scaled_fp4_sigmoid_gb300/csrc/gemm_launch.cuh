@@ -50,6 +50,10 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   p.h32 = a.h32;
   p.h_dbg = a.h_dbg;
   p.out_acc = a.out_acc;
+  if (GATEUP && a.zero_acc) {
+    p.zero_buf = reinterpret_cast<float4*>(a.out_acc);
+    p.zero_n4 = (int64_t)d.T * d.H / 4;
+  }
   p.amax_h = a.amax_h;
   p.status = a.status;
   p.E = d.E;

@@ -118,7 +118,8 @@ struct GemmArgs {
   float *h32;                      // gate/up, NVFP4 (pre-quantisation h)
   uint32_t *amax_h;                // gate/up, NVFP4
   float *h_dbg;                    // optional copy of h
-  float *out_acc;                  // down
+  float *out_acc;                  // down; gate/up: zeroed there when zero_acc
+  bool zero_acc;                   // gate/up zeroes out_acc ([T, H] fp32) for the down GEMM
   int32_t *status;
 };
 
