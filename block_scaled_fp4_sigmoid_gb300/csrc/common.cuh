@@ -193,6 +193,41 @@ __device__ __forceinline__ void tc_mma_fp4(uint32_t d, uint64_t a, uint64_t b, u
   }
 }
 
+// Warp-issued forms: the whole (converged) warp executes the call and
+// elect.sync picks the one lane that issues the instruction, so the operands
+// are computed warp-uniformly instead of in one divergent lane.
+__device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
+      "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_cp_sf_elect(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
+      "@p tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr), "l"(sdesc)
+      : "memory");
+}
+
+template <bool kNV>
+__device__ __forceinline__ void tc_mma_fp4_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                                 uint32_t sfb, uint32_t accumulate) {
+  if constexpr (kNV) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\telect.sync _|p, 0xffffffff;\n\tsetp.ne.b32 q, %6, 0;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], q;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\telect.sync _|p, 0xffffffff;\n\tsetp.ne.b32 q, %6, 0;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], q;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+  }
+}
+
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane.

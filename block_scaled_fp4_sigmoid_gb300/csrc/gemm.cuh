@@ -314,58 +314,66 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
     }
   } else if (warp == 1 || warp == 6) {
     // ------------------------------------------------------------ MMA issuers
-    // issuer mi (warp 1 or 6) drives its MMAs into accumulator block mi
-    if (lane == 0) {
-      const int mi = warp == 1 ? 0 : 1;
-      const uint32_t t_sfa = tmem + C::kSfaCol + mi * C::kAtoms * 4;
-      const uint32_t t_sfb = tmem + C::kSfbCol + mi * C::kAtoms * 4;
-      const uint32_t off_a = (!C::kKSplit && mi) ? C::kOffA1 : 0u;
-      const uint32_t off_sfa = (!C::kKSplit && mi) ? C::kOffSFA1 : C::kOffSFA0;
-      int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      int as = 0;  // accumulator set of this unit
-      for (int u = blockIdx.x; u < total && !*abort_v; u += gridDim.x) {
-        bool ok = mbar_wait(smem_u32(&bar_tempty[as]), acc_phase ^ 1u);
-        tc_fence_after();
-        const uint32_t t_acc = tmem + as * C::kAccCols + mi * N;
-        for (int kt = 0; ok && kt < KT; ++kt) {
-          if (C::kKSplit && (kt & 1) != mi) {  // the other issuer's K tile
-            if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
-            continue;
-          }
-          if (!mbar_wait(smem_u32(&bar_full[stage]), phase)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t base = sbase + stage * C::kStage;
-          const bool first = C::kKSplit ? kt == mi : kt == 0;  // first K tile of this accumulator
-#pragma unroll
-          for (int a = 0; a < C::kAtoms; ++a) {
-            tc_cp_sf(t_sfa + 4 * a, desc_sf(base + off_sfa + 512 * a));
-            tc_cp_sf(t_sfb + 4 * a, desc_sf(base + C::kOffSFB + 512 * a));
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int atom = NV ? j : (j >> 1);
-            const uint32_t sfid = NV ? 0u : (uint32_t)(j & 1) * 2u;
-            const uint32_t idesc = idesc_fp4(N, NV, sfid, sfid);
-            const uint32_t accum = (!first || j) ? 1u : 0u;
-            tc_mma_fp4<NV>(t_acc, desc_sw128(base + off_a + 32 * j), desc_sw128(base + C::kOffB + 32 * j), idesc,
-                           t_sfa + 4 * atom, t_sfb + 4 * atom, accum);
-          }
-          tc_commit(smem_u32(&bar_empty[stage]));
+    // Issuer mi (warp 1 or 6) drives its MMAs into accumulator block mi.  The
+    // whole warp runs the loop, so every operand (descriptors, tensor-memory
+    // addresses) is warp-uniform; each tcgen05 instruction is issued by one
+    // lane picked with elect.sync.
+    const int mi = warp == 1 ? 0 : 1;
+    const uint32_t t_sfa = tmem + C::kSfaCol + mi * C::kAtoms * 4;
+    const uint32_t t_sfb = tmem + C::kSfbCol + mi * C::kAtoms * 4;
+    const uint32_t off_a = (!C::kKSplit && mi) ? C::kOffA1 : 0u;
+    const uint32_t off_sfa = (!C::kKSplit && mi) ? C::kOffSFA1 : C::kOffSFA0;
+    // descriptors of stage 0; a stage s adds s * kStage / 16 to the start
+    // address field (every address stays below 2^18, so the 14-bit field
+    // does not carry)
+    const uint64_t a_desc0 = desc_sw128(sbase + off_a), b_desc0 = desc_sw128(sbase + C::kOffB);
+    const uint64_t sfa_desc0 = desc_sf(sbase + off_sfa), sfb_desc0 = desc_sf(sbase + C::kOffSFB);
+    // bounded wait with a warp-uniform outcome
+    auto wait_w = [](uint32_t bar, uint32_t par) { return __all_sync(0xffffffffu, mbar_wait(bar, par)); };
+    int stage = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    int as = 0;  // accumulator set of this unit
+    for (int u = blockIdx.x; u < total && !__any_sync(0xffffffffu, *abort_v); u += gridDim.x) {
+      bool ok = wait_w(smem_u32(&bar_tempty[as]), acc_phase ^ 1u);
+      tc_fence_after();
+      const uint32_t t_acc = tmem + as * C::kAccCols + mi * N;
+      for (int kt = 0; ok && kt < KT; ++kt) {
+        if (C::kKSplit && (kt & 1) != mi) {  // the other issuer's K tile
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+          continue;
         }
-        if (!ok) {
-          *abort_v = 1;
-          record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
-          break;
+        if (!wait_w(smem_u32(&bar_full[stage]), phase)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t so = (uint64_t)((stage * C::kStage) >> 4);
+        const bool first = C::kKSplit ? kt == mi : kt == 0;  // first K tile of this accumulator
+#pragma unroll
+        for (int a = 0; a < C::kAtoms; ++a) {
+          tc_cp_sf_elect(t_sfa + 4 * a, sfa_desc0 + so + 32 * a);  // 512 bytes per scale group
+          tc_cp_sf_elect(t_sfb + 4 * a, sfb_desc0 + so + 32 * a);
         }
-        tc_commit(smem_u32(&bar_tfull[as]));
-        if (++as == C::kAccStages) { as = 0; acc_phase ^= 1u; }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int atom = NV ? j : (j >> 1);
+          const uint32_t sfid = NV ? 0u : (uint32_t)(j & 1) * 2u;
+          const uint32_t idesc = idesc_fp4(N, NV, sfid, sfid);
+          const uint32_t accum = (!first || j) ? 1u : 0u;
+          tc_mma_fp4_elect<NV>(t_acc, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc, t_sfa + 4 * atom,
+                               t_sfb + 4 * atom, accum);  // K = 64 per MMA: 32 bytes into the swizzle row
+        }
+        tc_commit_elect(smem_u32(&bar_empty[stage]));
+        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
       }
-      // all issued MMAs must finish before tensor memory is released
-      tc_commit(smem_u32(&bar_done));
-      (void)mbar_wait(smem_u32(&bar_done), 0);
+      if (!ok) {
+        *abort_v = 1;
+        if (lane == 0) record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
+        break;
+      }
+      tc_commit_elect(smem_u32(&bar_tfull[as]));
+      if (++as == C::kAccStages) { as = 0; acc_phase ^= 1u; }
     }
+    // all issued MMAs must finish before tensor memory is released
+    tc_commit_elect(smem_u32(&bar_done));
+    (void)mbar_wait(smem_u32(&bar_done), 0);
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // tensor-memory lane quadrant of this warp
