@@ -11,6 +11,10 @@ Between timed steps a 256 MiB buffer is written to flush L2 (untimed).  Each
 step is timed with CUDA events on the launching stream; the dominant kernel
 (gate/up GEMM) is timed by events recorded around its launch.
 
+--w8a8 times the W8A8 layer instead: the same synthetic MXFP4 experts after the
+exact per-channel FP8 conversion, per-token dynamic E4M3 activations
+(fp4moe_forward_w8a8).
+
 With torchrun (N > 1) each rank runs an independent replica on its own batch
 (no collective on the data path); the line reports the max over ranks.
 
@@ -129,7 +133,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle timing
-def oracle_route_sample(cfg_name: str, n_routes: int, frac: float = 1.0, start_token: int = 0):
+def oracle_route_sample(cfg_name: str, n_routes: int, frac: float = 1.0, start_token: int = 0, w8a8: bool = False):
     """Times the FP64 oracle on n_routes (token, expert) routes of the
     workload: each token's routing and x quantisation, then its expert MLPs.
     frac < 1 evaluates each MLP on the first frac * I intermediate channels
@@ -142,11 +146,12 @@ def oracle_route_sample(cfg_name: str, n_routes: int, frac: float = 1.0, start_t
     from oracle import inputs as OI
     from oracle import moe as M
     from oracle import quant as Q
+    from oracle import w8a8 as W8
     from oracle.router import route, router_logits
     cfg = synth.configs()[cfg_name]
     Ip = cfg.I if frac >= 1 else max(32, int(cfg.I * frac) // 32 * 32)
     sub = replace(cfg, I=Ip)
-    ws = OI.oracle_weights(cfg)
+    ws = W8.fp8_weight_source(cfg) if w8a8 else OI.oracle_weights(cfg)
     wr = synth.bf16_bits_to_f64(synth.gen_router_bf16(cfg))
     bias = synth.gen_bias_f32(cfg)
     done, t_total, t = 0, 0.0, start_token
@@ -155,8 +160,11 @@ def oracle_route_sample(cfg_name: str, n_routes: int, frac: float = 1.0, start_t
         t0 = time.perf_counter()
         logits, _ = router_logits(x, wr)
         idx, w = route(logits, bias, cfg.top_k, cfg.n_group, cfg.topk_group, cfg.routed_scaling, cfg.renormalize)
-        xc, xs, gx = Q.quantize(x, cfg.fmt)
-        a = Q.dequant(xc, xs, cfg.fmt, gx)
+        if w8a8:
+            a = W8.fp8_dequant(*W8.fp8_quantize(x))
+        else:
+            xc, xs, gx = Q.quantize(x, cfg.fmt)
+            a = Q.dequant(xc, xs, cfg.fmt, gx)
         t_total += time.perf_counter() - t0
         experts = [int(e) for e in idx[0]] + list(range(cfg.E, cfg.E + cfg.n_shared))
         for j, e in enumerate(experts):
@@ -169,11 +177,17 @@ def oracle_route_sample(cfg_name: str, n_routes: int, frac: float = 1.0, start_t
             w2 = ws.get(names[1], ee)
             blk = 16 if cfg.fmt == "nvfp4" else 32
             keep = np.r_[0:Ip, cfg.I:cfg.I + Ip]
-            s13 = (w13[0][keep], w13[1][keep], w13[2])
-            s2 = (np.ascontiguousarray(w2[0][:, :Ip]), np.ascontiguousarray(w2[1][:, :Ip // blk]), w2[2])
+            if w8a8:  # value matrices
+                s13, s2 = w13[keep], np.ascontiguousarray(w2[:, :Ip])
+            else:
+                s13 = (w13[0][keep], w13[1][keep], w13[2])
+                s2 = (np.ascontiguousarray(w2[0][:, :Ip]), np.ascontiguousarray(w2[1][:, :Ip // blk]), w2[2])
             sub_ws = M.WeightSource(lambda which, _e, _a=s13, _b=s2: _a if which in ("w13", "sh13") else _b)
             t0 = time.perf_counter()
-            M.expert_rows(sub, e, a, np.array([wt]), sub_ws, with_ambiguity=False)
+            if w8a8:
+                W8.expert_rows_fp8(sub, e, a, np.array([wt]), sub_ws, with_ambiguity=False)
+            else:
+                M.expert_rows(sub, e, a, np.array([wt]), sub_ws, with_ambiguity=False)
             t_total += time.perf_counter() - t0
             ws.drop(names[0], ee)
             ws.drop(names[1], ee)
@@ -187,12 +201,12 @@ def reference_arm(args, cfg, rank, world):
     if rank != 0:
         return
     # size each step so that warm-up + steps take about two minutes
-    t_one, _ = oracle_route_sample(args.config, 1)
+    t_one, _ = oracle_route_sample(args.config, 1, w8a8=args.w8a8)
     budget = 120.0 / (args.steps + args.warmup)
     frac = min(1.0, budget / max(t_one, 1e-3))
     secs, toks = [], 0.0
     for i in range(args.warmup + args.steps):
-        sec, n = oracle_route_sample(args.config, 1, frac, start_token=i)
+        sec, n = oracle_route_sample(args.config, 1, frac, start_token=i, w8a8=args.w8a8)
         if i >= args.warmup:
             secs.append(sec)
             toks += n
@@ -203,7 +217,7 @@ def reference_arm(args, cfg, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(secs),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": cfg_label(cfg),
+            "data": "synthetic", "config": {"workload": cfg_label(cfg, args.w8a8),
                                             "step": f"one (token, expert) route on {Ip} of {cfg.I} channels"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"{args.steps} routes of the {cfg.name} workload, {Ip}/{cfg.I} "
@@ -212,10 +226,11 @@ def reference_arm(args, cfg, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def cfg_label(cfg) -> str:
+def cfg_label(cfg, w8a8: bool = False) -> str:
+    fmt = "FP8 W8A8 (experts exactly converted from MXFP4)" if w8a8 else f"{cfg.fmt.upper()} A4W4"
     return (f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.top_k}"
             f"{f' groups {cfg.n_group}/{cfg.topk_group}' if cfg.n_group > 1 else ''}"
-            f"{' +1 shared' if cfg.n_shared else ''} {cfg.fmt.upper()} A4W4")
+            f"{' +1 shared' if cfg.n_shared else ''} {fmt}")
 
 
 # ------------------------------------------------------------------ MXFP4 -> FP8 conversion
@@ -271,6 +286,14 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     s = stream.cuda_stream
     layer = MoELayer.synthetic(cfg, device=dev)
+    if args.w8a8:
+        from block_scaled_fp4_sigmoid_gb300.layer import W8A8Layer
+        if cfg.fmt != "mxfp4":
+            raise SystemExit("--w8a8 converts MXFP4 experts")
+        mx = layer
+        layer = W8A8Layer(mx)
+        del mx.w13, mx.w2  # the converted copies are what the W8A8 layer reads
+        torch.cuda.empty_cache()
     # each rank runs its own batch: tokens rank*T .. (rank+1)*T of the stream
     x = layer.synthetic_x(rank * cfg.T, (rank + 1) * cfg.T)
     out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
@@ -385,10 +408,14 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     routes = int(count.sum())
     wpe = layer.weight_bytes_per_expert()
     d = layer.dims
-    blk = 16 if cfg.fmt == "nvfp4" else 32
-    act = 0.5 + 1.0 / blk                              # bytes per FP4 value incl. scale
-    gu_bytes = touched * (2 * d.I * d.H * act) + routes * d.H * act + routes * d.I * act
-    dn_bytes = touched * (d.H * d.I * act) + routes * d.I * act + routes * d.H * 4
+    if args.w8a8:  # E4M3 bytes, fp32 row scales; gate/up writes fp32 h, down reads E4M3 h
+        gu_bytes = touched * (2 * d.I * d.H + 2 * d.I * 4) + routes * (d.H + 4) + routes * d.I * 4
+        dn_bytes = touched * (d.H * d.I + d.H * 4) + routes * (d.I + 4) + routes * d.H * 4
+    else:
+        blk = 16 if cfg.fmt == "nvfp4" else 32
+        act = 0.5 + 1.0 / blk                              # bytes per FP4 value incl. scale
+        gu_bytes = touched * (2 * d.I * d.H * act) + routes * d.H * act + routes * d.I * act
+        dn_bytes = touched * (d.H * d.I * act) + routes * d.I * act + routes * d.H * 4
     flops = 2.0 * 3 * d.I * d.H * routes
 
     # max over ranks
@@ -400,18 +427,21 @@ def gpu_arm(args, cfg, rank, world, local_rank):
         return
     peaks = measured_peaks()
     achieved = gu_bytes / (gu_max * 1e-3) / 1e9
-    traffic = profiled_traffic(cfg.name)
+    traffic = profiled_traffic(cfg.name + ("_w8a8" if args.w8a8 else ""))
     clocks = clk.summary()
     # few tokens: front end (routing, plan, x quantisation), gate/up, down,
     # finalise; else router, top-k, plan, scatter, gather, gate/up, down, finalise
-    if cfg.fmt == "mxfp4":
+    if args.w8a8:  # router, top-k, plan, scatter, x quantisation, gate/up, h quantisation, down, finalise
+        launches_per_step = 9
+    elif cfg.fmt == "mxfp4":
         launches_per_step = 4 if cfg.T <= 16 else 8
     else:
         launches_per_step = 10
-    conversion = time_conversion(layer, peaks, stream) if args.conversion else None
+    conversion = time_conversion(layer, peaks, stream) if args.conversion and not args.w8a8 else None
     # CPU baseline: the oracle on a bounded sample of this workload
     n_routes = 16 if args.cpu_routes is None else args.cpu_routes
-    cpu_s, cpu_tok = oracle_route_sample(args.config, n_routes) if n_routes > 0 else (float("nan"), 0.0)
+    cpu_s, cpu_tok = (oracle_route_sample(args.config, n_routes, w8a8=args.w8a8) if n_routes > 0
+                      else (float("nan"), 0.0))
     line = {
         "metric": METRIC,
         "value": cfg.T * world / (ms_max * 1e-3),
@@ -423,9 +453,9 @@ def gpu_arm(args, cfg, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "mxfp4" if cfg.fmt == "mxfp4" else "nvfp4",
+        "dtype": "e4m3" if args.w8a8 else ("mxfp4" if cfg.fmt == "mxfp4" else "nvfp4"),
         "data": "synthetic (seeded; weights drawn on the device)",
-        "config": {"workload": cfg_label(cfg), "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+        "config": {"workload": cfg_label(cfg, args.w8a8), "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "launch": "one fp4moe_forward captured in a CUDA graph, replayed per step",
                    "l2": "flushed between steps (256 MiB write, untimed)", "touched_experts": touched,
                    "routes": routes},
@@ -460,6 +490,8 @@ def main():
     ap.add_argument("--experts", type=int, default=None,
                     help="override E (smaller device footprint for profiler captures)")
     ap.add_argument("--tokens", type=int, default=None, help="override T")
+    ap.add_argument("--w8a8", action="store_true",
+                    help="the W8A8 layer: experts exactly converted to FP8 per channel, FP8 per-token activations")
     ap.add_argument("--conversion", action="store_true",
                     help="also time the MXFP4 -> FP8 conversion of all routed expert rows")
     args = ap.parse_args()

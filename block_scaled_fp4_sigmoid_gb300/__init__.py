@@ -20,6 +20,7 @@ HEADER = _PKG.parent / "include" / "fp4moe.h"
 
 MXFP4 = 0
 NVFP4 = 1
+FP8 = 2  # W8A8 layer (fp4moe_forward_w8a8)
 
 STATUS = {0: "FP4MOE_OK", 1: "FP4MOE_ERR_INVALID_ARG", 2: "FP4MOE_ERR_UNSUPPORTED_SHAPE",
           3: "FP4MOE_ERR_WORKSPACE", 4: "FP4MOE_ERR_CUDA", 5: "FP4MOE_ERR_TIMEOUT",
@@ -44,6 +45,12 @@ class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("w13", "w13_scale", "w2", "w2_scale", "g13", "g2", "sh13", "sh13_scale", "sh2",
                  "sh2_scale", "w_router", "bias")]
+
+
+class Fp8Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w13", "w13_scale", "w2", "w2_scale", "sh13", "sh13_scale", "sh2", "sh2_scale", "w_router",
+                 "bias")]
 
 
 class WsLayout(ctypes.Structure):
@@ -82,11 +89,12 @@ def lib() -> ctypes.CDLL:
         L.fp4moe_route.argtypes = [P(Dims), vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.fp4moe_quantize_act.argtypes = [vp, i32, i64, i32, i32, vp, vp, vp, vp, vp, sz, vp]
         L.fp4moe_forward.argtypes = [P(Dims), P(Weights), vp, vp, P(Debug), vp, sz, vp]
+        L.fp4moe_forward_w8a8.argtypes = [P(Dims), P(Fp8Weights), vp, vp, P(Debug), vp, sz, vp]
         L.fp4moe_mxfp4_to_fp8_rowscale.argtypes = [vp, vp, i64, i32, vp, vp, vp, vp, sz, vp]
         L.fp4moe_clear_status.argtypes = [vp, vp]
         L.fp4moe_get_status.argtypes = [vp, vp, P(i32), P(i64)]
         for name in ("fp4moe_workspace_layout", "fp4moe_pack_scales", "fp4moe_route", "fp4moe_quantize_act",
-                     "fp4moe_forward", "fp4moe_mxfp4_to_fp8_rowscale", "fp4moe_clear_status",
+                     "fp4moe_forward", "fp4moe_forward_w8a8", "fp4moe_mxfp4_to_fp8_rowscale", "fp4moe_clear_status",
                      "fp4moe_get_status"):
             getattr(L, name).restype = i32
         _LIB = L
@@ -151,6 +159,13 @@ def forward(dims: Dims, weights: Weights, x: int, out: int, ws: int, ws_bytes: i
     dbg = ctypes.byref(debug) if debug is not None else None
     _ok(lib().fp4moe_forward(ctypes.byref(dims), ctypes.byref(weights), x, out, dbg, ws, ws_bytes, stream),
         "fp4moe_forward")
+
+
+def forward_w8a8(dims: Dims, weights: Fp8Weights, x: int, out: int, ws: int, ws_bytes: int, stream: int = 0,
+                 debug: Debug | None = None) -> None:
+    dbg = ctypes.byref(debug) if debug is not None else None
+    _ok(lib().fp4moe_forward_w8a8(ctypes.byref(dims), ctypes.byref(weights), x, out, dbg, ws, ws_bytes, stream),
+        "fp4moe_forward_w8a8")
 
 
 def mxfp4_to_fp8_rowscale(codes: int, scales: int, rows: int, K: int, fp8_out: int, row_scale: int,

@@ -39,7 +39,7 @@ bool dims_ok(const fp4moe_dims& d) {
   if (d.topk_group < 1 || d.topk_group > d.n_group) return false;
   if (d.n_group > 1 && (d.E / d.n_group > 64 || d.topk_group * (d.E / d.n_group) < d.top_k)) return false;
   if (d.n_shared < 0 || d.n_shared > 1) return false;
-  if (d.fmt != FP4MOE_MXFP4 && d.fmt != FP4MOE_NVFP4) return false;
+  if (d.fmt != FP4MOE_MXFP4 && d.fmt != FP4MOE_NVFP4 && d.fmt != FP4MOE_FP8) return false;
   if (!(d.routed_scaling == d.routed_scaling)) return false;
   return true;
 }
@@ -86,6 +86,7 @@ bool make_layout(const fp4moe_dims& d, Layout* L) {
   if (!dims_ok(d)) return false;
   memset(L, 0, sizeof(*L));
   const bool nv = d.fmt == FP4MOE_NVFP4;
+  const bool f8 = d.fmt == FP4MOE_FP8;  // W8A8: E4M3 rows with one fp32 scale each
   L->n_exp = d.E + d.n_shared;
   L->n_chunks = (d.T + kChunkTokens - 1) / kChunkTokens;
   L->n_route_per_tok = d.top_k + d.n_shared;
@@ -102,7 +103,7 @@ bool make_layout(const fp4moe_dims& d, Layout* L) {
       if ((d.H / 256) % s == 0 && d.H / s <= cap) L->front_splits = s;
     if (L->front_splits) break;
   }
-  L->front = !nv && d.T <= kFrontMaxT && L->front_splits > 0;
+  L->front = !nv && !f8 && d.T <= kFrontMaxT && L->front_splits > 0;
   w.x_by_token = L->front ? 1 : 0;
   // few tokens: one 16-token tile holds every token (the gate/up B operand)
   // and every expert's routes; half the B bytes and MMA columns of 32
@@ -132,13 +133,14 @@ bool make_layout(const fp4moe_dims& d, Layout* L) {
   w.row_tok = take((int64_t)w.rows_cap * 4);
   w.row_w = take((int64_t)w.rows_cap * 4);
   L->row_e = take((int64_t)w.rows_cap * 4);
-  w.xq = take((int64_t)w.rows_cap * (d.H / 2));
-  w.xsf = take((int64_t)slots_cap * katoms_padded(d.H, nv) * 512);
-  w.hq = take((int64_t)w.rows_cap * (d.I / 2));
-  w.hsf = take((int64_t)slots_cap * katoms_padded(d.I, nv) * 512);
-  w.h32 = nv ? take((int64_t)w.rows_cap * d.I * 4) : take(0);
+  w.xq = take((int64_t)w.rows_cap * (f8 ? d.H : d.H / 2));
+  w.xsf = f8 ? take((int64_t)w.rows_cap * 4) : take((int64_t)slots_cap * katoms_padded(d.H, nv) * 512);
+  w.hq = take((int64_t)w.rows_cap * (f8 ? d.I : d.I / 2));
+  w.hsf = f8 ? take((int64_t)w.rows_cap * 4) : take((int64_t)slots_cap * katoms_padded(d.I, nv) * 512);
+  w.h32 = (nv || f8) ? take((int64_t)w.rows_cap * d.I * 4) : take(0);
   w.gscale = take((int64_t)(2 + L->n_exp) * 4);
-  L->amax = take((int64_t)(2 + L->n_exp) * 4);
+  // amax bits: NVFP4 x, spare, h per expert; W8A8 h per permuted row
+  L->amax = take(f8 ? (int64_t)w.rows_cap * 4 : (int64_t)(2 + L->n_exp) * 4);
   w.out_acc = take((int64_t)d.T * d.H * 4);
   w.total_bytes = off;
   return true;
@@ -247,6 +249,7 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
   const fp4moe_dims& d = *dims;
   Layout L;
   if (!make_layout(d, &L)) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d.fmt == FP4MOE_FP8) return FP4MOE_ERR_INVALID_ARG;  // fp4moe_forward_w8a8
   if (ws_bytes < (size_t)L.ws.total_bytes) return FP4MOE_ERR_WORKSPACE;
   const bool nv = d.fmt == FP4MOE_NVFP4;
   if (!w->w13 || !w->w13_scale || !w->w2 || !w->w2_scale || !w->w_router || !w->bias) return FP4MOE_ERR_INVALID_ARG;
@@ -393,6 +396,120 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
     g.bsf = hsf;
     g.unit_start = dn_start;
     g.g_b = gscale + 2;  // g_h per expert
+    g.out_acc = acc;
+    e = launch_down(g, s);
+  }
+  if (e == cudaSuccess) e = rec(6);
+  if (e == cudaSuccess) e = launch_finalize(acc, out, (int64_t)d.T * d.H, s);
+  if (e == cudaSuccess) e = rec(7);
+  return cuda_status(e);
+}
+
+fp4moe_status fp4moe_forward_w8a8(const fp4moe_dims* dims, const fp4moe_fp8_weights* w, const uint16_t* x,
+                                  uint16_t* out, const fp4moe_debug* dbg, void* ws, size_t ws_bytes, void* stream) {
+  if (!dims || !w || !x || !out || !ws) return FP4MOE_ERR_INVALID_ARG;
+  const fp4moe_dims& d = *dims;
+  if (d.fmt != FP4MOE_FP8) return FP4MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(d, &L)) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  if (ws_bytes < (size_t)L.ws.total_bytes) return FP4MOE_ERR_WORKSPACE;
+  if (!w->w13 || !w->w13_scale || !w->w2 || !w->w2_scale || !w->w_router || !w->bias) return FP4MOE_ERR_INVALID_ARG;
+  if (d.n_shared && (!w->sh13 || !w->sh13_scale || !w->sh2 || !w->sh2_scale)) return FP4MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w->w13) || !aligned16(w->w2) || !aligned16(w->w_router) || !aligned16(ws) ||
+      !aligned16(out))
+    return FP4MOE_ERR_INVALID_ARG;
+  if (d.n_shared && (!aligned16(w->sh13) || !aligned16(w->sh2))) return FP4MOE_ERR_INVALID_ARG;
+  if (fp4moe_status st = check_device()) return st;
+  const int num_sms = device_sm_count();
+  if (num_sms <= 0) return FP4MOE_ERR_DEVICE;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  auto P = [&](int64_t off) { return base + off; };
+  int32_t* status = reinterpret_cast<int32_t*>(P(L.ws.status));
+  float* partial = reinterpret_cast<float*>(P(L.ws.logits));
+  int32_t* idx = reinterpret_cast<int32_t*>(P(L.ws.topk_idx));
+  float* tw = reinterpret_cast<float*>(P(L.ws.topk_w));
+  Plan* plan = reinterpret_cast<Plan*>(P(L.plan));
+  int32_t* ecount = reinterpret_cast<int32_t*>(P(L.ws.expert_count));
+  int32_t* eslot = reinterpret_cast<int32_t*>(P(L.ws.expert_slot));
+  int32_t* gu_start = reinterpret_cast<int32_t*>(P(L.gu_start));
+  int32_t* dn_start = reinterpret_cast<int32_t*>(P(L.dn_start));
+  int32_t* cc = reinterpret_cast<int32_t*>(P(L.chunk_counts));
+  int32_t* route_row = reinterpret_cast<int32_t*>(P(L.ws.route_row));
+  int32_t* row_tok = reinterpret_cast<int32_t*>(P(L.ws.row_tok));
+  float* row_w = reinterpret_cast<float*>(P(L.ws.row_w));
+  int32_t* row_e = reinterpret_cast<int32_t*>(P(L.row_e));
+  uint8_t* xq = P(L.ws.xq);
+  float* xsig = reinterpret_cast<float*>(P(L.ws.xsf));
+  uint8_t* hq = P(L.ws.hq);
+  float* hsig = reinterpret_cast<float*>(P(L.ws.hsf));
+  float* h32 = reinterpret_cast<float*>(P(L.ws.h32));
+  uint32_t* amax_row = reinterpret_cast<uint32_t*>(P(L.amax));
+  float* acc = reinterpret_cast<float*>(P(L.ws.out_acc));
+  const int n_tile = L.ws.n_tile;
+  auto rec = [&](int i) -> cudaError_t {
+    if (dbg && dbg->events[i]) return cudaEventRecord(static_cast<cudaEvent_t>(dbg->events[i]), s);
+    return cudaSuccess;
+  };
+
+  cudaError_t e = rec(0);
+  const size_t clear_bytes = (size_t)(L.chunk_counts - L.ws.status) + (size_t)L.n_chunks * L.n_exp * 4;
+  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, clear_bytes, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(amax_row, 0, (size_t)L.ws.rows_cap * 4, s);
+  if (e == cudaSuccess) e = launch_router_logits(x, w->w_router, partial, d.T, d.H, d.E, L.ws.n_splits, status, s);
+  if (e == cudaSuccess) e = rec(1);
+  if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, nullptr, cc, L.n_exp, s);
+  if (e == cudaSuccess) e = rec(2);
+  if (e == cudaSuccess)
+    e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, ecount, eslot, gu_start, dn_start, plan,
+                    status + ST_TICKET_PLAN, s);
+  if (e == cudaSuccess)
+    e = launch_scatter(d, idx, tw, cc, L.n_chunks, L.n_exp, n_tile, eslot, route_row, row_tok, row_w, row_e, s);
+  if (e == cudaSuccess) e = rec(3);
+  if (e == cudaSuccess) e = launch_fp8_x_quant(d, x, route_row, xq, xsig, s);
+  if (e == cudaSuccess) e = rec(4);
+
+  GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  a.d = &d;
+  a.f8 = true;
+  a.n_tile = n_tile;
+  a.num_sms = num_sms;
+  a.rows_cap = L.ws.rows_cap;
+  a.expert_count = ecount;
+  a.expert_slot = eslot;
+  a.plan = plan;
+  a.row_tok = row_tok;
+  a.row_w = row_w;
+  a.status = status;
+  if (e == cudaSuccess) {
+    GemmArgs g = a;
+    g.w = w->w13;
+    g.wrs = w->w13_scale;
+    g.sh = d.n_shared ? w->sh13 : nullptr;
+    g.shrs = d.n_shared ? w->sh13_scale : nullptr;
+    g.b = xq;
+    g.brs = xsig;
+    g.unit_start = gu_start;
+    g.h32 = h32;
+    g.amax_h = amax_row;
+    g.h_dbg = dbg ? dbg->h_pre : nullptr;
+    g.out_acc = acc;
+    g.zero_acc = true;
+    e = launch_gateup(g, s);
+  }
+  if (e == cudaSuccess) e = rec(5);
+  if (e == cudaSuccess) e = launch_fp8_h_quant(d, h32, route_row, amax_row, hq, hsig, s);
+  if (e == cudaSuccess) {
+    GemmArgs g = a;
+    g.w = w->w2;
+    g.wrs = w->w2_scale;
+    g.sh = d.n_shared ? w->sh2 : nullptr;
+    g.shrs = d.n_shared ? w->sh2_scale : nullptr;
+    g.b = hq;
+    g.brs = hsig;
+    g.unit_start = dn_start;
     g.out_acc = acc;
     e = launch_down(g, s);
   }

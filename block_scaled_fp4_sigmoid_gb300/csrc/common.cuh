@@ -228,6 +228,17 @@ __device__ __forceinline__ void tc_mma_fp4_elect(uint32_t d, uint64_t a, uint64_
   }
 }
 
+// E4M3 x E4M3 MMA (kind::f8f6f4, K = 32 per instruction), fp32 accumulate,
+// issued by one elected lane of the calling warp.
+__device__ __forceinline__ void tc_mma_f8_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\telect.sync _|p, 0xffffffff;\n\tsetp.ne.b32 q, %4, 0;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, q;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane.
@@ -272,6 +283,16 @@ __host__ __device__ constexpr uint32_t idesc_fp4(uint32_t n, bool nv, uint32_t s
          | (sfa_id & 3u) << 29;    // A scale-factor id
 }
 
+// Instruction descriptor of a dense E4M3 MMA: fp32 D, E4M3 A and B (format
+// code 0), both K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_f8(uint32_t n) {
+  return 1u << 4              // D format: fp32
+         | 0u << 7            // A format: E4M3
+         | 0u << 10           // B format: E4M3
+         | (n >> 3) << 17     // N / 8
+         | (128u >> 4) << 24; // M / 16
+}
+
 // ---------------------------------------------------------------- FP4 / FP8 encoders
 // Round-to-nearest-even magnitude code of E2M1 for a non-negative value:
 // grid 0, .5, 1, 1.5, 2, 3, 4, 6; ties to the even code; saturating.
@@ -299,6 +320,13 @@ __device__ __forceinline__ uint32_t e4m3_pos(float x) {
   uint32_t r = (mant + 0x7FFFFu + ((mant >> 20) & 1u)) >> 20;
   uint32_t code = ((uint32_t)e << 3) + r;  // a carry out of r bumps the exponent
   return code > 0x7Eu ? 0x7Eu : code;
+}
+
+// Signed E4M3 byte of v / sigma (W8A8 activations): round-to-nearest-even,
+// saturating at 448; sigma = 0 gives the signed zero of v.
+__device__ __forceinline__ uint32_t fp8_code(float v, float sigma) {
+  const uint32_t sign = (__float_as_uint(v) >> 24) & 0x80u;
+  return (sigma > 0.f ? e4m3_pos(fabsf(__fdiv_rn(v, sigma))) : 0u) | sign;
 }
 
 __device__ __forceinline__ float e4m3_value(uint32_t s) {

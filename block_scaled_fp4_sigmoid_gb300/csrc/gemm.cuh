@@ -60,12 +60,18 @@ struct KParams {
   int32_t* status;
   int E, n_exp, H, I, K, rows_per_expert, m_tiles, katoms_a, katoms_b, katoms_h, has_shared, T;
   int plan_early;  // the plan was written at least two kernels back (see the kernel)
+  // W8A8 (E4M3 operands): per-row fp32 scales of the weights (routed [E,
+  // rows], shared [rows]) and of the B rows (per permuted row); amax_h then
+  // holds the gate/up intermediate's |max| per permuted row
+  const float *wrs, *shrs, *brs;
 };
 
-template <int N, bool GATEUP, bool NV>
+// F8: E4M3 operands (W8A8), 128-value K tiles and no scale factors; else
+// block-scaled FP4, 256-value K tiles.
+template <int N, bool GATEUP, bool NV, bool F8 = false>
 struct GemmCfg {
   static constexpr int kA = GATEUP ? 2 : 1;          // A operands per unit (gate and up)
-  static constexpr int kAtoms = NV ? 4 : 2;          // scale groups per 256-wide K tile
+  static constexpr int kAtoms = F8 ? 0 : NV ? 4 : 2; // scale groups per K tile
   static constexpr int kABytes = 128 * 128;          // 128 rows x 128 bytes
   static constexpr int kBBytes = N * 128;
   static constexpr int kSFBytes = kAtoms * 512;      // per 128-row operand and K tile
@@ -131,9 +137,10 @@ __device__ __forceinline__ void decode_unit(const int32_t* s_start, const int32_
   cnt = min(N, count - ti * N);
 }
 
-template <int N, bool GATEUP, bool NV>
+template <int N, bool GATEUP, bool NV, bool F8 = false>
 __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant__ KParams p) {
-  using C = GemmCfg<N, GATEUP, NV>;
+  using C = GemmCfg<N, GATEUP, NV, F8>;
+  static_assert(!(F8 && NV), "one operand format");
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[C::kStages];
   __shared__ __align__(8) uint64_t bar_empty[C::kStages];
@@ -147,7 +154,7 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int KT = (p.K + 255) / 256;
+  const int KT = F8 ? (p.K + 127) / 128 : (p.K + 255) / 256;  // K tiles of 128 bytes
 
   static_assert(C::kThreads == 256, "launch bounds");
   if (threadIdx.x == 0) {
@@ -228,18 +235,22 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
     if (st.once) {
       tma_load_3d_hint(base, st.tmA, fb, kt * 128, st.row0, st.ec, pol_once);
       if constexpr (GATEUP) tma_load_3d_hint(base + C::kOffA1, st.tmA, fb, kt * 128, st.row1, st.ec, pol_once);
-      bulk_load_hint(base + C::kOffSFA0, st.sfa0 + kt * C::kSFBytes, C::kSFBytes, fb, pol_once);
-      if constexpr (GATEUP) bulk_load_hint(base + C::kOffSFA1, st.sfa1 + kt * C::kSFBytes, C::kSFBytes, fb, pol_once);
+      if constexpr (!F8) {
+        bulk_load_hint(base + C::kOffSFA0, st.sfa0 + kt * C::kSFBytes, C::kSFBytes, fb, pol_once);
+        if constexpr (GATEUP) bulk_load_hint(base + C::kOffSFA1, st.sfa1 + kt * C::kSFBytes, C::kSFBytes, fb, pol_once);
+      }
     } else {
       tma_load_3d(base, st.tmA, fb, kt * 128, st.row0, st.ec);
       if constexpr (GATEUP) tma_load_3d(base + C::kOffA1, st.tmA, fb, kt * 128, st.row1, st.ec);
-      bulk_load(base + C::kOffSFA0, st.sfa0 + kt * C::kSFBytes, C::kSFBytes, fb);
-      if constexpr (GATEUP) bulk_load(base + C::kOffSFA1, st.sfa1 + kt * C::kSFBytes, C::kSFBytes, fb);
+      if constexpr (!F8) {
+        bulk_load(base + C::kOffSFA0, st.sfa0 + kt * C::kSFBytes, C::kSFBytes, fb);
+        if constexpr (GATEUP) bulk_load(base + C::kOffSFA1, st.sfa1 + kt * C::kSFBytes, C::kSFBytes, fb);
+      }
     }
   };
   auto load_acts = [&](const Step& st, int kt, uint32_t base, uint32_t fb) {
     tma_load_2d(base + C::kOffB, &p.tmB, fb, kt * 128, st.slot * kSlotRows);
-    bulk_load(base + C::kOffSFB, st.sfb + kt * C::kSFBytes, C::kSFBytes, fb);
+    if constexpr (!F8) bulk_load(base + C::kOffSFB, st.sfb + kt * C::kSFBytes, C::kSFBytes, fb);
   };
 
   // The first pipeline stages start streaming weights before the wait, so
@@ -352,13 +363,17 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
           tc_cp_sf_elect(t_sfb + 4 * a, sfb_desc0 + so + 32 * a);
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int atom = NV ? j : (j >> 1);
-          const uint32_t sfid = NV ? 0u : (uint32_t)(j & 1) * 2u;
-          const uint32_t idesc = idesc_fp4(N, NV, sfid, sfid);
+        for (int j = 0; j < 4; ++j) {  // 32 bytes of the 128-byte swizzle row per MMA
           const uint32_t accum = (!first || j) ? 1u : 0u;
-          tc_mma_fp4_elect<NV>(t_acc, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc, t_sfa + 4 * atom,
-                               t_sfb + 4 * atom, accum);  // K = 64 per MMA: 32 bytes into the swizzle row
+          if constexpr (F8) {
+            tc_mma_f8_elect(t_acc, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc_f8(N), accum);  // K = 32
+          } else {
+            const int atom = NV ? j : (j >> 1);
+            const uint32_t sfid = NV ? 0u : (uint32_t)(j & 1) * 2u;
+            const uint32_t idesc = idesc_fp4(N, NV, sfid, sfid);
+            tc_mma_fp4_elect<NV>(t_acc, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc, t_sfa + 4 * atom,
+                                 t_sfb + 4 * atom, accum);  // K = 64
+          }
         }
         tc_commit_elect(smem_u32(&bar_empty[stage]));
         if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -399,10 +414,20 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
         float amax = 0.f;
         const uint32_t mask = p.tok_mask ? s_mask[e] : 0u;
         const int ncol = p.tok_mask ? p.T : cnt;  // accumulator columns holding tokens
+        // W8A8: this lane's gate and up row scales (channel scales of the
+        // converted weights)
+        float rg = 1.f, ru = 1.f;
+        if constexpr (F8) {
+          const float* rs = e >= p.E ? p.shrs : p.wrs + (int64_t)e * p.rows_per_expert;
+          rg = __ldg(rs + i0 + lane);
+          ru = __ldg(rs + p.I + i0 + lane);
+        }
         for (int c0 = 0; c0 < ncol; c0 += 32) {
           float g[32], uu[32];
           tc_ld32(ta + c0, g);
           tc_ld32(ta + N + c0, uu);
+          float sx = 0.f;  // W8A8: scale of the activation row of column c0 + lane
+          if constexpr (F8) sx = c0 + lane < ncol ? __ldg(p.brs + row0 + c0 + lane) : 0.f;
           tc_wait_ld();
           // lane l holds h(i0 + l, token c0 + j); transpose through shared memory
           // so that lane j then holds the 32 values of token c0 + j, one block
@@ -412,6 +437,11 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
             if constexpr (NV) {
               gv = gv * sc;
               uv = uv * sc;
+            }
+            if constexpr (F8) {
+              const float sxj = __shfl_sync(0xffffffffu, sx, j);
+              gv = gv * rg * sxj;
+              uv = uv * ru * sxj;
             }
             // silu(g) u with the hardware exponential and a correctly rounded
             // reciprocal (e^-g = inf for g < -88 gives -0, the limit)
@@ -432,12 +462,15 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
 #pragma unroll
               for (int r = 0; r < 8; ++r) dst[r] = make_float4(v[4 * r], v[4 * r + 1], v[4 * r + 2], v[4 * r + 3]);
             }
-            if constexpr (NV) {
+            if constexpr (NV || F8) {
               float4* dst = reinterpret_cast<float4*>(p.h32 + row * p.I + i0);
 #pragma unroll
               for (int r = 0; r < 8; ++r) dst[r] = make_float4(v[4 * r], v[4 * r + 1], v[4 * r + 2], v[4 * r + 3]);
+              float m = 0.f;
 #pragma unroll
-              for (int r = 0; r < 32; ++r) amax = fmaxf(amax, fabsf(v[r]));
+              for (int r = 0; r < 32; ++r) m = fmaxf(m, fabsf(v[r]));
+              if constexpr (F8) atomicMax(p.amax_h + row, __float_as_uint(m));  // per permuted row
+              else amax = fmaxf(amax, m);                                      // per expert
             } else {
               uint32_t pk[4], sb;
               mx_quant32(v, pk, &sb);
@@ -462,6 +495,9 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
         const int h0 = mt * 128 + 32 * q + 4 * (lane & 7);
         float sc = 1.f;
         if constexpr (NV) sc = __fmul_rn(__ldg(p.gb + e), __ldg(p.gw + e));
+        float rho = 1.f;  // W8A8: channel scale of this lane's output row
+        if constexpr (F8)
+          rho = __ldg((e >= p.E ? p.shrs : p.wrs + (int64_t)e * p.rows_per_expert) + mt * 128 + 32 * q + lane);
         for (int c0 = 0; c0 < cnt; c0 += 32) {
           float y[32];
           tc_ld32(ta + c0, y);  // even K tiles
@@ -479,9 +515,10 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
           if (lane < jn) {  // lane j fetches token and weight of column c0 + j
             tk = __ldg(p.row_tok + row0 + c0 + lane);
             wk = __ldg(p.row_w + row0 + c0 + lane) * sc;
+            if constexpr (F8) wk = __ldg(p.row_w + row0 + c0 + lane) * __ldg(p.brs + row0 + c0 + lane);
           }
 #pragma unroll
-          for (int j = 0; j < 32; ++j) tile[j][lane] = y[j];
+          for (int j = 0; j < 32; ++j) tile[j][lane] = F8 ? y[j] * rho : y[j];
           __syncwarp();
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -511,10 +548,10 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
   }
 }
 
-template <int N, bool GATEUP, bool NV>
+template <int N, bool GATEUP, bool NV, bool F8 = false>
 cudaError_t launch_gemm_t(const KParams& p, int grid, cudaStream_t s) {
-  using C = GemmCfg<N, GATEUP, NV>;
-  auto k = moe_gemm_kernel<N, GATEUP, NV>;
+  using C = GemmCfg<N, GATEUP, NV, F8>;
+  auto k = moe_gemm_kernel<N, GATEUP, NV, F8>;
   static bool attr_set[64] = {};  // once per device and template instance
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -13,21 +13,22 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   memset(&p, 0, sizeof(p));
   const int K = GATEUP ? d.H : d.I;
   const int rows = GATEUP ? 2 * d.I : d.H;
+  const uint64_t Kb = a.f8 ? (uint64_t)K : (uint64_t)K / 2;  // bytes of one K row (E4M3: 1, FP4: 1/2 per value)
   {
-    const uint64_t dims[3] = {(uint64_t)K / 2, (uint64_t)rows, (uint64_t)d.E};
-    const uint64_t strides[2] = {(uint64_t)K / 2, (uint64_t)rows * (K / 2)};
+    const uint64_t dims[3] = {Kb, (uint64_t)rows, (uint64_t)d.E};
+    const uint64_t strides[2] = {Kb, (uint64_t)rows * Kb};
     const uint32_t box[3] = {128, 128, 1};
     if (!encode_tmap_u8(&p.tmA, a.w, 3, dims, strides, box, true)) return cudaErrorInvalidValue;
   }
   if (a.sh) {
-    const uint64_t dims[3] = {(uint64_t)K / 2, (uint64_t)rows, 1};
-    const uint64_t strides[2] = {(uint64_t)K / 2, (uint64_t)rows * (K / 2)};
+    const uint64_t dims[3] = {Kb, (uint64_t)rows, 1};
+    const uint64_t strides[2] = {Kb, (uint64_t)rows * Kb};
     const uint32_t box[3] = {128, 128, 1};
     if (!encode_tmap_u8(&p.tmA_sh, a.sh, 3, dims, strides, box, true)) return cudaErrorInvalidValue;
   }
   {
-    const uint64_t dims[2] = {(uint64_t)K / 2, (uint64_t)a.rows_cap};
-    const uint64_t strides[1] = {(uint64_t)K / 2};
+    const uint64_t dims[2] = {Kb, (uint64_t)a.rows_cap};
+    const uint64_t strides[1] = {Kb};
     const uint32_t box[2] = {128, (uint32_t)a.n_tile};
     if (!encode_tmap_u8(&p.tmB, a.b, 2, dims, strides, box, true)) return cudaErrorInvalidValue;
   }
@@ -67,7 +68,19 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   p.katoms_b = (int)katoms_padded(K, a.nv);
   p.katoms_h = (int)katoms_padded(d.I, a.nv);
   p.has_shared = a.sh != nullptr;
+  p.wrs = a.wrs;
+  p.shrs = a.shrs;
+  p.brs = a.brs;
   const int grid = a.num_sms > 0 ? a.num_sms : 1;
+  if (a.f8) {
+    if (a.nv) return cudaErrorInvalidValue;
+    switch (a.n_tile) {
+      case 32: return launch_gemm_t<32, GATEUP, false, true>(p, grid, s);
+      case 64: return launch_gemm_t<64, GATEUP, false, true>(p, grid, s);
+      case 112: return launch_gemm_t<112, GATEUP, false, true>(p, grid, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (a.n_tile * 2 + (a.nv ? 1 : 0)) {
     case 32: return launch_gemm_t<16, GATEUP, false>(p, grid, s);  // few-token path (MXFP4)
     case 64: return launch_gemm_t<32, GATEUP, false>(p, grid, s);

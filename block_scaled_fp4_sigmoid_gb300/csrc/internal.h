@@ -84,6 +84,12 @@ cudaError_t launch_h_quant_nv_routes(const fp4moe_dims& d, const float* h32, con
                                      const int32_t* row_e, const uint32_t* amax_h, float* gh_out, uint8_t* hq,
                                      uint8_t* hsf, cudaStream_t s);
 cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, cudaStream_t s);
+// W8A8: x per token to E4M3 into its route rows (+ sigma per row); h per route
+// row to E4M3 with sigma from amax_row
+cudaError_t launch_fp8_x_quant(const fp4moe_dims& d, const uint16_t* x, const int32_t* route_row, uint8_t* xq,
+                               float* xsig, cudaStream_t s);
+cudaError_t launch_fp8_h_quant(const fp4moe_dims& d, const float* h32, const int32_t* route_row,
+                               const uint32_t* amax_row, uint8_t* hq, float* hsig, cudaStream_t s);
 cudaError_t launch_quantize_rows(const void* x, int x_is_fp32, int64_t rows, int cols, bool nv,
                                  const float* global_in, const uint32_t* amax_bits, uint8_t* codes,
                                  uint8_t* scales, float* global_out, cudaStream_t s);
@@ -96,6 +102,7 @@ cudaError_t launch_convert(const uint8_t* codes, const uint8_t* scales, int64_t 
 struct GemmArgs {
   const fp4moe_dims* d;
   bool nv;
+  bool f8;                         // W8A8: E4M3 operands with per-row fp32 scales (below)
   int n_tile;
   int num_sms;
   // weights
@@ -121,6 +128,9 @@ struct GemmArgs {
   float *out_acc;                  // down; gate/up: zeroed there when zero_acc
   bool zero_acc;                   // gate/up zeroes out_acc ([T, H] fp32) for the down GEMM
   int32_t *status;
+  // W8A8: channel scales of the weights (routed [E, rows], shared [rows]),
+  // scales of the B rows (per permuted row); amax_h is then per permuted row
+  const float *wrs, *shrs, *brs;
 };
 
 cudaError_t launch_gateup(const GemmArgs& a, cudaStream_t s);

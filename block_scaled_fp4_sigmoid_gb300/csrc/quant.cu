@@ -161,6 +161,79 @@ __global__ void h_quant_nv_kernel(const float* h32, int I, int64_t n_routes, con
 
 // ---------------------------------------------------------------- scale repacking
 // One thread per 4-byte word of the destination: (matrix, row tile, group, m0, m1).
+// ---------------------------------------------------------------- W8A8 activations
+// Per-token dynamic E4M3 ("Kimi-K2.7-Code on Gaudi 2", section "Exact MXFP4
+// to FP8 per-channel conversion": the converted experts run with per-channel
+// weights and dynamic per-token activations).  sigma = amax / 448 and each
+// code = RNE_E4M3(v / sigma), saturating, both correctly rounded fp32 steps.
+constexpr int kF8Threads = 256;
+
+__device__ __forceinline__ float block_max(float m, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  float r = 0.f;
+#pragma unroll
+  for (int w = 0; w < kF8Threads / 32; ++w) r = fmaxf(r, red[w]);
+  return r;
+}
+
+// Four E4M3 codes packed little-endian: value j in byte j.
+__device__ __forceinline__ uint32_t fp8_pack4(float a, float b, float c, float d, float sigma) {
+  return fp8_code(a, sigma) | fp8_code(b, sigma) << 8 | fp8_code(c, sigma) << 16 | fp8_code(d, sigma) << 24;
+}
+
+// One CTA per token: the codes go to every route row of the token, sigma to
+// the row-scale array at those rows.
+__global__ void __launch_bounds__(kF8Threads) fp8_x_quant_kernel(const uint16_t* __restrict__ x, int H, int rpt,
+                                                                 const int32_t* __restrict__ route_row,
+                                                                 uint8_t* __restrict__ xq, float* __restrict__ xsig) {
+  __shared__ float red[kF8Threads / 32];
+  const int t = blockIdx.x;
+  const uint16_t* xr = x + (int64_t)t * H;
+  float m = 0.f;
+  for (int i = threadIdx.x * 8; i < H; i += kF8Threads * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xr + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      m = fmaxf(m, fmaxf(fabsf(bf16_to_f32((uint16_t)(w[k] & 0xFFFFu))), fabsf(bf16_to_f32((uint16_t)(w[k] >> 16)))));
+  }
+  const float sig = __fdiv_rn(block_max(m, red), 448.0f);
+  for (int i = threadIdx.x * 8; i < H; i += kF8Threads * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xr + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float f[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      f[2 * k] = bf16_to_f32((uint16_t)(w[k] & 0xFFFFu));
+      f[2 * k + 1] = bf16_to_f32((uint16_t)(w[k] >> 16));
+    }
+    const uint2 c = make_uint2(fp8_pack4(f[0], f[1], f[2], f[3], sig), fp8_pack4(f[4], f[5], f[6], f[7], sig));
+    for (int j = 0; j < rpt; ++j) *reinterpret_cast<uint2*>(xq + (int64_t)route_row[(int64_t)t * rpt + j] * H + i) = c;
+  }
+  if (threadIdx.x < rpt) xsig[route_row[(int64_t)t * rpt + threadIdx.x]] = sig;
+}
+
+// One CTA per route: the intermediate row h (fp32) to E4M3 with sigma from
+// the row's |max|, gathered by the gate/up epilogue.
+__global__ void __launch_bounds__(kF8Threads) fp8_h_quant_kernel(const float* __restrict__ h32, int I,
+                                                                 const int32_t* __restrict__ route_row,
+                                                                 const uint32_t* __restrict__ amax_row,
+                                                                 uint8_t* __restrict__ hq, float* __restrict__ hsig) {
+  const int64_t row = route_row[blockIdx.x];
+  const float sig = __fdiv_rn(__uint_as_float(amax_row[row]), 448.0f);
+  const float* hr = h32 + row * I;
+  for (int i = threadIdx.x * 8; i < I; i += kF8Threads * 8) {
+    const float4 a = *reinterpret_cast<const float4*>(hr + i);
+    const float4 b = *reinterpret_cast<const float4*>(hr + i + 4);
+    *reinterpret_cast<uint2*>(hq + row * I + i) =
+        make_uint2(fp8_pack4(a.x, a.y, a.z, a.w, sig), fp8_pack4(b.x, b.y, b.z, b.w, sig));
+  }
+  if (threadIdx.x == 0) hsig[row] = sig;
+}
+
 __global__ void pack_scales_kernel(const uint8_t* src, uint8_t* dst, int64_t n_mat, int rows, int kblocks,
                                    int64_t katoms, uint8_t pad) {
   const int64_t words = n_mat * (rows / 128) * katoms * 128;
@@ -512,6 +585,21 @@ cudaError_t launch_h_quant_nv_routes(const fp4moe_dims& d, const float* h32, con
   const int64_t n = std::max<int64_t>(n_routes * (d.I >> 5), d.E + d.n_shared);
   h_quant_nv_kernel<<<blocks_for(n, 256), 256, 0, s>>>(h32, d.I, n_routes, route_row, row_e, amax_h, gh_out, hq,
                                                         hsf, d.E + d.n_shared);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_x_quant(const fp4moe_dims& d, const uint16_t* x, const int32_t* route_row, uint8_t* xq,
+                               float* xsig, cudaStream_t s) {
+  if (d.T <= 0) return cudaSuccess;
+  fp8_x_quant_kernel<<<(unsigned)d.T, kF8Threads, 0, s>>>(x, d.H, d.top_k + d.n_shared, route_row, xq, xsig);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_h_quant(const fp4moe_dims& d, const float* h32, const int32_t* route_row,
+                               const uint32_t* amax_row, uint8_t* hq, float* hsig, cudaStream_t s) {
+  const int64_t n_routes = (int64_t)d.T * (d.top_k + d.n_shared);
+  if (n_routes <= 0) return cudaSuccess;
+  fp8_h_quant_kernel<<<(unsigned)n_routes, kF8Threads, 0, s>>>(h32, d.I, route_row, amax_row, hq, hsig);
   return cudaGetLastError();
 }
 

@@ -14,8 +14,9 @@ import ctypes
 
 import torch
 
-from . import (MXFP4, NVFP4, Debug, Weights, forward, make_dims, pack_scales, packed_scales_bytes,
-               quantize_act, workspace_layout, workspace_size)
+from . import (FP8, MXFP4, NVFP4, Debug, Fp8Weights, Weights, forward, forward_w8a8, get_status, make_dims,
+               mxfp4_to_fp8_rowscale, pack_scales, packed_scales_bytes, quantize_act, workspace_layout,
+               workspace_size)
 
 
 def _ptr(t):
@@ -31,6 +32,7 @@ class MoELayer:
         self.dims = dims
         self.fmt = dims.fmt
         self.device = w13.device
+        self.raw = dict(w13_scale=w13_scale, w2_scale=w2_scale, sh13_scale=sh13_scale, sh2_scale=sh2_scale)
         blk = 16 if dims.fmt == NVFP4 else 32
         self.w13, self.w2 = w13.contiguous(), w2.contiguous()
         self.w13_scale = self._pack(w13_scale, dims.E, 2 * dims.I, dims.H // blk)
@@ -135,3 +137,66 @@ class MoELayer:
         x = torch.empty((t1 - t0, cfg.H), dtype=torch.int16, device=self.device)
         synth.dev_normal_bf16(cfg.seed, synth.S_X, t0 * cfg.H, x, cfg.x_std)
         return x.view(torch.bfloat16)
+
+
+class W8A8Layer:
+    """The W8A8 form of an MXFP4 ``MoELayer``: every expert matrix converted
+    exactly to E4M3 with one fp32 power-of-two scale per row by
+    fp4moe_mxfp4_to_fp8_rowscale, run by fp4moe_forward_w8a8 (per-token
+    dynamic E4M3 activations).  Same routing weights, shape and device."""
+
+    def __init__(self, mx: MoELayer):
+        d = mx.dims
+        if d.fmt != MXFP4:
+            raise ValueError("the exact FP8 conversion starts from MXFP4 experts")
+        self.mx = mx
+        self.device = mx.device
+        self.dims = make_dims(d.T, d.H, d.I, d.E, d.top_k, d.n_group, d.topk_group, d.n_shared, d.routed_scaling,
+                              d.renormalize, FP8)
+        s = torch.cuda.current_stream(self.device).cuda_stream
+        ws = torch.zeros(256, dtype=torch.uint8, device=self.device)
+
+        def conv(codes, raw, n_mat, rows, K):
+            out = torch.empty((n_mat, rows, K), dtype=torch.uint8, device=self.device)
+            rs = torch.empty((n_mat, rows), dtype=torch.float32, device=self.device)
+            mxfp4_to_fp8_rowscale(codes.data_ptr(), raw.data_ptr(), n_mat * rows, K, out.data_ptr(), rs.data_ptr(),
+                                  None, ws.data_ptr(), 256, s)
+            return out, rs
+
+        self.w13, self.w13_scale = conv(mx.w13, mx.raw["w13_scale"], d.E, 2 * d.I, d.H)
+        self.w2, self.w2_scale = conv(mx.w2, mx.raw["w2_scale"], d.E, d.H, d.I)
+        self.sh13 = self.sh13_scale = self.sh2 = self.sh2_scale = None
+        if d.n_shared:
+            self.sh13, self.sh13_scale = conv(mx.sh13, mx.raw["sh13_scale"], 1, 2 * d.I, d.H)
+            self.sh2, self.sh2_scale = conv(mx.sh2, mx.raw["sh2_scale"], 1, d.H, d.I)
+        st, n = get_status(ws.data_ptr(), s)
+        if st != 0:
+            raise ValueError(f"{n} expert rows are outside the exact conversion's contract (status {st})")
+        self.ws_bytes = workspace_size(self.dims)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        self.layout = workspace_layout(self.dims)
+        self.weights = Fp8Weights(_ptr(self.w13), _ptr(self.w13_scale), _ptr(self.w2), _ptr(self.w2_scale),
+                                  _ptr(self.sh13), _ptr(self.sh13_scale), _ptr(self.sh2), _ptr(self.sh2_scale),
+                                  _ptr(mx.w_router), _ptr(mx.bias))
+        self.cfg = getattr(mx, "cfg", None)
+
+    def weight_bytes_per_expert(self) -> int:
+        """E4M3 bytes plus fp32 row scales of one routed expert (w13 and w2)."""
+        d = self.dims
+        return 3 * d.H * d.I + 4 * (2 * d.I + d.H)
+
+    def forward(self, x, out=None, debug: Debug | None = None, stream=None):
+        d = self.dims
+        if out is None:
+            out = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=self.device)
+        s = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
+        forward_w8a8(d, self.weights, x.data_ptr(), out.data_ptr(), self.ws.data_ptr(), self.ws_bytes, s, debug)
+        return out
+
+    def ws_view(self, name: str, dtype, count: int):
+        off = getattr(self.layout, name)
+        nbytes = count * torch.empty((), dtype=dtype).element_size()
+        return self.ws[off:off + nbytes].view(dtype)
+
+    def synthetic_x(self, t0: int = 0, t1: int | None = None):
+        return self.mx.synthetic_x(t0, t1)

@@ -61,7 +61,9 @@ typedef enum {
   FP4MOE_ERR_DEVICE = 8             /* no sm_103 device is current             */
 } fp4moe_status;
 
-typedef enum { FP4MOE_MXFP4 = 0, FP4MOE_NVFP4 = 1 } fp4moe_format;
+/* FP4MOE_FP8: the W8A8 layer of fp4moe_forward_w8a8 (E4M3 experts from the
+ * exact conversion, per-token dynamic E4M3 activations). */
+typedef enum { FP4MOE_MXFP4 = 0, FP4MOE_NVFP4 = 1, FP4MOE_FP8 = 2 } fp4moe_format;
 
 /* Layer shape and routing parameters.
  *   T tokens, H hidden size, I expert intermediate size, E routed experts,
@@ -97,6 +99,26 @@ typedef struct {
   const float *bias;
 } fp4moe_weights;
 
+/* W8A8 expert weights: each expert matrix as fp4moe_mxfp4_to_fp8_rowscale
+ * leaves it ("Kimi-K2.7-Code on Gaudi 2", section "Exact MXFP4 to FP8
+ * per-channel conversion": E4M3 bytes and one fp32 power-of-two scale per row).
+ *   w13 [E, 2I, H] E4M3 (gate rows, then up rows), w13_scale [E, 2I] fp32;
+ *   w2 [E, H, I] E4M3, w2_scale [E, H] fp32;
+ *   sh13 / sh13_scale / sh2 / sh2_scale: the shared expert (E = 1), NULL
+ *   when n_shared == 0;  w_router bf16 [E, H];  bias fp32 [E]. */
+typedef struct {
+  const uint8_t *w13;
+  const float *w13_scale;
+  const uint8_t *w2;
+  const float *w2_scale;
+  const uint8_t *sh13;
+  const float *sh13_scale;
+  const uint8_t *sh2;
+  const float *sh2_scale;
+  const uint16_t *w_router;
+  const float *bias;
+} fp4moe_fp8_weights;
+
 /* Byte offsets of the forward's intermediates inside the workspace, for
  * inspection after a call (all relative to the workspace base).  Row indices
  * refer to the padded permuted layout: routes of one expert occupy tiles of
@@ -113,11 +135,14 @@ typedef struct {
   int64_t route_row;    /* int32 [T, top_k + n_shared] padded row of route  */
   int64_t row_tok;      /* int32 [rows_cap] token of each padded row        */
   int64_t row_w;        /* fp32  [rows_cap] routing weight of each row      */
-  int64_t xq;           /* u8 [rows_cap, H/2] quantised activations         */
-  int64_t xsf;          /* u8 tiled scales of xq (fp4moe_pack_scales layout) */
-  int64_t hq;           /* u8 [rows_cap, I/2] quantised intermediate        */
-  int64_t hsf;          /* u8 tiled scales of hq                            */
-  int64_t h32;          /* fp32 [rows_cap, I] pre-quantisation h (NVFP4)    */
+  int64_t xq;           /* u8 [rows_cap, H/2] quantised activations (FP8:
+                         * [rows_cap, H] E4M3)                               */
+  int64_t xsf;          /* u8 tiled scales of xq (fp4moe_pack_scales layout);
+                         * FP8: fp32 [rows_cap] per-row scales              */
+  int64_t hq;           /* u8 [rows_cap, I/2] quantised intermediate (FP8:
+                         * [rows_cap, I] E4M3)                               */
+  int64_t hsf;          /* u8 tiled scales of hq; FP8: fp32 [rows_cap]      */
+  int64_t h32;          /* fp32 [rows_cap, I] pre-quantisation h (NVFP4, FP8) */
   int64_t gscale;       /* fp32 [2 + E + n_shared]: g_x, spare, g_h[e]       */
   int64_t out_acc;      /* fp32 [T, H] combine accumulator                  */
   int64_t total_bytes;
@@ -224,6 +249,22 @@ fp4moe_status fp4moe_quantize_act(const void *x, int32_t x_is_fp32, int64_t rows
 fp4moe_status fp4moe_forward(const fp4moe_dims *dims, const fp4moe_weights *w, const uint16_t *x,
                              uint16_t *out, const fp4moe_debug *dbg, void *ws, size_t ws_bytes,
                              void *stream);
+
+/* The W8A8 MoE layer on the exactly converted FP8 experts ("Kimi-K2.7-Code on
+ * Gaudi 2", section "Exact MXFP4 to FP8 per-channel conversion": per-channel
+ * FP8 weights, dynamic per-token FP8 activations).  Routing and permutation
+ * as in fp4moe_forward; each token's x and each route's intermediate h are
+ * quantised to E4M3 with sigma = amax / 448 over the row (code = RNE(v /
+ * sigma), saturating; both correctly rounded fp32 steps; sigma = 0 gives
+ * signed zeros); the expert GEMMs multiply E4M3 by E4M3 on the tensor cores
+ * and apply the weight row scale and sigma in their epilogues.
+ *   dims->fmt must be FP4MOE_FP8; w as fp4moe_fp8_weights; x, out bf16
+ *   [T, H]; ws: fp4moe_workspace_size(dims) bytes (its layout as
+ *   fp4moe_workspace_layout describes, with the FP8 meanings); dbg as for
+ *   fp4moe_forward (nullable).  Pointers 16-byte aligned. */
+fp4moe_status fp4moe_forward_w8a8(const fp4moe_dims *dims, const fp4moe_fp8_weights *w, const uint16_t *x,
+                                  uint16_t *out, const fp4moe_debug *dbg, void *ws, size_t ws_bytes,
+                                  void *stream);
 
 /* Exact MXFP4 -> FP8 (E4M3) per-channel conversion ("Kimi-K2.7-Code on
  * Gaudi 2", section "Exact MXFP4 to FP8 per-channel conversion").
