@@ -270,6 +270,115 @@ def time_conversion(layer, peaks, stream, reps: int = 5):
             "bound": "hbm", "l2": "inputs and outputs (25.9 GB) far exceed L2"}
 
 
+# ------------------------------------------------------------------ dense linear
+def linear_arm(args, rank, world, local_rank):
+    """fp4moe_linear on one dense shape: out[T, N] = quantize(x)[T, K] . W^T,
+    MXFP4 weights of the synthetic recipe, bf16 x ~ N(0, 1), drawn on the
+    device.  FLOPs 2 T K N per call; the roofline is the dense FP4 tensor
+    peak (6 x the measured bf16 peak, the nominal 13.5 / 2.25 ratio)."""
+    import numpy as np
+    import torch
+    import block_scaled_fp4_sigmoid_gb300 as fm
+    import synth
+    import __graft_entry__
+
+    __graft_entry__.build()
+    T, K, N = (int(v) for v in args.linear.split(","))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+    seed = 0
+    x = torch.empty((T, K), dtype=torch.int16, device=dev)
+    synth.dev_normal_bf16(seed, synth.S_X, rank * T * K, x, 1.0)
+    x = x.view(torch.bfloat16)
+    codes = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+    cs, ss = synth._mx_streams("w2")
+    synth.dev_uniform_bytes(seed, cs, 0, codes)
+    raw = torch.empty((N, K // 32), dtype=torch.uint8, device=dev)
+    synth.dev_e8m0_scales(seed, ss, 0, N, K // 32, raw)
+    sf = torch.empty(fm.packed_scales_bytes(1, N, K // 32, fm.MXFP4), dtype=torch.uint8, device=dev)
+    fm.pack_scales(raw.data_ptr(), sf.data_ptr(), 1, N, K // 32, fm.MXFP4, s)
+    out = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+    n = fm.linear_workspace_size(fm.MXFP4, T, K, N)
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def call(xp=None):
+        fm.linear(fm.MXFP4, T, K, N, (xp if xp is not None else x).data_ptr(), codes.data_ptr(), sf.data_ptr(),
+                  None, out.data_ptr(), ws.data_ptr(), n, s)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        call()
+    torch.cuda.synchronize()
+    assert fm.get_status(ws.data_ptr(), s) == (0, 0)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    # end to end: host x in, host out back, every step
+    xh = x.cpu().pin_memory()
+    oh = torch.empty((T, N), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(x)
+    e2e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+    for i in range(20):
+        flush.fill_(float(i))
+        e2e[i][0].record(stream)
+        xd.copy_(xh, non_blocking=True)
+        call(xd)
+        oh.copy_(out, non_blocking=True)
+        e2e[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e)
+    vals = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    ms, e2e_ms = vals.tolist()
+    if rank != 0:
+        return
+    flops = 2.0 * T * K * N
+    peaks = measured_peaks()
+    fp4_peak = 6 * peaks["bf16_tflops"]
+    tflops = flops * world / (ms * 1e-3) / 1e12
+    # CPU baseline: the oracle on a bounded sample of rows
+    from oracle import linear as LIN
+    from oracle.formats import unpack_nibbles
+    rows = 4
+    xs = x[:rows].float().cpu().numpy().astype(np.float64)
+    wc, wsc = unpack_nibbles(codes.cpu().numpy()), raw.cpu().numpy()
+    t0 = time.perf_counter()
+    LIN.linear_forward(xs, wc, wsc, "mxfp4")
+    cpu_s = time.perf_counter() - t0
+    line = {
+        "metric": "dense block-scaled FP4 linear TFLOP/s", "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "mxfp4", "data": "synthetic (seeded; drawn on the device)",
+        "config": {"workload": f"dense MXFP4 linear T={T} K={K} N={N} (bf16 in, on-the-fly activation quantisation, "
+                               f"bf16 out)", "l2": "flushed between steps (256 MiB write, untimed)"},
+        "clocks": clk.summary(),
+        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": T * K * 2, "d2h_bytes_per_step": T * N * 2},
+        "gpu_launches": 5 * args.steps,
+        "roofline": {"bound": "tensor", "kernel": "moe_gemm_kernel<down> (one expert)", "achieved": tflops / world,
+                     "peak": fp4_peak, "unit": "TFLOP/s", "frac": tflops / world / fp4_peak, "traffic": None,
+                     "peak_source": peaks["source"] + " bf16 x 6 (nominal dense FP4 / bf16)"},
+        "cpu_baseline": {"value": 2.0 * rows * K * N / cpu_s / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": f"{rows} rows of the same shape, FP64 numpy"},
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ GPU arm
 def gpu_arm(args, cfg, rank, world, local_rank):
     import numpy as np
@@ -490,6 +599,8 @@ def main():
     ap.add_argument("--experts", type=int, default=None,
                     help="override E (smaller device footprint for profiler captures)")
     ap.add_argument("--tokens", type=int, default=None, help="override T")
+    ap.add_argument("--linear", default=None, metavar="T,K,N",
+                    help="time the dense block-scaled FP4 linear (fp4moe_linear) on this shape instead")
     ap.add_argument("--w8a8", action="store_true",
                     help="the W8A8 layer: experts exactly converted to FP8 per channel, FP8 per-token activations")
     ap.add_argument("--conversion", action="store_true",
@@ -515,7 +626,10 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
-        gpu_arm(args, cfg, rank, world, local_rank)
+        if args.linear:
+            linear_arm(args, rank, world, local_rank)
+        else:
+            gpu_arm(args, cfg, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

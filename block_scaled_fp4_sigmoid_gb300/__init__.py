@@ -90,11 +90,15 @@ def lib() -> ctypes.CDLL:
         L.fp4moe_quantize_act.argtypes = [vp, i32, i64, i32, i32, vp, vp, vp, vp, vp, sz, vp]
         L.fp4moe_forward.argtypes = [P(Dims), P(Weights), vp, vp, P(Debug), vp, sz, vp]
         L.fp4moe_forward_w8a8.argtypes = [P(Dims), P(Fp8Weights), vp, vp, P(Debug), vp, sz, vp]
+        L.fp4moe_linear_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.fp4moe_linear_workspace_size.restype = sz
+        L.fp4moe_linear.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
         L.fp4moe_mxfp4_to_fp8_rowscale.argtypes = [vp, vp, i64, i32, vp, vp, vp, vp, sz, vp]
         L.fp4moe_clear_status.argtypes = [vp, vp]
         L.fp4moe_get_status.argtypes = [vp, vp, P(i32), P(i64)]
         for name in ("fp4moe_workspace_layout", "fp4moe_pack_scales", "fp4moe_route", "fp4moe_quantize_act",
-                     "fp4moe_forward", "fp4moe_forward_w8a8", "fp4moe_mxfp4_to_fp8_rowscale", "fp4moe_clear_status",
+                     "fp4moe_forward", "fp4moe_forward_w8a8", "fp4moe_linear", "fp4moe_mxfp4_to_fp8_rowscale",
+                     "fp4moe_clear_status",
                      "fp4moe_get_status"):
             getattr(L, name).restype = i32
         _LIB = L
@@ -166,6 +170,18 @@ def forward_w8a8(dims: Dims, weights: Fp8Weights, x: int, out: int, ws: int, ws_
     dbg = ctypes.byref(debug) if debug is not None else None
     _ok(lib().fp4moe_forward_w8a8(ctypes.byref(dims), ctypes.byref(weights), x, out, dbg, ws, ws_bytes, stream),
         "fp4moe_forward_w8a8")
+
+
+def linear_workspace_size(fmt: int, T: int, K: int, N: int) -> int:
+    n = lib().fp4moe_linear_workspace_size(fmt, T, K, N)
+    if n == 0:
+        raise Fp4MoeError(2, "fp4moe_linear_workspace_size")
+    return n
+
+
+def linear(fmt: int, T: int, K: int, N: int, x: int, w: int, w_scale: int, g_w: int | None, out: int, ws: int,
+           ws_bytes: int, stream: int = 0) -> None:
+    _ok(lib().fp4moe_linear(fmt, T, K, N, x, w, w_scale, g_w, out, ws, ws_bytes, stream), "fp4moe_linear")
 
 
 def mxfp4_to_fp8_rowscale(codes: int, scales: int, rows: int, K: int, fp8_out: int, row_scale: int,

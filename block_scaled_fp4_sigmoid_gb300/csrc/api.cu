@@ -146,6 +146,31 @@ bool make_layout(const fp4moe_dims& d, Layout* L) {
   return true;
 }
 
+// Dense linear as a one-expert MoE layer: the down GEMM's view (H = N output
+// rows, I = K), top-1, one token per route.
+fp4moe_dims linear_dims(int32_t fmt, int32_t T, int32_t K, int32_t N) {
+  fp4moe_dims d;
+  memset(&d, 0, sizeof(d));
+  d.T = T;
+  d.H = N;
+  d.I = K;
+  d.E = 1;
+  d.top_k = 1;
+  d.n_group = 1;
+  d.topk_group = 1;
+  d.n_shared = 0;
+  d.routed_scaling = 1.0f;
+  d.renormalize = 0;
+  d.fmt = fmt;
+  return d;
+}
+
+bool linear_layout(int32_t fmt, int32_t T, int32_t K, int32_t N, Layout* L) {
+  if (fmt != FP4MOE_MXFP4 && fmt != FP4MOE_NVFP4) return false;
+  if (K < 256 || K % 256 != 0 || N < 256 || N % 256 != 0) return false;
+  return make_layout(linear_dims(fmt, T, K, N), L);
+}
+
 }  // namespace fp4moe
 
 using namespace fp4moe;
@@ -516,6 +541,83 @@ fp4moe_status fp4moe_forward_w8a8(const fp4moe_dims* dims, const fp4moe_fp8_weig
   if (e == cudaSuccess) e = rec(6);
   if (e == cudaSuccess) e = launch_finalize(acc, out, (int64_t)d.T * d.H, s);
   if (e == cudaSuccess) e = rec(7);
+  return cuda_status(e);
+}
+
+size_t fp4moe_linear_workspace_size(int32_t fmt, int32_t T, int32_t K, int32_t N) {
+  Layout L;
+  if (!linear_layout(fmt, T, K, N, &L)) return 0;
+  return (size_t)L.ws.total_bytes;
+}
+
+fp4moe_status fp4moe_linear(int32_t fmt, int32_t T, int32_t K, int32_t N, const uint16_t* x, const uint8_t* w,
+                            const uint8_t* w_scale, const float* g_w, uint16_t* out, void* ws, size_t ws_bytes,
+                            void* stream) {
+  if (!x || !w || !w_scale || !out || !ws) return FP4MOE_ERR_INVALID_ARG;
+  if (fmt != FP4MOE_MXFP4 && fmt != FP4MOE_NVFP4) return FP4MOE_ERR_INVALID_ARG;
+  if (fmt == FP4MOE_NVFP4 && !g_w) return FP4MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (!linear_layout(fmt, T, K, N, &L)) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  if (ws_bytes < (size_t)L.ws.total_bytes) return FP4MOE_ERR_WORKSPACE;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(w_scale) || !aligned16(out) || !aligned16(ws))
+    return FP4MOE_ERR_INVALID_ARG;
+  if (fp4moe_status st = check_device()) return st;
+  const int num_sms = device_sm_count();
+  if (num_sms <= 0) return FP4MOE_ERR_DEVICE;
+  const bool nv = fmt == FP4MOE_NVFP4;
+  const fp4moe_dims dg = linear_dims(fmt, T, K, N);  // GEMM view: H = N output rows, I = K
+  fp4moe_dims dq = dg;                               // quantiser view: rows of K values, one route each
+  dq.H = K;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  auto P = [&](int64_t off) { return base + off; };
+  int32_t* status = reinterpret_cast<int32_t*>(P(L.ws.status));
+  Plan* plan = reinterpret_cast<Plan*>(P(L.plan));
+  int32_t* ecount = reinterpret_cast<int32_t*>(P(L.ws.expert_count));
+  int32_t* eslot = reinterpret_cast<int32_t*>(P(L.ws.expert_slot));
+  int32_t* dn_start = reinterpret_cast<int32_t*>(P(L.dn_start));
+  int32_t* route_row = reinterpret_cast<int32_t*>(P(L.ws.route_row));
+  int32_t* row_tok = reinterpret_cast<int32_t*>(P(L.ws.row_tok));
+  float* row_w = reinterpret_cast<float*>(P(L.ws.row_w));
+  uint8_t* xq = P(L.ws.hq);    // the B operand of the down GEMM: rows of K/2 bytes
+  uint8_t* xsf = P(L.ws.hsf);
+  float* gscale = reinterpret_cast<float*>(P(L.ws.gscale));
+  uint32_t* amax = reinterpret_cast<uint32_t*>(P(L.amax));
+  float* acc = reinterpret_cast<float*>(P(L.ws.out_acc));
+  const int n_tile = L.ws.n_tile;
+
+  cudaError_t e = cudaMemsetAsync(status, 0, kStatusInts * 4, s);
+  if (e == cudaSuccess && nv) e = cudaMemsetAsync(amax, 0, 8, s);
+  if (e == cudaSuccess)
+    e = launch_linear_plan(T, n_tile, N / 128, ecount, eslot, dn_start, plan, route_row, row_tok, row_w, acc,
+                           (int64_t)T * N, s);
+  if (e == cudaSuccess && nv) e = launch_amax(x, 0, (int64_t)T * K, amax, s);
+  if (e == cudaSuccess) e = launch_gather_quant(dq, x, route_row, xq, xsf, amax, gscale, s);
+  if (e == cudaSuccess) {
+    GemmArgs g;
+    memset(&g, 0, sizeof(g));
+    g.d = &dg;
+    g.nv = nv;
+    g.n_tile = n_tile;
+    g.num_sms = num_sms;
+    g.w = w;
+    g.wsf = w_scale;
+    g.gw = g_w;
+    g.b = xq;
+    g.bsf = xsf;
+    g.rows_cap = L.ws.rows_cap;
+    g.expert_count = ecount;
+    g.expert_slot = eslot;
+    g.unit_start = dn_start;
+    g.plan = plan;
+    g.row_tok = row_tok;
+    g.row_w = row_w;
+    g.g_b = gscale;  // NVFP4: g_x
+    g.out_acc = acc;
+    g.status = status;
+    e = launch_down(g, s);
+  }
+  if (e == cudaSuccess) e = launch_finalize(acc, out, (int64_t)T * N, s);
   return cuda_status(e);
 }
 

@@ -51,6 +51,11 @@ cudaError_t launch_topk(const fp4moe_dims& d, const float* partial, int n_splits
 cudaError_t launch_plan(const fp4moe_dims& d, int32_t* chunk_counts, int n_chunks, int n_exp, int n_tile,
                         int32_t* expert_count, int32_t* expert_slot, int32_t* gu_start, int32_t* dn_start,
                         Plan* plan, int32_t* ticket, cudaStream_t s);
+// Dense linear: one expert holding every token in order, weight 1; zeroes acc
+// (acc_n floats, a multiple of 4)
+cudaError_t launch_linear_plan(int T, int n_tile, int m_tiles, int32_t* count, int32_t* slot, int32_t* dn_start,
+                               Plan* plan, int32_t* route_row, int32_t* row_tok, float* row_w, float* acc,
+                               int64_t acc_n, cudaStream_t s);
 cudaError_t launch_scatter(const fp4moe_dims& d, const int32_t* idx, const float* w, const int32_t* chunk_counts,
                            int n_chunks, int n_exp, int n_tile, const int32_t* expert_slot, int32_t* route_row,
                            int32_t* row_tok, float* row_w, int32_t* row_e, cudaStream_t s);

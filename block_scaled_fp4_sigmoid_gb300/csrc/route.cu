@@ -648,6 +648,35 @@ __global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArg
   }
 }
 
+// ---------------------------------------------------------------- dense linear plan
+// The dense linear runs the down GEMM's mainloop with one "expert" that every
+// token routes to once with weight 1: token t sits at row (t / n_tile) * 128 +
+// t % n_tile of the padded layout.  Also zeroes the fp32 output accumulator.
+__global__ void linear_plan_kernel(int T, int n_tile, int m_tiles, int32_t* __restrict__ count,
+                                   int32_t* __restrict__ slot, int32_t* __restrict__ dn_start, Plan* __restrict__ plan,
+                                   int32_t* __restrict__ route_row, int32_t* __restrict__ row_tok,
+                                   float* __restrict__ row_w, float4* __restrict__ acc, int64_t acc_n4) {
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, nthr = (int64_t)gridDim.x * blockDim.x;
+  const int tiles = (T + n_tile - 1) / n_tile;
+  if (tid == 0) {
+    count[0] = T;
+    slot[0] = 0;
+    dn_start[0] = 0;
+    dn_start[1] = tiles * m_tiles;
+    plan->n_exp = 1;
+    plan->gu_units = 0;
+    plan->dn_units = tiles * m_tiles;
+    plan->slots = tiles;
+  }
+  for (int64_t t = tid; t < T; t += nthr) {
+    const int row = (int)(t / n_tile) * kSlotRows + (int)(t % n_tile);
+    route_row[t] = row;
+    row_tok[row] = (int32_t)t;
+    row_w[row] = 1.0f;
+  }
+  for (int64_t i = tid; i < acc_n4; i += nthr) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 }  // namespace
 
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* wr, float* partial, int T, int H, int E,
@@ -717,6 +746,14 @@ cudaError_t launch_decode_front(const FrontArgs& a, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_front_kernel, a);
+}
+
+cudaError_t launch_linear_plan(int T, int n_tile, int m_tiles, int32_t* count, int32_t* slot, int32_t* dn_start,
+                               Plan* plan, int32_t* route_row, int32_t* row_tok, float* row_w, float* acc,
+                               int64_t acc_n, cudaStream_t s) {
+  linear_plan_kernel<<<4 * 152, 256, 0, s>>>(T, n_tile, m_tiles, count, slot, dn_start, plan, route_row, row_tok,
+                                            row_w, reinterpret_cast<float4*>(acc), acc_n / 4);
+  return cudaGetLastError();
 }
 
 }  // namespace fp4moe

@@ -266,6 +266,21 @@ fp4moe_status fp4moe_forward_w8a8(const fp4moe_dims *dims, const fp4moe_fp8_weig
                                   uint16_t *out, const fp4moe_debug *dbg, void *ws, size_t ws_bytes,
                                   void *stream);
 
+/* Dense block-scaled FP4 linear layer ("Serve Kimi-K2.5-MXFP4 on MI355X with
+ * ATOM", section "Stage C: MXFP4 Linear GEMM": bf16 activations quantised
+ * on the fly, block-scaled FP4 product, bf16 output):
+ *   out[T, N] = quantize(x)[T, K] . W[N, K]^T
+ *   x bf16 [T, K] quantised as fp4moe_quantize_act does (MXFP4 per 32;
+ *   NVFP4 per 16 with one tensor scale over x); w packed FP4 [N, K/2];
+ *   w_scale its block scales repacked by fp4moe_pack_scales (n_mat = 1,
+ *   rows = N); g_w NVFP4 only: device fp32 tensor scale of W (NULL for MXFP4).
+ *   1 <= T <= 65536, K % 256 == 0, N % 256 == 0.  ws:
+ *   fp4moe_linear_workspace_size bytes.  Pointers 16-byte aligned. */
+size_t fp4moe_linear_workspace_size(int32_t fmt, int32_t T, int32_t K, int32_t N);
+fp4moe_status fp4moe_linear(int32_t fmt, int32_t T, int32_t K, int32_t N, const uint16_t *x, const uint8_t *w,
+                            const uint8_t *w_scale, const float *g_w, uint16_t *out, void *ws, size_t ws_bytes,
+                            void *stream);
+
 /* Exact MXFP4 -> FP8 (E4M3) per-channel conversion ("Kimi-K2.7-Code on
  * Gaudi 2", section "Exact MXFP4 to FP8 per-channel conversion").
  *   codes [rows, K/2] packed E2M1, scales [rows, K/32] E8M0 row-major ->
