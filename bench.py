@@ -319,12 +319,14 @@ def linear_arm(args, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
+        time.sleep(0.3)
         for i in range(args.steps):
             flush.fill_(float(i))
             ev[i][0].record(stream)
             call()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
+        time.sleep(0.3)
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     # end to end: host x in, host out back, every step
     xh = x.cpu().pin_memory()
