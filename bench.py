@@ -11,7 +11,8 @@ Between timed steps a 256 MiB buffer is written to flush L2 (untimed).  Each
 step is timed with CUDA events on the launching stream; the dominant kernel
 (gate/up GEMM) is timed by events recorded around its launch.
 
---w8a8 times the W8A8 layer instead: the same synthetic MXFP4 experts after the
+--emulate times an NVFP4 workload in emulation mode (BF16 dequantised experts,
+NVFP4 QDQ activations, BF16 GEMMs).  --w8a8 times the W8A8 layer instead: the same synthetic MXFP4 experts after the
 exact per-channel FP8 conversion, per-token dynamic E4M3 activations
 (fp4moe_forward_w8a8).
 
@@ -133,7 +134,8 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle timing
-def oracle_route_sample(cfg_name: str, n_routes: int, frac: float = 1.0, start_token: int = 0, w8a8: bool = False):
+def oracle_route_sample(cfg_name: str, n_routes: int, frac: float = 1.0, start_token: int = 0, w8a8: bool = False,
+                        emulate: bool = False):
     """Times the FP64 oracle on n_routes (token, expert) routes of the
     workload: each token's routing and x quantisation, then its expert MLPs.
     frac < 1 evaluates each MLP on the first frac * I intermediate channels
@@ -146,6 +148,7 @@ def oracle_route_sample(cfg_name: str, n_routes: int, frac: float = 1.0, start_t
     from oracle import inputs as OI
     from oracle import moe as M
     from oracle import quant as Q
+    from oracle import emulation as EM
     from oracle import w8a8 as W8
     from oracle.router import route, router_logits
     cfg = synth.configs()[cfg_name]
@@ -162,6 +165,8 @@ def oracle_route_sample(cfg_name: str, n_routes: int, frac: float = 1.0, start_t
         idx, w = route(logits, bias, cfg.top_k, cfg.n_group, cfg.topk_group, cfg.routed_scaling, cfg.renormalize)
         if w8a8:
             a = W8.fp8_dequant(*W8.fp8_quantize(x))
+        elif emulate:
+            a = EM.nv_dequant_bf16(*Q.nv_quantize(x))
         else:
             xc, xs, gx = Q.quantize(x, cfg.fmt)
             a = Q.dequant(xc, xs, cfg.fmt, gx)
@@ -186,6 +191,8 @@ def oracle_route_sample(cfg_name: str, n_routes: int, frac: float = 1.0, start_t
             t0 = time.perf_counter()
             if w8a8:
                 W8.expert_rows_fp8(sub, e, a, np.array([wt]), sub_ws, with_ambiguity=False)
+            elif emulate:
+                EM.emulated_expert_rows(sub, e, a, np.array([wt]), sub_ws, with_ambiguity=False)
             else:
                 M.expert_rows(sub, e, a, np.array([wt]), sub_ws, with_ambiguity=False)
             t_total += time.perf_counter() - t0
@@ -201,12 +208,12 @@ def reference_arm(args, cfg, rank, world):
     if rank != 0:
         return
     # size each step so that warm-up + steps take about two minutes
-    t_one, _ = oracle_route_sample(args.config, 1, w8a8=args.w8a8)
+    t_one, _ = oracle_route_sample(args.config, 1, w8a8=args.w8a8, emulate=args.emulate)
     budget = 120.0 / (args.steps + args.warmup)
     frac = min(1.0, budget / max(t_one, 1e-3))
     secs, toks = [], 0.0
     for i in range(args.warmup + args.steps):
-        sec, n = oracle_route_sample(args.config, 1, frac, start_token=i, w8a8=args.w8a8)
+        sec, n = oracle_route_sample(args.config, 1, frac, start_token=i, w8a8=args.w8a8, emulate=args.emulate)
         if i >= args.warmup:
             secs.append(sec)
             toks += n
@@ -217,7 +224,7 @@ def reference_arm(args, cfg, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(secs),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": cfg_label(cfg, args.w8a8),
+            "data": "synthetic", "config": {"workload": cfg_label(cfg, args.w8a8, args.emulate),
                                             "step": f"one (token, expert) route on {Ip} of {cfg.I} channels"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"{args.steps} routes of the {cfg.name} workload, {Ip}/{cfg.I} "
@@ -226,8 +233,10 @@ def reference_arm(args, cfg, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def cfg_label(cfg, w8a8: bool = False) -> str:
-    fmt = "FP8 W8A8 (experts exactly converted from MXFP4)" if w8a8 else f"{cfg.fmt.upper()} A4W4"
+def cfg_label(cfg, w8a8: bool = False, emulate: bool = False) -> str:
+    fmt = ("FP8 W8A8 (experts exactly converted from MXFP4)" if w8a8 else
+           "NVFP4 emulation (BF16 dequantised experts, NVFP4 QDQ activations)" if emulate else
+           f"{cfg.fmt.upper()} A4W4")
     return (f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.top_k}"
             f"{f' groups {cfg.n_group}/{cfg.topk_group}' if cfg.n_group > 1 else ''}"
             f"{' +1 shared' if cfg.n_shared else ''} {fmt}")
@@ -407,6 +416,9 @@ def gpu_arm(args, cfg, rank, world, local_rank):
         torch.cuda.empty_cache()
     # each rank runs its own batch: tokens rank*T .. (rank+1)*T of the stream
     x = layer.synthetic_x(rank * cfg.T, (rank + 1) * cfg.T)
+    if args.emulate and cfg.fmt != "nvfp4":
+        raise SystemExit("--emulate runs NVFP4 layers")
+    fwd = layer.forward_emulated if args.emulate else layer.forward
     out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     torch.cuda.synchronize()
@@ -426,7 +438,7 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     # warm-up (also compiles nothing: the library is prebuilt)
     for _ in range(args.warmup):
         flush.fill_(1.0)
-        layer.forward(x, out)
+        fwd(x, out)
     torch.cuda.synchronize()
     st, n_st = fm.get_status(layer.ws.data_ptr(), s)
     if st != 0:
@@ -440,7 +452,7 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     for i in range(eager_n):
         flush.fill_(float(i))
         eager_ev[i][0].record(stream)
-        layer.forward(x, out)
+        fwd(x, out)
         eager_ev[i][1].record(stream)
     torch.cuda.synchronize()
     eager_ms = statistics.mean(a.elapsed_time(b) for a, b in eager_ev)
@@ -449,7 +461,7 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     graph = torch.cuda.CUDAGraph()
     torch.cuda.synchronize()
     with torch.cuda.graph(graph):
-        layer.forward(x, out)
+        fwd(x, out)
     torch.cuda.synchronize()
     for _ in range(3):
         graph.replay()
@@ -483,7 +495,7 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     for i in range(min(steps, 50)):
         flush.fill_(float(i))
         torch.cuda.synchronize()
-        layer.forward(x, out, debug=gdbg)
+        fwd(x, out, debug=gdbg)
         torch.cuda.synchronize()
         stage_runs.append([gev[j].elapsed_time(gev[j + 1]) for j in range(7)])
         gu_ms.append(gev[4].elapsed_time(gev[5]))
@@ -497,7 +509,7 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     e2e_steps = max(10, min(steps, 200))
     for _ in range(3):
         x_dev.copy_(x_host, non_blocking=True)
-        layer.forward(x_dev, out)
+        fwd(x_dev, out)
         out_host.copy_(out, non_blocking=True)
     torch.cuda.synchronize()
     e2e_ev = [make_events(2) for _ in range(e2e_steps)]
@@ -506,7 +518,7 @@ def gpu_arm(args, cfg, rank, world, local_rank):
         flush.fill_(float(i))
         e2e_ev[i][0].record(stream)
         x_dev.copy_(x_host, non_blocking=True)
-        layer.forward(x_dev, out)
+        fwd(x_dev, out)
         out_host.copy_(out, non_blocking=True)
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
@@ -514,12 +526,17 @@ def gpu_arm(args, cfg, rank, world, local_rank):
 
     # work actually done: touched experts and routes
     ne = cfg.E + cfg.n_shared
-    count = layer.ws_view("expert_count", torch.int32, ne).cpu().numpy()
+    wsbuf = layer.emu_ws if args.emulate else layer.ws  # the emulation mode has a workspace of its own
+    off = layer.layout.expert_count
+    count = wsbuf[off:off + 4 * ne].view(torch.int32).cpu().numpy()
     touched = int(np.count_nonzero(count))
     routes = int(count.sum())
     wpe = layer.weight_bytes_per_expert()
     d = layer.dims
-    if args.w8a8:  # E4M3 bytes, fp32 row scales; gate/up writes fp32 h, down reads E4M3 h
+    if args.emulate:  # BF16 weights and activation rows; gate/up writes fp32 h
+        gu_bytes = touched * (2 * d.I * d.H * 2) + routes * d.H * 2 + routes * d.I * 4
+        dn_bytes = touched * (d.H * d.I * 2) + routes * d.I * 2 + routes * d.H * 4
+    elif args.w8a8:  # E4M3 bytes, fp32 row scales; gate/up writes fp32 h, down reads E4M3 h
         gu_bytes = touched * (2 * d.I * d.H + 2 * d.I * 4) + routes * (d.H + 4) + routes * d.I * 4
         dn_bytes = touched * (d.H * d.I + d.H * 4) + routes * (d.I + 4) + routes * d.H * 4
     else:
@@ -544,6 +561,8 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     # finalise; else router, top-k, plan, scatter, gather, gate/up, down, finalise
     if args.w8a8:  # router, top-k, plan, scatter, x quantisation, gate/up, h quantisation, down, finalise
         launches_per_step = 9
+    elif args.emulate:  # + weight dequantisation (w13, w2, shared), amax, x and h QDQ
+        launches_per_step = 11 + 2 * cfg.n_shared
     elif cfg.fmt == "mxfp4":
         launches_per_step = 4 if cfg.T <= 16 else 8
     else:
@@ -551,7 +570,7 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     conversion = time_conversion(layer, peaks, stream) if args.conversion and not args.w8a8 else None
     # CPU baseline: the oracle on a bounded sample of this workload
     n_routes = 16 if args.cpu_routes is None else args.cpu_routes
-    cpu_s, cpu_tok = (oracle_route_sample(args.config, n_routes, w8a8=args.w8a8) if n_routes > 0
+    cpu_s, cpu_tok = (oracle_route_sample(args.config, n_routes, w8a8=args.w8a8, emulate=args.emulate) if n_routes > 0
                       else (float("nan"), 0.0))
     line = {
         "metric": METRIC,
@@ -564,9 +583,9 @@ def gpu_arm(args, cfg, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3" if args.w8a8 else ("mxfp4" if cfg.fmt == "mxfp4" else "nvfp4"),
+        "dtype": "e4m3" if args.w8a8 else "bf16" if args.emulate else ("mxfp4" if cfg.fmt == "mxfp4" else "nvfp4"),
         "data": "synthetic (seeded; weights drawn on the device)",
-        "config": {"workload": cfg_label(cfg, args.w8a8), "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+        "config": {"workload": cfg_label(cfg, args.w8a8, args.emulate), "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "launch": "one fp4moe_forward captured in a CUDA graph, replayed per step",
                    "l2": "flushed between steps (256 MiB write, untimed)", "touched_experts": touched,
                    "routes": routes},
@@ -603,6 +622,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=None, help="override T")
     ap.add_argument("--linear", default=None, metavar="T,K,N",
                     help="time the dense block-scaled FP4 linear (fp4moe_linear) on this shape instead")
+    ap.add_argument("--emulate", action="store_true",
+                    help="NVFP4 workloads: the emulation mode (fp4moe_forward_nvfp4_emulated)")
     ap.add_argument("--w8a8", action="store_true",
                     help="the W8A8 layer: experts exactly converted to FP8 per channel, FP8 per-token activations")
     ap.add_argument("--conversion", action="store_true",

@@ -90,6 +90,9 @@ def lib() -> ctypes.CDLL:
         L.fp4moe_quantize_act.argtypes = [vp, i32, i64, i32, i32, vp, vp, vp, vp, vp, sz, vp]
         L.fp4moe_forward.argtypes = [P(Dims), P(Weights), vp, vp, P(Debug), vp, sz, vp]
         L.fp4moe_forward_w8a8.argtypes = [P(Dims), P(Fp8Weights), vp, vp, P(Debug), vp, sz, vp]
+        L.fp4moe_emulation_workspace_size.argtypes = [P(Dims)]
+        L.fp4moe_emulation_workspace_size.restype = sz
+        L.fp4moe_forward_nvfp4_emulated.argtypes = [P(Dims), P(Weights), vp, vp, P(Debug), vp, sz, vp]
         L.fp4moe_linear_workspace_size.argtypes = [i32, i32, i32, i32]
         L.fp4moe_linear_workspace_size.restype = sz
         L.fp4moe_linear.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -97,7 +100,8 @@ def lib() -> ctypes.CDLL:
         L.fp4moe_clear_status.argtypes = [vp, vp]
         L.fp4moe_get_status.argtypes = [vp, vp, P(i32), P(i64)]
         for name in ("fp4moe_workspace_layout", "fp4moe_pack_scales", "fp4moe_route", "fp4moe_quantize_act",
-                     "fp4moe_forward", "fp4moe_forward_w8a8", "fp4moe_linear", "fp4moe_mxfp4_to_fp8_rowscale",
+                     "fp4moe_forward", "fp4moe_forward_w8a8", "fp4moe_forward_nvfp4_emulated", "fp4moe_linear",
+                     "fp4moe_mxfp4_to_fp8_rowscale",
                      "fp4moe_clear_status",
                      "fp4moe_get_status"):
             getattr(L, name).restype = i32
@@ -170,6 +174,20 @@ def forward_w8a8(dims: Dims, weights: Fp8Weights, x: int, out: int, ws: int, ws_
     dbg = ctypes.byref(debug) if debug is not None else None
     _ok(lib().fp4moe_forward_w8a8(ctypes.byref(dims), ctypes.byref(weights), x, out, dbg, ws, ws_bytes, stream),
         "fp4moe_forward_w8a8")
+
+
+def emulation_workspace_size(dims: Dims) -> int:
+    n = lib().fp4moe_emulation_workspace_size(ctypes.byref(dims))
+    if n == 0:
+        raise Fp4MoeError(2, "fp4moe_emulation_workspace_size")
+    return n
+
+
+def forward_nvfp4_emulated(dims: Dims, weights: Weights, x: int, out: int, ws: int, ws_bytes: int, stream: int = 0,
+                           debug: Debug | None = None) -> None:
+    dbg = ctypes.byref(debug) if debug is not None else None
+    _ok(lib().fp4moe_forward_nvfp4_emulated(ctypes.byref(dims), ctypes.byref(weights), x, out, dbg, ws, ws_bytes,
+                                            stream), "fp4moe_forward_nvfp4_emulated")
 
 
 def linear_workspace_size(fmt: int, T: int, K: int, N: int) -> int:

@@ -146,6 +146,32 @@ bool make_layout(const fp4moe_dims& d, Layout* L) {
   return true;
 }
 
+// NVFP4 emulation mode: the NVFP4 forward's workspace followed by bf16 rows of
+// x and h and bf16 copies of the expert weights (touched experts written).
+struct EmuLayout {
+  Layout L;
+  int64_t xb, hb, w13b, w2b, sh13b, sh2b, total;
+};
+
+bool emulation_layout(const fp4moe_dims& d, EmuLayout* M) {
+  if (d.fmt != FP4MOE_NVFP4 || !make_layout(d, &M->L)) return false;
+  int64_t off = (M->L.ws.total_bytes + 255) / 256 * 256;
+  auto take = [&](int64_t bytes) {
+    const int64_t o = off;
+    off = (off + bytes + 255) / 256 * 256;
+    return o;
+  };
+  const int64_t rc = M->L.ws.rows_cap;
+  M->xb = take(rc * d.H * 2);
+  M->hb = take(rc * d.I * 2);
+  M->w13b = take((int64_t)d.E * 2 * d.I * d.H * 2);
+  M->w2b = take((int64_t)d.E * d.H * d.I * 2);
+  M->sh13b = take(d.n_shared ? (int64_t)2 * d.I * d.H * 2 : 0);
+  M->sh2b = take(d.n_shared ? (int64_t)d.H * d.I * 2 : 0);
+  M->total = off;
+  return true;
+}
+
 // Dense linear as a one-expert MoE layer: the down GEMM's view (H = N output
 // rows, I = K), top-1, one token per route.
 fp4moe_dims linear_dims(int32_t fmt, int32_t T, int32_t K, int32_t N) {
@@ -534,6 +560,134 @@ fp4moe_status fp4moe_forward_w8a8(const fp4moe_dims* dims, const fp4moe_fp8_weig
     g.shrs = d.n_shared ? w->sh2_scale : nullptr;
     g.b = hq;
     g.brs = hsig;
+    g.unit_start = dn_start;
+    g.out_acc = acc;
+    e = launch_down(g, s);
+  }
+  if (e == cudaSuccess) e = rec(6);
+  if (e == cudaSuccess) e = launch_finalize(acc, out, (int64_t)d.T * d.H, s);
+  if (e == cudaSuccess) e = rec(7);
+  return cuda_status(e);
+}
+
+size_t fp4moe_emulation_workspace_size(const fp4moe_dims* dims) {
+  EmuLayout M;
+  if (!dims || !emulation_layout(*dims, &M)) return 0;
+  return (size_t)M.total;
+}
+
+fp4moe_status fp4moe_forward_nvfp4_emulated(const fp4moe_dims* dims, const fp4moe_weights* w, const uint16_t* x,
+                                            uint16_t* out, const fp4moe_debug* dbg, void* ws, size_t ws_bytes,
+                                            void* stream) {
+  if (!dims || !w || !x || !out || !ws) return FP4MOE_ERR_INVALID_ARG;
+  const fp4moe_dims& d = *dims;
+  if (d.fmt != FP4MOE_NVFP4) return FP4MOE_ERR_INVALID_ARG;
+  EmuLayout M;
+  if (!emulation_layout(d, &M)) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  const Layout& L = M.L;
+  if (ws_bytes < (size_t)M.total) return FP4MOE_ERR_WORKSPACE;
+  if (!w->w13 || !w->w13_scale || !w->w2 || !w->w2_scale || !w->g13 || !w->g2 || !w->w_router || !w->bias)
+    return FP4MOE_ERR_INVALID_ARG;
+  if (d.n_shared && (!w->sh13 || !w->sh13_scale || !w->sh2 || !w->sh2_scale)) return FP4MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w->w13) || !aligned16(w->w2) || !aligned16(w->w_router) || !aligned16(ws) ||
+      !aligned16(out))
+    return FP4MOE_ERR_INVALID_ARG;
+  if (fp4moe_status st = check_device()) return st;
+  const int num_sms = device_sm_count();
+  if (num_sms <= 0) return FP4MOE_ERR_DEVICE;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  auto P = [&](int64_t off) { return base + off; };
+  int32_t* status = reinterpret_cast<int32_t*>(P(L.ws.status));
+  float* partial = reinterpret_cast<float*>(P(L.ws.logits));
+  int32_t* idx = reinterpret_cast<int32_t*>(P(L.ws.topk_idx));
+  float* tw = reinterpret_cast<float*>(P(L.ws.topk_w));
+  Plan* plan = reinterpret_cast<Plan*>(P(L.plan));
+  int32_t* ecount = reinterpret_cast<int32_t*>(P(L.ws.expert_count));
+  int32_t* eslot = reinterpret_cast<int32_t*>(P(L.ws.expert_slot));
+  int32_t* gu_start = reinterpret_cast<int32_t*>(P(L.gu_start));
+  int32_t* dn_start = reinterpret_cast<int32_t*>(P(L.dn_start));
+  int32_t* cc = reinterpret_cast<int32_t*>(P(L.chunk_counts));
+  int32_t* route_row = reinterpret_cast<int32_t*>(P(L.ws.route_row));
+  int32_t* row_tok = reinterpret_cast<int32_t*>(P(L.ws.row_tok));
+  float* row_w = reinterpret_cast<float*>(P(L.ws.row_w));
+  int32_t* row_e = reinterpret_cast<int32_t*>(P(L.row_e));
+  float* h32 = reinterpret_cast<float*>(P(L.ws.h32));
+  float* gscale = reinterpret_cast<float*>(P(L.ws.gscale));
+  uint32_t* amax = reinterpret_cast<uint32_t*>(P(L.amax));
+  float* acc = reinterpret_cast<float*>(P(L.ws.out_acc));
+  uint16_t* xb = reinterpret_cast<uint16_t*>(P(M.xb));
+  uint16_t* hb = reinterpret_cast<uint16_t*>(P(M.hb));
+  uint16_t* w13b = reinterpret_cast<uint16_t*>(P(M.w13b));
+  uint16_t* w2b = reinterpret_cast<uint16_t*>(P(M.w2b));
+  uint16_t* sh13b = d.n_shared ? reinterpret_cast<uint16_t*>(P(M.sh13b)) : nullptr;
+  uint16_t* sh2b = d.n_shared ? reinterpret_cast<uint16_t*>(P(M.sh2b)) : nullptr;
+  const int n_tile = L.ws.n_tile;
+  auto rec = [&](int i) -> cudaError_t {
+    if (dbg && dbg->events[i]) return cudaEventRecord(static_cast<cudaEvent_t>(dbg->events[i]), s);
+    return cudaSuccess;
+  };
+
+  cudaError_t e = rec(0);
+  const size_t clear_bytes = (size_t)(L.chunk_counts - L.ws.status) + (size_t)L.n_chunks * L.n_exp * 4;
+  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, clear_bytes, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(amax, 0, (size_t)(2 + L.n_exp) * 4, s);
+  if (e == cudaSuccess) e = launch_router_logits(x, w->w_router, partial, d.T, d.H, d.E, L.ws.n_splits, status, s);
+  if (e == cudaSuccess) e = rec(1);
+  if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, nullptr, cc, L.n_exp, s);
+  if (e == cudaSuccess) e = rec(2);
+  if (e == cudaSuccess)
+    e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, ecount, eslot, gu_start, dn_start, plan,
+                    status + ST_TICKET_PLAN, s);
+  if (e == cudaSuccess)
+    e = launch_scatter(d, idx, tw, cc, L.n_chunks, L.n_exp, n_tile, eslot, route_row, row_tok, row_w, row_e, s);
+  if (e == cudaSuccess) e = rec(3);
+  // BF16 copies of the dispatched experts' weights (at GEMM time, as the
+  // emulation pipeline does) and of the QDQ'd activations
+  if (e == cudaSuccess) e = launch_nv_weight_bf16(w->w13, w->w13_scale, w->g13, d.E, 2 * d.I, d.H, ecount, w13b, s);
+  if (e == cudaSuccess) e = launch_nv_weight_bf16(w->w2, w->w2_scale, w->g2, d.E, d.H, d.I, ecount, w2b, s);
+  if (e == cudaSuccess && d.n_shared)
+    e = launch_nv_weight_bf16(w->sh13, w->sh13_scale, w->g13 + d.E, 1, 2 * d.I, d.H, nullptr, sh13b, s);
+  if (e == cudaSuccess && d.n_shared)
+    e = launch_nv_weight_bf16(w->sh2, w->sh2_scale, w->g2 + d.E, 1, d.H, d.I, nullptr, sh2b, s);
+  if (e == cudaSuccess) e = launch_amax(x, 0, (int64_t)d.T * d.H, amax, s);
+  if (e == cudaSuccess) e = launch_nv_qdq_x_bf16(d, x, route_row, amax, gscale, xb, s);
+  if (e == cudaSuccess) e = rec(4);
+
+  GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  a.d = &d;
+  a.bf = true;
+  a.n_tile = n_tile;
+  a.num_sms = num_sms;
+  a.rows_cap = L.ws.rows_cap;
+  a.expert_count = ecount;
+  a.expert_slot = eslot;
+  a.plan = plan;
+  a.row_tok = row_tok;
+  a.row_w = row_w;
+  a.status = status;
+  if (e == cudaSuccess) {
+    GemmArgs g = a;
+    g.w = reinterpret_cast<const uint8_t*>(w13b);
+    g.sh = reinterpret_cast<const uint8_t*>(sh13b);
+    g.b = reinterpret_cast<const uint8_t*>(xb);
+    g.unit_start = gu_start;
+    g.h32 = h32;
+    g.amax_h = amax + 2;
+    g.h_dbg = dbg ? dbg->h_pre : nullptr;
+    g.out_acc = acc;
+    g.zero_acc = true;
+    e = launch_gateup(g, s);
+  }
+  if (e == cudaSuccess) e = rec(5);
+  if (e == cudaSuccess) e = launch_nv_qdq_h_bf16(d, h32, route_row, row_e, amax + 2, gscale + 2, hb, s);
+  if (e == cudaSuccess) {
+    GemmArgs g = a;
+    g.w = reinterpret_cast<const uint8_t*>(w2b);
+    g.sh = reinterpret_cast<const uint8_t*>(sh2b);
+    g.b = reinterpret_cast<const uint8_t*>(hb);
     g.unit_start = dn_start;
     g.out_acc = acc;
     e = launch_down(g, s);

@@ -239,6 +239,17 @@ __device__ __forceinline__ void tc_mma_f8_elect(uint32_t d, uint64_t a, uint64_t
       : "memory");
 }
 
+// BF16 x BF16 MMA (kind::f16, K = 16 per instruction), fp32 accumulate,
+// issued by one elected lane of the calling warp.
+__device__ __forceinline__ void tc_mma_bf16_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\telect.sync _|p, 0xffffffff;\n\tsetp.ne.b32 q, %4, 0;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, q;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane.
@@ -281,6 +292,12 @@ __host__ __device__ constexpr uint32_t idesc_fp4(uint32_t n, bool nv, uint32_t s
          | (nv ? 0u : 1u) << 23    // scale format: 0 = UE4M3, 1 = UE8M0
          | (128u >> 4) << 24       // M / 16
          | (sfa_id & 3u) << 29;    // A scale-factor id
+}
+
+// Instruction descriptor of kind::f16 with fp32 D and bf16 A and B, both
+// K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n) {
+  return 1u << 4 | 1u << 7 | 1u << 10 | (n >> 3) << 17 | (128u >> 4) << 24;
 }
 
 // Instruction descriptor of a dense E4M3 MMA: fp32 D, E4M3 A and B (format

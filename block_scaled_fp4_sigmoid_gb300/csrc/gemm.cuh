@@ -66,12 +66,16 @@ struct KParams {
   const float *wrs, *shrs, *brs;
 };
 
-// F8: E4M3 operands (W8A8), 128-value K tiles and no scale factors; else
-// block-scaled FP4, 256-value K tiles.
-template <int N, bool GATEUP, bool NV, bool F8 = false>
+// Operand kinds: block-scaled FP4 (MXFP4 or NVFP4 by NV; 256-value K tiles,
+// scale factors through tensor memory), E4M3 (W8A8; 128-value K tiles) and
+// BF16 (the NVFP4 emulation mode; 64-value K tiles).  Every K tile is one
+// 128-byte swizzle row per operand row, consumed by four MMAs of 32 bytes.
+constexpr int kOpFp4 = 0, kOpE4M3 = 1, kOpBf16 = 2;
+
+template <int N, bool GATEUP, bool NV, int OP = kOpFp4>
 struct GemmCfg {
-  static constexpr int kA = GATEUP ? 2 : 1;          // A operands per unit (gate and up)
-  static constexpr int kAtoms = F8 ? 0 : NV ? 4 : 2; // scale groups per K tile
+  static constexpr int kA = GATEUP ? 2 : 1;                // A operands per unit (gate and up)
+  static constexpr int kAtoms = OP != kOpFp4 ? 0 : NV ? 4 : 2;  // scale groups per K tile
   static constexpr int kABytes = 128 * 128;          // 128 rows x 128 bytes
   static constexpr int kBBytes = N * 128;
   static constexpr int kSFBytes = kAtoms * 512;      // per 128-row operand and K tile
@@ -137,10 +141,11 @@ __device__ __forceinline__ void decode_unit(const int32_t* s_start, const int32_
   cnt = min(N, count - ti * N);
 }
 
-template <int N, bool GATEUP, bool NV, bool F8 = false>
+template <int N, bool GATEUP, bool NV, int OP = kOpFp4>
 __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant__ KParams p) {
-  using C = GemmCfg<N, GATEUP, NV, F8>;
-  static_assert(!(F8 && NV), "one operand format");
+  using C = GemmCfg<N, GATEUP, NV, OP>;
+  constexpr bool F8 = OP == kOpE4M3, BF = OP == kOpBf16, SF = OP == kOpFp4;
+  static_assert(SF || !NV, "one operand format");
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[C::kStages];
   __shared__ __align__(8) uint64_t bar_empty[C::kStages];
@@ -154,7 +159,7 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int KT = F8 ? (p.K + 127) / 128 : (p.K + 255) / 256;  // K tiles of 128 bytes
+  const int KT = (p.K + (BF ? 63 : F8 ? 127 : 255)) / (BF ? 64 : F8 ? 128 : 256);  // K tiles of 128 bytes
 
   static_assert(C::kThreads == 256, "launch bounds");
   if (threadIdx.x == 0) {
@@ -235,14 +240,14 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
     if (st.once) {
       tma_load_3d_hint(base, st.tmA, fb, kt * 128, st.row0, st.ec, pol_once);
       if constexpr (GATEUP) tma_load_3d_hint(base + C::kOffA1, st.tmA, fb, kt * 128, st.row1, st.ec, pol_once);
-      if constexpr (!F8) {
+      if constexpr (SF) {
         bulk_load_hint(base + C::kOffSFA0, st.sfa0 + kt * C::kSFBytes, C::kSFBytes, fb, pol_once);
         if constexpr (GATEUP) bulk_load_hint(base + C::kOffSFA1, st.sfa1 + kt * C::kSFBytes, C::kSFBytes, fb, pol_once);
       }
     } else {
       tma_load_3d(base, st.tmA, fb, kt * 128, st.row0, st.ec);
       if constexpr (GATEUP) tma_load_3d(base + C::kOffA1, st.tmA, fb, kt * 128, st.row1, st.ec);
-      if constexpr (!F8) {
+      if constexpr (SF) {
         bulk_load(base + C::kOffSFA0, st.sfa0 + kt * C::kSFBytes, C::kSFBytes, fb);
         if constexpr (GATEUP) bulk_load(base + C::kOffSFA1, st.sfa1 + kt * C::kSFBytes, C::kSFBytes, fb);
       }
@@ -250,7 +255,7 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
   };
   auto load_acts = [&](const Step& st, int kt, uint32_t base, uint32_t fb) {
     tma_load_2d(base + C::kOffB, &p.tmB, fb, kt * 128, st.slot * kSlotRows);
-    if constexpr (!F8) bulk_load(base + C::kOffSFB, st.sfb + kt * C::kSFBytes, C::kSFBytes, fb);
+    if constexpr (SF) bulk_load(base + C::kOffSFB, st.sfb + kt * C::kSFBytes, C::kSFBytes, fb);
   };
 
   // The first pipeline stages start streaming weights before the wait, so
@@ -367,6 +372,8 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
           const uint32_t accum = (!first || j) ? 1u : 0u;
           if constexpr (F8) {
             tc_mma_f8_elect(t_acc, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc_f8(N), accum);  // K = 32
+          } else if constexpr (BF) {
+            tc_mma_bf16_elect(t_acc, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc_bf16(N), accum);  // K = 16
           } else {
             const int atom = NV ? j : (j >> 1);
             const uint32_t sfid = NV ? 0u : (uint32_t)(j & 1) * 2u;
@@ -462,7 +469,7 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
 #pragma unroll
               for (int r = 0; r < 8; ++r) dst[r] = make_float4(v[4 * r], v[4 * r + 1], v[4 * r + 2], v[4 * r + 3]);
             }
-            if constexpr (NV || F8) {
+            if constexpr (NV || F8 || BF) {
               float4* dst = reinterpret_cast<float4*>(p.h32 + row * p.I + i0);
 #pragma unroll
               for (int r = 0; r < 8; ++r) dst[r] = make_float4(v[4 * r], v[4 * r + 1], v[4 * r + 2], v[4 * r + 3]);
@@ -482,7 +489,7 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
           }
           __syncwarp();
         }
-        if constexpr (NV) {
+        if constexpr (NV || BF) {  // the intermediate's NVFP4 tensor scale is per expert
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
           if (lane == 0) atomicMax(p.amax_h + e, __float_as_uint(amax));
@@ -548,10 +555,10 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
   }
 }
 
-template <int N, bool GATEUP, bool NV, bool F8 = false>
+template <int N, bool GATEUP, bool NV, int OP = kOpFp4>
 cudaError_t launch_gemm_t(const KParams& p, int grid, cudaStream_t s) {
-  using C = GemmCfg<N, GATEUP, NV, F8>;
-  auto k = moe_gemm_kernel<N, GATEUP, NV, F8>;
+  using C = GemmCfg<N, GATEUP, NV, OP>;
+  auto k = moe_gemm_kernel<N, GATEUP, NV, OP>;
   static bool attr_set[64] = {};  // once per device and template instance
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -13,7 +13,8 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   memset(&p, 0, sizeof(p));
   const int K = GATEUP ? d.H : d.I;
   const int rows = GATEUP ? 2 * d.I : d.H;
-  const uint64_t Kb = a.f8 ? (uint64_t)K : (uint64_t)K / 2;  // bytes of one K row (E4M3: 1, FP4: 1/2 per value)
+  // bytes of one K row: E4M3 1, BF16 2, FP4 1/2 per value
+  const uint64_t Kb = a.f8 ? (uint64_t)K : a.bf ? 2 * (uint64_t)K : (uint64_t)K / 2;
   {
     const uint64_t dims[3] = {Kb, (uint64_t)rows, (uint64_t)d.E};
     const uint64_t strides[2] = {Kb, (uint64_t)rows * Kb};
@@ -72,12 +73,18 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   p.shrs = a.shrs;
   p.brs = a.brs;
   const int grid = a.num_sms > 0 ? a.num_sms : 1;
-  if (a.f8) {
-    if (a.nv) return cudaErrorInvalidValue;
+  if (a.f8 || a.bf) {
+    if (a.nv || (a.f8 && a.bf)) return cudaErrorInvalidValue;
+    if (a.f8) switch (a.n_tile) {
+        case 32: return launch_gemm_t<32, GATEUP, false, kOpE4M3>(p, grid, s);
+        case 64: return launch_gemm_t<64, GATEUP, false, kOpE4M3>(p, grid, s);
+        case 112: return launch_gemm_t<112, GATEUP, false, kOpE4M3>(p, grid, s);
+        default: return cudaErrorInvalidValue;
+      }
     switch (a.n_tile) {
-      case 32: return launch_gemm_t<32, GATEUP, false, true>(p, grid, s);
-      case 64: return launch_gemm_t<64, GATEUP, false, true>(p, grid, s);
-      case 112: return launch_gemm_t<112, GATEUP, false, true>(p, grid, s);
+      case 32: return launch_gemm_t<32, GATEUP, false, kOpBf16>(p, grid, s);
+      case 64: return launch_gemm_t<64, GATEUP, false, kOpBf16>(p, grid, s);
+      case 112: return launch_gemm_t<112, GATEUP, false, kOpBf16>(p, grid, s);
       default: return cudaErrorInvalidValue;
     }
   }

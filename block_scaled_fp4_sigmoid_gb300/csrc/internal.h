@@ -89,6 +89,15 @@ cudaError_t launch_h_quant_nv_routes(const fp4moe_dims& d, const float* h32, con
                                      const int32_t* row_e, const uint32_t* amax_h, float* gh_out, uint8_t* hq,
                                      uint8_t* hsf, cudaStream_t s);
 cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, cudaStream_t s);
+// NVFP4 emulation: weights of touched experts to bf16 (count nullable: all
+// n_mat matrices); x and h through NVFP4 QDQ into bf16 rows
+cudaError_t launch_nv_weight_bf16(const uint8_t* codes, const uint8_t* sf, const float* g, int n_mat, int rows,
+                                  int K, const int32_t* count, uint16_t* out, cudaStream_t s);
+cudaError_t launch_nv_qdq_x_bf16(const fp4moe_dims& d, const uint16_t* x, const int32_t* route_row,
+                                 const uint32_t* amax_x, float* g_out, uint16_t* xb, cudaStream_t s);
+cudaError_t launch_nv_qdq_h_bf16(const fp4moe_dims& d, const float* h32, const int32_t* route_row,
+                                 const int32_t* row_e, const uint32_t* amax_h, float* gh_out, uint16_t* hb,
+                                 cudaStream_t s);
 // W8A8: x per token to E4M3 into its route rows (+ sigma per row); h per route
 // row to E4M3 with sigma from amax_row
 cudaError_t launch_fp8_x_quant(const fp4moe_dims& d, const uint16_t* x, const int32_t* route_row, uint8_t* xq,
@@ -108,6 +117,7 @@ struct GemmArgs {
   const fp4moe_dims* d;
   bool nv;
   bool f8;                         // W8A8: E4M3 operands with per-row fp32 scales (below)
+  bool bf;                         // NVFP4 emulation: BF16 operands (dequantised), no scales
   int n_tile;
   int num_sms;
   // weights

@@ -1,3 +1,4 @@
+#include <cuda_bf16.h>
 // Activation quantisation (MXFP4 / NVFP4), scale repacking, the fused
 // gather-and-quantise step of the forward, NVFP4 requantisation of the
 // intermediate, the combine finaliser, and the exact MXFP4 -> FP8 conversion.
@@ -232,6 +233,116 @@ __global__ void __launch_bounds__(kF8Threads) fp8_h_quant_kernel(const float* __
         make_uint2(fp8_pack4(a.x, a.y, a.z, a.w, sig), fp8_pack4(b.x, b.y, b.z, b.w, sig));
   }
   if (threadIdx.x == 0) hsig[row] = sig;
+}
+
+// ---------------------------------------------------------------- NVFP4 emulation mode
+// "Serving NVFP4 models on AMD Instinct MI355 accelerators", sections "Weight
+// Dequantization and Activation QDQ" and "Memory Management": weights are
+// dequantised to BF16 at GEMM time (for MoE only the dispatched experts) and
+// activations pass through an NVFP4 quantise-dequantise round trip.  Each
+// BF16 value is bf16_rn(fp32(E2M1(q) * fp32(E4M3(s) * g))).
+
+// fp32(E2M1(c) * d) for a 4-bit code: twice the magnitude from a nibble
+// table (0, 1, 2, 3, 4, 6, 8, 12), halved exactly, times d, the sign bit of
+// the code moved to bit 31.  Equal to e2m1_val(c) * d.
+__device__ __forceinline__ float e2m1_times(uint32_t c, float d) {
+  const float mag = (float)((0xC8643210u >> (4u * (c & 7u))) & 15u) * 0.5f;
+  return __uint_as_float(__float_as_uint(__fmul_rn(mag, d)) ^ ((c & 8u) << 28));
+}
+
+// Two fp32 values to packed bf16 (round to nearest even; low half first).
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// 16 values of one NVFP4 block (codes: value i in nibble i) to BF16, 32 bytes.
+__device__ __forceinline__ void nv_block_bf16(uint64_t codes, uint32_t sbyte, float g, uint4* dst) {
+  const float d = __fmul_rn(e4m3_value(sbyte), g);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i] = bf16x2_rn(e2m1_times((uint32_t)(codes >> (8 * i)) & 0xFu, d),
+                     e2m1_times((uint32_t)(codes >> (8 * i + 4)) & 0xFu, d));
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Weights of n_mat matrices [rows, K] (codes [n_mat, rows, K/2], scales in
+// the tiled layout, tensor scale g[m]) to bf16 [n_mat, rows, K]; matrices
+// whose expert has no routes (count[m] == 0) are skipped.  Grid: (.., n_mat).
+constexpr int kDqBlocksPerThread = 4;
+__global__ void nv_weight_bf16_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ sf,
+                                      const float* __restrict__ g, int rows, int K,
+                                      const int32_t* __restrict__ count, uint16_t* __restrict__ out) {
+  const int m = blockIdx.y;
+  if (count && count[m] == 0) return;
+  const int per_row = K >> 4;
+  const int64_t katoms = katoms_padded(K, true);
+  const float gm = g[m];
+  const int64_t n = (int64_t)rows * per_row;
+  // consecutive threads take consecutive blocks, so a warp's loads and its
+  // 32-byte stores are contiguous
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, j = 0; j < kDqBlocksPerThread && i < n;
+       i += stride, ++j) {
+    const int64_t r = (int64_t)m * rows + i / per_row;  // row over all matrices
+    const int b = (int)(i % per_row);
+    const uint64_t c = *reinterpret_cast<const uint64_t*>(codes + r * (K >> 1) + 8 * b);
+    nv_block_bf16(c, sf[sf_tiled_offset(r, b, katoms)], gm, reinterpret_cast<uint4*>(out + r * K + 16 * b));
+  }
+}
+
+// x through NVFP4 QDQ into every route row of its token, as bf16 [rows, H]:
+// one thread per (token, 32 values); tensor scale from the amax of x.
+__global__ void nv_qdq_x_bf16_kernel(const uint16_t* __restrict__ x, int T, int H, int rpt,
+                                     const int32_t* __restrict__ route_row, const uint32_t* __restrict__ amax_x,
+                                     float* __restrict__ g_out, uint16_t* __restrict__ xb) {
+  const int per_row = H >> 5;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (tid >= (int64_t)T * per_row) return;
+  const int64_t t = tid / per_row;
+  const int b = (int)(tid - t * per_row);
+  const float g = nv_global(__uint_as_float(*amax_x));
+  if (tid == 0 && g_out) *g_out = g;
+  float v[32];
+  load32(x, 0, t * H + 32 * b, v);
+  uint32_t q[4], s0, s1;
+  nv_quant16(v, g, q, &s0);
+  nv_quant16(v + 16, g, q + 2, &s1);
+  uint4 o[4];
+  nv_block_bf16((uint64_t)q[0] | (uint64_t)q[1] << 32, s0, g, o);
+  nv_block_bf16((uint64_t)q[2] | (uint64_t)q[3] << 32, s1, g, o + 2);
+  for (int j = 0; j < rpt; ++j) {
+    uint4* dst = reinterpret_cast<uint4*>(xb + (int64_t)route_row[t * rpt + j] * H + 32 * b);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dst[k] = o[k];
+  }
+}
+
+// The intermediate h (fp32 [rows, I]) through NVFP4 QDQ per route row, with
+// the tensor scale of the row's expert (amax_h[e] / 2688), as bf16 [rows, I];
+// also stores the scales to gh_out.
+__global__ void nv_qdq_h_bf16_kernel(const float* __restrict__ h32, int I, int64_t n_routes,
+                                     const int32_t* __restrict__ route_row, const int32_t* __restrict__ row_e,
+                                     const uint32_t* __restrict__ amax_h, float* __restrict__ gh_out, int n_exp,
+                                     uint16_t* __restrict__ hb) {
+  const int per_row = I >> 5;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (tid < n_exp && gh_out) gh_out[tid] = nv_global(__uint_as_float(amax_h[tid]));
+  if (tid >= n_routes * per_row) return;
+  const int64_t rt = tid / per_row;
+  const int b = (int)(tid - rt * per_row);
+  const int64_t row = route_row[rt];
+  const float g = nv_global(__uint_as_float(amax_h[row_e[row]]));
+  float v[32];
+  load32(h32, 1, row * I + 32 * b, v);
+  uint32_t q[4], s0, s1;
+  nv_quant16(v, g, q, &s0);
+  nv_quant16(v + 16, g, q + 2, &s1);
+  uint4* dst = reinterpret_cast<uint4*>(hb + row * I + 32 * b);
+  nv_block_bf16((uint64_t)q[0] | (uint64_t)q[1] << 32, s0, g, dst);
+  nv_block_bf16((uint64_t)q[2] | (uint64_t)q[3] << 32, s1, g, dst + 2);
 }
 
 __global__ void pack_scales_kernel(const uint8_t* src, uint8_t* dst, int64_t n_mat, int rows, int kblocks,
@@ -600,6 +711,35 @@ cudaError_t launch_fp8_h_quant(const fp4moe_dims& d, const float* h32, const int
   const int64_t n_routes = (int64_t)d.T * (d.top_k + d.n_shared);
   if (n_routes <= 0) return cudaSuccess;
   fp8_h_quant_kernel<<<(unsigned)n_routes, kF8Threads, 0, s>>>(h32, d.I, route_row, amax_row, hq, hsig);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nv_weight_bf16(const uint8_t* codes, const uint8_t* sf, const float* g, int n_mat, int rows,
+                                  int K, const int32_t* count, uint16_t* out, cudaStream_t s) {
+  if (n_mat <= 0) return cudaSuccess;
+  const int64_t n = (int64_t)rows * (K >> 4);
+  const dim3 grid((unsigned)blocks_for((n + kDqBlocksPerThread - 1) / kDqBlocksPerThread, 256), (unsigned)n_mat);
+  nv_weight_bf16_kernel<<<grid, 256, 0, s>>>(codes, sf, g, rows, K, count, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nv_qdq_x_bf16(const fp4moe_dims& d, const uint16_t* x, const int32_t* route_row,
+                                 const uint32_t* amax_x, float* g_out, uint16_t* xb, cudaStream_t s) {
+  const int64_t n = (int64_t)d.T * (d.H >> 5);
+  if (n == 0) return cudaSuccess;
+  nv_qdq_x_bf16_kernel<<<blocks_for(n, 256), 256, 0, s>>>(x, d.T, d.H, d.top_k + d.n_shared, route_row, amax_x,
+                                                          g_out, xb);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nv_qdq_h_bf16(const fp4moe_dims& d, const float* h32, const int32_t* route_row,
+                                 const int32_t* row_e, const uint32_t* amax_h, float* gh_out, uint16_t* hb,
+                                 cudaStream_t s) {
+  const int64_t n_routes = (int64_t)d.T * (d.top_k + d.n_shared);
+  const int n_exp = d.E + d.n_shared;
+  const int64_t n = std::max<int64_t>(n_routes * (d.I >> 5), n_exp);
+  nv_qdq_h_bf16_kernel<<<blocks_for(n, 256), 256, 0, s>>>(h32, d.I, n_routes, route_row, row_e, amax_h, gh_out,
+                                                          n_exp, hb);
   return cudaGetLastError();
 }
 

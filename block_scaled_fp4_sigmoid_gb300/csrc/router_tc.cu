@@ -39,12 +39,6 @@ struct RtParams {
   int T, E, N, kc, mtiles;
 };
 
-// Instruction descriptor of kind::f16: fp32 D, bf16 A and B, both K-major,
-// N / 8 at bit 17, M / 16 at bit 24.
-__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n) {
-  return 1u << 4 | 1u << 7 | 1u << 10 | (n >> 3) << 17 | (128u >> 4) << 24;
-}
-
 __device__ __forceinline__ void tc_mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"

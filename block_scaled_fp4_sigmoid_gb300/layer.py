@@ -14,7 +14,8 @@ import ctypes
 
 import torch
 
-from . import (FP8, MXFP4, NVFP4, Debug, Fp8Weights, Weights, forward, forward_w8a8, get_status, make_dims,
+from . import (FP8, MXFP4, NVFP4, Debug, Fp8Weights, Weights, emulation_workspace_size, forward,
+               forward_nvfp4_emulated, forward_w8a8, get_status, make_dims,
                mxfp4_to_fp8_rowscale, pack_scales, packed_scales_bytes, quantize_act, workspace_layout,
                workspace_size)
 
@@ -69,6 +70,23 @@ class MoELayer:
             out = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=self.device)
         s = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
         forward(d, self.weights, x.data_ptr(), out.data_ptr(), self.ws.data_ptr(), self.ws_bytes, s, debug)
+        return out
+
+    def forward_emulated(self, x, out=None, debug: Debug | None = None, stream=None):
+        """NVFP4 layers only: the same layer in emulation mode
+        (fp4moe_forward_nvfp4_emulated: BF16 dequantised experts, NVFP4 QDQ
+        activations, BF16 GEMMs), with a workspace of its own."""
+        d = self.dims
+        if d.fmt != NVFP4:
+            raise ValueError("emulation mode is for NVFP4 layers")
+        if getattr(self, "emu_ws", None) is None:
+            self.emu_ws_bytes = emulation_workspace_size(d)
+            self.emu_ws = torch.empty(self.emu_ws_bytes, dtype=torch.uint8, device=self.device)
+        if out is None:
+            out = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=self.device)
+        s = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
+        forward_nvfp4_emulated(d, self.weights, x.data_ptr(), out.data_ptr(), self.emu_ws.data_ptr(),
+                               self.emu_ws_bytes, s, debug)
         return out
 
     # ------------------------------------------------------------ workspace views

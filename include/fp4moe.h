@@ -266,6 +266,22 @@ fp4moe_status fp4moe_forward_w8a8(const fp4moe_dims *dims, const fp4moe_fp8_weig
                                   uint16_t *out, const fp4moe_debug *dbg, void *ws, size_t ws_bytes,
                                   void *stream);
 
+/* The NVFP4 layer in emulation mode ("Serving NVFP4 models on AMD Instinct
+ * MI355 accelerators", sections "Weight Dequantization and Activation QDQ"
+ * and "Memory Management"): the dispatched experts' NVFP4 weights are
+ * dequantised to BF16 at call time into the workspace, x and the
+ * intermediate pass through an NVFP4 quantise-dequantise round trip into
+ * BF16, and the expert GEMMs multiply BF16 by BF16 with fp32 accumulation.
+ * Each BF16 value is bf16_rn(fp32(E2M1(q) * fp32(E4M3(s) * g))).  A reference
+ * and speed comparison for the native NVFP4 fp4moe_forward.
+ *   dims->fmt FP4MOE_NVFP4; w as for fp4moe_forward (NVFP4); ws:
+ *   fp4moe_emulation_workspace_size(dims) bytes (the forward's layout first,
+ *   then BF16 rows of x and h and BF16 copies of every expert matrix). */
+size_t fp4moe_emulation_workspace_size(const fp4moe_dims *dims);
+fp4moe_status fp4moe_forward_nvfp4_emulated(const fp4moe_dims *dims, const fp4moe_weights *w, const uint16_t *x,
+                                            uint16_t *out, const fp4moe_debug *dbg, void *ws, size_t ws_bytes,
+                                            void *stream);
+
 /* Dense block-scaled FP4 linear layer ("Serve Kimi-K2.5-MXFP4 on MI355X with
  * ATOM", section "Stage C: MXFP4 Linear GEMM": bf16 activations quantised
  * on the fly, block-scaled FP4 product, bf16 output):
