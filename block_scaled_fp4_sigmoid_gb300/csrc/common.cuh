@@ -311,16 +311,22 @@ __host__ __device__ constexpr uint32_t idesc_f8(uint32_t n) {
 }
 
 // ---------------------------------------------------------------- FP4 / FP8 encoders
-// Round-to-nearest-even magnitude code of E2M1 for a non-negative value:
-// grid 0, .5, 1, 1.5, 2, 3, 4, 6; ties to the even code; saturating.
-__device__ __forceinline__ uint32_t e2m1_mag(float m) {
-  return (uint32_t)(m > 0.25f) + (uint32_t)(m >= 0.75f) + (uint32_t)(m > 1.25f) + (uint32_t)(m >= 1.75f) +
-         (uint32_t)(m > 2.5f) + (uint32_t)(m >= 3.5f) + (uint32_t)(m > 5.0f);
-}
-
-// Full E2M1 code; the sign bit follows the sign bit of v (zero included).
-__device__ __forceinline__ uint32_t e2m1_code(float v) {
-  return e2m1_mag(fabsf(v)) | ((__float_as_uint(v) >> 28) & 8u);
+// E2M1 codes of eight fp32 values packed into one word, value j in bits
+// 4j..4j+3.  The hardware conversion rounds to nearest even on the grid
+// 0, .5, 1, 1.5, 2, 3, 4, 6, saturates at +-6 and keeps the sign bit (zero
+// included); cvt.rn.satfinite.e2m1x2.f32 puts its first source in the high
+// nibble of the byte.
+__device__ __forceinline__ uint32_t e2m1x8(const float* v) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
 }
 
 // Round-to-nearest-even E4M3 (OCP FN) byte of a non-negative finite value,
@@ -386,10 +392,10 @@ __device__ __forceinline__ void mx_quant32(const float* v, uint32_t* packed4, ui
   const float inv = exp2i(-e);
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    uint32_t word = 0;
+    float q[8];  // |v| * inv < 8; inv = 2^-e, so the product is exact above the subnormal range
 #pragma unroll
-    for (int j = 0; j < 8; ++j) word |= e2m1_code(v[8 * w + j] * inv) << (4 * j);
-    packed4[w] = word;
+    for (int j = 0; j < 8; ++j) q[j] = v[8 * w + j] * inv;
+    packed4[w] = e2m1x8(q);
   }
   *scale_byte = (uint32_t)(e + 127);
 }
@@ -409,14 +415,13 @@ __device__ __forceinline__ void nv_quant16(const float* v, float g, uint32_t* pa
   const float d = __fmul_rn(e4m3_value(s), g);
 #pragma unroll
   for (int w = 0; w < 2; ++w) {
-    uint32_t word = 0;
+    float q[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const float x = v[8 * w + j];
-      const float q = d > 0.f ? __fdiv_rn(x, d) : x * 0.f;
-      word |= e2m1_code(q) << (4 * j);
+      q[j] = d > 0.f ? __fdiv_rn(x, d) : x * 0.f;
     }
-    packed2[w] = word;
+    packed2[w] = e2m1x8(q);
   }
   *scale_byte = s;
 }
