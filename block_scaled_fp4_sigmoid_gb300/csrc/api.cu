@@ -253,6 +253,19 @@ fp4moe_status fp4moe_pack_scales(const uint8_t* src, uint8_t* dst, int64_t n_mat
                                         static_cast<cudaStream_t>(stream)));
 }
 
+size_t fp4moe_packed_weights_bytes(int64_t n_mat, int32_t rows, int32_t kbytes) {
+  if (n_mat < 0 || rows <= 0 || rows % 128 != 0 || kbytes <= 0 || kbytes % 16 != 0) return 0;
+  return (size_t)(n_mat * rows * (int64_t)((kbytes + 127) / 128) * 128);
+}
+
+fp4moe_status fp4moe_pack_weights(const uint8_t* src, uint8_t* dst, int64_t n_mat, int32_t rows, int32_t kbytes,
+                                  void* stream) {
+  if (!src || !dst) return FP4MOE_ERR_INVALID_ARG;
+  if (fp4moe_packed_weights_bytes(n_mat, rows, kbytes) == 0 && n_mat != 0) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  if (fp4moe_status st = check_device()) return st;
+  return cuda_status(launch_pack_weights(src, dst, n_mat * rows, kbytes, static_cast<cudaStream_t>(stream)));
+}
+
 fp4moe_status fp4moe_route(const fp4moe_dims* dims, const uint16_t* x, const uint16_t* w_router, const float* bias,
                            int32_t* topk_idx, float* topk_w, float* logits_out, void* ws, size_t ws_bytes,
                            void* stream) {
@@ -415,6 +428,7 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
   if (e == cudaSuccess) {
     GemmArgs g = a;
     g.w = w->w13;
+    g.w_tiled = w->packed != 0;
     g.wsf = w->w13_scale;
     g.sh = d.n_shared ? w->sh13 : nullptr;
     g.shsf = d.n_shared ? w->sh13_scale : nullptr;
@@ -439,6 +453,7 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
   if (e == cudaSuccess) {
     GemmArgs g = a;
     g.w = w->w2;
+    g.w_tiled = w->packed != 0;
     g.wsf = w->w2_scale;
     g.sh = d.n_shared ? w->sh2 : nullptr;
     g.shsf = d.n_shared ? w->sh2_scale : nullptr;
@@ -645,12 +660,12 @@ fp4moe_status fp4moe_forward_nvfp4_emulated(const fp4moe_dims* dims, const fp4mo
   if (e == cudaSuccess) e = rec(3);
   // BF16 copies of the dispatched experts' weights (at GEMM time, as the
   // emulation pipeline does) and of the QDQ'd activations
-  if (e == cudaSuccess) e = launch_nv_weight_bf16(w->w13, w->w13_scale, w->g13, d.E, 2 * d.I, d.H, ecount, w13b, s);
-  if (e == cudaSuccess) e = launch_nv_weight_bf16(w->w2, w->w2_scale, w->g2, d.E, d.H, d.I, ecount, w2b, s);
+  if (e == cudaSuccess) e = launch_nv_weight_bf16(w->w13, w->packed != 0, w->w13_scale, w->g13, d.E, 2 * d.I, d.H, ecount, w13b, s);
+  if (e == cudaSuccess) e = launch_nv_weight_bf16(w->w2, w->packed != 0, w->w2_scale, w->g2, d.E, d.H, d.I, ecount, w2b, s);
   if (e == cudaSuccess && d.n_shared)
-    e = launch_nv_weight_bf16(w->sh13, w->sh13_scale, w->g13 + d.E, 1, 2 * d.I, d.H, nullptr, sh13b, s);
+    e = launch_nv_weight_bf16(w->sh13, w->packed != 0, w->sh13_scale, w->g13 + d.E, 1, 2 * d.I, d.H, nullptr, sh13b, s);
   if (e == cudaSuccess && d.n_shared)
-    e = launch_nv_weight_bf16(w->sh2, w->sh2_scale, w->g2 + d.E, 1, d.H, d.I, nullptr, sh2b, s);
+    e = launch_nv_weight_bf16(w->sh2, w->packed != 0, w->sh2_scale, w->g2 + d.E, 1, d.H, d.I, nullptr, sh2b, s);
   if (e == cudaSuccess) e = launch_amax(x, 0, (int64_t)d.T * d.H, amax, s);
   if (e == cudaSuccess) e = launch_nv_qdq_x_bf16(d, x, route_row, amax, gscale, xb, s);
   if (e == cudaSuccess) e = rec(4);

@@ -426,6 +426,15 @@ __device__ __forceinline__ void nv_quant16(const float* v, float g, uint32_t* pa
   *scale_byte = s;
 }
 
+// ---------------------------------------------------------------- tiled weight layout
+// Byte offset of (row r, byte cb) of an FP4 payload in the layout of
+// fp4moe_pack_weights: blocks of 128 rows x 128 bytes (one K tile of 256
+// values), K tiles innermost, rows counted over all matrices (rows per
+// matrix a multiple of 128); ktb = K tiles per row.
+__host__ __device__ __forceinline__ int64_t w_tiled_offset(int64_t r, int64_t cb, int64_t ktb) {
+  return (((r >> 7) * ktb + (cb >> 7)) << 14) + ((r & 127) << 7) + (cb & 127);
+}
+
 // ---------------------------------------------------------------- tiled scale layout
 // For a matrix of `rows` rows and `katoms` groups of four scale blocks
 // (padded to whole K tiles), the byte of (row r, block kb) sits at

@@ -40,8 +40,8 @@
 namespace fp4moe {
 
 struct KParams {
-  CUtensorMap tmA;     // routed weights, uint8 [E, rows_per_expert, K/2]
-  CUtensorMap tmA_sh;  // shared expert weights, uint8 [1, rows_per_expert, K/2]
+  CUtensorMap tmA;     // routed weights, uint8 [E, rows_per_expert, K/2] (or the tiled layout)
+  CUtensorMap tmA_sh;  // shared expert weights, uint8 [1, rows_per_expert, K/2] (or tiled)
   CUtensorMap tmB;     // activations, uint8 [rows_cap, K/2]
   const uint8_t *wsf, *shsf, *bsf;
   const float *gw, *gb;
@@ -60,6 +60,7 @@ struct KParams {
   int32_t* status;
   int E, n_exp, H, I, K, rows_per_expert, m_tiles, katoms_a, katoms_b, katoms_h, has_shared, T;
   int plan_early;  // the plan was written at least two kernels back (see the kernel)
+  int w_tiled;     // weights in the tiled layout (tmA / tmA_sh are views of 128-byte rows)
   // W8A8 (E4M3 operands): per-row fp32 scales of the weights (routed [E,
   // rows], shared [rows]) and of the B rows (per permuted row); amax_h then
   // holds the gate/up intermediate's |max| per permuted row
@@ -236,17 +237,22 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
   // shared by the units of several token tiles keep the default policy so
   // that those units find them in L2.
   const uint64_t pol_once = l2_evict_first();
+  // Coordinates of the (row tile, K tile) box: row-major (byte column, row)
+  // or, in the tiled layout, the block's first 128-byte row of the view.
+  auto a_x = [&](int kt) { return p.w_tiled ? 0 : kt * 128; };
+  auto a_y = [&](int row, int kt) { return p.w_tiled ? ((row >> 7) * KT + kt) * 128 : row; };
   auto load_weights = [&](const Step& st, int kt, uint32_t base, uint32_t fb) {
     if (st.once) {
-      tma_load_3d_hint(base, st.tmA, fb, kt * 128, st.row0, st.ec, pol_once);
-      if constexpr (GATEUP) tma_load_3d_hint(base + C::kOffA1, st.tmA, fb, kt * 128, st.row1, st.ec, pol_once);
+      tma_load_3d_hint(base, st.tmA, fb, a_x(kt), a_y(st.row0, kt), st.ec, pol_once);
+      if constexpr (GATEUP)
+        tma_load_3d_hint(base + C::kOffA1, st.tmA, fb, a_x(kt), a_y(st.row1, kt), st.ec, pol_once);
       if constexpr (SF) {
         bulk_load_hint(base + C::kOffSFA0, st.sfa0 + kt * C::kSFBytes, C::kSFBytes, fb, pol_once);
         if constexpr (GATEUP) bulk_load_hint(base + C::kOffSFA1, st.sfa1 + kt * C::kSFBytes, C::kSFBytes, fb, pol_once);
       }
     } else {
-      tma_load_3d(base, st.tmA, fb, kt * 128, st.row0, st.ec);
-      if constexpr (GATEUP) tma_load_3d(base + C::kOffA1, st.tmA, fb, kt * 128, st.row1, st.ec);
+      tma_load_3d(base, st.tmA, fb, a_x(kt), a_y(st.row0, kt), st.ec);
+      if constexpr (GATEUP) tma_load_3d(base + C::kOffA1, st.tmA, fb, a_x(kt), a_y(st.row1, kt), st.ec);
       if constexpr (SF) {
         bulk_load(base + C::kOffSFA0, st.sfa0 + kt * C::kSFBytes, C::kSFBytes, fb);
         if constexpr (GATEUP) bulk_load(base + C::kOffSFA1, st.sfa1 + kt * C::kSFBytes, C::kSFBytes, fb);

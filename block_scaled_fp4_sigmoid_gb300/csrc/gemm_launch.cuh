@@ -15,15 +15,22 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   const int rows = GATEUP ? 2 * d.I : d.H;
   // bytes of one K row: E4M3 1, BF16 2, FP4 1/2 per value
   const uint64_t Kb = a.f8 ? (uint64_t)K : a.bf ? 2 * (uint64_t)K : (uint64_t)K / 2;
+  // Weights: row-major [n_mat, rows, Kb], or the tiled layout (per matrix,
+  // 128-row tile and 128-byte K tile, one contiguous 16 KB block: a view of
+  // 128-byte rows in which the block of (row tile rt, K tile kt) starts at
+  // view row (rt * KTb + kt) * 128)
+  const uint64_t KTb = (Kb + 127) / 128;
+  const uint64_t a_dim0 = a.w_tiled ? 128 : Kb, a_dim1 = a.w_tiled ? (uint64_t)rows * KTb : (uint64_t)rows;
+  const uint64_t a_mat = a.w_tiled ? (uint64_t)rows * KTb * 128 : (uint64_t)rows * Kb;
   {
-    const uint64_t dims[3] = {Kb, (uint64_t)rows, (uint64_t)d.E};
-    const uint64_t strides[2] = {Kb, (uint64_t)rows * Kb};
+    const uint64_t dims[3] = {a_dim0, a_dim1, (uint64_t)d.E};
+    const uint64_t strides[2] = {a_dim0, a_mat};
     const uint32_t box[3] = {128, 128, 1};
     if (!encode_tmap_u8(&p.tmA, a.w, 3, dims, strides, box, true)) return cudaErrorInvalidValue;
   }
   if (a.sh) {
-    const uint64_t dims[3] = {Kb, (uint64_t)rows, 1};
-    const uint64_t strides[2] = {Kb, (uint64_t)rows * Kb};
+    const uint64_t dims[3] = {a_dim0, a_dim1, 1};
+    const uint64_t strides[2] = {a_dim0, a_mat};
     const uint32_t box[3] = {128, 128, 1};
     if (!encode_tmap_u8(&p.tmA_sh, a.sh, 3, dims, strides, box, true)) return cudaErrorInvalidValue;
   }
@@ -69,6 +76,7 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   p.katoms_b = (int)katoms_padded(K, a.nv);
   p.katoms_h = (int)katoms_padded(d.I, a.nv);
   p.has_shared = a.sh != nullptr;
+  p.w_tiled = a.w_tiled ? 1 : 0;
   p.wrs = a.wrs;
   p.shrs = a.shrs;
   p.brs = a.brs;

@@ -90,9 +90,9 @@ cudaError_t launch_h_quant_nv_routes(const fp4moe_dims& d, const float* h32, con
                                      uint8_t* hsf, cudaStream_t s);
 cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, cudaStream_t s);
 // NVFP4 emulation: weights of touched experts to bf16 (count nullable: all
-// n_mat matrices); x and h through NVFP4 QDQ into bf16 rows
-cudaError_t launch_nv_weight_bf16(const uint8_t* codes, const uint8_t* sf, const float* g, int n_mat, int rows,
-                                  int K, const int32_t* count, uint16_t* out, cudaStream_t s);
+// n_mat matrices; tiled: payloads in the layout of fp4moe_pack_weights); x and h through NVFP4 QDQ into bf16 rows
+cudaError_t launch_nv_weight_bf16(const uint8_t* codes, bool tiled, const uint8_t* sf, const float* g, int n_mat,
+                                  int rows, int K, const int32_t* count, uint16_t* out, cudaStream_t s);
 cudaError_t launch_nv_qdq_x_bf16(const fp4moe_dims& d, const uint16_t* x, const int32_t* route_row,
                                  const uint32_t* amax_x, float* g_out, uint16_t* xb, cudaStream_t s);
 cudaError_t launch_nv_qdq_h_bf16(const fp4moe_dims& d, const float* h32, const int32_t* route_row,
@@ -107,6 +107,7 @@ cudaError_t launch_fp8_h_quant(const fp4moe_dims& d, const float* h32, const int
 cudaError_t launch_quantize_rows(const void* x, int x_is_fp32, int64_t rows, int cols, bool nv,
                                  const float* global_in, const uint32_t* amax_bits, uint8_t* codes,
                                  uint8_t* scales, float* global_out, cudaStream_t s);
+cudaError_t launch_pack_weights(const uint8_t* src, uint8_t* dst, int64_t rows_total, int kbytes, cudaStream_t s);
 cudaError_t launch_pack_scales(const uint8_t* src, uint8_t* dst, int64_t n_mat, int rows, int kblocks, bool nv,
                                cudaStream_t s);
 cudaError_t launch_convert(const uint8_t* codes, const uint8_t* scales, int64_t rows, int K, uint8_t* out,
@@ -122,6 +123,7 @@ struct GemmArgs {
   int num_sms;
   // weights
   const uint8_t *w, *wsf;          // routed experts
+  bool w_tiled;                    // w and sh in the tiled layout of fp4moe_pack_weights
   const uint8_t *sh, *shsf;        // shared expert (nullable)
   const float *gw;                 // NVFP4 tensor scales [E + n_shared]
   // activations (B operand)

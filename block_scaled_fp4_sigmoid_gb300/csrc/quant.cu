@@ -273,7 +273,7 @@ __device__ __forceinline__ void nv_block_bf16(uint64_t codes, uint32_t sbyte, fl
 // whose expert has no routes (count[m] == 0) are skipped.  Grid: (.., n_mat).
 constexpr int kDqBlocksPerThread = 4;
 __global__ void nv_weight_bf16_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ sf,
-                                      const float* __restrict__ g, int rows, int K,
+                                      const float* __restrict__ g, int rows, int K, bool tiled,
                                       const int32_t* __restrict__ count, uint16_t* __restrict__ out) {
   const int m = blockIdx.y;
   if (count && count[m] == 0) return;
@@ -288,7 +288,8 @@ __global__ void nv_weight_bf16_kernel(const uint8_t* __restrict__ codes, const u
        i += stride, ++j) {
     const int64_t r = (int64_t)m * rows + i / per_row;  // row over all matrices
     const int b = (int)(i % per_row);
-    const uint64_t c = *reinterpret_cast<const uint64_t*>(codes + r * (K >> 1) + 8 * b);
+    const int64_t off = tiled ? w_tiled_offset(r, 8 * b, (K + 255) >> 8) : r * (K >> 1) + 8 * b;
+    const uint64_t c = *reinterpret_cast<const uint64_t*>(codes + off);
     nv_block_bf16(c, sf[sf_tiled_offset(r, b, katoms)], gm, reinterpret_cast<uint4*>(out + r * K + 16 * b));
   }
 }
@@ -714,12 +715,12 @@ cudaError_t launch_fp8_h_quant(const fp4moe_dims& d, const float* h32, const int
   return cudaGetLastError();
 }
 
-cudaError_t launch_nv_weight_bf16(const uint8_t* codes, const uint8_t* sf, const float* g, int n_mat, int rows,
-                                  int K, const int32_t* count, uint16_t* out, cudaStream_t s) {
+cudaError_t launch_nv_weight_bf16(const uint8_t* codes, bool tiled, const uint8_t* sf, const float* g, int n_mat,
+                                  int rows, int K, const int32_t* count, uint16_t* out, cudaStream_t s) {
   if (n_mat <= 0) return cudaSuccess;
   const int64_t n = (int64_t)rows * (K >> 4);
   const dim3 grid((unsigned)blocks_for((n + kDqBlocksPerThread - 1) / kDqBlocksPerThread, 256), (unsigned)n_mat);
-  nv_weight_bf16_kernel<<<grid, 256, 0, s>>>(codes, sf, g, rows, K, count, out);
+  nv_weight_bf16_kernel<<<grid, 256, 0, s>>>(codes, sf, g, rows, K, tiled, count, out);
   return cudaGetLastError();
 }
 
@@ -746,6 +747,31 @@ cudaError_t launch_nv_qdq_h_bf16(const fp4moe_dims& d, const float* h32, const i
 cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   return launch_pdl(finalize_kernel, dim3(blocks_for((n + 3) / 4, 256)), dim3(256), 0, s, acc, out, n);
+}
+
+// Row-major FP4 payloads [rows_total, kbytes] -> the tiled layout (see
+// w_tiled_offset): one thread per 16 bytes of the output, so a warp writes
+// 512 contiguous bytes and reads four 128-byte row pieces; bytes past
+// kbytes (K padded to whole K tiles) are zero codes.
+__global__ void pack_weights_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t n16,
+                                    int kbytes, int ktb) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t blk = i >> 10;          // 1024 pieces of 16 bytes per 128 x 128-byte block
+    const int64_t r = (blk / ktb) * 128 + ((i >> 3) & 127);
+    const int cb = (int)(blk % ktb) * 128 + (int)(i & 7) * 16;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (cb < kbytes) v = *reinterpret_cast<const uint4*>(src + r * kbytes + cb);
+    reinterpret_cast<uint4*>(dst)[i] = v;
+  }
+}
+
+cudaError_t launch_pack_weights(const uint8_t* src, uint8_t* dst, int64_t rows_total, int kbytes, cudaStream_t s) {
+  const int ktb = (kbytes + 127) / 128;
+  const int64_t n16 = rows_total * ktb * 8;
+  if (n16 == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>(blocks_for(n16, 256), 1 << 20);
+  pack_weights_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, dst, n16, kbytes, ktb);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_pack_scales(const uint8_t* src, uint8_t* dst, int64_t n_mat, int rows, int kblocks, bool nv,

@@ -1,7 +1,9 @@
 """A routed block-scaled FP4 MoE layer held in device memory.
 
-``MoELayer`` owns the expert weights (packed FP4 codes, repacked block
-scales, NVFP4 tensor scales), the router weights and bias, and a workspace;
+``MoELayer`` owns the expert weights (packed FP4 codes, by default also
+repacked into the tiled payload layout the GEMMs stream as whole tiles;
+repacked block scales; NVFP4 tensor scales), the router weights and bias,
+and a workspace;
 ``forward`` calls fp4moe_forward.  PyTorch only allocates device memory and
 supplies the stream.  ``MoELayer.synthetic`` draws a layer from the seeded
 generator in ``synth`` directly on the GPU (weights of the NVFP4
@@ -16,8 +18,8 @@ import torch
 
 from . import (FP8, MXFP4, NVFP4, Debug, Fp8Weights, Weights, emulation_workspace_size, forward,
                forward_nvfp4_emulated, forward_w8a8, get_status, make_dims,
-               mxfp4_to_fp8_rowscale, pack_scales, packed_scales_bytes, quantize_act, workspace_layout,
-               workspace_size)
+               mxfp4_to_fp8_rowscale, pack_scales, pack_weights, packed_scales_bytes, packed_weights_bytes,
+               quantize_act, workspace_layout, workspace_size)
 
 
 def _ptr(t):
@@ -26,10 +28,13 @@ def _ptr(t):
 
 class MoELayer:
     def __init__(self, dims, w13, w13_scale, w2, w2_scale, w_router, bias, g13=None, g2=None,
-                 sh13=None, sh13_scale=None, sh2=None, sh2_scale=None):
+                 sh13=None, sh13_scale=None, sh2=None, sh2_scale=None, packed: bool = True):
         """Tensors on one CUDA device.  Scales are the raw row-major block
         scales ([E, rows, K/32] E8M0 or [E, rows, K/16] E4M3); they are
-        repacked here into the layout the GEMMs load."""
+        repacked here into the layout the GEMMs load.  packed: the forward
+        reads the payloads in the tiled layout (fp4moe_pack_weights), else the
+        row-major tensors themselves; the row-major tensors are kept either
+        way (the FP8 conversion reads them)."""
         self.dims = dims
         self.fmt = dims.fmt
         self.device = w13.device
@@ -43,12 +48,25 @@ class MoELayer:
         self.sh13, self.sh2 = sh13, sh2
         self.sh13_scale = self._pack(sh13_scale, 1, 2 * dims.I, dims.H // blk) if sh13 is not None else None
         self.sh2_scale = self._pack(sh2_scale, 1, dims.H, dims.I // blk) if sh2 is not None else None
+        self.packed = packed
+        pw = self._pack_w if packed else (lambda t, *_: t)
+        self.w13_t = pw(self.w13, dims.E, 2 * dims.I, dims.H // 2)
+        self.w2_t = pw(self.w2, dims.E, dims.H, dims.I // 2)
+        self.sh13_t = pw(sh13, 1, 2 * dims.I, dims.H // 2) if sh13 is not None else None
+        self.sh2_t = pw(sh2, 1, dims.H, dims.I // 2) if sh2 is not None else None
         self.ws_bytes = workspace_size(dims)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
         self.layout = workspace_layout(dims)
-        self.weights = Weights(_ptr(self.w13), _ptr(self.w13_scale), _ptr(self.w2), _ptr(self.w2_scale),
-                               _ptr(self.g13), _ptr(self.g2), _ptr(self.sh13), _ptr(self.sh13_scale),
-                               _ptr(self.sh2), _ptr(self.sh2_scale), _ptr(self.w_router), _ptr(self.bias))
+        self.weights = Weights(_ptr(self.w13_t), _ptr(self.w13_scale), _ptr(self.w2_t), _ptr(self.w2_scale),
+                               _ptr(self.g13), _ptr(self.g2), _ptr(self.sh13_t), _ptr(self.sh13_scale),
+                               _ptr(self.sh2_t), _ptr(self.sh2_scale), _ptr(self.w_router), _ptr(self.bias),
+                               1 if packed else 0)
+
+    def _pack_w(self, codes, n_mat, rows, kbytes):
+        dst = torch.empty(packed_weights_bytes(n_mat, rows, kbytes), dtype=torch.uint8, device=codes.device)
+        pack_weights(codes.data_ptr(), dst.data_ptr(), n_mat, rows, kbytes,
+                     torch.cuda.current_stream(codes.device).cuda_stream)
+        return dst
 
     def _pack(self, raw, n_mat, rows, kblocks):
         dst = torch.empty(packed_scales_bytes(n_mat, rows, kblocks, self.fmt), dtype=torch.uint8,
@@ -97,7 +115,7 @@ class MoELayer:
 
     # ------------------------------------------------------------ synthetic layers
     @classmethod
-    def synthetic(cls, cfg, device="cuda"):
+    def synthetic(cls, cfg, device="cuda", packed: bool = True):
         import synth
         fmt = NVFP4 if cfg.fmt == "nvfp4" else MXFP4
         dims = make_dims(cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k, cfg.n_group, cfg.topk_group, cfg.n_shared,
@@ -142,7 +160,7 @@ class MoELayer:
             if fmt == NVFP4:
                 g13 = torch.cat([g13, sg13])
                 g2 = torch.cat([g2, sg2])
-        layer = cls(dims, w13, w13s, w2, w2s, wr, bias, g13=g13, g2=g2, **sh)
+        layer = cls(dims, w13, w13s, w2, w2s, wr, bias, g13=g13, g2=g2, packed=packed, **sh)
         layer.cfg = cfg
         layer.raw_scales = (w13s, w2s)
         return layer

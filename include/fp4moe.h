@@ -90,13 +90,17 @@ typedef struct {
  *             last); NULL for MXFP4.
  *   sh13, sh13_scale, sh2, sh2_scale: the shared expert, same layouts with
  *             E = 1; NULL when n_shared == 0.
- *   w_router  bf16 [E, H].   bias  fp32 [E] correction bias. */
+ *   w_router  bf16 [E, H].   bias  fp32 [E] correction bias.
+ *   packed    0: the payloads w13, w2, sh13, sh2 are row-major as above;
+ *             1: they hold the tiled layout of fp4moe_pack_weights (the
+ *             GEMMs then read each weight tile as one contiguous block). */
 typedef struct {
   const uint8_t *w13, *w13_scale, *w2, *w2_scale;
   const float *g13, *g2;
   const uint8_t *sh13, *sh13_scale, *sh2, *sh2_scale;
   const uint16_t *w_router;
   const float *bias;
+  int32_t packed;
 } fp4moe_weights;
 
 /* W8A8 expert weights: each expert matrix as fp4moe_mxfp4_to_fp8_rowscale
@@ -192,6 +196,27 @@ size_t fp4moe_packed_scales_bytes(int64_t n_mat, int32_t rows, int32_t kblocks, 
  * fp4moe_packed_scales_bytes bytes. */
 fp4moe_status fp4moe_pack_scales(const uint8_t *src, uint8_t *dst, int64_t n_mat, int32_t rows,
                                  int32_t kblocks, int32_t fmt, void *stream);
+
+/* Bytes of the tiled payload layout for n_mat FP4 matrices of `rows` rows
+ * and `kbytes` bytes per row (rows % 128 == 0, kbytes % 16 == 0): each row
+ * padded to whole K tiles of 128 bytes (256 FP4 values).  0 for an
+ * unsupported shape. */
+size_t fp4moe_packed_weights_bytes(int64_t n_mat, int32_t rows, int32_t kbytes);
+
+/* Repacks row-major FP4 payloads src[n_mat, rows, kbytes] into the tiled
+ * layout the GEMMs can stream as whole tiles: for each matrix, 128-row tile
+ * rt and K tile kt (row-major order, kt innermost), one contiguous block of
+ * 128 rows x 128 bytes holding bytes kt*128 .. kt*128+127 of those rows,
+ * zero codes past kbytes.  Byte (r, c) of matrix m lands at
+ *   m*rows*KT*128 + ((r/128)*KT + c/128)*16384 + (r%128)*128 + c%128,
+ * KT = ceil(kbytes/128).  With the scale repacking of fp4moe_pack_scales
+ * this is the one-time weight preparation, the counterpart of the
+ * pre-shuffled weight operand of "Serve Kimi-K2.5-MXFP4 on MI355X with
+ * ATOM", section "Stage C: MXFP4 Linear GEMM".  src and dst are device
+ * buffers (dst: fp4moe_packed_weights_bytes bytes, not overlapping src);
+ * stream ordered.  Errors: INVALID_ARG (null pointer), UNSUPPORTED_SHAPE. */
+fp4moe_status fp4moe_pack_weights(const uint8_t *src, uint8_t *dst, int64_t n_mat, int32_t rows, int32_t kbytes,
+                                  void *stream);
 
 /* Router: logits, sigmoid + bias, grouped top-k and routing weights
  * ("Kimi-K2.7-Code on Gaudi 2", section "What was built").

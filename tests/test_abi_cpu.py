@@ -66,6 +66,18 @@ def test_packed_scale_sizes(lib):
     assert fm.packed_scales_bytes(1, 100, 8, fm.MXFP4) == 0
 
 
+def test_packed_weight_sizes(lib):
+    # rows padded to nothing (multiples of 128 required), K to whole 128-byte tiles
+    assert fm.packed_weights_bytes(384, 4096, 3584) == 384 * 4096 * 3584
+    assert fm.packed_weights_bytes(2, 256, 192) == 2 * 256 * 256
+    assert fm.packed_weights_bytes(1, 100, 128) == 0
+    assert fm.packed_weights_bytes(1, 128, 24) == 0  # rows of 16-byte multiples only
+    # unsupported shapes and null pointers are refused before any device work
+    assert lib.fp4moe_pack_weights(None, None, 1, 128, 128, None) == 1
+    buf = ctypes.create_string_buffer(256)
+    assert lib.fp4moe_pack_weights(buf, buf, 1, 100, 128, None) == 2
+
+
 def test_argument_errors_need_no_gpu(lib):
     d = fm.make_dims(4, 256, 128, 8, 2)
     # null pointers are refused before any device work

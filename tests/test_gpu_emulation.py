@@ -31,11 +31,11 @@ def _align(v):
 
 
 class RunEm:
-    def __init__(self, cfg):
+    def __init__(self, cfg, packed=True):
         torch = torch_cuda()
         ensure_built()
         from block_scaled_fp4_sigmoid_gb300.layer import MoELayer
-        layer = MoELayer.synthetic(cfg)
+        layer = MoELayer.synthetic(cfg, packed=packed)
         x = layer.synthetic_x()
         L = layer.layout
         self.L = L
@@ -73,8 +73,8 @@ class RunEm:
         del out, h_pre, layer
 
 
-def check_em(cfg, tokens):
-    run = RunEm(cfg)
+def check_em(cfg, tokens, packed=True):
+    run = RunEm(cfg, packed)
     assert run.status == (0, 0), run.status
     x, wr, b = OI.layer_inputs(cfg)
     assert np.array_equal(run.x_bits, synth.gen_x_bf16(cfg))
@@ -123,6 +123,12 @@ def check_em(cfg, tokens):
 def test_small_layers_emulated(name):
     cfg = SMALL[name]
     print(name, check_em(cfg, np.arange(cfg.T)))
+
+
+def test_emulated_row_major_weights():
+    """The weight dequantisation reading row-major payloads (packed = 0)."""
+    cfg = SMALL["nv_wide_padK"]
+    print(check_em(cfg, np.arange(cfg.T), packed=False))
 
 
 def test_deepseek_nvfp4_emulated_full_size():

@@ -55,13 +55,13 @@ SMALL = {
 class GpuRun:
     """One forward on the GPU plus host copies of its intermediates."""
 
-    def __init__(self, cfg, h_debug=True):
+    def __init__(self, cfg, h_debug=True, packed=True):
         torch = torch_cuda()
         ensure_built()
         from block_scaled_fp4_sigmoid_gb300.layer import MoELayer
         self.torch = torch
         self.cfg = cfg
-        layer = MoELayer.synthetic(cfg)
+        layer = MoELayer.synthetic(cfg, packed=packed)
         x = layer.synthetic_x()
         L = layer.layout
         self.L = L
@@ -215,8 +215,8 @@ def check_output(run, ref, S, A, tokens, skip):
     return worst
 
 
-def full_check(cfg, tokens=None, h_debug=True):
-    run = GpuRun(cfg, h_debug=h_debug)
+def full_check(cfg, tokens=None, h_debug=True, packed=True):
+    run = GpuRun(cfg, h_debug=h_debug, packed=packed)
     assert run.status == (0, 0), run.status
     x, wr, b = OI.layer_inputs(cfg)
     assert np.array_equal(run.x_bits, synth.gen_x_bf16(cfg))
@@ -253,6 +253,13 @@ def full_check(cfg, tokens=None, h_debug=True):
 def test_small_layers_full_oracle(name):
     stats = full_check(SMALL[name])
     print(name, stats)
+
+
+@pytest.mark.parametrize("name", ["tiny", "wide_padK", "nv_grouped", "nv_wide_padK"])
+def test_small_layers_row_major_weights(name):
+    """The same parity with the expert payloads left row-major (packed = 0);
+    the other tests use the tiled layout of fp4moe_pack_weights."""
+    print(name, full_check(SMALL[name], packed=False))
 
 
 def test_route_entry_point_matches_forward_routing():
