@@ -39,7 +39,7 @@ class Run8:
         from block_scaled_fp4_sigmoid_gb300.layer import MoELayer, W8A8Layer
         mx = MoELayer.synthetic(cfg)
         layer = W8A8Layer(mx)
-        del mx.w13, mx.w2  # the W8A8 layer keeps its own converted copies
+        del mx.w13, mx.w2, mx.w13_t, mx.w2_t  # the W8A8 layer keeps its own converted copies
         x = layer.synthetic_x()
         L = layer.layout
         self.L = L
