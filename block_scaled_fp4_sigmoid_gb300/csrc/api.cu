@@ -393,6 +393,18 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
     f.xq = xq;
     f.xsf = xsf;
     f.tok_mask = reinterpret_cast<uint32_t*>(cc);  // the per-chunk counters are not used here
+    if (d.n_shared) {  // the shared expert's weights (payloads and scales of w13, w2)
+      const uint8_t* r[4] = {w->sh13, w->sh13_scale, w->sh2, w->sh2_scale};
+      const int64_t n[4] = {
+          w->packed ? (int64_t)fp4moe_packed_weights_bytes(1, 2 * d.I, d.H / 2) : (int64_t)d.I * d.H,
+          (int64_t)fp4moe_packed_scales_bytes(1, 2 * d.I, d.H / 32, d.fmt),
+          w->packed ? (int64_t)fp4moe_packed_weights_bytes(1, d.H, d.I / 2) : (int64_t)d.H * (d.I / 2),
+          (int64_t)fp4moe_packed_scales_bytes(1, d.H, d.I / 32, d.fmt)};
+      for (int i = 0; i < 4; ++i) {
+        f.l2_pf[i] = r[i];
+        f.l2_pf_bytes[i] = n[i];
+      }
+    }
     if (e == cudaSuccess) e = launch_decode_front(f, s);
     for (int i = 1; i <= 4 && e == cudaSuccess; ++i) e = rec(i);
   } else {

@@ -77,6 +77,10 @@ struct FrontArgs {
   int32_t* ticket;  // zero on entry
   uint8_t *xq, *xsf;     // quantised x: token rows (slot 0 of the permuted layout)
   uint32_t* tok_mask;    // [n_exp] bit t: token t routes to the expert
+  // weights that do not depend on routing (the shared expert's), pulled
+  // into L2 by the helper CTAs while the last CTA routes; nullable
+  const uint8_t* l2_pf[4];
+  int64_t l2_pf_bytes[4];
 };
 constexpr int kFrontMaxT = 16;
 constexpr int kFrontMaxKc = 2048;  // router columns per split of the front end

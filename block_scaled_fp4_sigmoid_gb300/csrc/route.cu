@@ -509,6 +509,20 @@ __global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArg
     const int64_t helpers = a.n_splits == 1 ? gridDim.x : gridDim.x - gridDim.x / a.n_splits;
     const int64_t hid = a.n_splits == 1 ? blockIdx.x : blockIdx.x - blockIdx.x / a.n_splits - 1;
     const int64_t hthr = hid * kFrontThreads + tid, hn = helpers * kFrontThreads;
+    // DRAM is idle until routing ends: pull this CTA's slice of the shared
+    // expert's weights into L2 (evict-last, so that they outlast the routed
+    // weight stream that follows) for the two expert GEMMs.
+    if (tid == 0) {
+      const uint64_t pol = l2_evict_last();
+      for (int r = 0; r < 4; ++r) {
+        const int64_t n = a.l2_pf_bytes[r];
+        if (!a.l2_pf[r] || n <= 0) continue;
+        const int64_t slice = ((n + helpers - 1) / helpers + 255) / 256 * 256;
+        const int64_t lo = hid * slice, hi = lo + slice < n ? lo + slice : n;
+        for (int64_t o = lo; o < hi; o += 32768)
+          l2_prefetch(a.l2_pf[r] + o, (uint32_t)(hi - o < 32768 ? hi - o : 32768), pol);
+      }
+    }
     for (int64_t i = hthr; i < (int64_t)T * H / 4; i += hn)
       reinterpret_cast<float4*>(a.out_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     const int per_row = H >> 5;
