@@ -129,19 +129,6 @@ __device__ __forceinline__ uint64_t l2_evict_first() {
   return pol;
 }
 
-__device__ __forceinline__ uint64_t l2_evict_last() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
-// Prefetch of a 16-byte aligned global range into L2 with a cache policy (a
-// hint: nothing waits for it); size a multiple of 16.
-__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes, uint64_t policy) {
-  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(policy)
-               : "memory");
-}
-
 // Plain (untiled) bulk copy global -> shared; both addresses 16-byte aligned,
 // size a multiple of 16.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

@@ -466,6 +466,19 @@ __device__ __forceinline__ float2 front_gemv_any(const FrontArgs& a, uint16_t* x
   return front_gemv<TMAX, kFrontMaxKc / 256>(a, xs, sp, e0, lane);
 }
 
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Prefetch of a 16-byte aligned global range into L2 with a cache policy (a
+// hint: nothing waits for it); size a multiple of 16.
+__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(policy)
+               : "memory");
+}
+
 __global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArgs a) {
   extern __shared__ __align__(16) uint16_t front_xs[];  // [T][kc] bf16 of this CTA's split
   __shared__ __align__(16) float s_sc[kFrontWarps][2][512];  // scores of the token a warp routes
