@@ -37,7 +37,10 @@ bool dims_ok(const fp4moe_dims& d) {
   if (d.top_k < 1 || d.top_k > 16 || d.top_k > d.E) return false;
   if (d.n_group < 1 || d.n_group > 32 || d.E % d.n_group != 0) return false;
   if (d.topk_group < 1 || d.topk_group > d.n_group) return false;
-  if (d.n_group > 1 && (d.E / d.n_group > 64 || d.topk_group * (d.E / d.n_group) < d.top_k)) return false;
+  // grouped routing scores a group by its two largest corrected scores, so
+  // a group holds at least two experts
+  if (d.n_group > 1 && (d.E / d.n_group < 2 || d.E / d.n_group > 64 || d.topk_group * (d.E / d.n_group) < d.top_k))
+    return false;
   if (d.n_shared < 0 || d.n_shared > 1) return false;
   if (d.fmt != FP4MOE_MXFP4 && d.fmt != FP4MOE_NVFP4 && d.fmt != FP4MOE_FP8) return false;
   if (!(d.routed_scaling == d.routed_scaling)) return false;

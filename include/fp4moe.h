@@ -72,8 +72,9 @@ typedef enum { FP4MOE_MXFP4 = 0, FP4MOE_NVFP4 = 1, FP4MOE_FP8 = 2 } fp4moe_forma
  *   routed_scaling multiplies the routing weights, renormalize != 0 divides
  *   the chosen sigmoid scores by their sum first, fmt an fp4moe_format.
  * Supported: 1 <= T <= 65536; H % 256 == 0; I % 128 == 0; 1 <= E <= 512;
- *   1 <= top_k <= 16 and top_k <= E; E % n_group == 0; E / n_group <= 64 when
- *   n_group > 1; 1 <= topk_group <= n_group <= 32; n_shared in {0, 1}. */
+ *   1 <= top_k <= 16 and top_k <= E; E % n_group == 0; 2 <= E / n_group <= 64
+ *   when n_group > 1 (a group's score sums its two largest scores);
+ *   1 <= topk_group <= n_group <= 32; n_shared in {0, 1}. */
 typedef struct {
   int32_t T, H, I, E, top_k, n_group, topk_group, n_shared;
   float routed_scaling;

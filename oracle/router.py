@@ -45,6 +45,7 @@ def route_token(logit: np.ndarray, bias: np.ndarray, top_k: int, n_group: int,
     gscore = None
     if n_group > 1:
         gsz = E // n_group
+        assert gsz >= 2, "a group's score sums its two largest corrected scores"
         cg = c.reshape(n_group, gsz)
         top2 = np.sort(cg, axis=1)[:, -2:]
         gscore = top2[:, 0] + top2[:, 1]

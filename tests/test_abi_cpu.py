@@ -78,6 +78,13 @@ def test_packed_weight_sizes(lib):
     assert lib.fp4moe_pack_weights(buf, buf, 1, 100, 128, None) == 2
 
 
+def test_group_of_one_expert_is_refused(lib):
+    # a group's score sums its two largest corrected scores: groups of one
+    # expert are outside the supported shapes, two are inside
+    assert lib.fp4moe_workspace_size(ctypes.byref(fm.make_dims(4, 256, 128, 8, 2, n_group=8, topk_group=4))) == 0
+    assert lib.fp4moe_workspace_size(ctypes.byref(fm.make_dims(4, 256, 128, 8, 2, n_group=4, topk_group=2))) > 0
+
+
 def test_argument_errors_need_no_gpu(lib):
     d = fm.make_dims(4, 256, 128, 8, 2)
     # null pointers are refused before any device work

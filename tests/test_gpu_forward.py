@@ -262,6 +262,31 @@ def test_small_layers_row_major_weights(name):
     print(name, full_check(SMALL[name], packed=False))
 
 
+# Limits of the supported shapes and degenerate routings: 512 experts with
+# top-16 through the few-token front end and through the many-token path, 32
+# expert groups (NVFP4), a single expert, every expert chosen by every token.
+EDGE = {
+    "E512_top16_front": _cfg("tiny", name="E512_top16_front", T=16, H=256, I=128, E=512, top_k=16, n_shared=1),
+    "E512_top16": _cfg("tiny", name="E512_top16", T=96, H=512, I=256, E=512, top_k=16),
+    "nv_group32": _cfg("deepseek_nvfp4", name="nv_group32", T=40, H=256, I=128, E=512, top_k=8, n_group=32,
+                       topk_group=4, n_shared=1),
+    "single_expert": _cfg("tiny", name="single_expert", T=20, H=256, I=128, E=1, top_k=1, n_shared=1),
+    "topk_all": _cfg("tiny", name="topk_all", T=33, H=256, I=128, E=8, top_k=8),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE))
+def test_edge_layers_full_oracle(name):
+    print(name, full_check(EDGE[name]))
+
+
+def test_max_tokens_sampled():
+    """T = 65536, the largest supported batch: first and last tokens, chunk
+    and half boundaries of the permutation."""
+    cfg = _cfg("tiny", name="T_max", T=65536, H=256, I=128, E=16, top_k=4)
+    print(full_check(cfg, tokens=[0, 1, 31, 32, 4095, 32767, 32768, 65534, 65535]))
+
+
 def test_route_entry_point_matches_forward_routing():
     torch = torch_cuda()
     ensure_built()
