@@ -204,6 +204,28 @@ def oracle_route_sample(cfg_name: str, n_routes: int, frac: float = 1.0, start_t
     return t_total, n_routes / rpt * (Ip / cfg.I)
 
 
+def rank_token_range(rank: int, T: int) -> tuple[int, int]:
+    """Weak scaling: every rank runs its own batch of T tokens, tokens
+    rank*T .. (rank+1)*T of the seeded stream."""
+    return rank * T, (rank + 1) * T
+
+
+def max_over_ranks(vals, world: int, device) -> list:
+    """Element-wise maximum over the ranks (the slowest rank's times); the
+    identity for one rank."""
+    import torch
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Units all ranks processed per second, over the slowest rank's time."""
+    return units_per_rank * world / (ms_max * 1e-3)
+
+
 def reference_arm(args, cfg, rank, world):
     if rank != 0:
         return
@@ -351,17 +373,13 @@ def linear_arm(args, rank, world, local_rank):
         e2e[i][1].record(stream)
     torch.cuda.synchronize()
     e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e)
-    vals = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    ms, e2e_ms = vals.tolist()
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], world, dev)
     if rank != 0:
         return
     flops = 2.0 * T * K * N
     peaks = measured_peaks()
     fp4_peak = 6 * peaks["bf16_tflops"]
-    tflops = flops * world / (ms * 1e-3) / 1e12
+    tflops = whole_job_rate(flops, world, ms) / 1e12
     # CPU baseline: the oracle on a bounded sample of rows
     from oracle import linear as LIN
     from oracle.formats import unpack_nibbles
@@ -378,7 +396,7 @@ def linear_arm(args, rank, world, local_rank):
         "config": {"workload": f"dense MXFP4 linear T={T} K={K} N={N} (bf16 in, on-the-fly activation quantisation, "
                                f"bf16 out)", "l2": "flushed between steps (256 MiB write, untimed)"},
         "clocks": clk.summary(),
-        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": whole_job_rate(flops, world, e2e_ms) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": T * K * 2, "d2h_bytes_per_step": T * N * 2},
         "gpu_launches": 5 * args.steps,
         "roofline": {"bound": "tensor", "kernel": "moe_gemm_kernel<down> (one expert)", "achieved": tflops / world,
@@ -412,10 +430,10 @@ def gpu_arm(args, cfg, rank, world, local_rank):
             raise SystemExit("--w8a8 converts MXFP4 experts")
         mx = layer
         layer = W8A8Layer(mx)
-        del mx.w13, mx.w2  # the converted copies are what the W8A8 layer reads
+        del mx.w13, mx.w2, mx.w13_t, mx.w2_t  # the converted copies are what the W8A8 layer reads
         torch.cuda.empty_cache()
     # each rank runs its own batch: tokens rank*T .. (rank+1)*T of the stream
-    x = layer.synthetic_x(rank * cfg.T, (rank + 1) * cfg.T)
+    x = layer.synthetic_x(*rank_token_range(rank, cfg.T))
     if args.emulate and cfg.fmt != "nvfp4":
         raise SystemExit("--emulate runs NVFP4 layers")
     fwd = layer.forward_emulated if args.emulate else layer.forward
@@ -547,10 +565,7 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     flops = 2.0 * 3 * d.I * d.H * routes
 
     # max over ranks
-    vals = torch.tensor([ms, e2e_ms, statistics.mean(gu_ms)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    ms_max, e2e_max, gu_max = vals.tolist()
+    ms_max, e2e_max, gu_max = max_over_ranks([ms, e2e_ms, statistics.mean(gu_ms)], world, dev)
     if rank != 0:
         return
     peaks = measured_peaks()
@@ -574,7 +589,7 @@ def gpu_arm(args, cfg, rank, world, local_rank):
                       else (float("nan"), 0.0))
     line = {
         "metric": METRIC,
-        "value": cfg.T * world / (ms_max * 1e-3),
+        "value": whole_job_rate(cfg.T, world, ms_max),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": steps,
@@ -590,7 +605,7 @@ def gpu_arm(args, cfg, rank, world, local_rank):
                    "l2": "flushed between steps (256 MiB write, untimed)", "touched_experts": touched,
                    "routes": routes},
         "clocks": clocks,
-        "e2e": {"value": cfg.T * world / (e2e_max * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": whole_job_rate(cfg.T, world, e2e_max), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x.numel() * 2), "d2h_bytes_per_step": int(out.numel() * 2)},
         "gpu_launches": launches_per_step * steps,
         "roofline": {"bound": "hbm", "kernel": "gate/up grouped GEMM", "achieved": achieved,
