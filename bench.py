@@ -57,10 +57,36 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
+def code_text(src: str) -> str:
+    """C++/CUDA source without comments and blank space: a comment-only edit
+    leaves the kernel, and so this text, unchanged.  String literals (inline
+    PTX) are kept as they are."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"':  # string literal, escapes included
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_sha(paths) -> str:
+    """Hash of the code (comments and spacing excluded) of the given files."""
     h = hashlib.sha256()
     for p in paths:
-        h.update((ROOT / p).read_bytes())
+        h.update(code_text((ROOT / p).read_text()).encode())
     return h.hexdigest()[:16]
 
 

@@ -13,14 +13,18 @@
 // (expert, 128-row weight tile, token tile); units of one expert are laid
 // out weight-tile-major so concurrent CTAs share each weight tile through L2.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over units):
+// Warp roles (256 threads, one CTA per SM, persistent over units):
 //   warp 0     TMA producer: weight tiles (3-D tensor map over [E, rows,
-//              K/2]), token tiles (2-D map over the padded permuted rows),
-//              scale groups (bulk copies of the tiled scale layout);
-//   warp 1     tensor-memory owner and single-thread MMA issuer: copies the
-//              stage's scale factors to tensor memory (tcgen05.cp), issues
-//              four K=64 MMAs per 256-wide K tile and per A operand, commits
-//              the stage back to the producer;
+//              K/2], or over the tiled payload layout), token tiles (2-D map
+//              over the padded permuted rows), scale groups (bulk copies of
+//              the tiled scale layout);
+//   warps 1, 6 MMA issuers (warp 1 also owns tensor memory): copy each
+//              stage's scale factors to tensor memory (tcgen05.cp), issue four
+//              K=64 MMAs per 256-wide K tile (gate/up: one A operand each;
+//              down: alternate K tiles into two accumulators), and commit the
+//              stage back to the producer;
+//   warp 7     gate/up: zeroes the combine buffer when asked; down: second
+//              TMA producer (the token tiles and their scale groups);
 //   warps 2-5  epilogue, one per tensor-memory lane quadrant:
 //              gate/up: SwiGLU, then MXFP4 requantisation of h across the
 //              32 lanes of a warp (= one 32-block along I), or (NVFP4) fp32
@@ -99,7 +103,7 @@ struct GemmCfg {
   // issuer copies its own A and B scale factors.
   static constexpr int kIssuers = 2;
   static constexpr bool kKSplit = !GATEUP;
-  static constexpr int kThreads = 256;  // + warp 7: zeroes the combine buffer (gate/up, when asked)
+  static constexpr int kThreads = 256;  // warp 7: combine-buffer zeroing (gate/up) or second producer (down)
   static constexpr int kAccCols = 2 * N;                            // one accumulator set: two N-column blocks
   static constexpr int kSfCols = kIssuers * 2 * kAtoms * 4;         // scale factors of one K tile
   // two accumulator sets when they fit: the epilogue of one unit then
