@@ -258,8 +258,11 @@ fp4moe_status fp4moe_route_noalloc(const fp4moe_dims *dims, const uint16_t *x, c
  * AMD Instinct MI355 accelerators", section "Weight Dequantization and
  * Activation QDQ").
  *   x [rows, cols] bf16 (x_is_fp32 = 0) or fp32 (x_is_fp32 = 1), row-major.
- *   codes [rows, cols/2] packed E2M1.  scales row-major: MXFP4 [rows, cols/32]
- *   E8M0 bytes, e = floor(log2 amax) - 2; NVFP4 [rows, cols/16] E4M3 bytes.
+ *   codes [rows, cols/2] packed E2M1 (element 2j in the low nibble), each the
+ *   round-to-nearest-even grid point (ties to the even code, saturating at
+ *   +-6, sign bit kept: a negative value that rounds to zero gives code 0x8).
+ *   scales row-major: MXFP4 [rows, cols/32] E8M0 bytes, e = floor(log2 amax)
+ *   - 2; NVFP4 [rows, cols/16] E4M3 bytes.
  *   NVFP4 tensor scale: global_in (nullable, fp32 device scalar) is used when
  *   given, else g = amax(x) / 2688 is computed over the whole tensor; the g
  *   used is written to global_out (nullable).
