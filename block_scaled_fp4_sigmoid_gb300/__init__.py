@@ -93,6 +93,7 @@ def lib() -> ctypes.CDLL:
         L.fp4moe_route.argtypes = [P(Dims), vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.fp4moe_quantize_act.argtypes = [vp, i32, i64, i32, i32, vp, vp, vp, vp, vp, sz, vp]
         L.fp4moe_forward.argtypes = [P(Dims), P(Weights), vp, vp, P(Debug), vp, sz, vp]
+        L.fp4moe_forward_cols.argtypes = [P(Dims), P(Weights), vp, vp, i32, i32, P(Debug), vp, sz, vp]
         L.fp4moe_forward_w8a8.argtypes = [P(Dims), P(Fp8Weights), vp, vp, P(Debug), vp, sz, vp]
         L.fp4moe_emulation_workspace_size.argtypes = [P(Dims)]
         L.fp4moe_emulation_workspace_size.restype = sz
@@ -104,7 +105,7 @@ def lib() -> ctypes.CDLL:
         L.fp4moe_clear_status.argtypes = [vp, vp]
         L.fp4moe_get_status.argtypes = [vp, vp, P(i32), P(i64)]
         for name in ("fp4moe_workspace_layout", "fp4moe_pack_scales", "fp4moe_pack_weights", "fp4moe_route", "fp4moe_quantize_act",
-                     "fp4moe_forward", "fp4moe_forward_w8a8", "fp4moe_forward_nvfp4_emulated", "fp4moe_linear",
+                     "fp4moe_forward", "fp4moe_forward_cols", "fp4moe_forward_w8a8", "fp4moe_forward_nvfp4_emulated", "fp4moe_linear",
                      "fp4moe_mxfp4_to_fp8_rowscale",
                      "fp4moe_clear_status",
                      "fp4moe_get_status"):
@@ -179,6 +180,13 @@ def forward(dims: Dims, weights: Weights, x: int, out: int, ws: int, ws_bytes: i
     dbg = ctypes.byref(debug) if debug is not None else None
     _ok(lib().fp4moe_forward(ctypes.byref(dims), ctypes.byref(weights), x, out, dbg, ws, ws_bytes, stream),
         "fp4moe_forward")
+
+
+def forward_cols(dims: Dims, weights: Weights, x: int, out: int, h_begin: int, h_end: int, ws: int, ws_bytes: int,
+                 stream: int = 0, debug: Debug | None = None) -> None:
+    dbg = ctypes.byref(debug) if debug is not None else None
+    _ok(lib().fp4moe_forward_cols(ctypes.byref(dims), ctypes.byref(weights), x, out, h_begin, h_end, dbg, ws,
+                                  ws_bytes, stream), "fp4moe_forward_cols")
 
 
 def forward_w8a8(dims: Dims, weights: Fp8Weights, x: int, out: int, ws: int, ws_bytes: int, stream: int = 0,

@@ -310,12 +310,19 @@ fp4moe_status fp4moe_quantize_act(const void* x, int32_t x_is_fp32, int64_t rows
   return cuda_status(e);
 }
 
-fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, const uint16_t* x, uint16_t* out,
-                             const fp4moe_debug* dbg, void* ws, size_t ws_bytes, void* stream) {
+// The layer over output columns [h_begin, h_end): everything up to the
+// intermediate is computed in full; the down GEMM reads the weight rows of
+// those columns only and the other columns of out come out zero.
+static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights* w, const uint16_t* x,
+                                  uint16_t* out, int32_t h_begin, int32_t h_end, const fp4moe_debug* dbg, void* ws,
+                                  size_t ws_bytes, void* stream) {
   if (!dims || !w || !x || !out || !ws) return FP4MOE_ERR_INVALID_ARG;
   const fp4moe_dims& d = *dims;
   Layout L;
   if (!make_layout(d, &L)) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  if (h_begin < 0 || h_end > d.H || h_begin >= h_end || h_begin % 128 != 0 || h_end % 128 != 0)
+    return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  const int dn_mtiles = (h_end - h_begin) / 128;
   if (d.fmt == FP4MOE_FP8) return FP4MOE_ERR_INVALID_ARG;  // fp4moe_forward_w8a8
   if (ws_bytes < (size_t)L.ws.total_bytes) return FP4MOE_ERR_WORKSPACE;
   const bool nv = d.fmt == FP4MOE_NVFP4;
@@ -380,6 +387,7 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
     f.n_splits = L.front_splits;
     f.n_tile = n_tile;
     f.n_exp = L.n_exp;
+    f.dn_mtiles = dn_mtiles;
     f.out_acc = acc;
     f.idx = idx;
     f.w = tw;
@@ -417,7 +425,7 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
     if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, nullptr, cc, L.n_exp, s);
     if (e == cudaSuccess) e = rec(2);
     if (e == cudaSuccess)
-      e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, ecount, eslot, gu_start, dn_start, plan,
+      e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, dn_mtiles, ecount, eslot, gu_start, dn_start, plan,
                       status + ST_TICKET_PLAN, s);
     if (e == cudaSuccess)
       e = launch_scatter(d, idx, tw, cc, L.n_chunks, L.n_exp, n_tile, eslot, route_row, row_tok, row_w, row_e, s);
@@ -469,6 +477,8 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
     GemmArgs g = a;
     g.w = w->w2;
     g.w_tiled = w->packed != 0;
+    g.row_begin = h_begin;
+    g.row_count = h_end - h_begin;
     g.wsf = w->w2_scale;
     g.sh = d.n_shared ? w->sh2 : nullptr;
     g.shsf = d.n_shared ? w->sh2_scale : nullptr;
@@ -484,6 +494,18 @@ fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, c
   if (e == cudaSuccess) e = launch_finalize(acc, out, (int64_t)d.T * d.H, s);
   if (e == cudaSuccess) e = rec(7);
   return cuda_status(e);
+}
+
+fp4moe_status fp4moe_forward(const fp4moe_dims* dims, const fp4moe_weights* w, const uint16_t* x, uint16_t* out,
+                             const fp4moe_debug* dbg, void* ws, size_t ws_bytes, void* stream) {
+  if (!dims) return FP4MOE_ERR_INVALID_ARG;
+  return forward_cols(dims, w, x, out, 0, dims->H, dbg, ws, ws_bytes, stream);
+}
+
+fp4moe_status fp4moe_forward_cols(const fp4moe_dims* dims, const fp4moe_weights* w, const uint16_t* x,
+                                  uint16_t* out, int32_t h_begin, int32_t h_end, const fp4moe_debug* dbg, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  return forward_cols(dims, w, x, out, h_begin, h_end, dbg, ws, ws_bytes, stream);
 }
 
 fp4moe_status fp4moe_forward_w8a8(const fp4moe_dims* dims, const fp4moe_fp8_weights* w, const uint16_t* x,
@@ -543,7 +565,7 @@ fp4moe_status fp4moe_forward_w8a8(const fp4moe_dims* dims, const fp4moe_fp8_weig
   if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, nullptr, cc, L.n_exp, s);
   if (e == cudaSuccess) e = rec(2);
   if (e == cudaSuccess)
-    e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, ecount, eslot, gu_start, dn_start, plan,
+    e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, d.H / 128, ecount, eslot, gu_start, dn_start, plan,
                     status + ST_TICKET_PLAN, s);
   if (e == cudaSuccess)
     e = launch_scatter(d, idx, tw, cc, L.n_chunks, L.n_exp, n_tile, eslot, route_row, row_tok, row_w, row_e, s);
@@ -668,7 +690,7 @@ fp4moe_status fp4moe_forward_nvfp4_emulated(const fp4moe_dims* dims, const fp4mo
   if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, nullptr, cc, L.n_exp, s);
   if (e == cudaSuccess) e = rec(2);
   if (e == cudaSuccess)
-    e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, ecount, eslot, gu_start, dn_start, plan,
+    e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, d.H / 128, ecount, eslot, gu_start, dn_start, plan,
                     status + ST_TICKET_PLAN, s);
   if (e == cudaSuccess)
     e = launch_scatter(d, idx, tw, cc, L.n_chunks, L.n_exp, n_tile, eslot, route_row, row_tok, row_w, row_e, s);

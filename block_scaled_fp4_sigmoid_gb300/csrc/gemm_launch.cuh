@@ -20,19 +20,27 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   // 128-byte rows in which the block of (row tile rt, K tile kt) starts at
   // view row (rt * KTb + kt) * 128)
   const uint64_t KTb = (Kb + 127) / 128;
-  const uint64_t a_dim0 = a.w_tiled ? 128 : Kb, a_dim1 = a.w_tiled ? (uint64_t)rows * KTb : (uint64_t)rows;
-  const uint64_t a_mat = a.w_tiled ? (uint64_t)rows * KTb * 128 : (uint64_t)rows * Kb;
+  // Down over an output-column slice: weight rows [r0, r0 + vis) of every
+  // expert matrix (the maps start at row r0 and see vis rows; the matrix
+  // stride stays that of all rows), and the same columns of the combine
+  // buffer.  A row's bytes in memory: Kb, or whole K tiles when tiled.
+  const int r0 = GATEUP ? 0 : a.row_begin;
+  const int vis = (GATEUP || a.row_count <= 0) ? rows : a.row_count;
+  const uint64_t a_row = a.w_tiled ? KTb * 128 : Kb;
+  const uint64_t a_dim0 = a.w_tiled ? 128 : Kb, a_dim1 = a.w_tiled ? (uint64_t)vis * KTb : (uint64_t)vis;
+  const uint64_t a_mat = (uint64_t)rows * a_row;
   {
     const uint64_t dims[3] = {a_dim0, a_dim1, (uint64_t)d.E};
     const uint64_t strides[2] = {a_dim0, a_mat};
     const uint32_t box[3] = {128, 128, 1};
-    if (!encode_tmap_u8(&p.tmA, a.w, 3, dims, strides, box, true)) return cudaErrorInvalidValue;
+    if (!encode_tmap_u8(&p.tmA, a.w + (uint64_t)r0 * a_row, 3, dims, strides, box, true)) return cudaErrorInvalidValue;
   }
   if (a.sh) {
     const uint64_t dims[3] = {a_dim0, a_dim1, 1};
     const uint64_t strides[2] = {a_dim0, a_mat};
     const uint32_t box[3] = {128, 128, 1};
-    if (!encode_tmap_u8(&p.tmA_sh, a.sh, 3, dims, strides, box, true)) return cudaErrorInvalidValue;
+    if (!encode_tmap_u8(&p.tmA_sh, a.sh + (uint64_t)r0 * a_row, 3, dims, strides, box, true))
+      return cudaErrorInvalidValue;
   }
   {
     const uint64_t dims[2] = {Kb, (uint64_t)a.rows_cap};
@@ -40,8 +48,10 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
     const uint32_t box[2] = {128, (uint32_t)a.n_tile};
     if (!encode_tmap_u8(&p.tmB, a.b, 2, dims, strides, box, true)) return cudaErrorInvalidValue;
   }
-  p.wsf = a.wsf;
-  p.shsf = a.shsf;
+  // scale groups of the slice: 128-row tiles r0 / 128 on (tiled scale layout)
+  const int64_t sf_r0 = (int64_t)(r0 / 128) * katoms_padded(K, a.nv) * 512;
+  p.wsf = a.wsf ? a.wsf + sf_r0 : nullptr;
+  p.shsf = a.shsf ? a.shsf + sf_r0 : nullptr;
   p.bsf = a.bsf;
   p.gw = a.gw;
   p.gb = a.g_b;
@@ -58,7 +68,7 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   p.hsf = a.hsf;
   p.h32 = a.h32;
   p.h_dbg = a.h_dbg;
-  p.out_acc = a.out_acc;
+  p.out_acc = a.out_acc ? a.out_acc + r0 : nullptr;  // row stride stays H
   if (GATEUP && a.zero_acc) {
     p.zero_buf = reinterpret_cast<float4*>(a.out_acc);
     p.zero_n4 = (int64_t)d.T * d.H / 4;
@@ -71,14 +81,14 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   p.I = d.I;
   p.K = K;
   p.rows_per_expert = rows;
-  p.m_tiles = GATEUP ? d.I / 128 : d.H / 128;
+  p.m_tiles = GATEUP ? d.I / 128 : vis / 128;
   p.katoms_a = (int)katoms_padded(K, a.nv);
   p.katoms_b = (int)katoms_padded(K, a.nv);
   p.katoms_h = (int)katoms_padded(d.I, a.nv);
   p.has_shared = a.sh != nullptr;
   p.w_tiled = a.w_tiled ? 1 : 0;
-  p.wrs = a.wrs;
-  p.shrs = a.shrs;
+  p.wrs = a.wrs ? a.wrs + r0 : nullptr;
+  p.shrs = a.shrs ? a.shrs + r0 : nullptr;
   p.brs = a.brs;
   const int grid = a.num_sms > 0 ? a.num_sms : 1;
   if (a.f8 || a.bf) {

@@ -48,9 +48,11 @@ int router_tc_n(int E);
 cudaError_t launch_topk(const fp4moe_dims& d, const float* partial, int n_splits, const float* bias,
                         int32_t* idx, float* w, float* logits_out, int32_t* chunk_counts, int n_exp,
                         cudaStream_t s);
+// dn_mtiles: 128-column tiles of the layer output the down GEMM computes
+// (H / 128 for the whole output)
 cudaError_t launch_plan(const fp4moe_dims& d, int32_t* chunk_counts, int n_chunks, int n_exp, int n_tile,
-                        int32_t* expert_count, int32_t* expert_slot, int32_t* gu_start, int32_t* dn_start,
-                        Plan* plan, int32_t* ticket, cudaStream_t s);
+                        int dn_mtiles, int32_t* expert_count, int32_t* expert_slot, int32_t* gu_start,
+                        int32_t* dn_start, Plan* plan, int32_t* ticket, cudaStream_t s);
 // Dense linear: one expert holding every token in order, weight 1; zeroes acc
 // (acc_n floats, a multiple of 4)
 cudaError_t launch_linear_plan(int T, int n_tile, int m_tiles, int32_t* count, int32_t* slot, int32_t* dn_start,
@@ -67,6 +69,7 @@ struct FrontArgs {
   const float* bias;
   float* partial;
   int n_splits, n_tile, n_exp;  // n_splits: K splits (cluster size, <= 8), H / n_splits <= kFrontMaxKc
+  int dn_mtiles;                 // 128-column tiles of the output the down GEMM computes
   float* out_acc;                // zeroed here
   int32_t* idx;
   float* w;
@@ -128,6 +131,8 @@ struct GemmArgs {
   // weights
   const uint8_t *w, *wsf;          // routed experts
   bool w_tiled;                    // w and sh in the tiled layout of fp4moe_pack_weights
+  int row_begin, row_count;        // down: weight rows (= output columns) [row_begin, +row_count);
+                                   // row_count 0: all H rows
   const uint8_t *sh, *shsf;        // shared expert (nullable)
   const float *gw;                 // NVFP4 tensor scales [E + n_shared]
   // activations (B operand)

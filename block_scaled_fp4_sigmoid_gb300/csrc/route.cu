@@ -613,7 +613,7 @@ __global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArg
   __syncthreads();
   for (int e = tid; e < n_exp; e += blockDim.x) a.tok_mask[e] = s_mask[e];
   // plan: exclusive scan of tiles over experts; thread j owns experts 3j..3j+2
-  const int gm = d.I / 128, dm = H / 128;
+  const int gm = d.I / 128, dm = a.dn_mtiles;
   int tl[3], my = 0;
 #pragma unroll
   for (int q = 0; q < 3; ++q) {
@@ -729,11 +729,11 @@ cudaError_t launch_topk(const fp4moe_dims& d, const float* partial, int n_splits
 }
 
 cudaError_t launch_plan(const fp4moe_dims& d, int32_t* chunk_counts, int n_chunks, int n_exp, int n_tile,
-                        int32_t* expert_count, int32_t* expert_slot, int32_t* gu_start, int32_t* dn_start,
-                        Plan* plan, int32_t* ticket, cudaStream_t s) {
+                        int dn_mtiles, int32_t* expert_count, int32_t* expert_slot, int32_t* gu_start,
+                        int32_t* dn_start, Plan* plan, int32_t* ticket, cudaStream_t s) {
   const unsigned blocks = (unsigned)((n_exp + kPlanWarps - 1) / kPlanWarps);
   plan_kernel<<<blocks, 32 * kPlanWarps, 0, s>>>(chunk_counts, n_chunks, n_exp, d.E, d.T, n_tile, d.I / 128,
-                                                 d.H / 128, expert_count, expert_slot, gu_start, dn_start, plan,
+                                                 dn_mtiles, expert_count, expert_slot, gu_start, dn_start, plan,
                                                  ticket);
   return cudaGetLastError();
 }

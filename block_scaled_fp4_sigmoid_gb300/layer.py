@@ -16,7 +16,7 @@ import ctypes
 
 import torch
 
-from . import (FP8, MXFP4, NVFP4, Debug, Fp8Weights, Weights, emulation_workspace_size, forward,
+from . import (FP8, MXFP4, NVFP4, Debug, Fp8Weights, Weights, emulation_workspace_size, forward, forward_cols,
                forward_nvfp4_emulated, forward_w8a8, get_status, make_dims,
                mxfp4_to_fp8_rowscale, pack_scales, pack_weights, packed_scales_bytes, packed_weights_bytes,
                quantize_act, workspace_layout, workspace_size)
@@ -24,6 +24,28 @@ from . import (FP8, MXFP4, NVFP4, Debug, Fp8Weights, Weights, emulation_workspac
 
 def _ptr(t):
     return t.data_ptr() if t is not None else None
+
+
+def column_block(H: int, rank: int, world: int) -> tuple[int, int]:
+    """Output columns [h0, h1) of rank `rank` of `world` in an
+    output-partitioned layer: whole 128-column tiles, as even as possible."""
+    tiles = H // 128
+    if not 0 < world <= tiles or not 0 <= rank < world:
+        raise ValueError(f"{world} ranks over {tiles} column tiles")
+    return 128 * (tiles * rank // world), 128 * (tiles * (rank + 1) // world)
+
+
+def tp_forward(layer, x, group=None):
+    """Output-partitioned forward over a torch.distributed group: each rank
+    computes its block of output columns (zero elsewhere) and one all-reduce
+    (sum) assembles the layer output on every rank ("Inside the Kimi K3
+    optimization effort", section "MoE: remove duplicate work across GPUs")."""
+    import torch.distributed as dist
+    rank, world = dist.get_rank(group), dist.get_world_size(group)
+    h0, h1 = column_block(layer.dims.H, rank, world)
+    out = layer.forward_cols(x, h0, h1)
+    dist.all_reduce(out, group=group)
+    return out
 
 
 class MoELayer:
@@ -88,6 +110,17 @@ class MoELayer:
             out = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=self.device)
         s = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
         forward(d, self.weights, x.data_ptr(), out.data_ptr(), self.ws.data_ptr(), self.ws_bytes, s, debug)
+        return out
+
+    def forward_cols(self, x, h_begin: int, h_end: int, out=None, debug: Debug | None = None, stream=None):
+        """The layer output restricted to columns [h_begin, h_end); the other
+        columns of out are zero (fp4moe_forward_cols)."""
+        d = self.dims
+        if out is None:
+            out = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=self.device)
+        s = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
+        forward_cols(d, self.weights, x.data_ptr(), out.data_ptr(), h_begin, h_end, self.ws.data_ptr(),
+                     self.ws_bytes, s, debug)
         return out
 
     def forward_emulated(self, x, out=None, debug: Debug | None = None, stream=None):

@@ -279,6 +279,21 @@ fp4moe_status fp4moe_forward(const fp4moe_dims *dims, const fp4moe_weights *w, c
                              uint16_t *out, const fp4moe_debug *dbg, void *ws, size_t ws_bytes,
                              void *stream);
 
+/* The layer restricted to output columns [h_begin, h_end): the per-rank step
+ * of an output-partitioned tensor-parallel MoE ("Inside the Kimi K3
+ * optimization effort", section "MoE: remove duplicate work across GPUs":
+ * each rank adds only its owned output coordinates, the existing all-reduce
+ * assembles the layer output, and each rank needs only its rows of the down
+ * projection).  Routing, activation quantisation and the gate/up GEMM run in
+ * full; the down GEMM reads rows [h_begin, h_end) of w2 (and sh2) only and
+ * writes those columns of out; every other column of out is zero, so the
+ * ranks' outputs sum exactly to the layer output.  Arguments as for
+ * fp4moe_forward (MXFP4 / NVFP4); 0 <= h_begin < h_end <= H, both multiples
+ * of 128, else FP4MOE_ERR_UNSUPPORTED_SHAPE. */
+fp4moe_status fp4moe_forward_cols(const fp4moe_dims *dims, const fp4moe_weights *w, const uint16_t *x,
+                                  uint16_t *out, int32_t h_begin, int32_t h_end, const fp4moe_debug *dbg,
+                                  void *ws, size_t ws_bytes, void *stream);
+
 /* The W8A8 MoE layer on the exactly converted FP8 experts ("Kimi-K2.7-Code on
  * Gaudi 2", section "Exact MXFP4 to FP8 per-channel conversion": per-channel
  * FP8 weights, dynamic per-token FP8 activations).  Routing and permutation

@@ -287,6 +287,64 @@ def test_max_tokens_sampled():
     print(full_check(cfg, tokens=[0, 1, 31, 32, 4095, 32767, 32768, 65534, 65535]))
 
 
+def _column_slices(cfg, layer, x, world):
+    """fp4moe_forward_cols for every rank's block of output columns, run one
+    after another on this GPU (no rank waits for another); each block's
+    output is zero outside its columns.  Returns their sum (exact: the
+    blocks are disjoint)."""
+    torch = torch_cuda()
+    from block_scaled_fp4_sigmoid_gb300.layer import column_block
+    total = np.zeros((cfg.T, cfg.H))
+    for r in range(world):
+        h0, h1 = column_block(cfg.H, r, world)
+        out = layer.forward_cols(x, h0, h1)
+        torch.cuda.synchronize()
+        assert fm.get_status(layer.ws.data_ptr()) == (0, 0)
+        o = synth.bf16_bits_to_f64(out.view(torch.int16).cpu().numpy().view(np.uint16))
+        assert not np.any(o[:, :h0]) and not np.any(o[:, h1:]), (r, h0, h1)
+        total += o
+    return total
+
+
+@pytest.mark.parametrize("name,world", [("ragged_shared", 2), ("ragged_shared", 4), ("front_cluster3", 3),
+                                        ("nv_grouped", 2), ("wide_padK", 8)])
+def test_output_column_blocks_sum_to_the_layer(name, world):
+    """Output-partitioned layer: the ranks' column blocks, summed, meet the
+    layer tolerance against the whole oracle (the few-token front end, the
+    many-token path, a shared expert, NVFP4, K padding)."""
+    from types import SimpleNamespace
+    torch_cuda()
+    ensure_built()
+    from block_scaled_fp4_sigmoid_gb300.layer import MoELayer
+    cfg = SMALL[name]
+    layer = MoELayer.synthetic(cfg)
+    total = _column_slices(cfg, layer, layer.synthetic_x(), world)
+    x, wr, b = OI.layer_inputs(cfg)
+    tokens = np.arange(cfg.T)
+    orc = M.layer_forward(cfg, x, wr, b, OI.oracle_weights(cfg), tokens=tokens)
+    amb = _ambiguous_tokens(cfg, orc["logits"], orc["lsum"], orc["margins"], tokens)
+    print(name, world, check_output(SimpleNamespace(out=total), orc["ref"], orc["S"], orc["A"], tokens, amb))
+
+
+def test_kimi_decode_output_column_blocks_full_size():
+    """The Kimi decode layer as two ranks' column blocks (3584 columns
+    each), sampled tokens against the oracle."""
+    from types import SimpleNamespace
+    torch_cuda()
+    ensure_built()
+    from block_scaled_fp4_sigmoid_gb300.layer import MoELayer
+    cfg = synth.configs()["kimi_decode"]
+    layer = MoELayer.synthetic(cfg)
+    total = _column_slices(cfg, layer, layer.synthetic_x(), 2)
+    del layer
+    tokens = np.array([0, 5])
+    xr = np.concatenate([synth.bf16_bits_to_f64(synth.gen_x_bf16(cfg, int(t), int(t) + 1)) for t in tokens])
+    wr = synth.bf16_bits_to_f64(synth.gen_router_bf16(cfg))
+    orc = M.token_forward(cfg, xr, wr, synth.gen_bias_f32(cfg), OI.oracle_weights(cfg))
+    amb = _ambiguous_tokens(cfg, orc["logits"], orc["lsum"], orc["margins"], tokens)
+    print(check_output(SimpleNamespace(out=total), orc["ref"], orc["S"], orc["A"], tokens, amb))
+
+
 def test_route_entry_point_matches_forward_routing():
     torch = torch_cuda()
     ensure_built()
