@@ -404,13 +404,15 @@ static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights*
     f.xq = xq;
     f.xsf = xsf;
     f.tok_mask = reinterpret_cast<uint32_t*>(cc);  // the per-chunk counters are not used here
-    if (d.n_shared) {  // the shared expert's weights (payloads and scales of w13, w2)
-      const uint8_t* r[4] = {w->sh13, w->sh13_scale, w->sh2, w->sh2_scale};
+    if (d.n_shared) {  // the shared expert's weights: w13 whole, the rows of w2 this call's columns need
+      const int64_t w2_row = w->packed ? (int64_t)fp4moe_packed_weights_bytes(1, d.H, d.I / 2) / d.H : d.I / 2;
+      const int64_t w2_sf_tile = (int64_t)fp4moe_packed_scales_bytes(1, 128, d.I / 32, d.fmt);
+      const uint8_t* r[4] = {w->sh13, w->sh13_scale, w->sh2 + h_begin * w2_row,
+                             w->sh2_scale + (h_begin / 128) * w2_sf_tile};
       const int64_t n[4] = {
           w->packed ? (int64_t)fp4moe_packed_weights_bytes(1, 2 * d.I, d.H / 2) : (int64_t)d.I * d.H,
-          (int64_t)fp4moe_packed_scales_bytes(1, 2 * d.I, d.H / 32, d.fmt),
-          w->packed ? (int64_t)fp4moe_packed_weights_bytes(1, d.H, d.I / 2) : (int64_t)d.H * (d.I / 2),
-          (int64_t)fp4moe_packed_scales_bytes(1, d.H, d.I / 32, d.fmt)};
+          (int64_t)fp4moe_packed_scales_bytes(1, 2 * d.I, d.H / 32, d.fmt), (h_end - h_begin) * w2_row,
+          (int64_t)dn_mtiles * w2_sf_tile};
       for (int i = 0; i < 4; ++i) {
         f.l2_pf[i] = r[i];
         f.l2_pf_bytes[i] = n[i];
