@@ -52,7 +52,7 @@ SMALL = {
 }
 
 
-class GpuRun:
+class DeviceRun:
     """One forward on the GPU plus host copies of its intermediates."""
 
     def __init__(self, cfg, h_debug=True, packed=True):
@@ -216,7 +216,7 @@ def check_output(run, ref, S, A, tokens, skip):
 
 
 def full_check(cfg, tokens=None, h_debug=True, packed=True):
-    run = GpuRun(cfg, h_debug=h_debug, packed=packed)
+    run = DeviceRun(cfg, h_debug=h_debug, packed=packed)
     assert run.status == (0, 0), run.status
     x, wr, b = OI.layer_inputs(cfg)
     assert np.array_equal(run.x_bits, synth.gen_x_bf16(cfg))
@@ -373,7 +373,7 @@ def test_route_entry_point_matches_forward_routing():
 # ------------------------------------------------------------------ full-size workloads
 def _token_check(name, tokens):
     cfg = synth.configs()[name]
-    run = GpuRun(cfg, h_debug=True)
+    run = DeviceRun(cfg, h_debug=True)
     assert run.status == (0, 0), run.status
     tokens = np.asarray(tokens)
     xr = np.concatenate([synth.bf16_bits_to_f64(synth.gen_x_bf16(cfg, int(t), int(t) + 1)) for t in tokens])
