@@ -230,6 +230,31 @@ def oracle_route_sample(cfg_name: str, n_routes: int, frac: float = 1.0, start_t
     return t_total, n_routes / rpt * (Ip / cfg.I)
 
 
+def algorithmic_bytes(H: int, I: int, fmt: str, mode: str, touched: int, routes: int) -> tuple[float, float]:
+    """Bytes the gate/up and the down GEMM of one layer call must move at
+    least: the touched experts' weights (with their scales), the activation
+    rows each reads and what each writes, for R routes.
+      a4w4:    FP4 values at 0.5 B plus one scale byte per block (MXFP4 32,
+               NVFP4 16); gate/up reads x, writes the quantised h; down
+               reads it and adds fp32 rows into the combine buffer.
+      w8a8:    E4M3 bytes plus fp32 scales per weight row and per activation
+               row; gate/up writes fp32 h, down reads its E4M3 form.
+      emulate: BF16 weights and activation rows; gate/up writes fp32 h."""
+    if mode == "emulate":
+        gu = touched * (2 * I * H * 2) + routes * H * 2 + routes * I * 4
+        dn = touched * (H * I * 2) + routes * I * 2 + routes * H * 4
+    elif mode == "w8a8":
+        gu = touched * (2 * I * H + 2 * I * 4) + routes * (H + 4) + routes * I * 4
+        dn = touched * (H * I + H * 4) + routes * (I + 4) + routes * H * 4
+    elif mode == "a4w4":
+        act = 0.5 + 1.0 / (16 if fmt == "nvfp4" else 32)  # bytes per FP4 value incl. scale
+        gu = touched * (2 * I * H * act) + routes * H * act + routes * I * act
+        dn = touched * (H * I * act) + routes * I * act + routes * H * 4
+    else:
+        raise ValueError(mode)
+    return gu, dn
+
+
 def rank_token_range(rank: int, T: int) -> tuple[int, int]:
     """Weak scaling: every rank runs its own batch of T tokens, tokens
     rank*T .. (rank+1)*T of the seeded stream."""
@@ -577,17 +602,8 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     routes = int(count.sum())
     wpe = layer.weight_bytes_per_expert()
     d = layer.dims
-    if args.emulate:  # BF16 weights and activation rows; gate/up writes fp32 h
-        gu_bytes = touched * (2 * d.I * d.H * 2) + routes * d.H * 2 + routes * d.I * 4
-        dn_bytes = touched * (d.H * d.I * 2) + routes * d.I * 2 + routes * d.H * 4
-    elif args.w8a8:  # E4M3 bytes, fp32 row scales; gate/up writes fp32 h, down reads E4M3 h
-        gu_bytes = touched * (2 * d.I * d.H + 2 * d.I * 4) + routes * (d.H + 4) + routes * d.I * 4
-        dn_bytes = touched * (d.H * d.I + d.H * 4) + routes * (d.I + 4) + routes * d.H * 4
-    else:
-        blk = 16 if cfg.fmt == "nvfp4" else 32
-        act = 0.5 + 1.0 / blk                              # bytes per FP4 value incl. scale
-        gu_bytes = touched * (2 * d.I * d.H * act) + routes * d.H * act + routes * d.I * act
-        dn_bytes = touched * (d.H * d.I * act) + routes * d.I * act + routes * d.H * 4
+    mode = "emulate" if args.emulate else "w8a8" if args.w8a8 else "a4w4"
+    gu_bytes, dn_bytes = algorithmic_bytes(d.H, d.I, cfg.fmt, mode, touched, routes)
     flops = 2.0 * 3 * d.I * d.H * routes
 
     # max over ranks
