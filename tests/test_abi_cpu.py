@@ -99,3 +99,21 @@ def test_synth_device_library_builds():
     lib = ctypes.CDLL(str(so))
     for n in ("synth_words", "synth_e8m0", "synth_normal_bf16"):
         assert hasattr(lib, n)
+
+
+def test_tiled_payload_formula_in_the_header_matches_the_layout():
+    """The byte-offset formula fp4moe.h prints for fp4moe_pack_weights equals
+    the layout's definition (blocks of 128 rows x 128 bytes, K tiles
+    innermost, K zero-padded), written as a numpy reshape."""
+    import numpy as np
+    rng = np.random.default_rng(7)
+    for n_mat, rows, kbytes in ((2, 256, 192), (1, 384, 3584), (3, 128, 16)):
+        kt = -(-kbytes // 128)
+        src = rng.integers(0, 256, (n_mat, rows, kbytes), dtype=np.uint8)
+        pad = np.zeros((n_mat, rows, kt * 128), dtype=np.uint8)
+        pad[..., :kbytes] = src
+        tiled = pad.reshape(n_mat, rows // 128, 128, kt, 128).transpose(0, 1, 3, 2, 4).reshape(-1)
+        m, r, c = np.meshgrid(np.arange(n_mat), np.arange(rows), np.arange(kbytes), indexing="ij")
+        off = m * rows * kt * 128 + ((r // 128) * kt + c // 128) * 16384 + (r % 128) * 128 + c % 128
+        assert np.array_equal(tiled[off], src)
+        assert tiled.size == fm.packed_weights_bytes(n_mat, rows, kbytes)
