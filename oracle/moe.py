@@ -96,8 +96,16 @@ def _h_candidates_mx(h: np.ndarray, dh: np.ndarray, hq: np.ndarray, hs: np.ndarr
 
 
 def _h_candidates_nv(h: np.ndarray, dh: np.ndarray, hq: np.ndarray, hs: np.ndarray, g_h):
-    """NVFP4 counterpart of _h_candidates_mx: corners of the tensor scale, the
-    block scale and the element interval."""
+    """NVFP4 counterpart of _h_candidates_mx.  Any h' of the box moves the
+    tensor scale within [g_lo, g_hi] (from the box's smallest and largest
+    tensor maximum) and each block scale within [s_min, s_max] (from the
+    block's smallest and largest maximum at both ends of g).  For a block
+    scale s, the fp32 quotient v / fp32(s g) is monotone in v and in g, so
+    over the element's interval and [g_lo, g_hi] it spans the range between
+    its values at the four corners, and the code takes every E2M1 grid value
+    between theirs.  A dequantised value E2M1 * s * g is bilinear in the grid
+    value and g, so its largest distance from the reference over that range
+    is reached at a corner of (grid value, g)."""
     n, I = h.shape
     B = Q.NV_BLOCK
     hb = h.reshape(n, I // B, B)
@@ -107,6 +115,7 @@ def _h_candidates_nv(h: np.ndarray, dh: np.ndarray, hq: np.ndarray, hs: np.ndarr
     amax_hi_t = float(np.max(np.abs(h) + dh)) if h.size else 0.0
     amax_lo_t = float(np.max(np.maximum(np.abs(h) - dh, 0.0))) if h.size else 0.0
     g_cands = sorted({float(Q.nv_global_scale(amax_lo_t)), float(Q.nv_global_scale(amax_hi_t)), float(g_h)})
+    g_ends = (np.float32(g_cands[0]), np.float32(g_cands[-1]))
     amax_b_hi = np.max(np.maximum(np.abs(lo), np.abs(hi)), axis=-1)
     amin = np.where((lo <= 0) & (hi >= 0), 0.0, np.minimum(np.abs(lo), np.abs(hi)))
     amax_b_lo = np.max(amin, axis=-1)
@@ -114,26 +123,29 @@ def _h_candidates_nv(h: np.ndarray, dh: np.ndarray, hq: np.ndarray, hs: np.ndarr
     dmax = np.zeros_like(hb)
     s_min = np.full(amax_b_lo.shape, 255, dtype=np.int64)
     s_max = np.full(amax_b_lo.shape, -1, dtype=np.int64)
-    for g in (g_cands[0], g_cands[-1]):
-        g32 = np.float32(g)
+    for g32 in g_ends:
         six_g = np.float32(6.0) * g32
         for ab in (amax_b_lo, amax_b_hi):
             q_s = (ab.astype(np.float32) / six_g).astype(np.float32) if six_g > 0 else np.zeros_like(ab, dtype=np.float32)
             sb = (e4m3_encode(q_s.astype(np.float64)) & 0x7F).astype(np.int64)
             s_min = np.minimum(s_min, sb)
             s_max = np.maximum(s_max, sb)
-    for g in (g_cands[0], g_cands[-1]):
-        g32 = np.float32(g)
-        for ds in range(0, int(np.max(s_max - s_min)) + 1 if s_max.size else 1):
-            sb = np.minimum(s_min + ds, 126)
-            ok = (s_min + ds) <= s_max
-            d_b = (E4M3_TABLE[sb].astype(np.float32) * g32).astype(np.float32)
+    for ds in range(0, int(np.max(s_max - s_min)) + 1 if s_max.size else 1):
+        sb = np.minimum(s_min + ds, 126)
+        ok = (s_min + ds) <= s_max
+        sv = E4M3_TABLE[sb][..., None]
+        quots = []
+        for g32 in g_ends:
+            d_b = (E4M3_TABLE[sb].astype(np.float32) * g32).astype(np.float32)[..., None]
             for v in (lo, hi):
                 with np.errstate(divide="ignore", invalid="ignore"):
-                    sc = np.where(d_b[..., None] > 0, v.astype(np.float32) / d_b[..., None], 0.0)
-                c = e2m1_encode(sc.astype(np.float32).astype(np.float64)).astype(np.int64)
-                alt = E2M1_TABLE[c] * E4M3_TABLE[sb][..., None] * float(g32)
-                d = np.where(ok[..., None], np.abs(alt - ref), 0.0)
+                    q = np.where(d_b > 0, v.astype(np.float32) / d_b, 0.0)
+                quots.append(q.astype(np.float32).astype(np.float64))
+        grid_lo = E2M1_TABLE[e2m1_encode(np.minimum.reduce(quots)).astype(np.int64)]
+        grid_hi = E2M1_TABLE[e2m1_encode(np.maximum.reduce(quots)).astype(np.int64)]
+        for gv in (grid_lo, grid_hi):
+            for g32 in g_ends:
+                d = np.where(ok[..., None], np.abs(gv * sv * float(g32) - ref), 0.0)
                 dmax = np.maximum(dmax, d)
     return dmax.reshape(n, I), (s_min, s_max)
 

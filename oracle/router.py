@@ -91,3 +91,51 @@ def decision_margins(logit: np.ndarray, bias: np.ndarray, top_k: int, n_group: i
         gs = np.sort(info["gscore"])[::-1]
         gm = gs[topk_group - 1] - gs[topk_group]
     return em, gm
+
+
+def select_fp32(s32: np.ndarray, bias32: np.ndarray, top_k: int, n_group: int, topk_group: int,
+                routed_scaling: float, renormalize: int):
+    """The selection step of one token taken in fp32, from fp32 sigmoid
+    scores: the integer decisions of route_token (group choice, top-k) made on
+    fp32 values, as a router that keeps its scores in fp32 makes them.  Each
+    step is one correctly rounded fp32 operation:
+
+        c           = fp32(s + bias)
+        group score = fp32(largest c + second largest c)   (per group)
+        keep the topk_group groups with the largest scores (ties: lower group)
+        idx         = the top_k kept experts by descending c (ties: lower index)
+        tot         = fp32 running sum of s[idx_0], s[idx_1], ... from 0
+        w_j         = fp32(fp32(s[idx_j] / tot) * routed_scaling)   (renormalize)
+                      fp32(s[idx_j] * routed_scaling)                (otherwise)
+
+    Returns (idx [top_k] int64, w [top_k] float32)."""
+    s = np.asarray(s32, dtype=np.float32)
+    b = np.asarray(bias32, dtype=np.float32)
+    E = s.shape[0]
+    c = (s + b).astype(np.float32)
+    allowed = np.ones(E, dtype=bool)
+    if n_group > 1:
+        gsz = E // n_group
+        assert gsz >= 2, "a group's score sums its two largest corrected scores"
+        top2 = np.sort(c.reshape(n_group, gsz), axis=1)[:, -2:]
+        gscore = (top2[:, 1] + top2[:, 0]).astype(np.float32)
+        allowed = np.zeros(E, dtype=bool)
+        for g in _top_order(gscore.astype(np.float64))[:topk_group]:
+            allowed[g * gsz:(g + 1) * gsz] = True
+    cand = np.where(allowed)[0]
+    idx = cand[_top_order(c[cand].astype(np.float64))][:top_k]
+    tot = np.float32(0.0)
+    for e in idx:
+        tot = np.float32(tot + s[e])
+    scal = np.float32(routed_scaling)
+    if renormalize:
+        w = np.array([np.float32(np.float32(s[e] / tot) * scal) for e in idx], dtype=np.float32)
+    else:
+        w = np.array([np.float32(s[e] * scal) for e in idx], dtype=np.float32)
+    return idx.astype(np.int64), w
+
+
+def sigmoid_f64(logit: np.ndarray) -> np.ndarray:
+    """1 / (1 + exp(-l)) in float64 (the score the fp32 router approximates)."""
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-np.asarray(logit, dtype=np.float64)))

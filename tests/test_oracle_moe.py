@@ -145,3 +145,138 @@ def test_token_forward_matches_layer_forward():
         assert np.array_equal(one["idx"][0], full["idx"][t])
         np.testing.assert_allclose(one["ref"][0], full["ref"][t], rtol=1e-13, atol=1e-16)
         np.testing.assert_allclose(one["S"][0], full["S"][t], rtol=1e-13, atol=1e-16)
+
+
+# ------------------------------------------------------------------ NVFP4 flip allowance
+def _nv_case(n_blocks=2):
+    """One row of n_blocks NVFP4 blocks: element 0 holds the tensor maximum
+    2688 * 2^-10, so g = 2^-10 exactly and block 0's scale is 448
+    (d = 448 g = 0.4375); element 1 sits on the E2M1 midpoint 2.5 d."""
+    h = np.zeros((1, 16 * n_blocks))
+    h[0, 0] = 2688 * 2.0 ** -10
+    h[0, 1] = 2.5 * 0.4375
+    return h
+
+
+def _nv_sampled_alternatives(h, dh, hq, hs, g_h, rng, n=400):
+    """Brute force: quantise fp32 points h' of the box |h' - h| <= dh (its
+    corners, random points, and the points that move only the tensor
+    maximum) with their own tensor scale; return the largest change of each
+    dequantised element and the range of block-scale bytes seen."""
+    ref = Q.nv_dequant(hq, hs, g_h)
+    worst = np.zeros_like(h)
+    s_lo = hs.astype(np.int64).copy()
+    s_hi = hs.astype(np.int64).copy()
+    for i in range(n):
+        mode = i % 3
+        d = rng.choice([-1.0, 1.0], h.shape) if mode == 0 else rng.uniform(-1, 1, h.shape)
+        if mode == 2:
+            d = np.zeros_like(h)
+            d.flat[int(np.argmax(np.abs(h)))] = rng.choice([-1.0, 1.0])
+        hp = (h + d * dh).astype(np.float32).astype(np.float64)
+        hp = np.where(np.abs(hp - h) <= dh, hp, h)
+        c, s, g = Q.nv_quantize(hp)
+        worst = np.maximum(worst, np.abs(Q.nv_dequant(c, s, g) - ref))
+        s_lo = np.minimum(s_lo, s.astype(np.int64))
+        s_hi = np.maximum(s_hi, s.astype(np.int64))
+    return worst, (s_lo, s_hi)
+
+
+def test_nv_allowance_planted_midpoint():
+    """An element on the E2M1 midpoint 2.5 d under a fixed block scale
+    (nothing else may move): the allowance is exactly one grid step d there
+    (2 d by ties-to-even, 3 d on the other side) and zero elsewhere; with no
+    interval it is zero everywhere."""
+    h = _nv_case()
+    hq, hs, g = Q.nv_quantize(h)
+    assert g == np.float32(2.0 ** -10) and F.E4M3_TABLE[hs[0, 0]] == 448.0
+    assert F.E2M1_TABLE[hq[0, 1]] == 2.0
+    none, (lo, hi) = M._h_candidates_nv(h, np.zeros_like(h), hq, hs, g)
+    assert not none.any() and np.array_equal(lo, hs) and np.array_equal(hi, hs)
+    dh = np.zeros_like(h)
+    dh[0, 1] = 2.0 ** -20
+    dmax, (lo, hi) = M._h_candidates_nv(h, dh, hq, hs, g)
+    assert dmax[0, 1] == 0.4375
+    assert np.count_nonzero(dmax) == 1
+    assert np.array_equal(lo, hs) and np.array_equal(hi, hs)
+    worst, (slo, shi) = _nv_sampled_alternatives(h, dh, hq, hs, g, np.random.default_rng(31))
+    assert np.array_equal(worst, dmax)
+
+
+def test_nv_allowance_planted_block_scale_boundary():
+    """Block 1's maximum makes amax_b / (6 g) = 8.5, the midpoint of the
+    E4M3 values 8 and 9, and may move by one fp32 step: its scale byte may
+    be either (8 by ties-to-even),
+    and its maximum element, 6 * 8 g under scale 8, becomes 6 * 9 g under 9."""
+    h = _nv_case()
+    g = 2.0 ** -10
+    h[0, 16] = 8.5 * 6 * g
+    hq, hs, gq = Q.nv_quantize(h)
+    assert gq == np.float32(g) and F.E4M3_TABLE[hs[0, 1]] == 8.0
+    dh = np.zeros_like(h)
+    dh[0, 16] = float(np.spacing(np.float32(h[0, 16])))  # one fp32 step: the box holds amax_b +- that step
+    dmax, (lo, hi) = M._h_candidates_nv(h, dh, hq, hs, gq)
+    assert F.E4M3_TABLE[lo[0, 1]] == 8.0 and F.E4M3_TABLE[hi[0, 1]] == 9.0
+    assert lo[0, 0] == hi[0, 0] == hs[0, 0]
+    assert dmax[0, 16] == 6 * g
+    assert np.count_nonzero(dmax) == 1
+    worst, (slo, shi) = _nv_sampled_alternatives(h, dh, hq, hs, gq, np.random.default_rng(32))
+    assert np.array_equal(worst, dmax)
+    assert np.array_equal(slo, lo) and np.array_equal(shi, hi)
+
+
+def test_nv_allowance_planted_tensor_scale_change():
+    """The tensor maximum may move by one fp32 step either way, which moves
+    g = amax / 2688 and with it every quotient of the tensor: the midpoint
+    element, with no interval of its own, may round to 3 * 448 g_lo (the
+    smaller g) instead of 2 * 448 g.  The allowance admits that flip; it
+    exceeds the exact largest change by at most the spread of the grid
+    value times 448 (g_hi - g_lo), its bilinear corner bound."""
+    h = _nv_case()
+    hq, hs, g = Q.nv_quantize(h)
+    dh = np.zeros_like(h)
+    dh[0, 0] = float(np.spacing(np.float32(h[0, 0])))
+    dmax, (lo, hi) = M._h_candidates_nv(h, dh, hq, hs, g)
+    g_lo = float(Q.nv_global_scale(np.float32(h[0, 0] - dh[0, 0])))
+    g_hi = float(Q.nv_global_scale(np.float32(h[0, 0] + dh[0, 0])))
+    assert g_lo < g < g_hi and np.array_equal(lo, hs) and np.array_equal(hi, hs)
+    exact = 3 * 448 * g_lo - 2 * 448 * float(g)  # dequantised values are E2M1 * E4M3 * g exactly
+    assert exact <= dmax[0, 1] <= exact + 3 * 448 * (g_hi - g_lo)
+    worst, _ = _nv_sampled_alternatives(h, dh, hq, hs, g, np.random.default_rng(33))
+    assert worst[0, 1] == exact
+    assert np.all(worst <= dmax) and np.all((dmax > 0) == (h != 0))
+
+
+def test_nv_allowance_bounds_random_boxes():
+    """Soundness on random rows with intervals wide enough to cross many
+    boundaries: no sampled quantisation of the box changes an element by
+    more than the allowance, and every sampled scale byte is in its range."""
+    rng = np.random.default_rng(34)
+    for trial in range(6):
+        h = (rng.standard_normal((3, 64)) * 2.0 ** rng.integers(-8, 4)).astype(np.float32).astype(np.float64)
+        dh = np.abs(h) * 2.0 ** -rng.integers(6, 14) + 2.0 ** -40
+        hq, hs, g = Q.nv_quantize(h)
+        dmax, (lo, hi) = M._h_candidates_nv(h, dh, hq, hs, g)
+        worst, (slo, shi) = _nv_sampled_alternatives(h, dh, hq, hs, g, rng, n=300)
+        assert np.all(worst <= dmax * (1 + 1e-12)), (trial, float(np.max(worst - dmax)))
+        assert np.all(slo >= lo) and np.all(shi <= hi)
+
+
+def test_mx_allowance_bounds_random_boxes():
+    """The MXFP4 allowance, the same way: no sampled fp32 point of a wide box
+    quantises to a value further from the reference than the allowance, and
+    every sampled scale byte lies in the allowed range."""
+    rng = np.random.default_rng(35)
+    for trial in range(6):
+        h = (rng.standard_normal((3, 64)) * 2.0 ** rng.integers(-8, 4)).astype(np.float32).astype(np.float64)
+        dh = np.abs(h) * 2.0 ** -rng.integers(4, 12) + 2.0 ** -40
+        hq, hs = Q.mx_quantize(h)
+        dmax, (lo, hi) = M._h_candidates_mx(h, dh, hq, hs)
+        ref = Q.mx_dequant(hq, hs)
+        for i in range(300):
+            d = rng.choice([-1.0, 1.0], h.shape) if i % 2 else rng.uniform(-1, 1, h.shape)
+            hp = (h + d * dh).astype(np.float32).astype(np.float64)
+            hp = np.where(np.abs(hp - h) <= dh, hp, h)
+            c, s = Q.mx_quantize(hp)
+            assert np.all(np.abs(Q.mx_dequant(c, s) - ref) <= dmax), (trial, i)
+            assert np.all(s >= lo) and np.all(s <= hi)
