@@ -25,6 +25,7 @@ FP8 = 2  # W8A8 layer (fp4moe_forward_w8a8)
 STATUS = {0: "FP4MOE_OK", 1: "FP4MOE_ERR_INVALID_ARG", 2: "FP4MOE_ERR_UNSUPPORTED_SHAPE",
           3: "FP4MOE_ERR_WORKSPACE", 4: "FP4MOE_ERR_CUDA", 5: "FP4MOE_ERR_TIMEOUT",
           6: "FP4MOE_ERR_NAN_SCALE", 7: "FP4MOE_ERR_INEXACT", 8: "FP4MOE_ERR_DEVICE"}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
 STAGES = ("router", "topk", "permute", "quant", "gateup", "down", "finalize", "end")
 
 
@@ -62,7 +63,11 @@ class WsLayout(ctypes.Structure):
 
 
 class Debug(ctypes.Structure):
-    _fields_ = [("events", ctypes.c_void_p * 8), ("h_pre", ctypes.c_void_p)]
+    """fp4moe_debug: stage events, h before quantisation, router logits and
+    scores, the pipeline wait limit and the timeout test knob."""
+    _fields_ = [("events", ctypes.c_void_p * 8), ("h_pre", ctypes.c_void_p), ("logits", ctypes.c_void_p),
+                ("scores", ctypes.c_void_p), ("wait_limit_ns", ctypes.c_int64),
+                ("withhold_first_stage", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _LIB = None
@@ -104,11 +109,17 @@ def lib() -> ctypes.CDLL:
         L.fp4moe_mxfp4_to_fp8_rowscale.argtypes = [vp, vp, i64, i32, vp, vp, vp, vp, sz, vp]
         L.fp4moe_clear_status.argtypes = [vp, vp]
         L.fp4moe_get_status.argtypes = [vp, vp, P(i32), P(i64)]
+        L.fp4moe_route_noalloc.argtypes = [P(Dims), vp, vp, vp, vp, vp, vp, vp]
+        L.fp4moe_check_scales.argtypes = [vp, i64, i32, vp, sz, vp]
+        L.fp4moe_route_noalloc_scratch_bytes.argtypes = [P(Dims)]
+        L.fp4moe_route_noalloc_scratch_bytes.restype = sz
+        L.fp4moe_route_noalloc_status.argtypes = [vp, P(i32), P(i64)]
         for name in ("fp4moe_workspace_layout", "fp4moe_pack_scales", "fp4moe_pack_weights", "fp4moe_route", "fp4moe_quantize_act",
                      "fp4moe_forward", "fp4moe_forward_cols", "fp4moe_forward_w8a8", "fp4moe_forward_nvfp4_emulated", "fp4moe_linear",
                      "fp4moe_mxfp4_to_fp8_rowscale",
                      "fp4moe_clear_status",
-                     "fp4moe_get_status"):
+                     "fp4moe_get_status", "fp4moe_route_noalloc", "fp4moe_route_noalloc_status",
+                     "fp4moe_check_scales"):
             getattr(L, name).restype = i32
         _LIB = L
     return _LIB
@@ -228,6 +239,11 @@ def mxfp4_to_fp8_rowscale(codes: int, scales: int, rows: int, K: int, fp8_out: i
                                            stream), "fp4moe_mxfp4_to_fp8_rowscale")
 
 
+def check_scales(scales: int, n: int, fmt: int, ws: int, ws_bytes: int, stream: int = 0) -> None:
+    """Records the NaN scale bytes among n bytes in the status word of ws (fp4moe_check_scales)."""
+    _ok(lib().fp4moe_check_scales(scales, n, fmt, ws, ws_bytes, stream), "fp4moe_check_scales")
+
+
 def clear_status(ws: int, stream: int = 0) -> None:
     _ok(lib().fp4moe_clear_status(ws, stream), "fp4moe_clear_status")
 
@@ -241,8 +257,17 @@ def get_status(ws: int, stream: int = 0) -> tuple[int, int]:
 def route_noalloc(dims: Dims, x: int, w_router: int, bias: int, topk_idx: int, topk_w: int,
                   logits_out: int | None, stream: int = 0) -> None:
     """fp4moe_route without a workspace: the library's fixed scratch array is used."""
-    L = lib()
-    f = L.fp4moe_route_noalloc
-    f.argtypes = [ctypes.POINTER(Dims)] + [ctypes.c_void_p] * 7
-    f.restype = ctypes.c_int32
-    _ok(f(ctypes.byref(dims), x, w_router, bias, topk_idx, topk_w, logits_out, stream), "fp4moe_route_noalloc")
+    _ok(lib().fp4moe_route_noalloc(ctypes.byref(dims), x, w_router, bias, topk_idx, topk_w, logits_out, stream),
+        "fp4moe_route_noalloc")
+
+
+def route_noalloc_scratch_bytes(dims: Dims) -> int:
+    """Bytes of the fixed scratch array a route_noalloc call with these dims uses (0: does not fit)."""
+    return lib().fp4moe_route_noalloc_scratch_bytes(ctypes.byref(dims))
+
+
+def route_noalloc_status(stream: int = 0) -> tuple[int, int]:
+    """Status word of the last route_noalloc call on the current device."""
+    st, n = ctypes.c_int32(0), ctypes.c_int64(0)
+    _ok(lib().fp4moe_route_noalloc_status(stream, ctypes.byref(st), ctypes.byref(n)), "fp4moe_route_noalloc_status")
+    return st.value, n.value

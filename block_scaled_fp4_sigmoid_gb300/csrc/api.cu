@@ -15,19 +15,7 @@ namespace {
 constexpr int64_t kAlign = 256;
 inline int64_t align_up(int64_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
-fp4moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FP4MOE_OK : FP4MOE_ERR_CUDA; }
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// The GEMMs use sm_103a instructions: refuse any other device up front.
-fp4moe_status check_device() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FP4MOE_ERR_DEVICE;
-  int major = 0, minor = 0;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return FP4MOE_ERR_DEVICE;
-  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return FP4MOE_ERR_DEVICE;
-  return (major == 10 && minor == 3) ? FP4MOE_OK : FP4MOE_ERR_DEVICE;
-}
 
 bool dims_ok(const fp4moe_dims& d) {
   if (d.T < 1 || d.T > 65536) return false;
@@ -84,6 +72,17 @@ int pick_splits(const fp4moe_dims& d) {
 }
 
 }  // namespace
+
+fp4moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FP4MOE_OK : FP4MOE_ERR_CUDA; }
+
+fp4moe_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FP4MOE_ERR_DEVICE;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return FP4MOE_ERR_DEVICE;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return FP4MOE_ERR_DEVICE;
+  return (major == 10 && minor == 3) ? FP4MOE_OK : FP4MOE_ERR_DEVICE;
+}
 
 bool make_layout(const fp4moe_dims& d, Layout* L) {
   if (!dims_ok(d)) return false;
@@ -287,7 +286,8 @@ fp4moe_status fp4moe_route(const fp4moe_dims* dims, const uint16_t* x, const uin
   if (e == cudaSuccess)
     e = launch_router_logits(x, w_router, partial, d.T, d.H, d.E, L.ws.n_splits,
                              reinterpret_cast<int32_t*>(base + L.ws.status), s);
-  if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, bias, topk_idx, topk_w, logits_out, cc, L.n_exp, s);
+  if (e == cudaSuccess)
+    e = launch_topk(d, partial, L.ws.n_splits, bias, topk_idx, topk_w, logits_out, nullptr, cc, L.n_exp, s);
   return cuda_status(e);
 }
 
@@ -404,6 +404,8 @@ static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights*
     f.xq = xq;
     f.xsf = xsf;
     f.tok_mask = reinterpret_cast<uint32_t*>(cc);  // the per-chunk counters are not used here
+    f.logits_dbg = dbg ? dbg->logits : nullptr;
+    f.scores_dbg = dbg ? dbg->scores : nullptr;
     if (d.n_shared) {  // the shared expert's weights: w13 whole, the rows of w2 this call's columns need
       const int64_t w2_row = w->packed ? (int64_t)fp4moe_packed_weights_bytes(1, d.H, d.I / 2) / d.H : d.I / 2;
       const int64_t w2_sf_tile = (int64_t)fp4moe_packed_scales_bytes(1, 128, d.I / 32, d.fmt);
@@ -424,7 +426,8 @@ static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights*
     if (e == cudaSuccess && nv) e = cudaMemsetAsync(amax, 0, (size_t)(2 + L.n_exp) * 4, s);
     if (e == cudaSuccess) e = launch_router_logits(x, w->w_router, partial, d.T, d.H, d.E, L.ws.n_splits, status, s);
     if (e == cudaSuccess) e = rec(1);
-    if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, nullptr, cc, L.n_exp, s);
+    if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, dbg ? dbg->logits : nullptr,
+                                            dbg ? dbg->scores : nullptr, cc, L.n_exp, s);
     if (e == cudaSuccess) e = rec(2);
     if (e == cudaSuccess)
       e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, dn_mtiles, ecount, eslot, gu_start, dn_start, plan,
@@ -450,6 +453,7 @@ static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights*
   a.row_tok = row_tok;
   a.row_w = row_w;
   a.status = status;
+  a.wait_ns = (dbg && dbg->wait_limit_ns > 0) ? (uint64_t)dbg->wait_limit_ns : 0;
   if (e == cudaSuccess) {
     GemmArgs g = a;
     g.w = w->w13;
@@ -471,6 +475,7 @@ static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights*
     g.plan_from_prev = L.front;  // the front end, launched just before, wrote the plan
     g.out_acc = acc;
     g.zero_acc = !L.front;  // the front end zeroes it itself
+    g.withhold = dbg && dbg->withhold_first_stage;
     e = launch_gateup(g, s);
   }
   if (e == cudaSuccess && nv) e = launch_h_quant_nv_routes(d, h32, route_row, row_e, amax + 2, gscale + 2, hq, hsf, s);
@@ -564,7 +569,8 @@ fp4moe_status fp4moe_forward_w8a8(const fp4moe_dims* dims, const fp4moe_fp8_weig
   if (e == cudaSuccess) e = cudaMemsetAsync(amax_row, 0, (size_t)L.ws.rows_cap * 4, s);
   if (e == cudaSuccess) e = launch_router_logits(x, w->w_router, partial, d.T, d.H, d.E, L.ws.n_splits, status, s);
   if (e == cudaSuccess) e = rec(1);
-  if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, nullptr, cc, L.n_exp, s);
+  if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, dbg ? dbg->logits : nullptr,
+                                            dbg ? dbg->scores : nullptr, cc, L.n_exp, s);
   if (e == cudaSuccess) e = rec(2);
   if (e == cudaSuccess)
     e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, d.H / 128, ecount, eslot, gu_start, dn_start, plan,
@@ -588,6 +594,7 @@ fp4moe_status fp4moe_forward_w8a8(const fp4moe_dims* dims, const fp4moe_fp8_weig
   a.row_tok = row_tok;
   a.row_w = row_w;
   a.status = status;
+  a.wait_ns = (dbg && dbg->wait_limit_ns > 0) ? (uint64_t)dbg->wait_limit_ns : 0;
   if (e == cudaSuccess) {
     GemmArgs g = a;
     g.w = w->w13;
@@ -689,7 +696,8 @@ fp4moe_status fp4moe_forward_nvfp4_emulated(const fp4moe_dims* dims, const fp4mo
   if (e == cudaSuccess) e = cudaMemsetAsync(amax, 0, (size_t)(2 + L.n_exp) * 4, s);
   if (e == cudaSuccess) e = launch_router_logits(x, w->w_router, partial, d.T, d.H, d.E, L.ws.n_splits, status, s);
   if (e == cudaSuccess) e = rec(1);
-  if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, nullptr, cc, L.n_exp, s);
+  if (e == cudaSuccess) e = launch_topk(d, partial, L.ws.n_splits, w->bias, idx, tw, dbg ? dbg->logits : nullptr,
+                                            dbg ? dbg->scores : nullptr, cc, L.n_exp, s);
   if (e == cudaSuccess) e = rec(2);
   if (e == cudaSuccess)
     e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, d.H / 128, ecount, eslot, gu_start, dn_start, plan,
@@ -722,6 +730,7 @@ fp4moe_status fp4moe_forward_nvfp4_emulated(const fp4moe_dims* dims, const fp4mo
   a.row_tok = row_tok;
   a.row_w = row_w;
   a.status = status;
+  a.wait_ns = (dbg && dbg->wait_limit_ns > 0) ? (uint64_t)dbg->wait_limit_ns : 0;
   if (e == cudaSuccess) {
     GemmArgs g = a;
     g.w = reinterpret_cast<const uint8_t*>(w13b);
@@ -839,6 +848,17 @@ fp4moe_status fp4moe_mxfp4_to_fp8_rowscale(const uint8_t* codes, const uint8_t* 
   if (fp4moe_status st = check_device()) return st;
   return cuda_status(launch_convert(codes, scales_e8m0, rows, K, fp8_out, row_scale, row_status,
                                     static_cast<int32_t*>(ws), static_cast<cudaStream_t>(stream)));
+}
+
+fp4moe_status fp4moe_check_scales(const uint8_t* scales, int64_t n, int32_t fmt, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  if (!scales || !ws || n < 0) return FP4MOE_ERR_INVALID_ARG;
+  if (fmt != FP4MOE_MXFP4 && fmt != FP4MOE_NVFP4) return FP4MOE_ERR_INVALID_ARG;
+  if (ws_bytes < 256) return FP4MOE_ERR_WORKSPACE;
+  if (!aligned16(scales)) return FP4MOE_ERR_INVALID_ARG;
+  if (fp4moe_status st = check_device()) return st;
+  return cuda_status(launch_nan_scales(scales, n, fmt == FP4MOE_NVFP4, static_cast<int32_t*>(ws),
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 fp4moe_status fp4moe_clear_status(void* ws, void* stream) {

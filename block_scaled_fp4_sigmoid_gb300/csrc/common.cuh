@@ -92,6 +92,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// As mbar_wait with a limit of its own (limit_ns), and giving up as soon as
+// *abort is set (another role of the CTA has stopped, so the phase may
+// never complete).  Returns false on either; only waits whose arrivals
+// depend on other roles use it.  Drains of copies already issued keep
+// mbar_wait: those copies always land.
+__device__ __forceinline__ bool mbar_wait_abortable(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                    const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0 && (*abort || globaltimer() - t0 > limit_ns)) return false;
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar, int32_t c0,
                                             int32_t c1) {

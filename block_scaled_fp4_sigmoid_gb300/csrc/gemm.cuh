@@ -31,9 +31,10 @@
 //              h plus a per-expert amax;
 //              down: routing weight times y, added into the fp32 combine
 //              buffer (red.global.add).
-// Every wait is bounded; a timeout sets a CTA-wide abort flag, records
-// FP4MOE_ERR_TIMEOUT in the status word, drains in-flight copies and MMAs,
-// frees tensor memory and returns.
+// Every wait is bounded (pipeline waits by KParams::wait_ns, and they give
+// up once another role of the CTA has aborted); a timeout sets a CTA-wide
+// abort flag, records FP4MOE_ERR_TIMEOUT in the status word, drains
+// in-flight copies and MMAs, frees tensor memory and returns.
 #pragma once
 
 #include <cuda.h>
@@ -65,6 +66,8 @@ struct KParams {
   int E, n_exp, H, I, K, rows_per_expert, m_tiles, katoms_a, katoms_b, katoms_h, has_shared, T;
   int plan_early;  // the plan was written at least two kernels back (see the kernel)
   int w_tiled;     // weights in the tiled layout (tmA / tmA_sh are views of 128-byte rows)
+  uint64_t wait_ns;  // limit of the pipeline waits (drains keep kWaitLimitNs)
+  int withhold;      // gate/up test knob: CTA 0 never fills its first pipeline stage
   // W8A8 (E4M3 operands): per-row fp32 scales of the weights (routed [E,
   // rows], shared [rows]) and of the B rows (per permuted row); amax_h then
   // holds the gate/up intermediate's |max| per permuted row
@@ -271,6 +274,9 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
     if constexpr (SF) bulk_load(base + C::kOffSFB, st.sfb + kt * C::kSFBytes, C::kSFBytes, fb);
   };
 
+  // Test knob (gate/up): CTA 0 never fills pipeline step 0, so its MMA
+  // issuer's wait for it runs out (KParams::withhold).
+  const int withheld = (GATEUP && p.withhold && blockIdx.x == 0) ? 0 : -1;
   // The first pipeline stages start streaming weights before the wait, so
   // they overlap the tail of the previous kernel.
   int pre = 0;
@@ -278,6 +284,7 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
     for (int u = blockIdx.x; u < total && pre < C::kStages; u += gridDim.x) {
       const Step st = unit_step(u);
       for (int kt = 0; kt < KT && pre < C::kStages; ++kt, ++pre) {
+        if (pre == withheld) continue;
         const uint32_t fb = smem_u32(&bar_full[pre]);
         mbar_arrive_expect_tx(fb, C::kStage);  // stage is empty: first use
         load_weights(st, kt, sbase + pre * C::kStage, fb);
@@ -306,8 +313,15 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
         for (int kt = 0; kt < KT; ++kt, ++step) {
           const uint32_t fb = smem_u32(&bar_full[stage]);
           const uint32_t base = sbase + stage * C::kStage;
+          if (step == withheld) {  // never armed, never filled
+            if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+            continue;
+          }
           if (step >= pre) {
-            if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u)) { ok = false; break; }
+            if (!mbar_wait_abortable(smem_u32(&bar_empty[stage]), phase ^ 1u, p.wait_ns, abort_v)) {
+              ok = false;
+              break;
+            }
             mbar_arrive_expect_tx(fb, C::kStage);
             if constexpr (kSplitProducer) {  // the stage is free and armed (release to the second producer)
               __threadfence_block();
@@ -321,8 +335,8 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) {
+          if (!*abort_v) record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
           *abort_v = 1;
-          record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
           break;
         }
       }
@@ -344,7 +358,7 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
         for (int u = blockIdx.x; u < total && s2 < pre; u += gridDim.x) {
           const Step st = unit_step(u);
           for (int kt = 0; kt < KT && s2 < pre; ++kt, ++s2)
-            if (s2 >= step) {
+            if (s2 >= step && s2 != withheld) {
               load_acts(st, kt, sbase + s2 * C::kStage, smem_u32(&bar_full[s2]));
               armed |= 1u << s2;
               armed_par &= ~(1u << s2);  // first use: phase 0
@@ -368,7 +382,7 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
         auto wait_armed = [&](int j) {
           const uint64_t t0 = globaltimer();
           while (*armed_v <= j) {
-            if (*abort_v || globaltimer() - t0 > kWaitLimitNs) return false;
+            if (*abort_v || globaltimer() - t0 > p.wait_ns) return false;
             __nanosleep(32);
           }
           return true;
@@ -429,7 +443,9 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
     const uint64_t a_desc0 = desc_sw128(sbase + off_a), b_desc0 = desc_sw128(sbase + C::kOffB);
     const uint64_t sfa_desc0 = desc_sf(sbase + off_sfa), sfb_desc0 = desc_sf(sbase + C::kOffSFB);
     // bounded wait with a warp-uniform outcome
-    auto wait_w = [](uint32_t bar, uint32_t par) { return __all_sync(0xffffffffu, mbar_wait(bar, par)); };
+    auto wait_w = [&](uint32_t bar, uint32_t par) {
+      return __all_sync(0xffffffffu, mbar_wait_abortable(bar, par, p.wait_ns, abort_v));
+    };
     int stage = 0;
     uint32_t phase = 0, acc_phase = 0;
     int as = 0;  // accumulator set of this unit
@@ -470,8 +486,9 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
         if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
       }
       if (!ok) {
+        if (lane == 0 && !*abort_v) record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
+        __syncwarp();
         *abort_v = 1;
-        if (lane == 0) record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
         break;
       }
       tc_commit_elect(smem_u32(&bar_tfull[as]));
@@ -487,12 +504,14 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
     float(*tile)[33] = epi_tile[warp - 2];
     uint32_t acc_phase = 0;
     int as = 0;
-    for (int u = blockIdx.x; u < total && !*abort_v; u += gridDim.x) {
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      if (__any_sync(0xffffffffu, *abort_v)) break;  // warp-uniform: the loop body holds .sync.aligned loads
       int e, mt, slot, cnt;
       decode_unit<N>(s_start, s_count, s_slot, p.n_exp, u, e, mt, slot, cnt);
-      if (!mbar_wait(smem_u32(&bar_tfull[as]), acc_phase)) {
+      if (!__all_sync(0xffffffffu, mbar_wait_abortable(smem_u32(&bar_tfull[as]), acc_phase, p.wait_ns, abort_v))) {
+        if (lane == 0 && !*abort_v) record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
+        __syncwarp();
         *abort_v = 1;
-        if (lane == 0) record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
         break;
       }
       tc_fence_after();

@@ -87,6 +87,8 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   p.katoms_h = (int)katoms_padded(d.I, a.nv);
   p.has_shared = a.sh != nullptr;
   p.w_tiled = a.w_tiled ? 1 : 0;
+  p.wait_ns = a.wait_ns ? a.wait_ns : kWaitLimitNs;
+  p.withhold = (GATEUP && a.withhold) ? 1 : 0;
   p.wrs = a.wrs ? a.wrs + r0 : nullptr;
   p.shrs = a.shrs ? a.shrs + r0 : nullptr;
   p.brs = a.brs;

@@ -38,6 +38,12 @@ struct Layout {
 
 bool make_layout(const fp4moe_dims& d, Layout* L);
 
+// FP4MOE_OK for cudaSuccess, else FP4MOE_ERR_CUDA.
+fp4moe_status cuda_status(cudaError_t e);
+// FP4MOE_OK when the current device is sm_103 (the kernels use sm_103a
+// instructions), else FP4MOE_ERR_DEVICE; every attribute query checked.
+fp4moe_status check_device();
+
 // ------------------------------------------------------------- launchers
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* wr, float* partial, int T, int H, int E,
                                  int n_splits, int32_t* status, cudaStream_t s);
@@ -45,9 +51,10 @@ cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* wr, float* p
 cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* wr, float* partial, int T, int H, int E, int n_splits,
                              int32_t* status, cudaStream_t s);
 int router_tc_n(int E);
+// logits_out / scores_out (nullable): fp32 [T, E] summed logits and sigmoid scores
 cudaError_t launch_topk(const fp4moe_dims& d, const float* partial, int n_splits, const float* bias,
-                        int32_t* idx, float* w, float* logits_out, int32_t* chunk_counts, int n_exp,
-                        cudaStream_t s);
+                        int32_t* idx, float* w, float* logits_out, float* scores_out, int32_t* chunk_counts,
+                        int n_exp, cudaStream_t s);
 // dn_mtiles: 128-column tiles of the layer output the down GEMM computes
 // (H / 128 for the whole output)
 cudaError_t launch_plan(const fp4moe_dims& d, int32_t* chunk_counts, int n_chunks, int n_exp, int n_tile,
@@ -80,6 +87,7 @@ struct FrontArgs {
   int32_t* ticket;  // zero on entry
   uint8_t *xq, *xsf;     // quantised x: token rows (slot 0 of the permuted layout)
   uint32_t* tok_mask;    // [n_exp] bit t: token t routes to the expert
+  float *logits_dbg, *scores_dbg;  // nullable: fp32 [T, E] logits and sigmoid scores
   // weights that do not depend on routing (the shared expert's), pulled
   // into L2 by the helper CTAs while the last CTA routes; nullable
   const uint8_t* l2_pf[4];
@@ -115,6 +123,8 @@ cudaError_t launch_quantize_rows(const void* x, int x_is_fp32, int64_t rows, int
                                  const float* global_in, const uint32_t* amax_bits, uint8_t* codes,
                                  uint8_t* scales, float* global_out, cudaStream_t s);
 cudaError_t launch_pack_weights(const uint8_t* src, uint8_t* dst, int64_t rows_total, int kbytes, cudaStream_t s);
+// NaN scale bytes (E8M0 255, E4M3 0x7F / 0xFF) of src[n] into the status word
+cudaError_t launch_nan_scales(const uint8_t* src, int64_t n, bool nv, int32_t* status, cudaStream_t s);
 cudaError_t launch_pack_scales(const uint8_t* src, uint8_t* dst, int64_t n_mat, int rows, int kblocks, bool nv,
                                cudaStream_t s);
 cudaError_t launch_convert(const uint8_t* codes, const uint8_t* scales, int64_t rows, int K, uint8_t* out,
@@ -154,6 +164,8 @@ struct GemmArgs {
   float *out_acc;                  // down; gate/up: zeroed there when zero_acc
   bool zero_acc;                   // gate/up zeroes out_acc ([T, H] fp32) for the down GEMM
   int32_t *status;
+  uint64_t wait_ns;                // pipeline wait limit; 0: kWaitLimitNs
+  bool withhold;                   // gate/up test knob (fp4moe_debug.withhold_first_stage)
   // W8A8: channel scales of the weights (routed [E, rows], shared [rows]),
   // scales of the B rows (per permuted row); amax_h is then per permuted row
   const float *wrs, *shrs, *brs;

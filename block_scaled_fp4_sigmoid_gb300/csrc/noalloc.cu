@@ -12,10 +12,15 @@
 // loads this library holds it until the process exits.  All calls share it, so
 // calls that overlap on the GPU (different streams, or different host threads
 // on one device) race; serialise them.  The array keeps the last call's
-// contents; the part that must start at zero is cleared by every call.
+// contents; the part that must start at zero (status word, counts) is cleared
+// by every call.
+//
+// Layout of the array: status word int32[16] (padded to 256 bytes), per-chunk
+// expert counts int32[ceil(T / 32), E + n_shared] (padded to 256 bytes), then
+// the partial logits fp32[n_splits, T, E].  n_splits is fp4moe_route's split
+// count when that fits, else the largest smaller split count that does (the
+// sum order of the logits then differs from fp4moe_route's).
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -24,26 +29,33 @@ namespace fp4moe {
 namespace {
 
 constexpr size_t kScratchBytes = FP4MOE_NOALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
+constexpr size_t kStatusBytes = 256;
 
 static __device__ __align__(256) uint8_t g_route_scratch[kScratchBytes];
 
-std::mutex g_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Scratch bytes of one call with n_splits splits.
+size_t scratch_bytes(const fp4moe_dims& d, const Layout& L, int n_splits) {
+  return kStatusBytes + align256((size_t)L.n_chunks * L.n_exp * 4) + (size_t)n_splits * d.T * d.E * 4;
+}
+
+// The split count: fp4moe_route's when it fits, else the largest divisor of
+// H / 256 below it that fits; 0 when not even one split fits.
+int noalloc_splits(const fp4moe_dims& d, const Layout& L) {
+  for (int s = L.ws.n_splits; s >= 1; --s)
+    if ((d.H / 256) % s == 0 && scratch_bytes(d, L, s) <= kScratchBytes) return s;
+  return 0;
+}
 
 // Device address of g_route_scratch on the current device.  In host code the
 // array's name is only a host-side stand-in, so the address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
-fp4moe_status scratch_for_current_device(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP4MOE_ERR_DEVICE;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return FP4MOE_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+// cudaGetSymbolAddress with the device current, looked up on every call (no
+// cached pointer can outlive a context).
+fp4moe_status scratch_for_current_device(uint8_t** out) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return FP4MOE_ERR_CUDA;
+  *out = static_cast<uint8_t*>(p);
   return FP4MOE_OK;
 }
 
@@ -51,6 +63,14 @@ fp4moe_status scratch_for_current_device(void** out) {
 }  // namespace fp4moe
 
 using namespace fp4moe;
+
+extern "C" size_t fp4moe_route_noalloc_scratch_bytes(const fp4moe_dims* dims) {
+  if (!dims) return 0;
+  Layout L;
+  if (!make_layout(*dims, &L)) return 0;
+  const int s = noalloc_splits(*dims, L);
+  return s ? scratch_bytes(*dims, L, s) : 0;
+}
 
 extern "C" fp4moe_status fp4moe_route_noalloc(const fp4moe_dims* dims, const uint16_t* x, const uint16_t* w_router,
                                               const float* bias, int32_t* topk_idx, float* topk_w,
@@ -61,24 +81,32 @@ extern "C" fp4moe_status fp4moe_route_noalloc(const fp4moe_dims* dims, const uin
   if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(w_router) & 15u))
     return FP4MOE_ERR_INVALID_ARG;
   const fp4moe_dims& d = *dims;
-  // scratch: partial logits [n_splits, T, E] fp32, then chunk counts [n_chunks, n_exp] int32
-  const size_t partial_bytes = (size_t)L.ws.n_splits * d.T * d.E * 4;
-  const size_t counts_off = (partial_bytes + 255) / 256 * 256;
-  const size_t counts_bytes = (size_t)L.n_chunks * L.n_exp * 4;
-  if (counts_off + counts_bytes > kScratchBytes) return FP4MOE_ERR_WORKSPACE;  // beyond the fixed maximum
-  int dev = 0, major = 0, minor = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FP4MOE_ERR_DEVICE;
-  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (major != 10 || minor != 3) return FP4MOE_ERR_DEVICE;
-  void* base = nullptr;
+  const int n_splits = noalloc_splits(d, L);
+  if (n_splits == 0) return FP4MOE_ERR_WORKSPACE;  // beyond the fixed maximum
+  if (fp4moe_status st = check_device()) return st;
+  uint8_t* base = nullptr;
   if (fp4moe_status st = scratch_for_current_device(&base)) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* partial = static_cast<float*>(base);
-  int32_t* cc = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(base) + counts_off);
-  cudaError_t e = cudaMemsetAsync(cc, 0, counts_bytes, s);  // counts accumulate atomically
-  if (e == cudaSuccess) e = launch_router_logits(x, w_router, partial, d.T, d.H, d.E, L.ws.n_splits, nullptr, s);
+  int32_t* status = reinterpret_cast<int32_t*>(base);
+  const size_t counts_bytes = (size_t)L.n_chunks * L.n_exp * 4;
+  int32_t* cc = reinterpret_cast<int32_t*>(base + kStatusBytes);
+  float* partial = reinterpret_cast<float*>(base + kStatusBytes + align256(counts_bytes));
+  // status word and counts (which accumulate atomically) start at zero
+  cudaError_t e = cudaMemsetAsync(base, 0, kStatusBytes + counts_bytes, s);
+  if (e == cudaSuccess) e = launch_router_logits(x, w_router, partial, d.T, d.H, d.E, n_splits, status, s);
   if (e == cudaSuccess)
-    e = launch_topk(d, partial, L.ws.n_splits, bias, topk_idx, topk_w, logits_out, cc, L.n_exp, s);
-  return e == cudaSuccess ? FP4MOE_OK : FP4MOE_ERR_CUDA;
+    e = launch_topk(d, partial, n_splits, bias, topk_idx, topk_w, logits_out, nullptr, cc, L.n_exp, s);
+  return cuda_status(e);
+}
+
+extern "C" fp4moe_status fp4moe_route_noalloc_status(void* stream, fp4moe_status* st, int64_t* count) {
+  if (fp4moe_status c = check_device()) return c;
+  uint8_t* base = nullptr;
+  if (fp4moe_status c = scratch_for_current_device(&base)) return c;
+  int32_t h[kStatusInts];
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP4MOE_ERR_CUDA;
+  if (cudaMemcpy(h, base, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FP4MOE_ERR_CUDA;
+  if (st) *st = static_cast<fp4moe_status>(h[ST_FIRST]);
+  if (count) *count = h[ST_COUNT];
+  return FP4MOE_OK;
 }

@@ -774,6 +774,42 @@ cudaError_t launch_pack_weights(const uint8_t* src, uint8_t* dst, int64_t rows_t
   return cudaGetLastError();
 }
 
+// Counts the NaN scale bytes of n bytes (E8M0: 255; E4M3: magnitude bits
+// 0x7F) and records them in the status word as FP4MOE_ERR_NAN_SCALE.
+__global__ void nan_scales_kernel(const uint8_t* __restrict__ src, int64_t n, int nv, int32_t* status) {
+  __shared__ int s_cnt;
+  if (threadIdx.x == 0) s_cnt = 0;
+  __syncthreads();
+  int cnt = 0;
+  const int64_t n16 = n / 16, stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint32_t byte = (w[j] >> (8 * b)) & 0xFFu;
+        cnt += nv ? ((byte & 0x7Fu) == 0x7Fu) : (byte == 0xFFu);
+      }
+  }
+  for (int64_t i = n16 * 16 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const uint32_t byte = src[i];
+    cnt += nv ? ((byte & 0x7Fu) == 0x7Fu) : (byte == 0xFFu);
+  }
+  if (cnt) atomicAdd(&s_cnt, cnt);
+  __syncthreads();
+  if (threadIdx.x == 0 && s_cnt) record_status(status, FP4MOE_ERR_NAN_SCALE, ST_NAN, s_cnt);
+}
+
+cudaError_t launch_nan_scales(const uint8_t* src, int64_t n, bool nv, int32_t* status, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t want = (n / 16 + 255) / 256;
+  const unsigned blocks = (unsigned)(want < 4 * 152 ? (want > 0 ? want : 1) : 4 * 152);
+  nan_scales_kernel<<<blocks, 256, 0, s>>>(src, n, nv ? 1 : 0, status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_pack_scales(const uint8_t* src, uint8_t* dst, int64_t n_mat, int rows, int kblocks, bool nv,
                                cudaStream_t s) {
   const int64_t katoms = katoms_padded((int64_t)kblocks * (nv ? 16 : 32), nv);

@@ -79,8 +79,8 @@ __device__ __forceinline__ void topk_select(const float* sv, float* cv, int E, i
 __device__ __forceinline__ void topk_token(const float* __restrict__ partial, int n_splits,
                                            const float* __restrict__ bias, int T, int t, int E, int k,
                                            int n_group, int topk_group, float scaling, int renorm,
-                                           float* __restrict__ logits_out, float* sv, float* cv, int lane,
-                                           int* idx, float* w) {
+                                           float* __restrict__ logits_out, float* __restrict__ scores_out,
+                                           float* sv, float* cv, int lane, int* idx, float* w) {
   // E <= 512: at most 16 logits per lane; issue each split's loads together
   float lv[16];
 #pragma unroll
@@ -101,6 +101,7 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ partial, in
     if (e < E) {
       if (logits_out) logits_out[(int64_t)t * E + e] = lv[q];
       const float s = 1.0f / (1.0f + expf(-lv[q]));
+      if (scores_out) scores_out[(int64_t)t * E + e] = s;
       sv[e] = s;
       cv[e] = s + bv16[q];
     }
@@ -202,7 +203,7 @@ constexpr int kTopkWarps = 4;
 __global__ void topk_kernel(const float* __restrict__ partial, int n_splits, const float* __restrict__ bias,
                             int T, int E, int k, int n_group, int topk_group, float scaling, int renorm,
                             int32_t* __restrict__ idx_out, float* __restrict__ w_out, float* __restrict__ logits_out,
-                            int32_t* __restrict__ chunk_counts, int n_exp) {
+                            float* __restrict__ scores_out, int32_t* __restrict__ chunk_counts, int n_exp) {
   __shared__ float s_s[kTopkWarps][512];
   __shared__ float s_c[kTopkWarps][512];
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -210,8 +211,8 @@ __global__ void topk_kernel(const float* __restrict__ partial, int n_splits, con
   if (t >= T) return;
   int my_idx;
   float my_w;
-  topk_token(partial, n_splits, bias, T, t, E, k, n_group, topk_group, scaling, renorm, logits_out, s_s[wib],
-             s_c[wib], lane, &my_idx, &my_w);
+  topk_token(partial, n_splits, bias, T, t, E, k, n_group, topk_group, scaling, renorm, logits_out, scores_out,
+             s_s[wib], s_c[wib], lane, &my_idx, &my_w);
   if (lane < k) {
     idx_out[(int64_t)t * k + lane] = my_idx;
     w_out[(int64_t)t * k + lane] = my_w;
@@ -510,7 +511,10 @@ __global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArg
     if (e < E && t < T) {
       float l = 0.f;
       for (int r = 0; r < a.n_splits; ++r) l += ld_dsmem(&s_part[j][t], (uint32_t)r);
-      a.partial[(int64_t)t * E + e] = 1.0f / (1.0f + expf(-l));  // sigmoid scores [T, E]
+      const float sc = 1.0f / (1.0f + expf(-l));
+      a.partial[(int64_t)t * E + e] = sc;  // sigmoid scores [T, E]
+      if (a.logits_dbg) a.logits_dbg[(int64_t)t * E + e] = l;
+      if (a.scores_dbg) a.scores_dbg[(int64_t)t * E + e] = sc;
     }
   }
   cluster_sync();  // the other CTAs' shared memory stays valid until rank 0 has read it
@@ -720,11 +724,12 @@ cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* wr, float* p
 }
 
 cudaError_t launch_topk(const fp4moe_dims& d, const float* partial, int n_splits, const float* bias, int32_t* idx,
-                        float* w, float* logits_out, int32_t* chunk_counts, int n_exp, cudaStream_t s) {
+                        float* w, float* logits_out, float* scores_out, int32_t* chunk_counts, int n_exp,
+                        cudaStream_t s) {
   const unsigned blocks = (unsigned)((d.T + kTopkWarps - 1) / kTopkWarps);
   topk_kernel<<<blocks, 32 * kTopkWarps, 0, s>>>(partial, n_splits, bias, d.T, d.E, d.top_k, d.n_group,
                                                  d.topk_group, d.routed_scaling, d.renormalize, idx, w, logits_out,
-                                                 chunk_counts, n_exp);
+                                                 scores_out, chunk_counts, n_exp);
   return cudaGetLastError();
 }
 

@@ -16,7 +16,8 @@ import ctypes
 
 import torch
 
-from . import (FP8, MXFP4, NVFP4, Debug, Fp8Weights, Weights, emulation_workspace_size, forward, forward_cols,
+from . import (FP8, MXFP4, NVFP4, Debug, Fp8Weights, Weights, check_scales, emulation_workspace_size, forward,
+               forward_cols,
                forward_nvfp4_emulated, forward_w8a8, get_status, make_dims,
                mxfp4_to_fp8_rowscale, pack_scales, pack_weights, packed_scales_bytes, packed_weights_bytes,
                quantize_act, workspace_layout, workspace_size)
@@ -76,6 +77,7 @@ class MoELayer:
         self.w2_t = pw(self.w2, dims.E, dims.H, dims.I // 2)
         self.sh13_t = pw(sh13, 1, 2 * dims.I, dims.H // 2) if sh13 is not None else None
         self.sh2_t = pw(sh2, 1, dims.H, dims.I // 2) if sh2 is not None else None
+        self._check_scales()
         self.ws_bytes = workspace_size(dims)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
         self.layout = workspace_layout(dims)
@@ -83,6 +85,18 @@ class MoELayer:
                                _ptr(self.g13), _ptr(self.g2), _ptr(self.sh13_t), _ptr(self.sh13_scale),
                                _ptr(self.sh2_t), _ptr(self.sh2_scale), _ptr(self.w_router), _ptr(self.bias),
                                1 if packed else 0)
+
+    def _check_scales(self):
+        """Refuses weights with NaN block scales (fp4moe_check_scales): the
+        layer does not test its scales on every call."""
+        ws = torch.zeros(256, dtype=torch.uint8, device=self.device)
+        s = torch.cuda.current_stream(self.device).cuda_stream
+        for name, t in self.raw.items():
+            if t is not None:
+                check_scales(t.data_ptr(), t.numel(), self.fmt, ws.data_ptr(), 256, s)
+        st, n = get_status(ws.data_ptr(), s)
+        if st != 0:
+            raise ValueError(f"{n} NaN block-scale bytes in the expert weights (status {st})")
 
     def _pack_w(self, codes, n_mat, rows, kbytes):
         dst = torch.empty(packed_weights_bytes(n_mat, rows, kbytes), dtype=torch.uint8, device=codes.device)

@@ -160,15 +160,34 @@ typedef struct {
                          * rows of the padded permuted layout               */
 } fp4moe_ws_layout;
 
-/* Optional instrumentation for fp4moe_forward.
+/* Optional instrumentation for fp4moe_forward (and the other layer entry
+ * points that take one).  A zero-filled struct changes nothing.
  *   events[i] (cudaEvent_t as void*, nullable) is recorded on the stream
  *     before stage i: 0 router, 1 top-k, 2 permutation, 3 activation
  *     quantisation, 4 gate/up GEMM, 5 down GEMM, 6 finalise, 7 end.
  *   h_pre (nullable): fp32 [rows_cap, I]; when set the gate/up epilogue also
- *     writes each h value there before quantising it. */
+ *     writes each h value there before quantising it.
+ *   logits (nullable): fp32 [T, E]; the router logits as the top-k step
+ *     summed them (split-K partials added in split order).
+ *   scores (nullable): fp32 [T, E]; the sigmoid scores s = 1 / (1 + e^-l)
+ *     the top-k step selected from (corrected scores are fp32(s + bias)).
+ *   wait_limit_ns: limit of the expert GEMMs' pipeline waits in
+ *     nanoseconds; 0 keeps the default of 2 s.  The waits that drain copies
+ *     already issued keep the default.
+ *   withhold_first_stage: test knob, 0 in normal use.  When non-zero, CTA 0
+ *     of the gate/up GEMM never fills its first pipeline stage, so that
+ *     CTA's MMA issuer waits for it until wait_limit_ns runs out; the call
+ *     then records FP4MOE_ERR_TIMEOUT in the status word, abandons that
+ *     CTA's work (the output is not valid) and returns normally.  It
+ *     exercises the timeout path without any fault. */
 typedef struct {
   void *events[8];
   float *h_pre;
+  float *logits;
+  float *scores;
+  int64_t wait_limit_ns;
+  int32_t withhold_first_stage;
+  int32_t reserved;
 } fp4moe_debug;
 
 /* Library version as major*10000 + minor*100 + patch. */
@@ -237,21 +256,36 @@ fp4moe_status fp4moe_route(const fp4moe_dims *dims, const uint16_t *x, const uin
  * Engines that plan all device memory ahead and forbid later allocations, or
  * code that must not call cudaMalloc because it may synchronise the device,
  * cannot hand fp4moe_route a workspace.  This entry point keeps the scratch
- * (split-K partial logits, per-chunk expert counts) in one file-scope device
- * array of FP4MOE_NOALLOC_SCRATCH_BYTES that every GPU loading the library
- * holds until process exit, and allocates nothing itself.
+ * in one file-scope device array of FP4MOE_NOALLOC_SCRATCH_BYTES that every
+ * GPU loading the library holds until process exit, and allocates nothing
+ * itself.
  *   Arguments and outputs as fp4moe_route, without the workspace.
- *   Returns FP4MOE_ERR_WORKSPACE when the dims need more scratch than the
- *   array holds (n_splits*T*E*4 bytes of partials, 256-byte aligned, plus
- *   ceil(T/256)*(E+n_shared)*4 bytes of counts).
- *   The first call on a device looks up the array's device address with that
- *   device current; make that first call before any stream capture.
+ *   Scratch per call: a 256-byte status word, then ceil(T/32) * (E +
+ *   n_shared) * 4 bytes of per-chunk expert counts rounded up to 256, then
+ *   n_splits * T * E * 4 bytes of partial logits.  n_splits is
+ *   fp4moe_route's split count (fp4moe_workspace_layout) when that fits, else
+ *   the largest divisor of H / 256 below it that fits; the logits are then
+ *   summed in another order than fp4moe_route's, so near-ties may route
+ *   differently.  fp4moe_route_noalloc_scratch_bytes gives the bytes a call
+ *   uses (0: the dims do not fit even with one split, or are invalid).
+ *   Returns FP4MOE_ERR_WORKSPACE when not even one split fits.
+ *   Each call looks up the array's device address with the device current;
+ *   make the first call on each device before any stream capture.
  *   All calls share the array: calls that overlap on the GPU race, so
  *   serialise them (one stream, or host-side ordering).  Each call clears the
- *   counts it accumulates; the array otherwise keeps the last call's data. */
+ *   status word and the counts; the array otherwise keeps the last call's
+ *   data.  A device wait that times out is recorded in the array's status
+ *   word; fp4moe_route_noalloc_status reads it. */
+size_t fp4moe_route_noalloc_scratch_bytes(const fp4moe_dims *dims);
 fp4moe_status fp4moe_route_noalloc(const fp4moe_dims *dims, const uint16_t *x, const uint16_t *w_router,
                                    const float *bias, int32_t *topk_idx, float *topk_w, float *logits_out,
                                    void *stream);
+
+/* Synchronises `stream` and reads the status word of the last
+ * fp4moe_route_noalloc call on the current device: *st the first recorded
+ * condition (FP4MOE_OK if none), *count how many were recorded.  Either
+ * output may be NULL.  Allocates nothing. */
+fp4moe_status fp4moe_route_noalloc_status(void *stream, fp4moe_status *st, int64_t *count);
 
 /* Activation quantisation ("Serve Kimi-K2.5-MXFP4 on MI355X with ATOM",
  * section "Stage B: Dynamic Activation Quantization"; "Serving NVFP4 models on
@@ -355,6 +389,18 @@ fp4moe_status fp4moe_mxfp4_to_fp8_rowscale(const uint8_t *codes, const uint8_t *
                                            int64_t rows, int32_t K, uint8_t *fp8_out,
                                            float *row_scale, uint8_t *row_status, void *ws,
                                            size_t ws_bytes, void *stream);
+
+/* Weight validation: counts the NaN block-scale bytes among n bytes of
+ * scales (MXFP4: E8M0 byte 255, "Serve Kimi-K2.5-MXFP4 on MI355X with ATOM",
+ * section "The Kimi-K2.5-MXFP4 Model on gfx950"; NVFP4: E4M3 bytes 0x7F and
+ * 0xFF).  The layer does not test its weight scales on every call, since
+ * that would read them again; run this once on each scale tensor (row-major
+ * or repacked by fp4moe_pack_scales: every byte is a scale or the padding
+ * scale 1.0).  NaN bytes are recorded in the status word of ws (>= 256
+ * bytes) as FP4MOE_ERR_NAN_SCALE with their count; fp4moe_get_status reads
+ * it.  scales 16-byte aligned.  Errors: INVALID_ARG, WORKSPACE, DEVICE. */
+fp4moe_status fp4moe_check_scales(const uint8_t *scales, int64_t n, int32_t fmt, void *ws, size_t ws_bytes,
+                                  void *stream);
 
 /* Clears the workspace status word (asynchronous). */
 fp4moe_status fp4moe_clear_status(void *ws, void *stream);

@@ -117,3 +117,84 @@ def test_tiled_payload_formula_in_the_header_matches_the_layout():
         off = m * rows * kt * 128 + ((r // 128) * kt + c // 128) * 16384 + (r % 128) * 128 + c % 128
         assert np.array_equal(tiled[off], src)
         assert tiled.size == fm.packed_weights_bytes(n_mat, rows, kbytes)
+
+
+def _noalloc_scratch_formula(d, route_splits):
+    """Scratch bytes of fp4moe_route_noalloc as the header states them: a
+    256-byte status word, ceil(T/32) * (E + n_shared) * 4 bytes of counts
+    rounded up to 256, then n_splits * T * E * 4 bytes of partial logits, with
+    the largest split count up to fp4moe_route's that divides H / 256 and fits."""
+    counts = (d.T + 31) // 32 * (d.E + d.n_shared) * 4
+    limit = 8 << 20
+    for s in range(route_splits, 0, -1):
+        if (d.H // 256) % s == 0:
+            n = 256 + (counts + 255) // 256 * 256 + s * d.T * d.E * 4
+            if n <= limit:
+                return n
+    return 0
+
+
+@pytest.mark.parametrize("E,H", [(384, 7168), (512, 7168), (256, 2048)])
+def test_noalloc_limit_from_header_formula(lib, E, H):
+    """The accept / refuse decision of fp4moe_route_noalloc at the edge of
+    its fixed scratch array follows the header's formula: the largest T that
+    fits is accepted (and fails only later, for want of a device here), the
+    next one is refused with FP4MOE_ERR_WORKSPACE before any device work.
+    The accepted call is made only where no CUDA device is present (its
+    pointers are placeholders)."""
+    def dims(T):
+        return fm.make_dims(T, H, 256, E, 8)
+
+    def fits(T):
+        d = dims(T)
+        return _noalloc_scratch_formula(d, fm.workspace_layout(d).n_splits) > 0
+
+    lo, hi = 1, 65536
+    assert fits(lo) and not fits(hi)
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        lo, hi = (mid, hi) if fits(mid) else (lo, mid)
+    import torch
+    for T, ok in ((lo, True), (hi, False)):
+        d = dims(T)
+        want = _noalloc_scratch_formula(d, fm.workspace_layout(d).n_splits)
+        assert fm.route_noalloc_scratch_bytes(d) == want and (want > 0) == ok
+        if ok and torch.cuda.is_available():
+            continue  # with a device the accepted call would launch on these placeholder pointers
+        code = lib.fp4moe_route_noalloc(ctypes.byref(d), 256, 256, 256, 256, 256, None, None)
+        assert code == (fm.STATUS_CODE["FP4MOE_ERR_DEVICE"] if ok else fm.STATUS_CODE["FP4MOE_ERR_WORKSPACE"]), (T, code)
+
+
+def test_short_workspace_refused_before_device_work(lib):
+    """A workspace one byte short of fp4moe_workspace_size is refused with
+    FP4MOE_ERR_WORKSPACE before anything is launched (placeholder pointers,
+    never dereferenced), for every layer entry point that takes one."""
+    d = fm.make_dims(4, 256, 128, 8, 2)
+    n = fm.workspace_size(d)
+    w = fm.Weights(*([256] * 12), 1)
+    code = lib.fp4moe_forward(ctypes.byref(d), ctypes.byref(w), 256, 256, None, 256, n - 1, None)
+    assert code == fm.STATUS_CODE["FP4MOE_ERR_WORKSPACE"]
+    code = lib.fp4moe_forward_cols(ctypes.byref(d), ctypes.byref(w), 256, 256, 0, 128, None, 256, n - 1, None)
+    assert code == fm.STATUS_CODE["FP4MOE_ERR_WORKSPACE"]
+    code = lib.fp4moe_route(ctypes.byref(d), 256, 256, 256, 256, 256, None, 256, n - 1, None)
+    assert code == fm.STATUS_CODE["FP4MOE_ERR_WORKSPACE"]
+    d8 = fm.make_dims(4, 256, 128, 8, 2, fmt=fm.FP8)
+    w8 = fm.Fp8Weights(*([256] * 10))
+    code = lib.fp4moe_forward_w8a8(ctypes.byref(d8), ctypes.byref(w8), 256, 256, None, 256,
+                                   fm.workspace_size(d8) - 1, None)
+    assert code == fm.STATUS_CODE["FP4MOE_ERR_WORKSPACE"]
+    dn = fm.make_dims(4, 256, 128, 8, 2, fmt=fm.NVFP4)
+    code = lib.fp4moe_forward_nvfp4_emulated(ctypes.byref(dn), ctypes.byref(w), 256, 256, None, 256,
+                                             fm.emulation_workspace_size(dn) - 1, None)
+    assert code == fm.STATUS_CODE["FP4MOE_ERR_WORKSPACE"]
+    n_lin = fm.linear_workspace_size(fm.MXFP4, 4, 256, 256)
+    code = lib.fp4moe_linear(fm.MXFP4, 4, 256, 256, 256, 256, 256, None, 256, 256, n_lin - 1, None)
+    assert code == fm.STATUS_CODE["FP4MOE_ERR_WORKSPACE"]
+    code = lib.fp4moe_check_scales(256, 64, fm.MXFP4, 256, 255, None)
+    assert code == fm.STATUS_CODE["FP4MOE_ERR_WORKSPACE"]
+
+
+def test_check_scales_argument_errors(lib):
+    assert lib.fp4moe_check_scales(None, 64, fm.MXFP4, 256, 256, None) == fm.STATUS_CODE["FP4MOE_ERR_INVALID_ARG"]
+    assert lib.fp4moe_check_scales(256, 64, 7, 256, 256, None) == fm.STATUS_CODE["FP4MOE_ERR_INVALID_ARG"]
+    assert lib.fp4moe_check_scales(256, -1, fm.MXFP4, 256, 256, None) == fm.STATUS_CODE["FP4MOE_ERR_INVALID_ARG"]

@@ -3,7 +3,9 @@
 The W8A8 layer runs the experts of an MXFP4 layer after the exact per-channel
 FP8 conversion, with per-token dynamic E4M3 activations.  Staged like the
 A4W4 parity tests:
-  1. routing and permutation (same kernels as the A4W4 layer);
+  1. routing (logits and scores within their bounds, the fp32 selection
+     replayed on the GPU's scores bit-exact on every token) and permutation
+     (same kernels as the A4W4 layer);
   2. quantised activations: E4M3 codes and the fp32 row scale bit-exact in
      every route row of a token;
   3. the intermediate h within its error bound before quantisation; its codes
@@ -25,7 +27,9 @@ from oracle import formats as F
 from oracle import w8a8 as W8
 
 from gpu_util import ensure_built, torch_cuda
-from test_gpu_forward import SMALL, check_output, check_permutation, check_routing
+from test_gpu_forward import (SMALL, check_output, check_permutation, check_router_numerics, check_routing,
+                              check_selection_replay)
+from oracle import router as R
 
 pytestmark = pytest.mark.gpu
 
@@ -46,8 +50,12 @@ class Run8:
         h_pre = torch.zeros((L.rows_cap, cfg.I), dtype=torch.float32, device="cuda")
         dbg = fm.Debug()
         dbg.h_pre = h_pre.data_ptr()
+        logits = torch.zeros((cfg.T, cfg.E), dtype=torch.float32, device="cuda")
+        scores = torch.zeros((cfg.T, cfg.E), dtype=torch.float32, device="cuda")
+        dbg.logits, dbg.scores = logits.data_ptr(), scores.data_ptr()
         out = layer.forward(x, debug=dbg)
         torch.cuda.synchronize()
+        self.logits, self.scores = logits.cpu().numpy(), scores.cpu().numpy()
         self.status = fm.get_status(layer.ws.data_ptr())
         T, k, ns = cfg.T, cfg.top_k, cfg.n_shared
         rpt = k + ns
@@ -103,6 +111,11 @@ def check8(cfg, tokens):
     keys = [(w, e) for e in need for w in ("w13", "w2")] + [(w, 0) for w in ("sh13", "sh2")][:2 * cfg.n_shared]
     _prefetch(ws, cfg, keys)
     orc = W8.token_forward_fp8(cfg, xr, wr, b, ws)
+    orc["bias"] = b
+    x_all = synth.bf16_bits_to_f64(run.x_bits)
+    exact, lsum = R.router_logits(x_all, wr)
+    check_router_numerics(run, cfg, exact, lsum)
+    check_selection_replay(run, cfg, b)
     amb = check_routing(run, cfg, orc, tokens)
     check_permutation(run, cfg)
     stats = {"ambiguous_tokens": len(amb), "h_flips": 0, "h_ambiguous": 0, "h_err_ratio": 0.0}
@@ -134,15 +147,18 @@ def check8(cfg, tokens):
     stats["worst_ratio"] = check_output(run, orc["ref"], orc["S"], orc["A"], tokens, amb)
     # replay: the oracle's down projection and combine on the GPU's quantised
     # intermediate meets the tolerance with no allowance for flips
+    # (with the GPU's routing, so every token is checked)
     ref2 = np.zeros_like(orc["ref"])
+    S2 = np.zeros_like(orc["ref"])
     for i, t in enumerate(tokens):
-        for j, info in enumerate(orc["routes"][i]):
-            jj = j if j >= cfg.top_k else int(np.flatnonzero(run.idx[t] == info["expert"])[0])
-            e = info["expert"]
+        for j in range(cfg.top_k + cfg.n_shared):
+            e = int(run.idx[t, j]) if j < cfg.top_k else cfg.E + j - cfg.top_k
             W2 = ws.get("w2", e) if e < cfg.E else ws.get("sh2", e - cfg.E)
-            hd = F.E4M3_TABLE[run.hq[t, jj]] * float(run.hsig[t, jj])
-            ref2[i] += info["wt"][0] * (hd @ W2.T)
-    stats["worst_ratio_replayed"] = check_output(run, ref2, orc["S"], np.zeros_like(orc["A"]), tokens, amb)
+            hd = F.E4M3_TABLE[run.hq[t, j]] * float(run.hsig[t, j])
+            wt = float(run.w[t, j]) if j < cfg.top_k else 1.0
+            ref2[i] += wt * (hd @ W2.T)
+            S2[i] += abs(wt) * (np.abs(hd) @ np.abs(W2).T)
+    stats["worst_ratio_replayed"] = check_output(run, ref2, S2, np.zeros_like(ref2), tokens)
     return stats
 
 
