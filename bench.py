@@ -230,26 +230,28 @@ def oracle_route_sample(cfg_name: str, n_routes: int, frac: float = 1.0, start_t
     return t_total, n_routes / rpt * (Ip / cfg.I)
 
 
-def algorithmic_bytes(H: int, I: int, fmt: str, mode: str, touched: int, routes: int) -> tuple[float, float]:
+def algorithmic_bytes(H: int, I: int, fmt: str, mode: str, touched: int, routes: int,
+                      tokens: int) -> tuple[float, float]:
     """Bytes the gate/up and the down GEMM of one layer call must move at
     least: the touched experts' weights (with their scales), the activation
-    rows each reads and what each writes, for R routes.
+    rows each reads and what each writes, for R routes of T tokens.
       a4w4:    FP4 values at 0.5 B plus one scale byte per block (MXFP4 32,
                NVFP4 16); gate/up reads x, writes the quantised h; down
-               reads it and adds fp32 rows into the combine buffer.
+               reads it and leaves one fp32 output row per token (the
+               weighted sum of the token's routes, written once).
       w8a8:    E4M3 bytes plus fp32 scales per weight row and per activation
                row; gate/up writes fp32 h, down reads its E4M3 form.
       emulate: BF16 weights and activation rows; gate/up writes fp32 h."""
     if mode == "emulate":
         gu = touched * (2 * I * H * 2) + routes * H * 2 + routes * I * 4
-        dn = touched * (H * I * 2) + routes * I * 2 + routes * H * 4
+        dn = touched * (H * I * 2) + routes * I * 2 + tokens * H * 4
     elif mode == "w8a8":
         gu = touched * (2 * I * H + 2 * I * 4) + routes * (H + 4) + routes * I * 4
-        dn = touched * (H * I + H * 4) + routes * (I + 4) + routes * H * 4
+        dn = touched * (H * I + H * 4) + routes * (I + 4) + tokens * H * 4
     elif mode == "a4w4":
         act = 0.5 + 1.0 / (16 if fmt == "nvfp4" else 32)  # bytes per FP4 value incl. scale
         gu = touched * (2 * I * H * act) + routes * H * act + routes * I * act
-        dn = touched * (H * I * act) + routes * I * act + routes * H * 4
+        dn = touched * (H * I * act) + routes * I * act + tokens * H * 4
     else:
         raise ValueError(mode)
     return gu, dn
@@ -459,9 +461,171 @@ def linear_arm(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ roofline
+def fp4_peak_tflops(peaks: dict) -> float:
+    """Dense FP4 tensor peak: the measured bf16 peak times the nominal dense
+    FP4 / bf16 ratio 13.5 / 2.25 = 6."""
+    return 6.0 * peaks["bf16_tflops"]
+
+
+def roofline(nbytes: float, flops: float, ms: float, peaks: dict) -> dict:
+    """The slower of the two rooflines for work that moves `nbytes` and does
+    `flops` in `ms`: time at the measured HBM bandwidth against time at the
+    dense FP4 tensor peak; the bound is the larger, and the fraction is that
+    time over the measured one (achieved over peak in the bound's unit)."""
+    t_b = nbytes / (peaks["hbm_gbs"] * 1e9) * 1e3
+    t_f = flops / (fp4_peak_tflops(peaks) * 1e12) * 1e3
+    if t_b >= t_f:
+        rec = {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        rec = {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": fp4_peak_tflops(peaks),
+               "unit": "TFLOP/s"}
+    rec.update({"frac": rec["achieved"] / rec["peak"], "ms": ms, "roofline_ms": max(t_b, t_f), "bytes_ms": t_b,
+                "flops_ms": t_f, "algorithmic_bytes": nbytes, "flops": flops})
+    return rec
+
+
+def layer_work(H: int, I: int, E: int, T: int, fmt: str, mode: str, touched: int, routes: int) -> dict:
+    """Algorithmic bytes and FLOPs of one layer call and of its two expert
+    GEMMs: the GEMMs' bytes as algorithmic_bytes gives them, plus the router
+    (its weights and x, bf16) and the bf16 output for the layer.  FLOPs: 2 *
+    3 * I * H per route (gate, up, down)."""
+    gu, dn = algorithmic_bytes(H, I, fmt, mode, touched, routes, T)
+    return {"gateup": (gu, 2.0 * 2 * I * H * routes), "down": (dn, 2.0 * H * I * routes),
+            "layer": (gu + dn + E * H * 2 + 2 * T * H * 2, 2.0 * 3 * I * H * routes)}
+
+
 # ------------------------------------------------------------------ GPU arm
+def _events(torch, stream, n):
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:
+        e.record(stream)
+    return evs
+
+
+def measure_layer(torch, fm, layer, x, fwd, steps: int, warmup: int, stream, flush, stage_runs: int = 50,
+                  clock_gpu: int | None = None, bracket=None):
+    """Times one layer configuration: warm-up calls, `steps` replays of one
+    forward captured in a CUDA graph (L2 flushed before each, untimed), and
+    eager forwards with events between the stages.  `bracket` (nullable) runs
+    right before and right after the timed replays (the ranks' barrier).
+    Returns per-step times, stage times, the GEMMs' times, touched experts
+    and routes."""
+    d = layer.dims
+    out = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=x.device)
+    s = stream.cuda_stream
+    for _ in range(warmup):
+        flush.fill_(1.0)
+        fwd(x, out)
+    torch.cuda.synchronize()
+    wsbuf = layer.emu_ws if getattr(layer, "emu_ws", None) is not None and fwd == getattr(layer, "forward_emulated",
+                                                                                          None) else layer.ws
+    st, _ = fm.get_status(wsbuf.data_ptr(), s)
+    if st != 0:
+        raise RuntimeError(f"device status {fm.STATUS.get(st, st)}")
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        fwd(x, out)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    ev = [_events(torch, stream, 2) for _ in range(steps)]
+    torch.cuda.synchronize()
+    if bracket:
+        bracket()
+    sampler = ClockSampler(clock_gpu) if clock_gpu is not None else None
+    if sampler:
+        sampler.__enter__()
+        time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for i in range(steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        graph.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if bracket:
+        bracket()
+    if sampler:
+        time.sleep(0.3)
+        sampler.__exit__(None, None, None)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    gev = _events(torch, stream, 8)
+    dbg = fm.Debug()
+    for i, e in enumerate(gev):
+        dbg.events[i] = e.cuda_event
+    runs, gu_ms, dn_ms = [], [], []
+    for i in range(min(steps, stage_runs)):
+        flush.fill_(float(i))
+        torch.cuda.synchronize()
+        fwd(x, out, debug=dbg)
+        torch.cuda.synchronize()
+        runs.append([gev[j].elapsed_time(gev[j + 1]) for j in range(7)])
+        gu_ms.append(gev[4].elapsed_time(gev[5]))
+        dn_ms.append(gev[5].elapsed_time(gev[6]))
+    ne = d.E + d.n_shared
+    off = layer.layout.expert_count
+    count = wsbuf[off:off + 4 * ne].view(torch.int32).cpu().numpy()
+    return {"step_ms": step_ms, "ms": statistics.mean(step_ms), "wall_s": wall, "graph": graph, "out": out,
+            "stages_ms": {fm.STAGES[j]: statistics.mean(r[j] for r in runs) for j in range(7)},
+            "gu_ms": statistics.mean(gu_ms), "dn_ms": statistics.mean(dn_ms),
+            "touched": int((count > 0).sum()), "routes": int(count.sum()),
+            "clocks": sampler.summary() if sampler else None}
+
+
+def config_record(cfg, layer, m: dict, peaks: dict, mode: str = "a4w4", w8a8: bool = False,
+                  emulate: bool = False) -> dict:
+    """One workload's sub-record: throughput, stage times and the rooflines
+    of the layer and of its two expert GEMMs."""
+    d = layer.dims
+    work = layer_work(d.H, d.I, d.E, d.T, cfg.fmt, mode, m["touched"], m["routes"])
+    kern = {"gateup": roofline(*work["gateup"], m["gu_ms"], peaks), "down": roofline(*work["down"], m["dn_ms"], peaks)}
+    dominant = max(kern, key=lambda k: kern[k]["ms"])
+    return {"workload": cfg_label(cfg, w8a8, emulate), "ms_per_step": m["ms"], "tokens_per_s": d.T / (m["ms"] * 1e-3),
+            "tflops": work["layer"][1] / (m["ms"] * 1e-3) / 1e12, "touched_experts": m["touched"],
+            "routes": m["routes"], "stages_ms": m["stages_ms"], "roofline": roofline(*work["layer"], m["ms"], peaks),
+            "kernels": kern, "dominant_kernel": dominant, "clocks": m["clocks"],
+            "launch": "one forward captured in a CUDA graph, replayed per step; L2 flushed between steps"}
+
+
+# the workloads measured beside the headline one, in this order
+OTHER_CONFIGS = ("kimi_prefill", "deepseek_nvfp4", "skewed_shared", "tiny")
+
+
+def other_configs(args, torch, fm, dev, stream, flush, peaks, local_rank):
+    """Every other workload of the layer (and the MXFP4 -> FP8 conversion of
+    the skewed workload's experts), one after another on this GPU.  The
+    384-expert MXFP4 layers share one set of expert tensors."""
+    import synth
+    from block_scaled_fp4_sigmoid_gb300.layer import MoELayer
+    cfgs = synth.configs()
+    steps = max(5, min(args.steps, 30))
+    recs = {}
+    base = MoELayer.synthetic(cfgs["skewed_shared"], device=dev)  # 384 experts + the shared one
+    for name in OTHER_CONFIGS:
+        cfg = cfgs[name]
+        if cfg.fmt == "mxfp4" and (cfg.E, cfg.H, cfg.I) == (base.dims.E, base.dims.H, base.dims.I):
+            layer = base.variant(cfg)
+        else:
+            layer = MoELayer.synthetic(cfg, device=dev)
+        x = layer.synthetic_x()
+        m = measure_layer(torch, fm, layer, x, layer.forward, steps, args.warmup, stream, flush, stage_runs=20,
+                          clock_gpu=local_rank)
+        recs[name] = config_record(cfg, layer, m, peaks)
+        if name == "tiny":
+            recs[name]["us_per_step"] = m["ms"] * 1e3
+        del layer, x, m
+        torch.cuda.synchronize()
+    recs["conversion"] = time_conversion(base, peaks, stream)
+    del base
+    torch.cuda.empty_cache()
+    return recs
+
+
 def gpu_arm(args, cfg, rank, world, local_rank):
-    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -473,7 +637,6 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     stream = torch.cuda.current_stream(dev)
-    s = stream.cuda_stream
     layer = MoELayer.synthetic(cfg, device=dev)
     if args.w8a8:
         from block_scaled_fp4_sigmoid_gb300.layer import W8A8Layer
@@ -488,35 +651,17 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     if args.emulate and cfg.fmt != "nvfp4":
         raise SystemExit("--emulate runs NVFP4 layers")
     fwd = layer.forward_emulated if args.emulate else layer.forward
-    out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     torch.cuda.synchronize()
+    steps = args.steps
 
-    def make_events(n):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        for e in evs:
-            e.record(stream)
-        return evs
-
-    def dbg_for(evs):
-        d = fm.Debug()
-        for i, e in enumerate(evs):
-            d.events[i] = e.cuda_event
-        return d
-
-    # warm-up (also compiles nothing: the library is prebuilt)
+    # eager calls (host launch overhead included), for context
+    out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
     for _ in range(args.warmup):
         flush.fill_(1.0)
         fwd(x, out)
-    torch.cuda.synchronize()
-    st, n_st = fm.get_status(layer.ws.data_ptr(), s)
-    if st != 0:
-        raise RuntimeError(f"device status {fm.STATUS.get(st, st)}")
-
-    steps = args.steps
-    # eager calls (host launch overhead included), for context
     eager_n = min(steps, 100)
-    eager_ev = [make_events(2) for _ in range(eager_n)]
+    eager_ev = [_events(torch, stream, 2) for _ in range(eager_n)]
     torch.cuda.synchronize()
     for i in range(eager_n):
         flush.fill_(float(i))
@@ -526,50 +671,15 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     torch.cuda.synchronize()
     eager_ms = statistics.mean(a.elapsed_time(b) for a, b in eager_ev)
 
-    # the timed step: one forward captured once into a CUDA graph and replayed
-    graph = torch.cuda.CUDAGraph()
-    torch.cuda.synchronize()
-    with torch.cuda.graph(graph):
-        fwd(x, out)
-    torch.cuda.synchronize()
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
-    ev = [make_events(2) for _ in range(steps)]
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clk:
-        time.sleep(0.3)
-        wall0 = time.perf_counter()
-        for i in range(steps):
-            flush.fill_(float(i))
-            ev[i][0].record(stream)
-            graph.replay()
-            ev[i][1].record(stream)
+    # the timed steps: graph replays bracketed by a barrier on every rank
+    def bracket():
+        if world > 1:
+            dist.barrier()
         torch.cuda.synchronize()
-        wall = time.perf_counter() - wall0
-        time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = statistics.mean(step_ms)
-    # per-stage times: eager forwards with events between the stages, one at a
-    # time (the host enqueues a whole forward before the GPU finishes it)
-    gev = make_events(8)
-    gdbg = dbg_for(gev)
-    stage_runs, gu_ms, dn_ms = [], [], []
-    for i in range(min(steps, 50)):
-        flush.fill_(float(i))
-        torch.cuda.synchronize()
-        fwd(x, out, debug=gdbg)
-        torch.cuda.synchronize()
-        stage_runs.append([gev[j].elapsed_time(gev[j + 1]) for j in range(7)])
-        gu_ms.append(gev[4].elapsed_time(gev[5]))
-        dn_ms.append(gev[5].elapsed_time(gev[6]))
-    stage_ms = {fm.STAGES[j]: statistics.mean(r[j] for r in stage_runs) for j in range(7)}
+
+    m = measure_layer(torch, fm, layer, x, fwd, steps, args.warmup, stream, flush, clock_gpu=local_rank,
+                      bracket=bracket)
+    ms = m["ms"]
 
     # end to end through the public API with host buffers
     x_host = x.cpu().pin_memory()
@@ -581,7 +691,7 @@ def gpu_arm(args, cfg, rank, world, local_rank):
         fwd(x_dev, out)
         out_host.copy_(out, non_blocking=True)
     torch.cuda.synchronize()
-    e2e_ev = [make_events(2) for _ in range(e2e_steps)]
+    e2e_ev = [_events(torch, stream, 2) for _ in range(e2e_steps)]
     torch.cuda.synchronize()
     for i in range(e2e_steps):
         flush.fill_(float(i))
@@ -593,27 +703,25 @@ def gpu_arm(args, cfg, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
 
-    # work actually done: touched experts and routes
-    ne = cfg.E + cfg.n_shared
-    wsbuf = layer.emu_ws if args.emulate else layer.ws  # the emulation mode has a workspace of its own
-    off = layer.layout.expert_count
-    count = wsbuf[off:off + 4 * ne].view(torch.int32).cpu().numpy()
-    touched = int(np.count_nonzero(count))
-    routes = int(count.sum())
+    touched, routes = m["touched"], m["routes"]
     wpe = layer.weight_bytes_per_expert()
     d = layer.dims
     mode = "emulate" if args.emulate else "w8a8" if args.w8a8 else "a4w4"
-    gu_bytes, dn_bytes = algorithmic_bytes(d.H, d.I, cfg.fmt, mode, touched, routes)
-    flops = 2.0 * 3 * d.I * d.H * routes
-
-    # max over ranks
-    ms_max, e2e_max, gu_max = max_over_ranks([ms, e2e_ms, statistics.mean(gu_ms)], world, dev)
+    work = layer_work(d.H, d.I, d.E, d.T, cfg.fmt, mode, touched, routes)
+    ms_max, e2e_max, gu_max, dn_max = max_over_ranks([ms, e2e_ms, m["gu_ms"], m["dn_ms"]], world, dev)
+    head = {"clocks": m["clocks"], "stages_ms": m["stages_ms"], "wall_s": m["wall_s"]}
+    del m
+    peaks = measured_peaks()
+    # the remaining workloads (default run, one GPU): measured after the headline
+    others = None
+    if world == 1 and not (args.w8a8 or args.emulate or args.no_configs or args.experts or args.tokens):
+        others = other_configs(args, torch, fm, dev, stream, flush, peaks, local_rank)
     if rank != 0:
         return
-    peaks = measured_peaks()
-    achieved = gu_bytes / (gu_max * 1e-3) / 1e9
-    traffic = profiled_traffic(cfg.name + ("_w8a8" if args.w8a8 else ""))
-    clocks = clk.summary()
+    gu = roofline(*work["gateup"], gu_max, peaks)
+    dn = roofline(*work["down"], dn_max, peaks)
+    dom_name, dom = ("gate/up grouped GEMM", gu) if gu["ms"] >= dn["ms"] else ("down grouped GEMM", dn)
+    traffic = profiled_traffic(cfg.name + ("_w8a8" if args.w8a8 else "")) if dom is gu else None
     # few tokens: front end (routing, plan, x quantisation), gate/up, down,
     # finalise; else router, top-k, plan, scatter, gather, gate/up, down, finalise
     if args.w8a8:  # router, top-k, plan, scatter, x quantisation, gate/up, h quantisation, down, finalise
@@ -624,7 +732,11 @@ def gpu_arm(args, cfg, rank, world, local_rank):
         launches_per_step = 4 if cfg.T <= 16 else 8
     else:
         launches_per_step = 10
-    conversion = time_conversion(layer, peaks, stream) if args.conversion and not args.w8a8 else None
+    conversion = None
+    if args.conversion and not args.w8a8:
+        conversion = time_conversion(layer, peaks, stream)
+    elif others is not None:
+        conversion = others.pop("conversion")
     # CPU baseline: the oracle on a bounded sample of this workload
     n_routes = 16 if args.cpu_routes is None else args.cpu_routes
     cpu_s, cpu_tok = (oracle_route_sample(args.config, n_routes, w8a8=args.w8a8, emulate=args.emulate) if n_routes > 0
@@ -646,22 +758,25 @@ def gpu_arm(args, cfg, rank, world, local_rank):
                    "launch": "one fp4moe_forward captured in a CUDA graph, replayed per step",
                    "l2": "flushed between steps (256 MiB write, untimed)", "touched_experts": touched,
                    "routes": routes},
-        "clocks": clocks,
+        "clocks": head["clocks"],
         "e2e": {"value": whole_job_rate(cfg.T, world, e2e_max), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x.numel() * 2), "d2h_bytes_per_step": int(out.numel() * 2)},
         "gpu_launches": launches_per_step * steps,
-        "roofline": {"bound": "hbm", "kernel": "gate/up grouped GEMM", "achieved": achieved,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": traffic, "algorithmic_bytes": gu_bytes, "peak_source": peaks["source"]},
+        "roofline": {"bound": dom["bound"], "kernel": dom_name, "achieved": dom["achieved"], "peak": dom["peak"],
+                     "unit": dom["unit"], "frac": dom["frac"], "traffic": traffic,
+                     "algorithmic_bytes": dom["algorithmic_bytes"], "flops": dom["flops"],
+                     "peak_source": peaks["source"] + ("" if dom["bound"] == "hbm" else
+                                                       " bf16 x 6 (nominal dense FP4 / bf16)")},
         "step": {"weight_stream_gbs": (touched * wpe) / (ms_max * 1e-3) / 1e9,
                  "weight_stream_frac": (touched * wpe) / (ms_max * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                 "tflops": flops / (ms_max * 1e-3) / 1e12, "stages_ms": stage_ms,
-                 "down_gemm_gbs": dn_bytes / (statistics.mean(dn_ms) * 1e-3) / 1e9,
-                 "wall_s": wall, "eager_ms_per_step": eager_ms},
+                 "tflops": work["layer"][1] / (ms_max * 1e-3) / 1e12, "stages_ms": head["stages_ms"],
+                 "layer_roofline": roofline(*work["layer"], ms_max, peaks), "kernels": {"gateup": gu, "down": dn},
+                 "wall_s": head["wall_s"], "eager_ms_per_step": eager_ms},
         "cpu_baseline": {"value": cpu_tok / cpu_s, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                          "sample": f"{n_routes} routes ({cpu_tok:g} tokens) of the same workload, FP64 numpy"},
         "context": "pages: 1.43 ms per MoE layer call at T=8 on one Gaudi 2 card holding 48 of 384 experts",
         "conversion": conversion,
+        "configs": others,
     }
     print(json.dumps(line), flush=True)
 
@@ -685,6 +800,9 @@ def main():
                     help="the W8A8 layer: experts exactly converted to FP8 per channel, FP8 per-token activations")
     ap.add_argument("--conversion", action="store_true",
                     help="also time the MXFP4 -> FP8 conversion of all routed expert rows")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time the chosen workload only (by default a one-GPU run also measures every other "
+                         "workload and the conversion, in the line's configs object)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     import synth

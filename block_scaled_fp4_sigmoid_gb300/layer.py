@@ -212,6 +212,35 @@ class MoELayer:
         layer.raw_scales = (w13s, w2s)
         return layer
 
+    def variant(self, cfg):
+        """A layer over the same routed experts and router weights for another
+        batch size or routing configuration of the same shape (E, H, I,
+        format): its own dims, correction bias and workspace, no copy of the
+        weights.  The shared expert is kept when cfg has one (this layer must
+        hold it then) and dropped otherwise."""
+        import copy
+        import synth
+        d = self.dims
+        if (cfg.E, cfg.H, cfg.I) != (d.E, d.H, d.I) or (NVFP4 if cfg.fmt == "nvfp4" else MXFP4) != d.fmt:
+            raise ValueError("a variant keeps the experts' shape and format")
+        if cfg.n_shared and self.sh13 is None:
+            raise ValueError("this layer holds no shared expert")
+        v = copy.copy(self)
+        v.cfg = cfg
+        v.dims = make_dims(cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k, cfg.n_group, cfg.topk_group, cfg.n_shared,
+                           cfg.routed_scaling, cfg.renormalize, d.fmt)
+        v.bias = torch.from_numpy(synth.gen_bias_f32(cfg)).to(self.device)
+        if not cfg.n_shared:
+            v.sh13 = v.sh2 = v.sh13_scale = v.sh2_scale = v.sh13_t = v.sh2_t = None
+        v.ws_bytes = workspace_size(v.dims)
+        v.ws = torch.empty(v.ws_bytes, dtype=torch.uint8, device=self.device)
+        v.layout = workspace_layout(v.dims)
+        v.emu_ws = None
+        v.weights = Weights(_ptr(v.w13_t), _ptr(v.w13_scale), _ptr(v.w2_t), _ptr(v.w2_scale), _ptr(v.g13),
+                            _ptr(v.g2), _ptr(v.sh13_t), _ptr(v.sh13_scale), _ptr(v.sh2_t), _ptr(v.sh2_scale),
+                            _ptr(v.w_router), _ptr(v.bias), 1 if v.packed else 0)
+        return v
+
     def synthetic_x(self, t0: int = 0, t1: int | None = None):
         """Activations of the synthetic configuration, drawn on the device."""
         import synth

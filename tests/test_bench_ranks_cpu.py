@@ -78,18 +78,22 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
 def test_algorithmic_bytes_match_the_per_expert_figures():
     """The roofline's byte counts: one touched expert with no routes is its
     weights (MXFP4 23,396,352 B and NVFP4 24,772,608 B at H=7168, I=2048;
-    E4M3 plus fp32 row scales; BF16), and one route with no weights is the
-    activation traffic of each GEMM; the Kimi decode line (44 touched
-    experts, 64 routes) is the 686,606,336 B of the committed profile."""
+    E4M3 plus fp32 row scales; BF16), one route of one token with no weights
+    is the activation traffic of each GEMM plus the token's fp32 output row,
+    further routes of that token add their activation rows only; the Kimi
+    decode line (44 touched experts, 64 routes) is the 686,606,336 B of the
+    committed profile."""
     sys.path.insert(0, str(ROOT))
     import bench
     H, I = 7168, 2048
-    assert sum(bench.algorithmic_bytes(H, I, "mxfp4", "a4w4", 1, 0)) == 23_396_352
-    assert sum(bench.algorithmic_bytes(H, I, "nvfp4", "a4w4", 1, 0)) == 24_772_608
-    assert sum(bench.algorithmic_bytes(H, I, "mxfp4", "w8a8", 1, 0)) == 3 * H * I + 4 * (2 * I + H)
-    assert sum(bench.algorithmic_bytes(H, I, "nvfp4", "emulate", 1, 0)) == 3 * H * I * 2
-    gu, dn = bench.algorithmic_bytes(H, I, "mxfp4", "a4w4", 0, 1)
+    assert sum(bench.algorithmic_bytes(H, I, "mxfp4", "a4w4", 1, 0, 0)) == 23_396_352
+    assert sum(bench.algorithmic_bytes(H, I, "nvfp4", "a4w4", 1, 0, 0)) == 24_772_608
+    assert sum(bench.algorithmic_bytes(H, I, "mxfp4", "w8a8", 1, 0, 0)) == 3 * H * I + 4 * (2 * I + H)
+    assert sum(bench.algorithmic_bytes(H, I, "nvfp4", "emulate", 1, 0, 0)) == 3 * H * I * 2
+    gu, dn = bench.algorithmic_bytes(H, I, "mxfp4", "a4w4", 0, 1, 1)
     assert gu == (H + I) * 17 / 32 and dn == I * 17 / 32 + 4 * H
-    assert bench.algorithmic_bytes(H, I, "mxfp4", "a4w4", 44, 64)[0] == 686_606_336
+    gu8, dn8 = bench.algorithmic_bytes(H, I, "mxfp4", "a4w4", 0, 8, 1)
+    assert gu8 == 8 * gu and dn8 == 8 * I * 17 / 32 + 4 * H
+    assert bench.algorithmic_bytes(H, I, "mxfp4", "a4w4", 44, 64, 8)[0] == 686_606_336
     with pytest.raises(ValueError):
-        bench.algorithmic_bytes(H, I, "mxfp4", "w4a16", 1, 1)
+        bench.algorithmic_bytes(H, I, "mxfp4", "w4a16", 1, 1, 1)
