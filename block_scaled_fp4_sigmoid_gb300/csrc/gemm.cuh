@@ -13,7 +13,8 @@
 // (expert, 128-row weight tile, token tile); units of one expert are laid
 // out weight-tile-major so concurrent CTAs share each weight tile through L2.
 //
-// Warp roles (256 threads, one CTA per SM, persistent over units):
+// Warp roles (288 threads for gate/up, 256 for down; one CTA per SM,
+// persistent over units):
 //   warp 0     TMA producer: weight tiles (3-D tensor map over [E, rows,
 //              K/2], or over the tiled payload layout), token tiles (2-D map
 //              over the padded permuted rows), scale groups (bulk copies of
@@ -23,8 +24,10 @@
 //              K=64 MMAs per 256-wide K tile (gate/up: one A operand each;
 //              down: alternate K tiles into two accumulators), and commit the
 //              stage back to the producer;
-//   warp 7     gate/up: zeroes the combine buffer when asked; down: second
-//              TMA producer (the token tiles and their scale groups);
+//   warp 7     second TMA producer: the token tile (2-D map over the padded
+//              permuted rows) and its scale groups, once warp 0 has armed
+//              the stage;
+//   warp 8     gate/up only: zeroes the combine buffer when asked;
 //   warps 2-5  epilogue, one per tensor-memory lane quadrant:
 //              gate/up: SwiGLU, then MXFP4 requantisation of h across the
 //              32 lanes of a warp (= one 32-block along I), or (NVFP4) fp32
@@ -106,7 +109,7 @@ struct GemmCfg {
   // issuer copies its own A and B scale factors.
   static constexpr int kIssuers = 2;
   static constexpr bool kKSplit = !GATEUP;
-  static constexpr int kThreads = 256;  // warp 7: combine-buffer zeroing (gate/up) or second producer (down)
+  static constexpr int kThreads = GATEUP ? 288 : 256;  // warp 7: second producer; warp 8: combine-buffer zeroing
   static constexpr int kAccCols = 2 * N;                            // one accumulator set: two N-column blocks
   static constexpr int kSfCols = kIssuers * 2 * kAtoms * 4;         // scale factors of one K tile
   // two accumulator sets when they fit: the epilogue of one unit then
@@ -150,7 +153,7 @@ __device__ __forceinline__ void decode_unit(const int32_t* s_start, const int32_
 }
 
 template <int N, bool GATEUP, bool NV, int OP = kOpFp4>
-__global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant__ KParams p) {
+__global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_gemm_kernel(const __grid_constant__ KParams p) {
   using C = GemmCfg<N, GATEUP, NV, OP>;
   constexpr bool F8 = OP == kOpE4M3, BF = OP == kOpBf16, SF = OP == kOpFp4;
   static_assert(SF || !NV, "one operand format");
@@ -170,7 +173,6 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
 
   const int KT = (p.K + (BF ? 63 : F8 ? 127 : 255)) / (BF ? 64 : F8 ? 128 : 256);  // K tiles of 128 bytes
 
-  static_assert(C::kThreads == 256, "launch bounds");
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
@@ -296,11 +298,11 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
   volatile int* armed_v = &armed_steps;
   volatile int* first_done_v = &first_done;
 
-  // Down: a second thread (warp 7, idle in this kernel) issues the
-  // activation copies of every stage, so that one thread's issue time no
-  // longer paces the stages (measured: DeepSeek NVFP4 down 268 -> 240 us).
-  // Gate/up keeps one producer: its warp 7 zeroes the combine buffer.
-  constexpr bool kSplitProducer = !GATEUP;
+  // A second thread (warp 7) issues the activation copies of every stage:
+  // a thread is held ~90-140 cycles by each copy it issues, so one thread's
+  // issue time paced the stages (measured: DeepSeek NVFP4 down 268 -> 240
+  // us; gate/up, prefill 0.604 -> 0.590 ms and skewed 1.955 -> 1.846 ms).
+  constexpr bool kSplitProducer = true;
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -344,6 +346,7 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
         // prologue stages this loop did not reach (abort): the second
         // producer completes them, and they are waited on below
         for (int s2 = step; s2 < pre; ++s2) {
+          if (s2 == withheld) continue;
           armed |= 1u << s2;
           armed_par &= ~(1u << s2);  // first use: phase 0
         }
@@ -392,6 +395,7 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
         for (int u = blockIdx.x; u < total && ok && !*abort_v; u += gridDim.x) {
           const Step st = unit_step(u);
           for (int kt = 0; kt < KT; ++kt, ++step) {
+            if (step == withheld) continue;  // never armed
             if (!wait_armed(step)) { ok = false; break; }
             __threadfence_block();  // acquire: the stage's release precedes these copies
             const int stage = step % C::kStages;
@@ -414,11 +418,13 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
           for (int u = blockIdx.x; u < total && s2 < armed; u += gridDim.x) {
             const Step st = unit_step(u);
             for (int kt = 0; kt < KT && s2 < armed; ++kt, ++s2)
-              if (s2 >= step) load_acts(st, kt, sbase + (s2 % C::kStages) * C::kStage, smem_u32(&bar_full[s2 % C::kStages]));
+              if (s2 >= step && s2 != withheld)
+                load_acts(st, kt, sbase + (s2 % C::kStages) * C::kStage, smem_u32(&bar_full[s2 % C::kStages]));
           }
         }
       }
     }
+  } else if (warp == 8) {
     // ------------------------------------------------------------ zeroing
     // The combine buffer is read by the down GEMM, which starts after this
     // grid has completed; the writes overlap this kernel's MMAs.
