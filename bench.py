@@ -110,6 +110,22 @@ def profiled_traffic(workload: str):
     return float(m.group(1))
 
 
+def profiled_ratios(workload: str):
+    """DRAM bytes over algorithmic bytes of the two expert GEMMs, from the
+    committed ncu summary of a smaller case of the workload (its file names
+    the case), if it was taken on the current kernel source; else None.  A
+    launch's traffic grows with the bytes it must move (touched experts and
+    routes), so the ratio carries over to the full workload."""
+    for f in sorted((ROOT / "profiles").glob(f"ncu_gemm_{workload}*.md")):
+        text = f.read_text()
+        s = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+        g = re.search(r"dram_ratio_gateup:\s*([0-9.]+)", text)
+        d = re.search(r"dram_ratio_down:\s*([0-9.]+)", text)
+        if s and g and d and s.group(1) == source_sha(GEMM_SOURCES):
+            return {"gateup": float(g.group(1)), "down": float(d.group(1)), "from": f.name}
+    return None
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples during the timed region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -583,6 +599,11 @@ def config_record(cfg, layer, m: dict, peaks: dict, mode: str = "a4w4", w8a8: bo
     d = layer.dims
     work = layer_work(d.H, d.I, d.E, d.T, cfg.fmt, mode, m["touched"], m["routes"])
     kern = {"gateup": roofline(*work["gateup"], m["gu_ms"], peaks), "down": roofline(*work["down"], m["dn_ms"], peaks)}
+    ratios = profiled_ratios(cfg.name)
+    for k, r in kern.items():
+        r["traffic"] = r["algorithmic_bytes"] * ratios[k] if ratios else None
+        if ratios:
+            r["traffic_source"] = f"ncu DRAM bytes / algorithmic bytes of {ratios['from']}, times this launch's"
     dominant = max(kern, key=lambda k: kern[k]["ms"])
     return {"workload": cfg_label(cfg, w8a8, emulate), "ms_per_step": m["ms"], "tokens_per_s": d.T / (m["ms"] * 1e-3),
             "tflops": work["layer"][1] / (m["ms"] * 1e-3) / 1e12, "touched_experts": m["touched"],
