@@ -183,7 +183,7 @@ def configs() -> dict:
     skewed routing with a shared expert."""
     from pathlib import Path
     import json
-    beta_file = Path(__file__).resolve().parent.parent / "tests" / "golden" / "zipf_bias_beta.json"
+    beta_file = Path(__file__).resolve().parent / "zipf_bias_beta.json"  # written by tests/golden/make_zipf_beta.py
     beta = json.loads(beta_file.read_text())["beta"] if beta_file.exists() else 0.0
     return {
         "tiny": LayerConfig("tiny", T=4, H=256, I=128, E=8, top_k=2),

@@ -1,4 +1,4 @@
-"""Writes zipf_bias_beta.json: the strength beta of the Zipf-shaped correction
+"""Writes synth/zipf_bias_beta.json: the strength beta of the Zipf-shaped correction
 bias of the skewed-routing workload (T=16384, H=7168, E=384, top-8), found by
 bisection with the oracle's router so that the most popular expert receives
 8.0% +- 0.2% of the routed assignments.
@@ -55,7 +55,7 @@ def main():
            "share_curve_top16": [float(c / (cfg.T * cfg.top_k)) for c in top[:16]],
            "touched_experts": int(np.count_nonzero(counts)),
            "note": "written by tests/golden/make_zipf_beta.py with the oracle router"}
-    (Path(__file__).parent / "zipf_bias_beta.json").write_text(json.dumps(out, indent=1) + "\n")
+    (ROOT / "synth" / "zipf_bias_beta.json").write_text(json.dumps(out, indent=1) + "\n")
     print(json.dumps(out))
 
 
