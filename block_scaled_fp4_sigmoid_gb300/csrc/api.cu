@@ -35,6 +35,19 @@ bool dims_ok(const fp4moe_dims& d) {
   return true;
 }
 
+// Down GEMM of the MXFP4 layers with 112-token tiles: one unit covers two
+// slots (up to 224 tokens, N = 240 MMAs), twice the work per pipeline step,
+// with one MMA issuer (two accumulator sets of 240 columns fill tensor
+// memory).  A unit that stays within one slot then runs at half the issue
+// rate of the unpaired kernel's two issuers, so pairing pays only when most
+// units fill both slots: at >= 160 routes per expert on average (measured:
+// skewed 16k-token layer down -6%, 4k-token prefill at 85 routes per
+// expert +6%).  NVFP4's larger scale groups leave no room for two such
+// accumulator sets.
+int fp4_down_pair(int n_tile, bool nv, double routes_per_expert) {
+  return (n_tile == 112 && !nv && routes_per_expert >= 160.0) ? 2 : 1;
+}
+
 int pick_n_tile(const fp4moe_dims& d) {
   const double avg = (double)d.T * d.top_k / d.E;
   // Every size keeps two accumulator sets in tensor memory (the epilogue of
@@ -430,7 +443,8 @@ static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights*
                                             dbg ? dbg->scores : nullptr, cc, L.n_exp, s);
     if (e == cudaSuccess) e = rec(2);
     if (e == cudaSuccess)
-      e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, dn_mtiles, ecount, eslot, gu_start, dn_start, plan,
+      e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, fp4_down_pair(n_tile, nv, (double)d.T * d.top_k / d.E), dn_mtiles, ecount, eslot, gu_start,
+                      dn_start, plan,
                       status + ST_TICKET_PLAN, s);
     if (e == cudaSuccess)
       e = launch_scatter(d, idx, tw, cc, L.n_chunks, L.n_exp, n_tile, eslot, route_row, row_tok, row_w, row_e, s);
@@ -495,6 +509,7 @@ static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights*
     g.unit_start = dn_start;
     g.g_b = gscale + 2;  // g_h per expert
     g.out_acc = acc;
+    g.dn_pair = fp4_down_pair(n_tile, nv, (double)d.T * d.top_k / d.E);
     e = launch_down(g, s);
   }
   if (e == cudaSuccess) e = rec(6);
@@ -573,7 +588,7 @@ fp4moe_status fp4moe_forward_w8a8(const fp4moe_dims* dims, const fp4moe_fp8_weig
                                             dbg ? dbg->scores : nullptr, cc, L.n_exp, s);
   if (e == cudaSuccess) e = rec(2);
   if (e == cudaSuccess)
-    e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, d.H / 128, ecount, eslot, gu_start, dn_start, plan,
+    e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, 1, d.H / 128, ecount, eslot, gu_start, dn_start, plan,
                     status + ST_TICKET_PLAN, s);
   if (e == cudaSuccess)
     e = launch_scatter(d, idx, tw, cc, L.n_chunks, L.n_exp, n_tile, eslot, route_row, row_tok, row_w, row_e, s);
@@ -700,7 +715,7 @@ fp4moe_status fp4moe_forward_nvfp4_emulated(const fp4moe_dims* dims, const fp4mo
                                             dbg ? dbg->scores : nullptr, cc, L.n_exp, s);
   if (e == cudaSuccess) e = rec(2);
   if (e == cudaSuccess)
-    e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, d.H / 128, ecount, eslot, gu_start, dn_start, plan,
+    e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, 1, d.H / 128, ecount, eslot, gu_start, dn_start, plan,
                     status + ST_TICKET_PLAN, s);
   if (e == cudaSuccess)
     e = launch_scatter(d, idx, tw, cc, L.n_chunks, L.n_exp, n_tile, eslot, route_row, row_tok, row_w, row_e, s);
@@ -806,7 +821,8 @@ fp4moe_status fp4moe_linear(int32_t fmt, int32_t T, int32_t K, int32_t N, const 
   cudaError_t e = cudaMemsetAsync(status, 0, kStatusInts * 4, s);
   if (e == cudaSuccess && nv) e = cudaMemsetAsync(amax, 0, 8, s);
   if (e == cudaSuccess)
-    e = launch_linear_plan(T, n_tile, N / 128, ecount, eslot, dn_start, plan, route_row, row_tok, row_w, acc,
+    e = launch_linear_plan(T, n_tile, fp4_down_pair(n_tile, nv, T), N / 128, ecount, eslot, dn_start, plan, route_row,
+                           row_tok, row_w, acc,
                            (int64_t)T * N, s);
   if (e == cudaSuccess && nv) e = launch_amax(x, 0, (int64_t)T * K, amax, s);
   if (e == cudaSuccess) e = launch_gather_quant(dq, x, route_row, xq, xsf, amax, gscale, s);
@@ -832,6 +848,7 @@ fp4moe_status fp4moe_linear(int32_t fmt, int32_t T, int32_t K, int32_t N, const 
     g.g_b = gscale;  // NVFP4: g_x
     g.out_acc = acc;
     g.status = status;
+    g.dn_pair = fp4_down_pair(n_tile, nv, T);
     e = launch_down(g, s);
   }
   if (e == cudaSuccess) e = launch_finalize(acc, out, (int64_t)T * N, s);

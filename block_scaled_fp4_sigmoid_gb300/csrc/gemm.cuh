@@ -85,17 +85,30 @@ constexpr int kOpFp4 = 0, kOpE4M3 = 1, kOpBf16 = 2;
 
 template <int N, bool GATEUP, bool NV, int OP = kOpFp4>
 struct GemmCfg {
+  // N = 240 (MXFP4 down only): a unit covers two slots of the padded layout
+  // (two 112-token tiles of one expert), so each pipeline step carries
+  // twice the MMA work of a 112-token unit.  The B tile is two 112-row
+  // boxes at rows 0 and 128, so that B row r keeps the scale row r of the
+  // slots' 128-row scale groups; columns 112..127 hold stale rows the
+  // epilogue never reads.
+  static constexpr int kPairSlots = N == 240 ? 2 : 1;
+  static constexpr int kUnitRoutes = kPairSlots == 2 ? 224 : N;  // routes one unit covers
+  static_assert(kPairSlots == 1 || (!GATEUP && OP == kOpFp4), "paired slots: FP4 down GEMM only");
   static constexpr int kA = GATEUP ? 2 : 1;                // A operands per unit (gate and up)
   static constexpr int kAtoms = OP != kOpFp4 ? 0 : NV ? 4 : 2;  // scale groups per K tile
   static constexpr int kABytes = 128 * 128;          // 128 rows x 128 bytes
   static constexpr int kBBytes = N * 128;
   static constexpr int kSFBytes = kAtoms * 512;      // per 128-row operand and K tile
+  static constexpr int kSFBBytes = kSFBytes * kPairSlots;  // B side: one set per 128 rows of B
   static constexpr int kOffA1 = kABytes;
   static constexpr int kOffB = kA * kABytes;
   static constexpr int kOffSFA0 = kOffB + kBBytes;
   static constexpr int kOffSFA1 = kOffSFA0 + kSFBytes;
   static constexpr int kOffSFB = kOffSFA0 + kA * kSFBytes;
-  static constexpr int kStage = kOffSFB + kSFBytes;
+  static constexpr int kStage = kOffSFB + kSFBBytes;
+  // bytes the copies of one stage deliver (paired slots: two 112-row boxes
+  // into the 240-row B tile)
+  static constexpr int kTx = kStage - kBBytes + (kPairSlots == 2 ? 2 * 112 * 128 : kBBytes);
   // 227 KB per CTA = pipeline stages + 1 KB alignment slack + static shared
   // memory (epilogue transpose tiles 16.5 KB, plan cache 6 KB, barriers)
   static constexpr int kBudget = 232448 - 1024 - 24576;
@@ -107,16 +120,20 @@ struct GemmCfg {
   // (gate, up).  Down (one A operand): issuer i takes the K tiles kt with
   // kt % 2 == i into its own accumulator; the epilogue adds the two.  Each
   // issuer copies its own A and B scale factors.
-  static constexpr int kIssuers = 2;
-  static constexpr bool kKSplit = !GATEUP;
+  // (N = 240: one issuer; its instructions already carry twice the work.)
+  static constexpr int kIssuers = kPairSlots == 2 ? 1 : 2;
+  static constexpr bool kKSplit = !GATEUP && kIssuers == 2;
   static constexpr int kThreads = GATEUP ? 288 : 256;  // warp 7: second producer; warp 8: combine-buffer zeroing
-  static constexpr int kAccCols = 2 * N;                            // one accumulator set: two N-column blocks
-  static constexpr int kSfCols = kIssuers * 2 * kAtoms * 4;         // scale factors of one K tile
+  static constexpr int kAccCols = (GATEUP || kKSplit) ? 2 * N : N;  // one accumulator set: one N-column block per issuer
+  // scale-factor columns of one K tile: 4 per group of 4 blocks per 128
+  // rows (row r of a group at lane r % 32, column r / 32)
+  static constexpr int kSfColsA = kAtoms * 4, kSfColsB = kAtoms * 4 * kPairSlots;
+  static constexpr int kSfCols = kIssuers * (kSfColsA + kSfColsB);
   // two accumulator sets when they fit: the epilogue of one unit then
   // overlaps the MMAs of the next
   static constexpr int kAccStages = (2 * kAccCols + kSfCols <= 512) ? 2 : 1;
   static constexpr int kSfaCol = kAccStages * kAccCols;
-  static constexpr int kSfbCol = kSfaCol + kIssuers * kAtoms * 4;   // issuer i's A scales at kSfaCol + i * kAtoms * 4, B at kSfbCol + i * kAtoms * 4
+  static constexpr int kSfbCol = kSfaCol + kIssuers * kSfColsA;   // issuer i's A scales at kSfaCol + i * kSfColsA, B at kSfbCol + i * kSfColsB
   static constexpr int kCols = kSfaCol + kSfCols;
   static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
   static_assert(kCols <= 512, "tensor memory");
@@ -145,11 +162,12 @@ __device__ __forceinline__ void decode_unit(const int32_t* s_start, const int32_
   e = lo;
   const int local = u - s_start[e];
   const int count = s_count[e];
-  const int nt = (count + N - 1) / N;
+  constexpr int kCap = GemmCfg<N, false, false>::kUnitRoutes;
+  const int nt = (count + kCap - 1) / kCap;
   mt = local / nt;
   const int ti = local - mt * nt;
-  slot = s_slot[e] + ti;
-  cnt = min(N, count - ti * N);
+  slot = s_slot[e] + ti * GemmCfg<N, false, false>::kPairSlots;
+  cnt = min(kCap, count - ti * kCap);
 }
 
 template <int N, bool GATEUP, bool NV, int OP = kOpFp4>
@@ -224,6 +242,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
     const CUtensorMap* tmA;
     int ec, row0, row1, slot;
     bool once;  // the expert has one token tile: no other unit reads these weight tiles
+    bool two;   // paired slots: the unit's routes reach into its second slot
     const uint8_t *sfa0, *sfa1, *sfb;
   };
   auto unit_step = [&](int u) {
@@ -238,7 +257,8 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
     st.row0 = mt * 128;
     st.row1 = p.I + mt * 128;  // up rows (gate/up only)
     st.slot = p.tok_mask ? 0 : slot;  // slot of the B rows
-    st.once = s_count[e] <= N;
+    st.once = s_count[e] <= C::kUnitRoutes;
+    st.two = C::kPairSlots == 2 && cnt > 112;
     st.sfa0 = sfw + ((int64_t)(st.ec * rt_per_e + (st.row0 >> 7)) * p.katoms_a) * 512;
     st.sfa1 = sfw + ((int64_t)(st.ec * rt_per_e + (st.row1 >> 7)) * p.katoms_a) * 512;
     st.sfb = p.bsf + ((int64_t)st.slot * p.katoms_b) * 512;
@@ -274,8 +294,18 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
   auto load_acts = [&](const Step& st, int kt, uint32_t base, uint32_t fb) {
     tma_load_2d(base + C::kOffB, &p.tmB, fb, kt * 128, st.slot * kSlotRows);
     if constexpr (SF) bulk_load(base + C::kOffSFB, st.sfb + kt * C::kSFBytes, C::kSFBytes, fb);
+    if (st.two) {  // the unit's second slot: B rows 128..239 and their scale groups
+      tma_load_2d(base + C::kOffB + 128 * 128, &p.tmB, fb, kt * 128, (st.slot + 1) * kSlotRows);
+      bulk_load(base + C::kOffSFB + C::kSFBytes, st.sfb + (int64_t)p.katoms_b * 512 + kt * C::kSFBytes, C::kSFBytes,
+                fb);
+    }
   };
 
+  // bytes one stage of the unit receives (paired slots: the second slot's
+  // box and scale groups only when the unit reaches into it)
+  auto stage_tx = [&](const Step& st) -> uint32_t {
+    return (C::kPairSlots == 2 && !st.two) ? C::kTx - 112 * 128 - C::kSFBytes : C::kTx;
+  };
   // Test knob (gate/up): CTA 0 never fills pipeline step 0, so its MMA
   // issuer's wait for it runs out (KParams::withhold).
   const int withheld = (GATEUP && p.withhold && blockIdx.x == 0) ? 0 : -1;
@@ -288,7 +318,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
       for (int kt = 0; kt < KT && pre < C::kStages; ++kt, ++pre) {
         if (pre == withheld) continue;
         const uint32_t fb = smem_u32(&bar_full[pre]);
-        mbar_arrive_expect_tx(fb, C::kStage);  // stage is empty: first use
+        mbar_arrive_expect_tx(fb, stage_tx(st));  // stage is empty: first use
         load_weights(st, kt, sbase + pre * C::kStage, fb);
       }
     }
@@ -324,7 +354,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(fb, C::kStage);
+            mbar_arrive_expect_tx(fb, stage_tx(st));
             if constexpr (kSplitProducer) {  // the stage is free and armed (release to the second producer)
               __threadfence_block();
               *armed_v = step + 1;
@@ -433,14 +463,15 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
       for (int64_t i = (int64_t)blockIdx.x * 32 + lane; i < p.zero_n4; i += (int64_t)gridDim.x * 32) p.zero_buf[i] = z;
     }
   } else if (warp == 1 || warp == 6) {
+   if (warp == 1 || C::kIssuers == 2) {
     // ------------------------------------------------------------ MMA issuers
     // Issuer mi (warp 1 or 6) drives its MMAs into accumulator block mi.  The
     // whole warp runs the loop, so every operand (descriptors, tensor-memory
     // addresses) is warp-uniform; each tcgen05 instruction is issued by one
     // lane picked with elect.sync.
     const int mi = warp == 1 ? 0 : 1;
-    const uint32_t t_sfa = tmem + C::kSfaCol + mi * C::kAtoms * 4;
-    const uint32_t t_sfb = tmem + C::kSfbCol + mi * C::kAtoms * 4;
+    const uint32_t t_sfa = tmem + C::kSfaCol + mi * C::kSfColsA;
+    const uint32_t t_sfb = tmem + C::kSfbCol + mi * C::kSfColsB;
     const uint32_t off_a = (!C::kKSplit && mi) ? C::kOffA1 : 0u;
     const uint32_t off_sfa = (!C::kKSplit && mi) ? C::kOffSFA1 : C::kOffSFA0;
     // descriptors of stage 0; a stage s adds s * kStage / 16 to the start
@@ -459,6 +490,14 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
       bool ok = wait_w(smem_u32(&bar_tempty[as]), acc_phase ^ 1u);
       tc_fence_after();
       const uint32_t t_acc = tmem + as * C::kAccCols + mi * N;
+      // paired slots: a unit within its first slot multiplies 112 columns
+      bool two = true;
+      if constexpr (C::kPairSlots == 2) {
+        int e_, mt_, slot_, cnt_;
+        decode_unit<N>(s_start, s_count, s_slot, p.n_exp, u, e_, mt_, slot_, cnt_);
+        two = cnt_ > 112;
+      }
+      const uint32_t n_mma = two ? N : 112;
       for (int kt = 0; ok && kt < KT; ++kt) {
         if (C::kKSplit && (kt & 1) != mi) {  // the other issuer's K tile
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -471,7 +510,10 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
 #pragma unroll
         for (int a = 0; a < C::kAtoms; ++a) {
           tc_cp_sf_elect(t_sfa + 4 * a, sfa_desc0 + so + 32 * a);  // 512 bytes per scale group
-          tc_cp_sf_elect(t_sfb + 4 * a, sfb_desc0 + so + 32 * a);
+#pragma unroll
+          for (int h = 0; h < C::kPairSlots; ++h)  // B rows 128 h .. 128 h + 127: columns 4 h .. 4 h + 3 of the group
+            if (h == 0 || two)
+              tc_cp_sf_elect(t_sfb + 4 * C::kPairSlots * a + 4 * h, sfb_desc0 + so + 32 * a + h * (C::kSFBytes >> 4));
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {  // 32 bytes of the 128-byte swizzle row per MMA
@@ -483,9 +525,9 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
           } else {
             const int atom = NV ? j : (j >> 1);
             const uint32_t sfid = NV ? 0u : (uint32_t)(j & 1) * 2u;
-            const uint32_t idesc = idesc_fp4(N, NV, sfid, sfid);
+            const uint32_t idesc = idesc_fp4(n_mma, NV, sfid, sfid);
             tc_mma_fp4_elect<NV>(t_acc, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc, t_sfa + 4 * atom,
-                                 t_sfb + 4 * atom, accum);  // K = 64
+                                 t_sfb + 4 * C::kPairSlots * atom, accum);  // K = 64
           }
         }
         tc_commit_elect(smem_u32(&bar_empty[stage]));
@@ -503,6 +545,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
     // all issued MMAs must finish before tensor memory is released
     tc_commit_elect(smem_u32(&bar_done));
     (void)mbar_wait(smem_u32(&bar_done), 0);
+   }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // tensor-memory lane quadrant of this warp
@@ -614,10 +657,17 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
         float rho = 1.f;  // W8A8: channel scale of this lane's output row
         if constexpr (F8)
           rho = __ldg((e >= p.E ? p.shrs : p.wrs + (int64_t)e * p.rows_per_expert) + mt * 128 + 32 * q + lane);
-        for (int c0 = 0; c0 < cnt; c0 += 32) {
+        // the unit's routes: columns 0 .. cnt0 - 1 and (paired slots) 128 ..
+        // 128 + cnt1 - 1, column n holding row row0 + n
+        const int cnt0 = C::kPairSlots == 2 ? min(cnt, 112) : cnt;
+        const int cnt1 = cnt - cnt0;
+        const int ncol = cnt1 > 0 ? 128 + cnt1 : cnt0;
+        auto col_ok = [&](int n) { return n < cnt0 || (n >= 128 && n < ncol); };
+        for (int c0 = 0; c0 < ncol; c0 += 32) {
+          if (C::kPairSlots == 2 && c0 >= cnt0 && c0 < 128) continue;  // stale columns only (warp-uniform)
           float y[32];
-          tc_ld32(ta + c0, y);  // even K tiles
-          if (KT > 1) {         // odd K tiles (the second issuer's accumulator)
+          tc_ld32(ta + c0, y);  // even K tiles (all of them with one issuer)
+          if (C::kKSplit && KT > 1) {  // odd K tiles (the second issuer's accumulator)
             float y1[32];
             tc_ld32(ta + N + c0, y1);
             tc_wait_ld();
@@ -625,13 +675,13 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
             for (int j = 0; j < 32; ++j) y[j] += y1[j];
           }
           tc_wait_ld();
-          const int jn = min(32, cnt - c0);
           int tk = 0;
           float wk = 0.f;
-          if (lane < jn) {  // lane j fetches token and weight of column c0 + j
-            tk = __ldg(p.row_tok + row0 + c0 + lane);
-            wk = __ldg(p.row_w + row0 + c0 + lane) * sc;
-            if constexpr (F8) wk = __ldg(p.row_w + row0 + c0 + lane) * __ldg(p.brs + row0 + c0 + lane);
+          if (col_ok(c0 + lane)) {  // lane j fetches token and weight of column c0 + j
+            const int64_t rr = row0 + c0 + lane;
+            tk = __ldg(p.row_tok + rr);
+            wk = __ldg(p.row_w + rr) * sc;
+            if constexpr (F8) wk = __ldg(p.row_w + rr) * __ldg(p.brs + rr);
           }
 #pragma unroll
           for (int j = 0; j < 32; ++j) tile[j][lane] = F8 ? y[j] * rho : y[j];
@@ -641,7 +691,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
             const int j = (lane >> 3) + 4 * k;
             const int t = __shfl_sync(0xffffffffu, tk, j);
             const float w = __shfl_sync(0xffffffffu, wk, j);
-            if (j < jn) {
+            if (col_ok(c0 + j)) {
               const float* src = &tile[j][4 * (lane & 7)];
               red_add_v4(p.out_acc + (int64_t)t * p.H + h0, src[0] * w, src[1] * w, src[2] * w, src[3] * w);
             }

@@ -108,6 +108,12 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
       default: return cudaErrorInvalidValue;
     }
   }
+  if constexpr (!GATEUP) {
+    if (a.dn_pair == 2) {  // MXFP4, 112-token tiles: two slots per unit
+      if (a.n_tile != 112 || a.nv || a.f8 || a.bf) return cudaErrorInvalidValue;
+      return launch_gemm_t<240, false, false>(p, grid, s);
+    }
+  }
   switch (a.n_tile * 2 + (a.nv ? 1 : 0)) {
     case 32: return launch_gemm_t<16, GATEUP, false>(p, grid, s);  // few-token path (MXFP4)
     case 64: return launch_gemm_t<32, GATEUP, false>(p, grid, s);

@@ -56,13 +56,14 @@ cudaError_t launch_topk(const fp4moe_dims& d, const float* partial, int n_splits
                         int32_t* idx, float* w, float* logits_out, float* scores_out, int32_t* chunk_counts,
                         int n_exp, cudaStream_t s);
 // dn_mtiles: 128-column tiles of the layer output the down GEMM computes
-// (H / 128 for the whole output)
-cudaError_t launch_plan(const fp4moe_dims& d, int32_t* chunk_counts, int n_chunks, int n_exp, int n_tile,
+// (H / 128 for the whole output); dn_pair: tiles (slots) per down unit
+cudaError_t launch_plan(const fp4moe_dims& d, int32_t* chunk_counts, int n_chunks, int n_exp, int n_tile, int dn_pair,
                         int dn_mtiles, int32_t* expert_count, int32_t* expert_slot, int32_t* gu_start,
                         int32_t* dn_start, Plan* plan, int32_t* ticket, cudaStream_t s);
 // Dense linear: one expert holding every token in order, weight 1; zeroes acc
 // (acc_n floats, a multiple of 4)
-cudaError_t launch_linear_plan(int T, int n_tile, int m_tiles, int32_t* count, int32_t* slot, int32_t* dn_start,
+cudaError_t launch_linear_plan(int T, int n_tile, int dn_pair, int m_tiles, int32_t* count, int32_t* slot,
+                               int32_t* dn_start,
                                Plan* plan, int32_t* route_row, int32_t* row_tok, float* row_w, float* acc,
                                int64_t acc_n, cudaStream_t s);
 cudaError_t launch_scatter(const fp4moe_dims& d, const int32_t* idx, const float* w, const int32_t* chunk_counts,
@@ -166,6 +167,7 @@ struct GemmArgs {
   int32_t *status;
   uint64_t wait_ns;                // pipeline wait limit; 0: kWaitLimitNs
   bool withhold;                   // gate/up test knob (fp4moe_debug.withhold_first_stage)
+  int dn_pair;                     // down, 112-token tiles: 2 = one unit covers two slots (224 tokens)
   // W8A8: channel scales of the weights (routed [E, rows], shared [rows]),
   // scales of the B rows (per permuted row); amax_h is then per permuted row
   const float *wrs, *shrs, *brs;

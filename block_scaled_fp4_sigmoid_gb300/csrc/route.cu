@@ -230,12 +230,13 @@ __global__ void topk_kernel(const float* __restrict__ partial, int n_splits, con
 constexpr int kPlanWarps = 8;
 
 __global__ void __launch_bounds__(32 * kPlanWarps) plan_kernel(int32_t* chunk_counts, int n_chunks, int n_exp, int E,
-                                                                int T, int n_tile, int gu_mtiles, int dn_mtiles,
+                                                                int T, int n_tile, int dn_pair, int gu_mtiles,
+                                                                int dn_mtiles,
                                                                 int32_t* expert_count, int32_t* expert_slot,
                                                                 int32_t* gu_start, int32_t* dn_start, Plan* plan,
                                                                 int32_t* ticket) {
   __shared__ int s_last;
-  __shared__ int32_t s_wsum[kPlanWarps];
+  __shared__ long long s_wsum[kPlanWarps];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int e = blockIdx.x * kPlanWarps + wib;
   if (e < n_exp) {
@@ -267,43 +268,50 @@ __global__ void __launch_bounds__(32 * kPlanWarps) plan_kernel(int32_t* chunk_co
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // last CTA: exclusive scan of tiles over the experts (thread j owns experts
-  // 3j .. 3j + 2; n_exp <= 520 < 3 * 256)
+  // last CTA: exclusive scans over the experts of their tiles (slots) and
+  // of their down tiles (dn_pair slots each), both in one 64-bit scan (tiles
+  // low, down tiles high); thread j owns experts 3j .. 3j + 2 (n_exp <= 520
+  // < 3 * 256)
   constexpr int kT = 32 * kPlanWarps;
-  int tl[3], my = 0;
+  int tl[3], td[3];
+  long long my = 0;
 #pragma unroll
   for (int q = 0; q < 3; ++q) {
     const int ee = threadIdx.x * 3 + q;
-    tl[q] = ee < n_exp ? (__ldcg(expert_count + ee) + n_tile - 1) / n_tile : 0;
-    my += tl[q];
+    const int c = ee < n_exp ? __ldcg(expert_count + ee) : 0;
+    tl[q] = (c + n_tile - 1) / n_tile;
+    td[q] = (c + n_tile * dn_pair - 1) / (n_tile * dn_pair);
+    my += (long long)tl[q] + ((long long)td[q] << 32);
   }
-  int incl = my;
+  long long incl = my;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    const long long v = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += v;
   }
   if (lane == 31) s_wsum[wib] = incl;
   __syncthreads();
-  int base = incl - my;
-  for (int w2 = 0; w2 < wib; ++w2) base += s_wsum[w2];
+  long long b = incl - my;
+  for (int w2 = 0; w2 < wib; ++w2) b += s_wsum[w2];
+  int base = (int)(b & 0xffffffffll), base_d = (int)(b >> 32);
 #pragma unroll
   for (int q = 0; q < 3; ++q) {
     const int ee = threadIdx.x * 3 + q;
     if (ee < n_exp) {
       expert_slot[ee] = base;
       gu_start[ee] = base * gu_mtiles;
-      dn_start[ee] = base * dn_mtiles;
+      dn_start[ee] = base_d * dn_mtiles;
     }
     base += tl[q];
+    base_d += td[q];
   }
   if (threadIdx.x == kT - 1) {
-    const int total = base;  // the last thread's running sum covers every expert
+    const int total = base, total_d = base_d;  // the last thread's running sums cover every expert
     gu_start[n_exp] = total * gu_mtiles;
-    dn_start[n_exp] = total * dn_mtiles;
+    dn_start[n_exp] = total_d * dn_mtiles;
     plan->n_exp = n_exp;
     plan->gu_units = total * gu_mtiles;
-    plan->dn_units = total * dn_mtiles;
+    plan->dn_units = total_d * dn_mtiles;
     plan->slots = total;
   }
 }
@@ -683,20 +691,21 @@ __global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArg
 // The dense linear runs the down GEMM's mainloop with one "expert" that every
 // token routes to once with weight 1: token t sits at row (t / n_tile) * 128 +
 // t % n_tile of the padded layout.  Also zeroes the fp32 output accumulator.
-__global__ void linear_plan_kernel(int T, int n_tile, int m_tiles, int32_t* __restrict__ count,
+__global__ void linear_plan_kernel(int T, int n_tile, int dn_pair, int m_tiles, int32_t* __restrict__ count,
                                    int32_t* __restrict__ slot, int32_t* __restrict__ dn_start, Plan* __restrict__ plan,
                                    int32_t* __restrict__ route_row, int32_t* __restrict__ row_tok,
                                    float* __restrict__ row_w, float4* __restrict__ acc, int64_t acc_n4) {
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, nthr = (int64_t)gridDim.x * blockDim.x;
   const int tiles = (T + n_tile - 1) / n_tile;
+  const int tiles_d = (T + n_tile * dn_pair - 1) / (n_tile * dn_pair);
   if (tid == 0) {
     count[0] = T;
     slot[0] = 0;
     dn_start[0] = 0;
-    dn_start[1] = tiles * m_tiles;
+    dn_start[1] = tiles_d * m_tiles;
     plan->n_exp = 1;
     plan->gu_units = 0;
-    plan->dn_units = tiles * m_tiles;
+    plan->dn_units = tiles_d * m_tiles;
     plan->slots = tiles;
   }
   for (int64_t t = tid; t < T; t += nthr) {
@@ -733,11 +742,11 @@ cudaError_t launch_topk(const fp4moe_dims& d, const float* partial, int n_splits
   return cudaGetLastError();
 }
 
-cudaError_t launch_plan(const fp4moe_dims& d, int32_t* chunk_counts, int n_chunks, int n_exp, int n_tile,
+cudaError_t launch_plan(const fp4moe_dims& d, int32_t* chunk_counts, int n_chunks, int n_exp, int n_tile, int dn_pair,
                         int dn_mtiles, int32_t* expert_count, int32_t* expert_slot, int32_t* gu_start,
                         int32_t* dn_start, Plan* plan, int32_t* ticket, cudaStream_t s) {
   const unsigned blocks = (unsigned)((n_exp + kPlanWarps - 1) / kPlanWarps);
-  plan_kernel<<<blocks, 32 * kPlanWarps, 0, s>>>(chunk_counts, n_chunks, n_exp, d.E, d.T, n_tile, d.I / 128,
+  plan_kernel<<<blocks, 32 * kPlanWarps, 0, s>>>(chunk_counts, n_chunks, n_exp, d.E, d.T, n_tile, dn_pair, d.I / 128,
                                                  dn_mtiles, expert_count, expert_slot, gu_start, dn_start, plan,
                                                  ticket);
   return cudaGetLastError();
@@ -780,10 +789,10 @@ cudaError_t launch_decode_front(const FrontArgs& a, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, decode_front_kernel, a);
 }
 
-cudaError_t launch_linear_plan(int T, int n_tile, int m_tiles, int32_t* count, int32_t* slot, int32_t* dn_start,
+cudaError_t launch_linear_plan(int T, int n_tile, int dn_pair, int m_tiles, int32_t* count, int32_t* slot, int32_t* dn_start,
                                Plan* plan, int32_t* route_row, int32_t* row_tok, float* row_w, float* acc,
                                int64_t acc_n, cudaStream_t s) {
-  linear_plan_kernel<<<4 * 152, 256, 0, s>>>(T, n_tile, m_tiles, count, slot, dn_start, plan, route_row, row_tok,
+  linear_plan_kernel<<<4 * 152, 256, 0, s>>>(T, n_tile, dn_pair, m_tiles, count, slot, dn_start, plan, route_row, row_tok,
                                             row_w, reinterpret_cast<float4*>(acc), acc_n / 4);
   return cudaGetLastError();
 }
