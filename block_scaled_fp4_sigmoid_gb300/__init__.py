@@ -67,7 +67,7 @@ class Debug(ctypes.Structure):
     scores, the pipeline wait limit and the timeout test knob."""
     _fields_ = [("events", ctypes.c_void_p * 8), ("h_pre", ctypes.c_void_p), ("logits", ctypes.c_void_p),
                 ("scores", ctypes.c_void_p), ("wait_limit_ns", ctypes.c_int64),
-                ("withhold_first_stage", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("withhold_first_stage", ctypes.c_int32), ("down_cta_pair", ctypes.c_int32)]
 
 
 _LIB = None

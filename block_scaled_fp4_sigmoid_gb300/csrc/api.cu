@@ -48,6 +48,17 @@ int fp4_down_pair(int n_tile, bool nv, double routes_per_expert) {
   return (n_tile == 112 && !nv && routes_per_expert >= 160.0) ? 2 : 1;
 }
 
+// Paired-slot down units over an output range of a multiple of 256 rows can
+// run on CTA pairs (M = 256 MMAs issued by one CTA for two SMs, half the
+// tcgen05 instructions per FLOP); their units then count 256-row tiles.  An
+// opt-in (fp4moe_debug::down_cta_pair): measured on GB300, the pair's MMAs
+// and scale copies each hold the issuing thread ~90 cycles against ~60 for
+// one CTA's, so the pair's K tile (1444 cycles) is slower than two single
+// CTAs' (1046): skewed 16k-token down 1.75 -> 2.16 ms.
+bool fp4_down_cta_pair(int dn_pair, int out_rows, const fp4moe_debug* dbg) {
+  return dbg && dbg->down_cta_pair && dn_pair == 2 && out_rows % 256 == 0;
+}
+
 int pick_n_tile(const fp4moe_dims& d) {
   const double avg = (double)d.T * d.top_k / d.E;
   // Every size keeps two accumulator sets in tensor memory (the epilogue of
@@ -335,10 +346,12 @@ static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights*
   if (!make_layout(d, &L)) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
   if (h_begin < 0 || h_end > d.H || h_begin >= h_end || h_begin % 128 != 0 || h_end % 128 != 0)
     return FP4MOE_ERR_UNSUPPORTED_SHAPE;
-  const int dn_mtiles = (h_end - h_begin) / 128;
   if (d.fmt == FP4MOE_FP8) return FP4MOE_ERR_INVALID_ARG;  // fp4moe_forward_w8a8
   if (ws_bytes < (size_t)L.ws.total_bytes) return FP4MOE_ERR_WORKSPACE;
   const bool nv = d.fmt == FP4MOE_NVFP4;
+  const int dn_pair = fp4_down_pair(L.ws.n_tile, nv, (double)d.T * d.top_k / d.E);
+  const bool dn_cta = fp4_down_cta_pair(dn_pair, h_end - h_begin, dbg);
+  const int dn_mtiles = (h_end - h_begin) / (dn_cta ? 256 : 128);  // weight-row tiles per down unit row
   if (!w->w13 || !w->w13_scale || !w->w2 || !w->w2_scale || !w->w_router || !w->bias) return FP4MOE_ERR_INVALID_ARG;
   if (nv && (!w->g13 || !w->g2)) return FP4MOE_ERR_INVALID_ARG;
   if (d.n_shared && (!w->sh13 || !w->sh13_scale || !w->sh2 || !w->sh2_scale)) return FP4MOE_ERR_INVALID_ARG;
@@ -427,7 +440,7 @@ static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights*
       const int64_t n[4] = {
           w->packed ? (int64_t)fp4moe_packed_weights_bytes(1, 2 * d.I, d.H / 2) : (int64_t)d.I * d.H,
           (int64_t)fp4moe_packed_scales_bytes(1, 2 * d.I, d.H / 32, d.fmt), (h_end - h_begin) * w2_row,
-          (int64_t)dn_mtiles * w2_sf_tile};
+          (int64_t)((h_end - h_begin) / 128) * w2_sf_tile};
       for (int i = 0; i < 4; ++i) {
         f.l2_pf[i] = r[i];
         f.l2_pf_bytes[i] = n[i];
@@ -443,8 +456,7 @@ static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights*
                                             dbg ? dbg->scores : nullptr, cc, L.n_exp, s);
     if (e == cudaSuccess) e = rec(2);
     if (e == cudaSuccess)
-      e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, fp4_down_pair(n_tile, nv, (double)d.T * d.top_k / d.E), dn_mtiles, ecount, eslot, gu_start,
-                      dn_start, plan,
+      e = launch_plan(d, cc, L.n_chunks, L.n_exp, n_tile, dn_pair, dn_mtiles, ecount, eslot, gu_start, dn_start, plan,
                       status + ST_TICKET_PLAN, s);
     if (e == cudaSuccess)
       e = launch_scatter(d, idx, tw, cc, L.n_chunks, L.n_exp, n_tile, eslot, route_row, row_tok, row_w, row_e, s);
@@ -509,7 +521,8 @@ static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights*
     g.unit_start = dn_start;
     g.g_b = gscale + 2;  // g_h per expert
     g.out_acc = acc;
-    g.dn_pair = fp4_down_pair(n_tile, nv, (double)d.T * d.top_k / d.E);
+    g.dn_pair = dn_pair;
+    g.dn_cta_pair = dn_cta;
     e = launch_down(g, s);
   }
   if (e == cudaSuccess) e = rec(6);
@@ -817,13 +830,14 @@ fp4moe_status fp4moe_linear(int32_t fmt, int32_t T, int32_t K, int32_t N, const 
   uint32_t* amax = reinterpret_cast<uint32_t*>(P(L.amax));
   float* acc = reinterpret_cast<float*>(P(L.ws.out_acc));
   const int n_tile = L.ws.n_tile;
+  const int dn_pair = fp4_down_pair(n_tile, nv, T);
+  const bool dn_cta = fp4_down_cta_pair(dn_pair, N, nullptr);
 
   cudaError_t e = cudaMemsetAsync(status, 0, kStatusInts * 4, s);
   if (e == cudaSuccess && nv) e = cudaMemsetAsync(amax, 0, 8, s);
   if (e == cudaSuccess)
-    e = launch_linear_plan(T, n_tile, fp4_down_pair(n_tile, nv, T), N / 128, ecount, eslot, dn_start, plan, route_row,
-                           row_tok, row_w, acc,
-                           (int64_t)T * N, s);
+    e = launch_linear_plan(T, n_tile, dn_pair, N / (dn_cta ? 256 : 128), ecount, eslot, dn_start, plan, route_row,
+                           row_tok, row_w, acc, (int64_t)T * N, s);
   if (e == cudaSuccess && nv) e = launch_amax(x, 0, (int64_t)T * K, amax, s);
   if (e == cudaSuccess) e = launch_gather_quant(dq, x, route_row, xq, xsf, amax, gscale, s);
   if (e == cudaSuccess) {
@@ -848,7 +862,8 @@ fp4moe_status fp4moe_linear(int32_t fmt, int32_t T, int32_t K, int32_t N, const 
     g.g_b = gscale;  // NVFP4: g_x
     g.out_acc = acc;
     g.status = status;
-    g.dn_pair = fp4_down_pair(n_tile, nv, T);
+    g.dn_pair = dn_pair;
+    g.dn_cta_pair = dn_cta;
     e = launch_down(g, s);
   }
   if (e == cudaSuccess) e = launch_finalize(acc, out, (int64_t)T * N, s);

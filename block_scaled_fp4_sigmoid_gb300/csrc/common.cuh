@@ -69,25 +69,39 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// kCluster: acquire at cluster scope (arrivals released by the other CTA of
+// a pair).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (kCluster) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 
 // Waits until the phase with the given parity has completed.  Gives up after
 // kWaitLimitNs and returns false; the caller records the timeout and unwinds.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<kCluster>(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kCluster>(bar, parity)) return true;
     if ((i & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
   }
 }
@@ -97,12 +111,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 // never complete).  Returns false on either; only waits whose arrivals
 // depend on other roles use it.  Drains of copies already issued keep
 // mbar_wait: those copies always land.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_abortable(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                                     const volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<kCluster>(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kCluster>(bar, parity)) return true;
     if ((i & 255u) == 0 && (*abort || globaltimer() - t0 > limit_ns)) return false;
   }
 }
@@ -243,6 +258,67 @@ __device__ __forceinline__ void tc_mma_fp4_elect(uint32_t d, uint64_t a, uint64_
   }
 }
 
+// ---------------------------------------------------------------- CTA pairs
+// A cluster of two CTAs on two SMs shares one M = 256 block-scaled MMA
+// (tcgen05 .cta_group::2): rank 0 issues it, each CTA supplies half of A
+// (its 128 rows) and half of B (N / 2 rows) from the same shared-memory
+// offsets, and each CTA's tensor memory holds its own 128 accumulator lanes
+// and scale factors at the same addresses.  Every tcgen05 allocation, copy,
+// MMA and commit of such a kernel uses .cta_group::2.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_arrive_wait() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void fence_barrier_init_cluster() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// Arrive (release, cluster scope) on the barrier at the same shared-memory
+// offset in CTA `rank` of this cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t rank) {
+  asm volatile(
+      "{\n\t.reg .b32 ra;\n\tmapa.shared::cluster.u32 ra, %0, %1;\n\t"
+      "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(bar), "r"(rank)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols));
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+// Arrives on the barrier at this offset in every CTA of cta_mask once the
+// pair MMAs and copies issued so far by this thread have completed.
+__device__ __forceinline__ void tc_commit_pair_elect(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
+      "@p tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+// Scale factors into both CTAs' tensor memory, each from its own shared memory.
+__device__ __forceinline__ void tc_cp_sf_pair_elect(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
+      "@p tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr), "l"(sdesc)
+      : "memory");
+}
+// MXFP4 (E8M0 per 32) MMA with M = 256 over the CTA pair.
+__device__ __forceinline__ void tc_mma_mx_pair_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                                     uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\telect.sync _|p, 0xffffffff;\n\tsetp.ne.b32 q, %6, 0;\n\t"
+      "@p tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], q;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
 // E4M3 x E4M3 MMA (kind::f8f6f4, K = 32 per instruction), fp32 accumulate,
 // issued by one elected lane of the calling warp.
 __device__ __forceinline__ void tc_mma_f8_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
@@ -297,15 +373,16 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 }
 
 // Instruction descriptor of a block-scaled FP4 MMA: E2M1 x E2M1, K-major A and
-// B, M = 128, N = n, scale type E8M0 (MXFP4) or E4M3 (NVFP4), scale-factor
+// B, M = m, N = n, scale type E8M0 (MXFP4) or E4M3 (NVFP4), scale-factor
 // byte ids for A and B.
-__host__ __device__ constexpr uint32_t idesc_fp4(uint32_t n, bool nv, uint32_t sfa_id, uint32_t sfb_id) {
+__host__ __device__ constexpr uint32_t idesc_fp4(uint32_t n, bool nv, uint32_t sfa_id, uint32_t sfb_id,
+                                                 uint32_t m = 128) {
   return (sfb_id & 3u) << 4        // B scale-factor id
          | 1u << 7                 // A format: E2M1
          | 1u << 10                // B format: E2M1
          | (n >> 3) << 17          // N / 8
          | (nv ? 0u : 1u) << 23    // scale format: 0 = UE4M3, 1 = UE8M0
-         | (128u >> 4) << 24       // M / 16
+         | (m >> 4) << 24          // M / 16 (256: a CTA pair)
          | (sfa_id & 3u) << 29;    // A scale-factor id
 }
 

@@ -83,7 +83,9 @@ struct KParams {
 // 128-byte swizzle row per operand row, consumed by four MMAs of 32 bytes.
 constexpr int kOpFp4 = 0, kOpE4M3 = 1, kOpBf16 = 2;
 
-template <int N, bool GATEUP, bool NV, int OP = kOpFp4>
+constexpr int kMaxExperts = 520;  // plan arrays cached in shared memory (E + n_shared <= 513)
+
+template <int N, bool GATEUP, bool NV, int OP = kOpFp4, bool PAIR = false>
 struct GemmCfg {
   // N = 240 (MXFP4 down only): a unit covers two slots of the padded layout
   // (two 112-token tiles of one expert), so each pipeline step carries
@@ -94,10 +96,19 @@ struct GemmCfg {
   static constexpr int kPairSlots = N == 240 ? 2 : 1;
   static constexpr int kUnitRoutes = kPairSlots == 2 ? 224 : N;  // routes one unit covers
   static_assert(kPairSlots == 1 || (!GATEUP && OP == kOpFp4), "paired slots: FP4 down GEMM only");
+  // PAIR: a cluster of two CTAs runs each unit as M = 256 MMAs (tcgen05
+  // .cta_group::2): CTA r of the pair holds weight rows 128 r .. 128 r + 127
+  // of the unit's 256 and B rows 120 r .. 120 r + 119 of the 240: CTA 0 the
+  // first slot's tokens at its rows 0..111, CTA 1 the second slot's at its
+  // rows 8..119 (B rows 128..239, matching the scale rows of the second
+  // slot's scale group).  Both CTAs hold both slots' B scale groups, as each
+  // SM's half of the MMA scales all 240 columns.
+  static_assert(!PAIR || (N == 240 && !GATEUP && !NV && OP == kOpFp4), "CTA pair: MXFP4 down GEMM with paired slots");
+  static constexpr int kBRows = PAIR ? N / 2 : N;  // B rows in this CTA's shared memory
   static constexpr int kA = GATEUP ? 2 : 1;                // A operands per unit (gate and up)
   static constexpr int kAtoms = OP != kOpFp4 ? 0 : NV ? 4 : 2;  // scale groups per K tile
   static constexpr int kABytes = 128 * 128;          // 128 rows x 128 bytes
-  static constexpr int kBBytes = N * 128;
+  static constexpr int kBBytes = kBRows * 128;
   static constexpr int kSFBytes = kAtoms * 512;      // per 128-row operand and K tile
   static constexpr int kSFBBytes = kSFBytes * kPairSlots;  // B side: one set per 128 rows of B
   static constexpr int kOffA1 = kABytes;
@@ -109,9 +120,16 @@ struct GemmCfg {
   // bytes the copies of one stage deliver (paired slots: two 112-row boxes
   // into the 240-row B tile)
   static constexpr int kTx = kStage - kBBytes + (kPairSlots == 2 ? 2 * 112 * 128 : kBBytes);
+  // Epilogue warps: one per tensor-memory lane quadrant, or (down GEMM with
+  // 64 or more token columns) two per quadrant, splitting the unit's 32-column
+  // chunks between them.  Gate/up transposes through shared memory (one
+  // 32 x 33 fp32 tile per epilogue warp); down transposes in registers.
+  static constexpr int kEpiWarps = (!GATEUP && N >= 64) ? 8 : 4;
+  static constexpr int kEpiTiles = GATEUP ? 4 : 1;
   // 227 KB per CTA = pipeline stages + 1 KB alignment slack + static shared
-  // memory (epilogue transpose tiles 16.5 KB, plan cache 6 KB, barriers)
-  static constexpr int kBudget = 232448 - 1024 - 24576;
+  // memory (epilogue transpose tiles, plan cache, barriers and flags)
+  static constexpr int kStaticBytes = kEpiTiles * 32 * 33 * 4 + 4 * 4 * kMaxExperts + 512;
+  static constexpr int kBudget = 232448 - 1024 - kStaticBytes;
   static constexpr int kStages = (kBudget / kStage) > 8 ? 8 : (kBudget / kStage);
   static constexpr int kSmem = kStages * kStage + 1024;
   // Two MMA-issuing threads (warps 1 and 6): a thread issues a tcgen05
@@ -121,9 +139,11 @@ struct GemmCfg {
   // kt % 2 == i into its own accumulator; the epilogue adds the two.  Each
   // issuer copies its own A and B scale factors.
   // (N = 240: one issuer; its instructions already carry twice the work.)
-  static constexpr int kIssuers = kPairSlots == 2 ? 1 : 2;
+  static constexpr int kIssuers = kPairSlots == 2 ? 1 : 2;  // (CTA pair: in CTA 0 only)
   static constexpr bool kKSplit = !GATEUP && kIssuers == 2;
-  static constexpr int kThreads = GATEUP ? 288 : 256;  // warp 7: second producer; warp 8: combine-buffer zeroing
+  // warp 7: second producer; gate/up warp 8: combine-buffer zeroing; down
+  // with eight epilogue warps: warps 8-11 are the second four
+  static constexpr int kThreads = GATEUP ? 288 : kEpiWarps == 8 ? 384 : 256;
   static constexpr int kAccCols = (GATEUP || kKSplit) ? 2 * N : N;  // one accumulator set: one N-column block per issuer
   // scale-factor columns of one K tile: 4 per group of 4 blocks per 128
   // rows (row r of a group at lane r % 32, column r / 32)
@@ -139,13 +159,11 @@ struct GemmCfg {
   static_assert(kCols <= 512, "tensor memory");
   static_assert(kStage % 1024 == 0, "stage alignment");
   static_assert(kStages >= 2, "pipeline depth");
-  static_assert(kStages * kStage + 1024 + 24576 <= 232448, "shared memory per CTA");
+  static_assert(kStages * kStage + 1024 + kStaticBytes <= 232448, "shared memory per CTA");
 };
 
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) { return smem_desc(saddr, 16, 1024, 2); }
 __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) { return smem_desc(saddr, 0, 128, 0); }
-
-constexpr int kMaxExperts = 520;  // plan arrays cached in shared memory (E + n_shared <= 513)
 
 // Unit u -> (expert, weight tile, token-tile slot, tokens in the tile), from
 // the plan cached in shared memory: the expert is the last one whose first
@@ -170,16 +188,18 @@ __device__ __forceinline__ void decode_unit(const int32_t* s_start, const int32_
   cnt = min(kCap, count - ti * kCap);
 }
 
-template <int N, bool GATEUP, bool NV, int OP = kOpFp4>
-__global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_gemm_kernel(const __grid_constant__ KParams p) {
-  using C = GemmCfg<N, GATEUP, NV, OP>;
+template <int N, bool GATEUP, bool NV, int OP = kOpFp4, bool PAIR = false>
+__global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ KParams p) {
+  using C = GemmCfg<N, GATEUP, NV, OP, PAIR>;
   constexpr bool F8 = OP == kOpE4M3, BF = OP == kOpBf16, SF = OP == kOpFp4;
   static_assert(SF || !NV, "one operand format");
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[C::kStages];
   __shared__ __align__(8) uint64_t bar_empty[C::kStages];
   __shared__ __align__(8) uint64_t bar_tfull[2], bar_tempty[2], bar_done;
-  __shared__ float epi_tile[4][32][33];  // per epilogue warp: 32 lanes x 32 columns, transposed
+  __shared__ __align__(8) uint64_t bar_pfull[PAIR ? C::kStages : 1];  // CTA pair, CTA 0: the peer's stage has landed
+  __shared__ float epi_tile[C::kEpiTiles][32][33];  // gate/up, per epilogue warp: 32 lanes x 32 columns, transposed
   __shared__ int32_t s_start[kMaxExperts], s_count[kMaxExperts], s_slot[kMaxExperts];
   __shared__ uint32_t s_mask[kMaxExperts];
   __shared__ uint32_t tmem_slot;
@@ -188,6 +208,11 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CTA pair: rank in the pair (0 issues the MMAs); both CTAs of a pair run
+  // the same units
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+  const int u_first = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int u_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   const int KT = (p.K + (BF ? 63 : F8 ? 127 : 255)) / (BF ? 64 : F8 ? 128 : 256);  // K tiles of 128 bytes
 
@@ -195,20 +220,27 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
       mbar_init(smem_u32(&bar_empty[s]), C::kKSplit ? 1 : C::kIssuers);  // the issuers that read the stage
+      if constexpr (PAIR) mbar_init(smem_u32(&bar_pfull[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&bar_tfull[a]), C::kIssuers);
-      mbar_init(smem_u32(&bar_tempty[a]), 4);
+      mbar_init(smem_u32(&bar_tempty[a]), C::kEpiWarps * (PAIR ? 2 : 1));  // (pair: both CTAs' epilogues)
     }
     mbar_init(smem_u32(&bar_done), C::kIssuers);
     abort_flag = 0;
     armed_steps = 0;
     first_done = 0;
-    fence_barrier_init();
+    if constexpr (PAIR) fence_barrier_init_cluster();
+    else fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {  // both CTAs allocate the pair's columns together
+      tmem_alloc_pair(smem_u32(&tmem_slot), C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&p.tmA);
@@ -231,7 +263,8 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
     }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_arrive_wait();  // the peer's barriers are initialised before any remote arrive
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort_v = &abort_flag;
@@ -254,7 +287,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
     st.ec = sh ? e - p.E : e;
     const uint8_t* sfw = sh ? p.shsf : p.wsf;
     const int rt_per_e = p.rows_per_expert >> 7;
-    st.row0 = mt * 128;
+    st.row0 = PAIR ? mt * 256 + (int)crank * 128 : mt * 128;  // (pair: mt counts 256-row tiles)
     st.row1 = p.I + mt * 128;  // up rows (gate/up only)
     st.slot = p.tok_mask ? 0 : slot;  // slot of the B rows
     st.once = s_count[e] <= C::kUnitRoutes;
@@ -292,6 +325,15 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
     }
   };
   auto load_acts = [&](const Step& st, int kt, uint32_t base, uint32_t fb) {
+    if constexpr (PAIR) {  // this CTA's slot box, and both slots' scale groups
+      if (crank == 0) tma_load_2d(base + C::kOffB, &p.tmB, fb, kt * 128, st.slot * kSlotRows);
+      else if (st.two) tma_load_2d(base + C::kOffB + 8 * 128, &p.tmB, fb, kt * 128, (st.slot + 1) * kSlotRows);
+      bulk_load(base + C::kOffSFB, st.sfb + kt * C::kSFBytes, C::kSFBytes, fb);
+      if (st.two)
+        bulk_load(base + C::kOffSFB + C::kSFBytes, st.sfb + (int64_t)p.katoms_b * 512 + kt * C::kSFBytes, C::kSFBytes,
+                  fb);
+      return;
+    }
     tma_load_2d(base + C::kOffB, &p.tmB, fb, kt * 128, st.slot * kSlotRows);
     if constexpr (SF) bulk_load(base + C::kOffSFB, st.sfb + kt * C::kSFBytes, C::kSFBytes, fb);
     if (st.two) {  // the unit's second slot: B rows 128..239 and their scale groups
@@ -304,6 +346,8 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
   // bytes one stage of the unit receives (paired slots: the second slot's
   // box and scale groups only when the unit reaches into it)
   auto stage_tx = [&](const Step& st) -> uint32_t {
+    if constexpr (PAIR)
+      return C::kABytes + C::kSFBytes + ((crank == 0 || st.two) ? 112 * 128 : 0) + (st.two ? 2 : 1) * C::kSFBytes;
     return (C::kPairSlots == 2 && !st.two) ? C::kTx - 112 * 128 - C::kSFBytes : C::kTx;
   };
   // Test knob (gate/up): CTA 0 never fills pipeline step 0, so its MMA
@@ -313,7 +357,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
   // they overlap the tail of the previous kernel.
   int pre = 0;
   if (warp == 0 && lane == 0) {
-    for (int u = blockIdx.x; u < total && pre < C::kStages; u += gridDim.x) {
+    for (int u = u_first; u < total && pre < C::kStages; u += u_step) {
       const Step st = unit_step(u);
       for (int kt = 0; kt < KT && pre < C::kStages; ++kt, ++pre) {
         if (pre == withheld) continue;
@@ -339,7 +383,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
       if constexpr (kSplitProducer) *armed_v = pre;
       int stage = 0, step = 0;
       uint32_t phase = 0, armed = 0, armed_par = 0;
-      for (int u = blockIdx.x; u < total && !*abort_v; u += gridDim.x) {
+      for (int u = u_first; u < total && !*abort_v; u += u_step) {
         const Step st = unit_step(u);
         bool ok = true;
         for (int kt = 0; kt < KT; ++kt, ++step) {
@@ -350,7 +394,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
             continue;
           }
           if (step >= pre) {
-            if (!mbar_wait_abortable(smem_u32(&bar_empty[stage]), phase ^ 1u, p.wait_ns, abort_v)) {
+            if (!mbar_wait_abortable<PAIR>(smem_u32(&bar_empty[stage]), phase ^ 1u, p.wait_ns, abort_v)) {
               ok = false;
               break;
             }
@@ -388,7 +432,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
       // their barriers complete (split: the second producer does it)
       if (!kSplitProducer && step < pre) {
         int s2 = 0;
-        for (int u = blockIdx.x; u < total && s2 < pre; u += gridDim.x) {
+        for (int u = u_first; u < total && s2 < pre; u += u_step) {
           const Step st = unit_step(u);
           for (int kt = 0; kt < KT && s2 < pre; ++kt, ++s2)
             if (s2 >= step && s2 != withheld) {
@@ -400,7 +444,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
       }
       // every armed stage must have landed before the CTA exits
       for (int s = 0; s < C::kStages; ++s)
-        if ((armed >> s) & 1u) (void)mbar_wait(smem_u32(&bar_full[s]), (armed_par >> s) & 1u);
+        if ((armed >> s) & 1u) (void)mbar_wait<PAIR>(smem_u32(&bar_full[s]), (armed_par >> s) & 1u);
     }
   } else if (warp == 7) {
     if constexpr (kSplitProducer) {
@@ -422,7 +466,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
         };
         int step = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < total && ok && !*abort_v; u += gridDim.x) {
+        for (int u = u_first; u < total && ok && !*abort_v; u += u_step) {
           const Step st = unit_step(u);
           for (int kt = 0; kt < KT; ++kt, ++step) {
             if (step == withheld) continue;  // never armed
@@ -445,7 +489,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
           __threadfence_block();
           const int armed = *armed_v;
           int s2 = 0;
-          for (int u = blockIdx.x; u < total && s2 < armed; u += gridDim.x) {
+          for (int u = u_first; u < total && s2 < armed; u += u_step) {
             const Step st = unit_step(u);
             for (int kt = 0; kt < KT && s2 < armed; ++kt, ++s2)
               if (s2 >= step && s2 != withheld)
@@ -454,7 +498,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
         }
       }
     }
-  } else if (warp == 8) {
+  } else if (GATEUP && warp == 8) {
     // ------------------------------------------------------------ zeroing
     // The combine buffer is read by the down GEMM, which starts after this
     // grid has completed; the writes overlap this kernel's MMAs.
@@ -463,7 +507,31 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
       for (int64_t i = (int64_t)blockIdx.x * 32 + lane; i < p.zero_n4; i += (int64_t)gridDim.x * 32) p.zero_buf[i] = z;
     }
   } else if (warp == 1 || warp == 6) {
-   if (warp == 1 || C::kIssuers == 2) {
+   if (PAIR && crank == 1) {
+    if (warp == 1) {
+      // ---------------------------------------------------------- pair relay
+      // CTA 1 of a pair: once a stage of this CTA has landed, tell CTA 0's
+      // issuer (its MMAs read this CTA's half of the operands).
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = u_first; ok && u < total && !__any_sync(0xffffffffu, *abort_v); u += u_step) {
+        for (int kt = 0; kt < KT; ++kt) {
+          if (!__all_sync(0xffffffffu, mbar_wait_abortable<PAIR>(smem_u32(&bar_full[stage]), phase, p.wait_ns, abort_v))) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive_remote(smem_u32(&bar_pfull[stage]), 0u);
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        if (lane == 0 && !*abort_v) record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
+        __syncwarp();
+        *abort_v = 1;
+      }
+    }
+   } else if (warp == 1 || C::kIssuers == 2) {
     // ------------------------------------------------------------ MMA issuers
     // Issuer mi (warp 1 or 6) drives its MMAs into accumulator block mi.  The
     // whole warp runs the loop, so every operand (descriptors, tensor-memory
@@ -481,12 +549,12 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
     const uint64_t sfa_desc0 = desc_sf(sbase + off_sfa), sfb_desc0 = desc_sf(sbase + C::kOffSFB);
     // bounded wait with a warp-uniform outcome
     auto wait_w = [&](uint32_t bar, uint32_t par) {
-      return __all_sync(0xffffffffu, mbar_wait_abortable(bar, par, p.wait_ns, abort_v));
+      return __all_sync(0xffffffffu, mbar_wait_abortable<PAIR>(bar, par, p.wait_ns, abort_v));
     };
     int stage = 0;
     uint32_t phase = 0, acc_phase = 0;
     int as = 0;  // accumulator set of this unit
-    for (int u = blockIdx.x; u < total && !__any_sync(0xffffffffu, *abort_v); u += gridDim.x) {
+    for (int u = u_first; u < total && !__any_sync(0xffffffffu, *abort_v); u += u_step) {
       bool ok = wait_w(smem_u32(&bar_tempty[as]), acc_phase ^ 1u);
       tc_fence_after();
       const uint32_t t_acc = tmem + as * C::kAccCols + mi * N;
@@ -504,16 +572,25 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
           continue;
         }
         if (!wait_w(smem_u32(&bar_full[stage]), phase)) { ok = false; break; }
+        if constexpr (PAIR)  // and the peer's half of the stage
+          if (!wait_w(smem_u32(&bar_pfull[stage]), phase)) { ok = false; break; }
         tc_fence_after();
         const uint64_t so = (uint64_t)((stage * C::kStage) >> 4);
         const bool first = C::kKSplit ? kt == mi : kt == 0;  // first K tile of this accumulator
 #pragma unroll
         for (int a = 0; a < C::kAtoms; ++a) {
-          tc_cp_sf_elect(t_sfa + 4 * a, sfa_desc0 + so + 32 * a);  // 512 bytes per scale group
+          // 512 bytes per scale group (pair: into both CTAs, each from its own
+          // shared memory)
+          if constexpr (PAIR) tc_cp_sf_pair_elect(t_sfa + 4 * a, sfa_desc0 + so + 32 * a);
+          else tc_cp_sf_elect(t_sfa + 4 * a, sfa_desc0 + so + 32 * a);
 #pragma unroll
           for (int h = 0; h < C::kPairSlots; ++h)  // B rows 128 h .. 128 h + 127: columns 4 h .. 4 h + 3 of the group
-            if (h == 0 || two)
-              tc_cp_sf_elect(t_sfb + 4 * C::kPairSlots * a + 4 * h, sfb_desc0 + so + 32 * a + h * (C::kSFBytes >> 4));
+            if (h == 0 || two) {
+              const uint32_t tb = t_sfb + 4 * C::kPairSlots * a + 4 * h;
+              const uint64_t sb = sfb_desc0 + so + 32 * a + h * (C::kSFBytes >> 4);
+              if constexpr (PAIR) tc_cp_sf_pair_elect(tb, sb);
+              else tc_cp_sf_elect(tb, sb);
+            }
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {  // 32 bytes of the 128-byte swizzle row per MMA
@@ -525,12 +602,18 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
           } else {
             const int atom = NV ? j : (j >> 1);
             const uint32_t sfid = NV ? 0u : (uint32_t)(j & 1) * 2u;
-            const uint32_t idesc = idesc_fp4(n_mma, NV, sfid, sfid);
-            tc_mma_fp4_elect<NV>(t_acc, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc, t_sfa + 4 * atom,
-                                 t_sfb + 4 * C::kPairSlots * atom, accum);  // K = 64
+            if constexpr (PAIR) {  // M = 256 over the pair, all 240 columns
+              tc_mma_mx_pair_elect(t_acc, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc_fp4(N, false, sfid, sfid, 256),
+                                   t_sfa + 4 * atom, t_sfb + 4 * C::kPairSlots * atom, accum);
+            } else {
+              const uint32_t idesc = idesc_fp4(n_mma, NV, sfid, sfid);
+              tc_mma_fp4_elect<NV>(t_acc, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, idesc, t_sfa + 4 * atom,
+                                   t_sfb + 4 * C::kPairSlots * atom, accum);  // K = 64
+            }
           }
         }
-        tc_commit_elect(smem_u32(&bar_empty[stage]));
+        if constexpr (PAIR) tc_commit_pair_elect(smem_u32(&bar_empty[stage]), 0x3);  // both CTAs' stage
+        else tc_commit_elect(smem_u32(&bar_empty[stage]));
         if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
       }
       if (!ok) {
@@ -539,34 +622,42 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
         *abort_v = 1;
         break;
       }
-      tc_commit_elect(smem_u32(&bar_tfull[as]));
+      if constexpr (PAIR) tc_commit_pair_elect(smem_u32(&bar_tfull[as]), 0x3);  // both CTAs' epilogues
+      else tc_commit_elect(smem_u32(&bar_tfull[as]));
       if (++as == C::kAccStages) { as = 0; acc_phase ^= 1u; }
     }
     // all issued MMAs must finish before tensor memory is released
-    tc_commit_elect(smem_u32(&bar_done));
-    (void)mbar_wait(smem_u32(&bar_done), 0);
+    if constexpr (PAIR) tc_commit_pair_elect(smem_u32(&bar_done), 0x1);
+    else tc_commit_elect(smem_u32(&bar_done));
+    (void)mbar_wait<PAIR>(smem_u32(&bar_done), 0);
    }
-  } else {
+  } else if (warp < 6 || C::kEpiWarps == 8) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // tensor-memory lane quadrant of this warp
+    const int half = warp >= 8 ? 1 : 0;  // eight epilogue warps: which chunks of the unit
     const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
-    float(*tile)[33] = epi_tile[warp - 2];
+    float(*tile)[33] = epi_tile[GATEUP ? warp - 2 : 0];
     uint32_t acc_phase = 0;
     int as = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+    for (int u = u_first; u < total; u += u_step) {
       if (__any_sync(0xffffffffu, *abort_v)) break;  // warp-uniform: the loop body holds .sync.aligned loads
       int e, mt, slot, cnt;
       decode_unit<N>(s_start, s_count, s_slot, p.n_exp, u, e, mt, slot, cnt);
-      if (!__all_sync(0xffffffffu, mbar_wait_abortable(smem_u32(&bar_tfull[as]), acc_phase, p.wait_ns, abort_v))) {
-        if (lane == 0 && !*abort_v) record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
-        __syncwarp();
-        *abort_v = 1;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t ta = tq + as * C::kAccCols;
+      // the unit's accumulator set is complete (bounded; warp-uniform outcome)
+      auto wait_acc = [&]() {
+        if (!__all_sync(0xffffffffu, mbar_wait_abortable<PAIR>(smem_u32(&bar_tfull[as]), acc_phase, p.wait_ns, abort_v))) {
+          if (lane == 0 && !*abort_v) record_status(p.status, FP4MOE_ERR_TIMEOUT, ST_TIMEOUT);
+          __syncwarp();
+          *abort_v = 1;
+          return false;
+        }
+        tc_fence_after();
+        return true;
+      };
       const int64_t row0 = (int64_t)slot * kSlotRows;
       if constexpr (GATEUP) {
+        if (!wait_acc()) break;
+        const uint32_t ta = tq + as * C::kAccCols;
         const int i0 = mt * 128 + 32 * q;  // first intermediate index of this warp's lanes
         float sc = 1.f;
         if constexpr (NV) sc = __fmul_rn(__ldg(p.gb), __ldg(p.gw + e));
@@ -647,11 +738,13 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
           if (lane == 0) atomicMax(p.amax_h + e, __float_as_uint(amax));
         }
       } else {
-        // routing weight times y added into the fp32 combine buffer: the
-        // warp's 32 rows x 32 token columns go through shared memory so that
-        // each lane adds 4 consecutive outputs of one token per 16-byte
-        // reduction (lane l: rows 4 (l % 8) .. + 3 of columns l / 8 + 4 k)
-        const int h0 = mt * 128 + 32 * q + 4 * (lane & 7);
+        // routing weight times y added into the fp32 combine buffer.  Lane l
+        // holds output row 32 q + l of the unit's 128 for the 32 token
+        // columns of a chunk; a 4 x 4 transpose within each group of four
+        // lanes (two shuffle rounds) leaves lane 4 m + r with rows 4 m ..
+        // 4 m + 3 of column 4 g + r, which one 16-byte reduction adds.
+        const int m4 = lane >> 2, r4 = lane & 3;
+        const int h0 = (PAIR ? mt * 256 + (int)crank * 128 : mt * 128) + 32 * q + 4 * m4;
         float sc = 1.f;
         if constexpr (NV) sc = __fmul_rn(__ldg(p.gb + e), __ldg(p.gw + e));
         float rho = 1.f;  // W8A8: channel scale of this lane's output row
@@ -663,8 +756,39 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
         const int cnt1 = cnt - cnt0;
         const int ncol = cnt1 > 0 ? 128 + cnt1 : cnt0;
         auto col_ok = [&](int n) { return n < cnt0 || (n >= 128 && n < ncol); };
-        for (int c0 = 0; c0 < ncol; c0 += 32) {
-          if (C::kPairSlots == 2 && c0 >= cnt0 && c0 < 128) continue;  // stale columns only (warp-uniform)
+        // this warp's chunks: 32-column chunk ci with ci % halves == half,
+        // skipping chunks of stale columns only
+        constexpr int kHalves = C::kEpiWarps / 4;
+        auto chunk_ok = [&](int ci) { return !(C::kPairSlots == 2 && 32 * ci >= cnt0 && 32 * ci < 128); };
+        auto next_chunk = [&](int ci) {
+          while (32 * ci < ncol && !chunk_ok(ci)) ci += kHalves;
+          return ci;
+        };
+        // token and weight of column 32 ci + lane, fetched one chunk ahead
+        // (the first before the accumulator is ready)
+        int tk_n = 0;
+        float wk_n = 0.f;
+        auto fetch = [&](int ci) {
+          tk_n = 0;
+          wk_n = 0.f;
+          const int n = 32 * ci + lane;
+          if (32 * ci < ncol && col_ok(n)) {
+            const int64_t rr = row0 + n;
+            tk_n = __ldg(p.row_tok + rr);
+            wk_n = __ldg(p.row_w + rr) * sc;
+            if constexpr (F8) wk_n = __ldg(p.row_w + rr) * __ldg(p.brs + rr);
+          }
+        };
+        int ci = next_chunk(half);
+        fetch(ci);
+        if (!wait_acc()) break;
+        const uint32_t ta = tq + as * C::kAccCols;
+        while (32 * ci < ncol) {
+          const int c0 = 32 * ci;
+          const int tk = tk_n;
+          const float wk = wk_n;
+          const int cn = next_chunk(ci + kHalves);
+          fetch(cn);
           float y[32];
           tc_ld32(ta + c0, y);  // even K tiles (all of them with one issuer)
           if (C::kKSplit && KT > 1) {  // odd K tiles (the second issuer's accumulator)
@@ -675,49 +799,57 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP>::kThreads, 1) moe_g
             for (int j = 0; j < 32; ++j) y[j] += y1[j];
           }
           tc_wait_ld();
-          int tk = 0;
-          float wk = 0.f;
-          if (col_ok(c0 + lane)) {  // lane j fetches token and weight of column c0 + j
-            const int64_t rr = row0 + c0 + lane;
-            tk = __ldg(p.row_tok + rr);
-            wk = __ldg(p.row_w + rr) * sc;
-            if constexpr (F8) wk = __ldg(p.row_w + rr) * __ldg(p.brs + rr);
-          }
 #pragma unroll
-          for (int j = 0; j < 32; ++j) tile[j][lane] = F8 ? y[j] * rho : y[j];
-          __syncwarp();
+          for (int g = 0; g < 8; ++g) {
+            float v[4];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int j = (lane >> 3) + 4 * k;
-            const int t = __shfl_sync(0xffffffffu, tk, j);
-            const float w = __shfl_sync(0xffffffffu, wk, j);
-            if (col_ok(c0 + j)) {
-              const float* src = &tile[j][4 * (lane & 7)];
-              red_add_v4(p.out_acc + (int64_t)t * p.H + h0, src[0] * w, src[1] * w, src[2] * w, src[3] * w);
+            for (int i = 0; i < 4; ++i) v[i] = F8 ? y[4 * g + i] * rho : y[4 * g + i];
+            // lane r of the group: v[i] = (row r, column 4 g + i) -> (row i, column 4 g + r)
+#pragma unroll
+            for (int m = 1; m <= 2; m <<= 1) {
+              const bool up = (r4 & m) != 0;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                if (i & m) continue;
+                const float got = __shfl_xor_sync(0xffffffffu, up ? v[i] : v[i | m], m);
+                if (up) v[i] = got;
+                else v[i | m] = got;
+              }
             }
+            const int src = 4 * g + r4;  // column of this lane's four rows
+            const int t = __shfl_sync(0xffffffffu, tk, src);
+            const float w = __shfl_sync(0xffffffffu, wk, src);
+            if (col_ok(c0 + src)) red_add_v4(p.out_acc + (int64_t)t * p.H + h0, v[0] * w, v[1] * w, v[2] * w, v[3] * w);
           }
-          __syncwarp();
+          ci = cn;
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[as]));
+      if (lane == 0) {  // (pair: the issuer's barrier is in CTA 0)
+        if (PAIR && crank != 0) mbar_arrive_remote(smem_u32(&bar_tempty[as]), 0u);
+        else mbar_arrive(smem_u32(&bar_tempty[as]));
+      }
       if (++as == C::kAccStages) { as = 0; acc_phase ^= 1u; }
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  // (pair: CTA 0's MMAs, which read this CTA's shared memory and write its
+  // tensor memory, have completed once CTA 0 passes its bar_done wait)
+  if constexpr (PAIR) cluster_arrive_wait();
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, C::kTmemCols);
+    else tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
-template <int N, bool GATEUP, bool NV, int OP = kOpFp4>
+template <int N, bool GATEUP, bool NV, int OP = kOpFp4, bool PAIR = false>
 cudaError_t launch_gemm_t(const KParams& p, int grid, cudaStream_t s) {
-  using C = GemmCfg<N, GATEUP, NV, OP>;
-  auto k = moe_gemm_kernel<N, GATEUP, NV, OP>;
+  using C = GemmCfg<N, GATEUP, NV, OP, PAIR>;
+  auto k = moe_gemm_kernel<N, GATEUP, NV, OP, PAIR>;
   static bool attr_set[64] = {};  // once per device and template instance
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -726,6 +858,32 @@ cudaError_t launch_gemm_t(const KParams& p, int grid, cudaStream_t s) {
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  if constexpr (PAIR) {
+    // CTA pairs: as many as can be resident at once (a pair needs two SMs
+    // of one cluster-capable group), at most grid / 2
+    static int max_pairs[64] = {};
+    if (dev >= 0 && dev < 64 && max_pairs[dev] == 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2);
+      cfg.blockDim = dim3(C::kThreads);
+      cfg.dynamicSmemBytes = C::kSmem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
+      if (e != cudaSuccess) return e;
+      max_pairs[dev] = n > 0 ? n : 1;
+    }
+    int pairs = grid / 2;
+    if (dev >= 0 && dev < 64 && pairs > max_pairs[dev]) pairs = max_pairs[dev];
+    if (pairs < 1) pairs = 1;
+    return launch_pdl_cluster(k, dim3(2 * pairs), dim3(C::kThreads), C::kSmem, s, 2u, p);
   }
   return launch_pdl(k, dim3(grid), dim3(C::kThreads), C::kSmem, s, p);
 }

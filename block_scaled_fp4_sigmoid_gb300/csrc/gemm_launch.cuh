@@ -111,6 +111,10 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   if constexpr (!GATEUP) {
     if (a.dn_pair == 2) {  // MXFP4, 112-token tiles: two slots per unit
       if (a.n_tile != 112 || a.nv || a.f8 || a.bf) return cudaErrorInvalidValue;
+      if (a.dn_cta_pair) {
+        if (vis % 256 != 0) return cudaErrorInvalidValue;
+        return launch_gemm_t<240, false, false, kOpFp4, true>(p, grid, s);
+      }
       return launch_gemm_t<240, false, false>(p, grid, s);
     }
   }

@@ -168,6 +168,7 @@ struct GemmArgs {
   uint64_t wait_ns;                // pipeline wait limit; 0: kWaitLimitNs
   bool withhold;                   // gate/up test knob (fp4moe_debug.withhold_first_stage)
   int dn_pair;                     // down, 112-token tiles: 2 = one unit covers two slots (224 tokens)
+  bool dn_cta_pair;                // down, dn_pair 2: run on CTA pairs (units of 256 weight rows)
   // W8A8: channel scales of the weights (routed [E, rows], shared [rows]),
   // scales of the B rows (per permuted row); amax_h is then per permuted row
   const float *wrs, *shrs, *brs;
@@ -194,6 +195,27 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// As launch_pdl, with thread-block clusters of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                               unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

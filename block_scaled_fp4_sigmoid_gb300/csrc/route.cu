@@ -390,14 +390,6 @@ constexpr int kFrontWarps = kFrontThreads / 32;
 constexpr int kFrontExperts = 2 * kFrontWarps;  // experts per CTA: two per warp
 static_assert(kFrontExperts * kFrontMaxT == kFrontThreads, "one rank-0 thread per (expert, token)");
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 // fp32 at a shared-memory address of CTA `rank` of this cluster
 __device__ __forceinline__ float ld_dsmem(const float* p, uint32_t rank) {
   uint32_t remote;
@@ -505,7 +497,7 @@ __global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArg
 
   pdl_trigger();  // the next kernel may launch and wait for this one
   // ---- phase A
-  const int sp = (int)cluster_rank();  // the cluster is one expert group, rank = K split
+  const int sp = (int)cluster_ctarank();  // the cluster is one expert group, rank = K split
   const int e0 = (blockIdx.x / a.n_splits) * kFrontExperts + 2 * wib;  // this warp: experts e0, e0 + 1
   const float2 part = T <= 8 ? front_gemv_any<8>(a, front_xs, sp, e0, lane)
                              : front_gemv_any<kFrontMaxT>(a, front_xs, sp, e0, lane);
@@ -513,7 +505,7 @@ __global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArg
     s_part[2 * wib][lane] = part.x;
     s_part[2 * wib + 1][lane] = part.y;
   }
-  cluster_sync();  // every split's partials are in its CTA's shared memory
+  cluster_arrive_wait();  // every split's partials are in its CTA's shared memory
   if (sp == 0) {  // thread (expert slot, token)
     const int j = tid / kFrontMaxT, t = tid % kFrontMaxT, e = (blockIdx.x / a.n_splits) * kFrontExperts + j;
     if (e < E && t < T) {
@@ -525,7 +517,7 @@ __global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArg
       if (a.scores_dbg) a.scores_dbg[(int64_t)t * E + e] = sc;
     }
   }
-  cluster_sync();  // the other CTAs' shared memory stays valid until rank 0 has read it
+  cluster_arrive_wait();  // the other CTAs' shared memory stays valid until rank 0 has read it
   // Off the critical path (the ranks other than 0 are done; with one split
   // the rank-0 CTAs do it): zero the combine buffer and quantise x to MXFP4
   // once per token, token t in row t of the layout.  The next kernel reads

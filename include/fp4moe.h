@@ -179,7 +179,15 @@ typedef struct {
  *     CTA's MMA issuer waits for it until wait_limit_ns runs out; the call
  *     then records FP4MOE_ERR_TIMEOUT in the status word, abandons that
  *     CTA's work (the output is not valid) and returns normally.  It
- *     exercises the timeout path without any fault. */
+ *     exercises the timeout path without any fault.
+ *   down_cta_pair: 0 in normal use.  When non-zero, down GEMM units that
+ *     cover two 112-token slots (MXFP4 layers with >= 160 routes per expert,
+ *     an output range of a multiple of 256 rows) run on clusters of two CTAs
+ *     as M = 256 MMAs (tcgen05 .cta_group::2): one CTA issues for both SMs,
+ *     each CTA holds half the weight rows and one slot of tokens.  Same
+ *     results as the default single-CTA units; measured slower on GB300
+ *     (the per-instruction cost of the pair's MMAs and scale copies), kept
+ *     selectable for comparison. */
 typedef struct {
   void *events[8];
   float *h_pre;
@@ -187,7 +195,7 @@ typedef struct {
   float *scores;
   int64_t wait_limit_ns;
   int32_t withhold_first_stage;
-  int32_t reserved;
+  int32_t down_cta_pair;
 } fp4moe_debug;
 
 /* Library version as major*10000 + minor*100 + patch. */

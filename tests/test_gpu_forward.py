@@ -65,6 +65,9 @@ SMALL = {
     # >= 160 routes per expert: the down GEMM's units cover two 112-token
     # slots (full pairs and single-slot remainders)
     "paired_padK": _cfg("tiny", name="paired_padK", T=600, H=1024, I=384, E=4, top_k=2, routed_scaling=2.827),
+    # paired slots on CTA pairs (256-row units) with a shared expert (paired
+    # slots on single CTAs: the 128-column blocks of the column-block test)
+    "pair_shared": _cfg("tiny", name="pair_shared", T=700, H=768, I=256, E=6, top_k=2, n_shared=1),
     "nv_grouped": _cfg("deepseek_nvfp4", name="nv_grouped", T=64, H=512, I=256, E=32, top_k=4, n_group=4,
                        topk_group=2),
     "nv_wide_padK": _cfg("deepseek_nvfp4", name="nv_wide_padK", T=200, H=256, I=128, E=4, top_k=2, n_group=2,
@@ -75,7 +78,7 @@ SMALL = {
 class DeviceRun:
     """One forward on the GPU plus host copies of its intermediates."""
 
-    def __init__(self, cfg, h_debug=True, packed=True, x=None, layer=None):
+    def __init__(self, cfg, h_debug=True, packed=True, x=None, layer=None, cta_pair=False):
         torch = torch_cuda()
         ensure_built()
         from block_scaled_fp4_sigmoid_gb300.layer import MoELayer
@@ -86,6 +89,7 @@ class DeviceRun:
         L = layer.layout
         self.L = L
         dbg = fm.Debug()
+        dbg.down_cta_pair = 1 if cta_pair else 0
         h_pre = None
         if h_debug:
             h_pre = torch.zeros((L.rows_cap, cfg.I), dtype=torch.float32, device="cuda")
@@ -350,8 +354,8 @@ def check_output_replay(run, cfg, ws, tokens):
 
 
 # ------------------------------------------------------------------ whole-layer check
-def full_check(cfg, tokens=None, h_debug=True, packed=True):
-    run = DeviceRun(cfg, h_debug=h_debug, packed=packed)
+def full_check(cfg, tokens=None, h_debug=True, packed=True, cta_pair=False):
+    run = DeviceRun(cfg, h_debug=h_debug, packed=packed, cta_pair=cta_pair)
     assert run.status == (0, 0), run.status
     x, wr, b = OI.layer_inputs(cfg)
     assert np.array_equal(run.x_bits, synth.gen_x_bf16(cfg))
@@ -403,6 +407,14 @@ def full_check(cfg, tokens=None, h_debug=True, packed=True):
 def test_small_layers_full_oracle(name):
     stats = full_check(SMALL[name])
     print(name, stats)
+
+
+@pytest.mark.parametrize("name", ["paired_padK", "pair_shared"])
+def test_paired_down_on_cta_pairs(name):
+    """The same parity with the paired-slot down units run on CTA pairs (M =
+    256 MMAs over two SMs, the fp4moe_debug::down_cta_pair opt-in): full
+    pairs, single-slot remainders and a shared expert."""
+    print(name, full_check(SMALL[name], cta_pair=True))
 
 
 @pytest.mark.parametrize("name", ["tiny", "wide_padK", "nv_grouped", "nv_wide_padK"])
@@ -561,11 +573,13 @@ def _ambiguous_tokens(cfg, orc, tokens, bias):
 
 
 @pytest.mark.parametrize("name,world", [("ragged_shared", 2), ("ragged_shared", 4), ("front_cluster3", 3),
-                                        ("nv_grouped", 2), ("wide_padK", 8)])
+                                        ("nv_grouped", 2), ("wide_padK", 8), ("paired_padK", 2),
+                                        ("paired_padK", 8)])
 def test_output_column_blocks_sum_to_the_layer(name, world):
     """Output-partitioned layer: the ranks' column blocks, summed, meet the
     layer tolerance against the whole oracle (the few-token front end, the
-    many-token path, a shared expert, NVFP4, K padding)."""
+    many-token path, a shared expert, NVFP4, K padding, paired down units on
+    CTA pairs (512-column blocks) and on single CTAs (128-column blocks))."""
     from types import SimpleNamespace
     torch_cuda()
     ensure_built()
