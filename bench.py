@@ -246,6 +246,110 @@ def oracle_route_sample(cfg_name: str, n_routes: int, frac: float = 1.0, start_t
     return t_total, n_routes / rpt * (Ip / cfg.I)
 
 
+def oracle_full_layer(cfg_name: str, max_experts: int | None = None, conv_rows: int = 0):
+    """The FP64 oracle over a whole workload on the host cores: routing of
+    every token, activation quantisation, the permutation, then every
+    touched expert's MLP on all of its routed rows (oracle.moe.expert_rows,
+    the combine included).  Weight generation is input preparation and stays
+    outside the timing.  max_experts bounds the run to the first experts of
+    the permutation (None: all); conv_rows > 0 also times the MXFP4 -> FP8
+    conversion oracle on that many expert rows.  Returns a dict of seconds
+    and counts."""
+    import numpy as np
+    import synth
+    from oracle import inputs as OI
+    from oracle import moe as M
+    from oracle import quant as Q
+    from oracle.convert import mxfp4_to_fp8_rowscale
+    from oracle.permute import permute
+    from oracle.router import route, router_logits
+    cfg = synth.configs()[cfg_name]
+    x = synth.bf16_bits_to_f64(synth.gen_x_bf16(cfg))
+    wr = synth.bf16_bits_to_f64(synth.gen_router_bf16(cfg))
+    bias = synth.gen_bias_f32(cfg)
+    ws = OI.oracle_weights(cfg)
+    t0 = time.perf_counter()
+    logits, _ = router_logits(x, wr)
+    idx, w = route(logits, bias, cfg.top_k, cfg.n_group, cfg.topk_group, cfg.routed_scaling, cfg.renormalize)
+    xc, xs, gx = Q.quantize(x, cfg.fmt)
+    counts, offsets, ptok, pslot = permute(idx, cfg.E, cfg.n_shared)
+    t_route = time.perf_counter() - t0
+    experts = [e for e in range(cfg.E + cfg.n_shared) if counts[e] > 0]
+    done = experts if max_experts is None else experts[:max_experts]
+    out = np.zeros((cfg.T, cfg.H))
+    t_experts, routes, flops = 0.0, 0, 0.0
+    for e in done:
+        rows = np.arange(offsets[e], offsets[e + 1])
+        toks, slots = ptok[rows], pslot[rows]
+        wts = w[toks, np.minimum(slots, cfg.top_k - 1)] if e < cfg.E else np.ones(len(rows))
+        names = ("w13", "w2") if e < cfg.E else ("sh13", "sh2")
+        ee = e if e < cfg.E else e - cfg.E
+        ws.get(names[0], ee), ws.get(names[1], ee)  # generated outside the timing
+        t0 = time.perf_counter()
+        a = Q.dequant(xc[toks], xs[toks], cfg.fmt, gx)
+        info = M.expert_rows(cfg, e, a, wts, ws, with_ambiguity=False)
+        np.add.at(out, toks, wts[:, None] * info["y"])
+        t_experts += time.perf_counter() - t0
+        routes += len(rows)
+        flops += 2.0 * 3 * cfg.I * cfg.H * len(rows)
+        ws.drop(names[0], ee)
+        ws.drop(names[1], ee)
+    res = {"config": cfg_name, "tokens": cfg.T, "experts_done": len(done), "experts_touched": len(experts),
+           "routes_done": routes, "routes_total": int(counts.sum()), "route_s": t_route, "expert_s": t_experts,
+           "expert_gflops": flops / max(t_experts, 1e-9) / 1e9, "cores": cpu_cores()}
+    if conv_rows:  # w13 rows (K = H) of consecutive experts, generation outside the timing
+        rows, _ = synth.weight_shape(cfg, "w13")
+        t_conv, done_rows, e = 0.0, 0, 0
+        while done_rows < conv_rows:
+            codes, scales = synth.gen_mx_weight(cfg, "w13", e)
+            take = min(rows, conv_rows - done_rows)
+            t1 = time.perf_counter()
+            mxfp4_to_fp8_rowscale(codes[:take], scales[:take])
+            t_conv += time.perf_counter() - t1
+            done_rows += take
+            e += 1
+        res["conversion_rows"] = done_rows
+        res["conversion_s"] = t_conv
+    return res
+
+
+def _conversion_task(args):
+    """One expert matrix through the conversion oracle, in row blocks (worker
+    process of oracle_full_conversion): (rows, seconds in the oracle)."""
+    import synth
+    from oracle.convert import mxfp4_to_fp8_rowscale
+    cfg_name, which, e = args
+    cfg = synth.configs()[cfg_name]
+    codes, scales = synth.gen_mx_weight(cfg, which, e)
+    secs = 0.0
+    for r0 in range(0, codes.shape[0], 1024):
+        t0 = time.perf_counter()
+        mxfp4_to_fp8_rowscale(codes[r0:r0 + 1024], scales[r0:r0 + 1024])
+        secs += time.perf_counter() - t0
+    return codes.shape[0], secs
+
+
+def oracle_full_conversion(cfg_name: str = "skewed_shared") -> dict:
+    """The MXFP4 -> FP8 conversion oracle over every routed expert row of a
+    layer (gate/up rows with K = H and down rows with K = I), one worker
+    process per host core.  Weight generation happens in the workers and is
+    not counted: each worker times its oracle calls only."""
+    import multiprocessing as mp
+    import synth
+    cfg = synth.configs()[cfg_name]
+    procs = cpu_cores()
+    tasks = [(cfg_name, w, e) for e in range(cfg.E) for w in ("w13", "w2")]
+    t0 = time.perf_counter()
+    with mp.get_context("spawn").Pool(procs) as pool:
+        res = pool.map(_conversion_task, tasks, chunksize=1)
+    wall = time.perf_counter() - t0
+    rows = sum(r for r, _ in res)
+    secs = sum(s for _, s in res)
+    return {"config": cfg_name, "conversion_rows": rows, "oracle_core_s": secs, "procs": procs,
+            "oracle_s_per_proc": secs / procs, "rows_per_s": rows / (secs / procs), "wall_s_with_generation": wall,
+            "cores": procs}
+
+
 def algorithmic_bytes(H: int, I: int, fmt: str, mode: str, touched: int, routes: int,
                       tokens: int) -> tuple[float, float]:
     """Bytes the gate/up and the down GEMM of one layer call must move at
@@ -758,10 +862,21 @@ def gpu_arm(args, cfg, rank, world, local_rank):
         conversion = time_conversion(layer, peaks, stream)
     elif others is not None:
         conversion = others.pop("conversion")
-    # CPU baseline: the oracle on a bounded sample of this workload
-    n_routes = 16 if args.cpu_routes is None else args.cpu_routes
-    cpu_s, cpu_tok = (oracle_route_sample(args.config, n_routes, w8a8=args.w8a8, emulate=args.emulate) if n_routes > 0
-                      else (float("nan"), 0.0))
+    # CPU baseline: the oracle on the whole step when that is a bounded
+    # amount of work (a decode-sized A4W4 layer: ~15 s on 16 cores), else on
+    # a bounded sample of routes
+    whole = (args.cpu_routes is None and cfg.T <= 16 and not (args.w8a8 or args.emulate)
+             and cfg.name == args.config)
+    if whole:
+        full = oracle_full_layer(cfg.name)
+        cpu_s, cpu_tok = full["route_s"] + full["expert_s"], float(cfg.T)
+        cpu_sample = (f"the whole step: {cfg.T} tokens, {full['routes_done']} routes over all "
+                      f"{full['experts_done']} touched experts, FP64 numpy")
+    else:
+        n_routes = 16 if args.cpu_routes is None else args.cpu_routes
+        cpu_s, cpu_tok = (oracle_route_sample(args.config, n_routes, w8a8=args.w8a8, emulate=args.emulate)
+                          if n_routes > 0 else (float("nan"), 0.0))
+        cpu_sample = f"{n_routes} routes ({cpu_tok:g} tokens) of the same workload, FP64 numpy"
     line = {
         "metric": METRIC,
         "value": whole_job_rate(cfg.T, world, ms_max),
@@ -794,7 +909,7 @@ def gpu_arm(args, cfg, rank, world, local_rank):
                  "layer_roofline": roofline(*work["layer"], ms_max, peaks), "kernels": {"gateup": gu, "down": dn},
                  "wall_s": head["wall_s"], "eager_ms_per_step": eager_ms},
         "cpu_baseline": {"value": cpu_tok / cpu_s, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": f"{n_routes} routes ({cpu_tok:g} tokens) of the same workload, FP64 numpy"},
+                         "sample": cpu_sample},
         "context": "pages: 1.43 ms per MoE layer call at T=8 on one Gaudi 2 card holding 48 of 384 experts",
         "conversion": conversion,
         "configs": others,
@@ -821,11 +936,25 @@ def main():
                     help="the W8A8 layer: experts exactly converted to FP8 per channel, FP8 per-token activations")
     ap.add_argument("--conversion", action="store_true",
                     help="also time the MXFP4 -> FP8 conversion of all routed expert rows")
+    ap.add_argument("--cpu-full", default=None, metavar="CONFIG[,MAX_EXPERTS]",
+                    help="time the FP64 oracle over a whole workload on the host cores (no GPU) and print a JSON line")
+    ap.add_argument("--cpu-conv-rows", type=int, default=0,
+                    help="with --cpu-full: also time the conversion oracle on this many expert rows")
+    ap.add_argument("--cpu-conv-full", action="store_true",
+                    help="time the conversion oracle over every routed expert row of the skewed layer on all host "
+                         "cores (no GPU) and print a JSON line")
     ap.add_argument("--no-configs", action="store_true",
                     help="time the chosen workload only (by default a one-GPU run also measures every other "
                          "workload and the conversion, in the line's configs object)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.cpu_conv_full:
+        print(json.dumps(oracle_full_conversion()), flush=True)
+        return
+    if args.cpu_full:
+        name, _, mx = args.cpu_full.partition(",")
+        print(json.dumps(oracle_full_layer(name, int(mx) if mx else None, args.cpu_conv_rows)), flush=True)
+        return
     import synth
     from dataclasses import replace
     cfg = synth.configs()[args.config]
