@@ -492,6 +492,14 @@ __device__ __forceinline__ void mx_quant32(const float* v, uint32_t* packed4, ui
   *scale_byte = (uint32_t)(e + 127);
 }
 
+// Hardware reciprocal (rcp.approx.ftz: relative error within about one unit
+// in the last place; subnormal results flush to zero).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // NVFP4: tensor scale g = amax / 2688 (correctly rounded fp32 division).
 __device__ __forceinline__ float nv_global(float amax) { return __fdiv_rn(amax, 2688.0f); }
 
