@@ -69,6 +69,8 @@ struct KParams {
   int E, n_exp, H, I, K, rows_per_expert, m_tiles, katoms_a, katoms_b, katoms_h, has_shared, T;
   int plan_early;  // the plan was written at least two kernels back (see the kernel)
   int w_tiled;     // weights in the tiled layout (tmA / tmA_sh are views of 128-byte rows)
+  int unit_mtiles;  // weight tiles per unit row (128 rows each; 256 on CTA pairs)
+  int m_group;      // weight tiles per group of the unit order (divides unit_mtiles)
   uint64_t wait_ns;  // limit of the pipeline waits (drains keep kWaitLimitNs)
   int withhold;      // gate/up test knob: CTA 0 never fills its first pipeline stage
   // W8A8 (E4M3 operands): per-row fp32 scales of the weights (routed [E,
@@ -166,24 +168,34 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) { return smem_des
 __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) { return smem_desc(saddr, 0, 128, 0); }
 
 // Unit u -> (expert, weight tile, token-tile slot, tokens in the tile), from
-// the plan cached in shared memory: the expert is the last one whose first
-// unit is <= u.
+// the plan cached in shared memory (s_start[e] = M x the token tiles of the
+// experts before e, s_start[n_exp] = all units).  The M weight tiles of a
+// unit row are taken in groups of G (G divides M): group g holds, expert by
+// expert, tiles g G .. g G + G - 1, each with all of the expert's token
+// tiles (token tile fastest).  G = M is expert-major order; a smaller G
+// keeps the down GEMM's combine rows of one group (T x G x 128 fp32) in L2
+// while every expert adds into them.
 template <int N>
 __device__ __forceinline__ void decode_unit(const int32_t* s_start, const int32_t* s_count, const int32_t* s_slot,
-                                            int n_exp, int u, int& e, int& mt, int& slot, int& cnt) {
+                                            int n_exp, int M, int G, int u, int& e, int& mt, int& slot, int& cnt) {
+  const int per_group = (s_start[n_exp] / M) * G;  // units of one group
+  const int g = u / per_group;
+  const int r = u - g * per_group;
+  const int key = (r / G) * M;  // the expert is the last one starting at or before it
   int lo = 0, hi = n_exp;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (s_start[mid] <= u) lo = mid;
+    if (s_start[mid] <= key) lo = mid;
     else hi = mid;
   }
   e = lo;
-  const int local = u - s_start[e];
+  const int local = r - (s_start[e] / M) * G;
   const int count = s_count[e];
   constexpr int kCap = GemmCfg<N, false, false>::kUnitRoutes;
   const int nt = (count + kCap - 1) / kCap;
-  mt = local / nt;
-  const int ti = local - mt * nt;
+  const int ml = local / nt;
+  const int ti = local - ml * nt;
+  mt = g * G + ml;
   slot = s_slot[e] + ti * GemmCfg<N, false, false>::kPairSlots;
   cnt = min(kCap, count - ti * kCap);
 }
@@ -280,7 +292,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
   };
   auto unit_step = [&](int u) {
     int e, mt, slot, cnt;
-    decode_unit<N>(s_start, s_count, s_slot, p.n_exp, u, e, mt, slot, cnt);
+    decode_unit<N>(s_start, s_count, s_slot, p.n_exp, p.unit_mtiles, p.m_group, u, e, mt, slot, cnt);
     const bool sh = e >= p.E;
     Step st;
     st.tmA = sh ? &p.tmA_sh : &p.tmA;
@@ -562,7 +574,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
       bool two = true;
       if constexpr (C::kPairSlots == 2) {
         int e_, mt_, slot_, cnt_;
-        decode_unit<N>(s_start, s_count, s_slot, p.n_exp, u, e_, mt_, slot_, cnt_);
+        decode_unit<N>(s_start, s_count, s_slot, p.n_exp, p.unit_mtiles, p.m_group, u, e_, mt_, slot_, cnt_);
         two = cnt_ > 112;
       }
       const uint32_t n_mma = two ? N : 112;
@@ -642,7 +654,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
     for (int u = u_first; u < total; u += u_step) {
       if (__any_sync(0xffffffffu, *abort_v)) break;  // warp-uniform: the loop body holds .sync.aligned loads
       int e, mt, slot, cnt;
-      decode_unit<N>(s_start, s_count, s_slot, p.n_exp, u, e, mt, slot, cnt);
+      decode_unit<N>(s_start, s_count, s_slot, p.n_exp, p.unit_mtiles, p.m_group, u, e, mt, slot, cnt);
       // the unit's accumulator set is complete (bounded; warp-uniform outcome)
       auto wait_acc = [&]() {
         if (!__all_sync(0xffffffffu, mbar_wait_abortable<PAIR>(smem_u32(&bar_tfull[as]), acc_phase, p.wait_ns, abort_v))) {

@@ -6,6 +6,21 @@
 
 namespace fp4moe {
 
+// L2 bytes the down GEMM's combine rows of one unit group may take (of the
+// 126 MB): the group's G weight tiles x 128 rows x T tokens x fp32.
+constexpr int64_t kCombineL2Bytes = 48ll << 20;
+
+// Weight tiles per group of the down GEMM's unit order: the largest divisor
+// of M whose combine rows fit kCombineL2Bytes (M when they all fit, or when
+// each token has one route, so that no row is added twice).
+inline int combine_group(int M, int64_t T, int routes_per_token) {
+  if (routes_per_token <= 1 || T * M * 512 <= kCombineL2Bytes) return M;
+  int g = 1;
+  for (int c = 1; c <= M; ++c)
+    if (M % c == 0 && T * c * 512 <= kCombineL2Bytes) g = c;
+  return g;
+}
+
 template <bool GATEUP>
 cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   const fp4moe_dims& d = *a.d;
@@ -82,6 +97,8 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   p.K = K;
   p.rows_per_expert = rows;
   p.m_tiles = GATEUP ? d.I / 128 : vis / 128;
+  p.unit_mtiles = GATEUP ? d.I / 128 : vis / (a.dn_cta_pair ? 256 : 128);
+  p.m_group = GATEUP ? p.unit_mtiles : combine_group(p.unit_mtiles, d.T, d.top_k + d.n_shared);
   p.katoms_a = (int)katoms_padded(K, a.nv);
   p.katoms_b = (int)katoms_padded(K, a.nv);
   p.katoms_h = (int)katoms_padded(d.I, a.nv);

@@ -509,8 +509,14 @@ __global__ void __launch_bounds__(kFrontThreads, 2) decode_front_kernel(FrontArg
   if (sp == 0) {  // thread (expert slot, token)
     const int j = tid / kFrontMaxT, t = tid % kFrontMaxT, e = (blockIdx.x / a.n_splits) * kFrontExperts + j;
     if (e < E && t < T) {
+      // every split's partial in flight at once, then summed in split order
+      float v[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) v[r] = r < a.n_splits ? ld_dsmem(&s_part[j][t], (uint32_t)r) : 0.f;
       float l = 0.f;
-      for (int r = 0; r < a.n_splits; ++r) l += ld_dsmem(&s_part[j][t], (uint32_t)r);
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        if (r < a.n_splits) l += v[r];
       const float sc = 1.0f / (1.0f + expf(-l));
       a.partial[(int64_t)t * E + e] = sc;  // sigmoid scores [T, E]
       if (a.logits_dbg) a.logits_dbg[(int64_t)t * E + e] = l;
