@@ -39,13 +39,14 @@ bool dims_ok(const fp4moe_dims& d) {
 // slots (up to 224 tokens, N = 240 MMAs), twice the work per pipeline step,
 // with one MMA issuer (two accumulator sets of 240 columns fill tensor
 // memory).  A unit that stays within one slot then runs at half the issue
-// rate of the unpaired kernel's two issuers, so pairing pays only when most
-// units fill both slots: at >= 160 routes per expert on average (measured:
-// skewed 16k-token layer down -6%, 4k-token prefill at 85 routes per
-// expert +6%).  NVFP4's larger scale groups leave no room for two such
-// accumulator sets.
+// rate of the unpaired kernel's two issuers, so pairing pays only when
+// enough units fill both slots: at >= 80 routes per expert on average
+// (measured with the register-transpose epilogue: skewed 16k-token layer
+// down -6%, 4k-token prefill at 85 routes per expert -11%; with the earlier
+// shared-memory epilogue prefill had been +6%).  NVFP4's larger scale
+// groups leave no room for two such accumulator sets.
 int fp4_down_pair(int n_tile, bool nv, double routes_per_expert) {
-  return (n_tile == 112 && !nv && routes_per_expert >= 160.0) ? 2 : 1;
+  return (n_tile == 112 && !nv && routes_per_expert >= 80.0) ? 2 : 1;
 }
 
 // Paired-slot down units over an output range of a multiple of 256 rows can

@@ -175,21 +175,43 @@ __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) { return smem_desc(s
 // tiles (token tile fastest).  G = M is expert-major order; a smaller G
 // keeps the down GEMM's combine rows of one group (T x G x 128 fp32) in L2
 // while every expert adds into them.
-template <int N>
-__device__ __forceinline__ void decode_unit(const int32_t* s_start, const int32_t* s_count, const int32_t* s_slot,
-                                            int n_exp, int M, int G, int u, int& e, int& mt, int& slot, int& cnt) {
+//
+// The grouped case (two integer divisions) stays out of line: the
+// producers decode every unit on their critical path.
+static __device__ __noinline__ int grouped_unit(const int32_t* s_start, int n_exp, int M, int G, int u, int* e_out) {
   const int per_group = (s_start[n_exp] / M) * G;  // units of one group
   const int g = u / per_group;
   const int r = u - g * per_group;
-  const int key = (r / G) * M;  // the expert is the last one starting at or before it
+  // the last expert whose first unit of the group, s_start / M x G, is <= r
+  // (s_start is a multiple of M)
   int lo = 0, hi = n_exp;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (s_start[mid] <= key) lo = mid;
+    if (s_start[mid] * G <= r * M) lo = mid;
     else hi = mid;
   }
-  e = lo;
-  const int local = r - (s_start[e] / M) * G;
+  *e_out = lo;
+  return g * (1 << 20) + (r - (s_start[lo] / M) * G);  // group and local unit (local < 2^20)
+}
+
+template <int N, bool kGrouped>
+__device__ __forceinline__ void decode_unit(const int32_t* s_start, const int32_t* s_count, const int32_t* s_slot,
+                                            int n_exp, int M, int G, int u, int& e, int& mt, int& slot, int& cnt) {
+  int g = 0, local;
+  if (!kGrouped || G == M) {  // the expert: the last one whose first unit is <= u
+    int lo = 0, hi = n_exp;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_start[mid] <= u) lo = mid;
+      else hi = mid;
+    }
+    e = lo;
+    local = u - s_start[lo];
+  } else {
+    const int gl = grouped_unit(s_start, n_exp, M, G, u, &e);
+    g = gl >> 20;
+    local = gl & ((1 << 20) - 1);
+  }
   const int count = s_count[e];
   constexpr int kCap = GemmCfg<N, false, false>::kUnitRoutes;
   const int nt = (count + kCap - 1) / kCap;
@@ -200,7 +222,11 @@ __device__ __forceinline__ void decode_unit(const int32_t* s_start, const int32_
   cnt = min(kCap, count - ti * kCap);
 }
 
-template <int N, bool GATEUP, bool NV, int OP = kOpFp4, bool PAIR = false>
+// GROUPED: the instance decodes the grouped unit order (KParams::m_group <
+// unit_mtiles); the others are compiled with the expert-major order only
+// (measured: the grouped decode merely present cost the decode and NVFP4
+// down GEMMs 2-3%).
+template <int N, bool GATEUP, bool NV, int OP = kOpFp4, bool PAIR = false, bool GROUPED = false>
 __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ KParams p) {
   using C = GemmCfg<N, GATEUP, NV, OP, PAIR>;
@@ -292,7 +318,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
   };
   auto unit_step = [&](int u) {
     int e, mt, slot, cnt;
-    decode_unit<N>(s_start, s_count, s_slot, p.n_exp, p.unit_mtiles, p.m_group, u, e, mt, slot, cnt);
+    decode_unit<N, GROUPED>(s_start, s_count, s_slot, p.n_exp, p.unit_mtiles, p.m_group, u, e, mt, slot, cnt);
     const bool sh = e >= p.E;
     Step st;
     st.tmA = sh ? &p.tmA_sh : &p.tmA;
@@ -574,7 +600,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
       bool two = true;
       if constexpr (C::kPairSlots == 2) {
         int e_, mt_, slot_, cnt_;
-        decode_unit<N>(s_start, s_count, s_slot, p.n_exp, p.unit_mtiles, p.m_group, u, e_, mt_, slot_, cnt_);
+        decode_unit<N, GROUPED>(s_start, s_count, s_slot, p.n_exp, p.unit_mtiles, p.m_group, u, e_, mt_, slot_, cnt_);
         two = cnt_ > 112;
       }
       const uint32_t n_mma = two ? N : 112;
@@ -654,7 +680,7 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
     for (int u = u_first; u < total; u += u_step) {
       if (__any_sync(0xffffffffu, *abort_v)) break;  // warp-uniform: the loop body holds .sync.aligned loads
       int e, mt, slot, cnt;
-      decode_unit<N>(s_start, s_count, s_slot, p.n_exp, p.unit_mtiles, p.m_group, u, e, mt, slot, cnt);
+      decode_unit<N, GROUPED>(s_start, s_count, s_slot, p.n_exp, p.unit_mtiles, p.m_group, u, e, mt, slot, cnt);
       // the unit's accumulator set is complete (bounded; warp-uniform outcome)
       auto wait_acc = [&]() {
         if (!__all_sync(0xffffffffu, mbar_wait_abortable<PAIR>(smem_u32(&bar_tfull[as]), acc_phase, p.wait_ns, abort_v))) {
@@ -860,10 +886,10 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
   }
 }
 
-template <int N, bool GATEUP, bool NV, int OP = kOpFp4, bool PAIR = false>
+template <int N, bool GATEUP, bool NV, int OP = kOpFp4, bool PAIR = false, bool GROUPED = false>
 cudaError_t launch_gemm_t(const KParams& p, int grid, cudaStream_t s) {
   using C = GemmCfg<N, GATEUP, NV, OP, PAIR>;
-  auto k = moe_gemm_kernel<N, GATEUP, NV, OP, PAIR>;
+  auto k = moe_gemm_kernel<N, GATEUP, NV, OP, PAIR, GROUPED>;
   static bool attr_set[64] = {};  // once per device and template instance
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -9,12 +9,17 @@ namespace fp4moe {
 // L2 bytes the down GEMM's combine rows of one unit group may take (of the
 // 126 MB): the group's G weight tiles x 128 rows x T tokens x fp32.
 constexpr int64_t kCombineL2Bytes = 48ll << 20;
+// Combine buffers up to this size keep the expert-major order: measured, a
+// 4096-token layer (117 MB) gained nothing from groups, a 16384-token layer
+// (470 MB) 19% of its down GEMM.
+constexpr int64_t kCombineGroupAbove = 256ll << 20;
 
 // Weight tiles per group of the down GEMM's unit order: the largest divisor
-// of M whose combine rows fit kCombineL2Bytes (M when they all fit, or when
-// each token has one route, so that no row is added twice).
+// of M whose combine rows fit kCombineL2Bytes; M (expert-major) when the
+// whole buffer is small, or when each token has one route, so that no row
+// is added twice.
 inline int combine_group(int M, int64_t T, int routes_per_token) {
-  if (routes_per_token <= 1 || T * M * 512 <= kCombineL2Bytes) return M;
+  if (routes_per_token <= 1 || T * M * 512 <= kCombineGroupAbove) return M;
   int g = 1;
   for (int c = 1; c <= M; ++c)
     if (M % c == 0 && T * c * 512 <= kCombineL2Bytes) g = c;
@@ -98,7 +103,9 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   p.rows_per_expert = rows;
   p.m_tiles = GATEUP ? d.I / 128 : vis / 128;
   p.unit_mtiles = GATEUP ? d.I / 128 : vis / (a.dn_cta_pair ? 256 : 128);
-  p.m_group = GATEUP ? p.unit_mtiles : combine_group(p.unit_mtiles, d.T, d.top_k + d.n_shared);
+  // grouped unit order: the paired-slot MXFP4 down instance only (the other
+  // instances take units expert-major)
+  p.m_group = (GATEUP || a.dn_pair != 2) ? p.unit_mtiles : combine_group(p.unit_mtiles, d.T, d.top_k + d.n_shared);
   p.katoms_a = (int)katoms_padded(K, a.nv);
   p.katoms_b = (int)katoms_padded(K, a.nv);
   p.katoms_h = (int)katoms_padded(d.I, a.nv);
@@ -130,8 +137,10 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
       if (a.n_tile != 112 || a.nv || a.f8 || a.bf) return cudaErrorInvalidValue;
       if (a.dn_cta_pair) {
         if (vis % 256 != 0) return cudaErrorInvalidValue;
+        p.m_group = p.unit_mtiles;  // (expert-major order only)
         return launch_gemm_t<240, false, false, kOpFp4, true>(p, grid, s);
       }
+      if (p.m_group < p.unit_mtiles) return launch_gemm_t<240, false, false, kOpFp4, false, true>(p, grid, s);
       return launch_gemm_t<240, false, false>(p, grid, s);
     }
   }

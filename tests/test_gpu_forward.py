@@ -62,7 +62,7 @@ SMALL = {
     "front_T16_shared": _cfg("tiny", name="front_T16_shared", T=16, H=768, I=256, E=24, top_k=4, n_shared=1),
     "front_cluster3": _cfg("tiny", name="front_cluster3", T=9, H=2304, I=256, E=40, top_k=3),
     "wide_padK": _cfg("tiny", name="wide_padK", T=300, H=1024, I=384, E=8, top_k=2, routed_scaling=2.827),
-    # >= 160 routes per expert: the down GEMM's units cover two 112-token
+    # >= 80 routes per expert: the down GEMM's units cover two 112-token
     # slots (full pairs and single-slot remainders)
     "paired_padK": _cfg("tiny", name="paired_padK", T=600, H=1024, I=384, E=4, top_k=2, routed_scaling=2.827),
     # paired slots on CTA pairs (256-row units) with a shared expert (paired
