@@ -43,7 +43,8 @@ class Dims(ctypes.Structure):
 
 
 class Weights(ctypes.Structure):
-    """fp4moe_weights; packed = 1: payloads in the tiled layout of pack_weights."""
+    """fp4moe_weights; packed = 1: payloads in the tiled layout of pack_weights;
+    2: as 1 with w13 / sh13 and their scales in the gate/up-paired layouts."""
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("w13", "w13_scale", "w2", "w2_scale", "g13", "g2", "sh13", "sh13_scale", "sh2",
                  "sh2_scale", "w_router", "bias")] + [("packed", ctypes.c_int32)]
@@ -95,6 +96,8 @@ def lib() -> ctypes.CDLL:
         L.fp4moe_packed_weights_bytes.argtypes = [i64, i32, i32]
         L.fp4moe_packed_weights_bytes.restype = sz
         L.fp4moe_pack_weights.argtypes = [vp, vp, i64, i32, i32, vp]
+        L.fp4moe_pack_gateup_weights.argtypes = [vp, vp, i64, i32, i32, vp]
+        L.fp4moe_pack_gateup_scales.argtypes = [vp, vp, i64, i32, i32, i32, vp]
         L.fp4moe_route.argtypes = [P(Dims), vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.fp4moe_quantize_act.argtypes = [vp, i32, i64, i32, i32, vp, vp, vp, vp, vp, sz, vp]
         L.fp4moe_forward.argtypes = [P(Dims), P(Weights), vp, vp, P(Debug), vp, sz, vp]
@@ -114,7 +117,8 @@ def lib() -> ctypes.CDLL:
         L.fp4moe_route_noalloc_scratch_bytes.argtypes = [P(Dims)]
         L.fp4moe_route_noalloc_scratch_bytes.restype = sz
         L.fp4moe_route_noalloc_status.argtypes = [vp, P(i32), P(i64)]
-        for name in ("fp4moe_workspace_layout", "fp4moe_pack_scales", "fp4moe_pack_weights", "fp4moe_route", "fp4moe_quantize_act",
+        for name in ("fp4moe_workspace_layout", "fp4moe_pack_scales", "fp4moe_pack_weights", "fp4moe_pack_gateup_weights",
+                     "fp4moe_pack_gateup_scales", "fp4moe_route", "fp4moe_quantize_act",
                      "fp4moe_forward", "fp4moe_forward_cols", "fp4moe_forward_w8a8", "fp4moe_forward_nvfp4_emulated", "fp4moe_linear",
                      "fp4moe_mxfp4_to_fp8_rowscale",
                      "fp4moe_clear_status",
@@ -172,6 +176,14 @@ def packed_weights_bytes(n_mat: int, rows: int, kbytes: int) -> int:
 
 def pack_weights(src: int, dst: int, n_mat: int, rows: int, kbytes: int, stream: int = 0) -> None:
     _ok(lib().fp4moe_pack_weights(src, dst, n_mat, rows, kbytes, stream), "fp4moe_pack_weights")
+
+
+def pack_gateup_weights(src: int, dst: int, n_mat: int, I: int, kbytes: int, stream: int = 0) -> None:
+    _ok(lib().fp4moe_pack_gateup_weights(src, dst, n_mat, I, kbytes, stream), "fp4moe_pack_gateup_weights")
+
+
+def pack_gateup_scales(src: int, dst: int, n_mat: int, I: int, kblocks: int, fmt: int, stream: int = 0) -> None:
+    _ok(lib().fp4moe_pack_gateup_scales(src, dst, n_mat, I, kblocks, fmt, stream), "fp4moe_pack_gateup_scales")
 
 
 def route(dims: Dims, x: int, w_router: int, bias: int, topk_idx: int, topk_w: int, logits_out: int | None,

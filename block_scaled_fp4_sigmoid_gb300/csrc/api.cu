@@ -276,7 +276,18 @@ fp4moe_status fp4moe_pack_scales(const uint8_t* src, uint8_t* dst, int64_t n_mat
   if (fp4moe_packed_scales_bytes(n_mat, rows, kblocks, fmt) == 0 && n_mat != 0) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
   if (fmt != FP4MOE_MXFP4 && fmt != FP4MOE_NVFP4) return FP4MOE_ERR_INVALID_ARG;
   if (fp4moe_status st = check_device()) return st;
-  return cuda_status(launch_pack_scales(src, dst, n_mat, rows, kblocks, fmt == FP4MOE_NVFP4,
+  return cuda_status(launch_pack_scales(src, dst, n_mat, rows, kblocks, fmt == FP4MOE_NVFP4, 0,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+fp4moe_status fp4moe_pack_gateup_scales(const uint8_t* src, uint8_t* dst, int64_t n_mat, int32_t I, int32_t kblocks,
+                                        int32_t fmt, void* stream) {
+  if (!src || !dst) return FP4MOE_ERR_INVALID_ARG;
+  if (I <= 0 || I % 128 != 0) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  if (fp4moe_packed_scales_bytes(n_mat, 2 * I, kblocks, fmt) == 0 && n_mat != 0) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  if (fmt != FP4MOE_MXFP4 && fmt != FP4MOE_NVFP4) return FP4MOE_ERR_INVALID_ARG;
+  if (fp4moe_status st = check_device()) return st;
+  return cuda_status(launch_pack_scales(src, dst, n_mat, 2 * I, kblocks, fmt == FP4MOE_NVFP4, I / 128,
                                         static_cast<cudaStream_t>(stream)));
 }
 
@@ -290,7 +301,16 @@ fp4moe_status fp4moe_pack_weights(const uint8_t* src, uint8_t* dst, int64_t n_ma
   if (!src || !dst) return FP4MOE_ERR_INVALID_ARG;
   if (fp4moe_packed_weights_bytes(n_mat, rows, kbytes) == 0 && n_mat != 0) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
   if (fp4moe_status st = check_device()) return st;
-  return cuda_status(launch_pack_weights(src, dst, n_mat * rows, kbytes, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_pack_weights(src, dst, n_mat * rows, kbytes, 0, static_cast<cudaStream_t>(stream)));
+}
+
+fp4moe_status fp4moe_pack_gateup_weights(const uint8_t* src, uint8_t* dst, int64_t n_mat, int32_t I, int32_t kbytes,
+                                         void* stream) {
+  if (!src || !dst) return FP4MOE_ERR_INVALID_ARG;
+  if (I <= 0 || I % 128 != 0) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  if (fp4moe_packed_weights_bytes(n_mat, 2 * I, kbytes) == 0 && n_mat != 0) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
+  if (fp4moe_status st = check_device()) return st;
+  return cuda_status(launch_pack_weights(src, dst, n_mat * 2 * I, kbytes, I / 128, static_cast<cudaStream_t>(stream)));
 }
 
 fp4moe_status fp4moe_route(const fp4moe_dims* dims, const uint16_t* x, const uint16_t* w_router, const float* bias,
@@ -355,6 +375,7 @@ static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights*
   const int dn_mtiles = (h_end - h_begin) / (dn_cta ? 256 : 128);  // weight-row tiles per down unit row
   if (!w->w13 || !w->w13_scale || !w->w2 || !w->w2_scale || !w->w_router || !w->bias) return FP4MOE_ERR_INVALID_ARG;
   if (nv && (!w->g13 || !w->g2)) return FP4MOE_ERR_INVALID_ARG;
+  if (w->packed < 0 || w->packed > 2) return FP4MOE_ERR_INVALID_ARG;
   if (d.n_shared && (!w->sh13 || !w->sh13_scale || !w->sh2 || !w->sh2_scale)) return FP4MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w->w13) || !aligned16(w->w2) || !aligned16(w->w13_scale) ||
       !aligned16(w->w2_scale) || !aligned16(w->w_router) || !aligned16(ws) || !aligned16(out))
@@ -485,6 +506,7 @@ static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights*
     GemmArgs g = a;
     g.w = w->w13;
     g.w_tiled = w->packed != 0;
+    g.gu_pairs = w->packed == 2 ? d.I / 128 : 0;
     g.wsf = w->w13_scale;
     g.sh = d.n_shared ? w->sh13 : nullptr;
     g.shsf = d.n_shared ? w->sh13_scale : nullptr;
@@ -679,6 +701,7 @@ fp4moe_status fp4moe_forward_nvfp4_emulated(const fp4moe_dims* dims, const fp4mo
   if (!w->w13 || !w->w13_scale || !w->w2 || !w->w2_scale || !w->g13 || !w->g2 || !w->w_router || !w->bias)
     return FP4MOE_ERR_INVALID_ARG;
   if (d.n_shared && (!w->sh13 || !w->sh13_scale || !w->sh2 || !w->sh2_scale)) return FP4MOE_ERR_INVALID_ARG;
+  if (w->packed < 0 || w->packed > 2) return FP4MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w->w13) || !aligned16(w->w2) || !aligned16(w->w_router) || !aligned16(ws) ||
       !aligned16(out))
     return FP4MOE_ERR_INVALID_ARG;
@@ -736,12 +759,12 @@ fp4moe_status fp4moe_forward_nvfp4_emulated(const fp4moe_dims* dims, const fp4mo
   if (e == cudaSuccess) e = rec(3);
   // BF16 copies of the dispatched experts' weights (at GEMM time, as the
   // emulation pipeline does) and of the QDQ'd activations
-  if (e == cudaSuccess) e = launch_nv_weight_bf16(w->w13, w->packed != 0, w->w13_scale, w->g13, d.E, 2 * d.I, d.H, ecount, w13b, s);
-  if (e == cudaSuccess) e = launch_nv_weight_bf16(w->w2, w->packed != 0, w->w2_scale, w->g2, d.E, d.H, d.I, ecount, w2b, s);
+  if (e == cudaSuccess) e = launch_nv_weight_bf16(w->w13, w->packed != 0, w->packed == 2 ? d.I / 128 : 0, w->w13_scale, w->g13, d.E, 2 * d.I, d.H, ecount, w13b, s);
+  if (e == cudaSuccess) e = launch_nv_weight_bf16(w->w2, w->packed != 0, 0, w->w2_scale, w->g2, d.E, d.H, d.I, ecount, w2b, s);
   if (e == cudaSuccess && d.n_shared)
-    e = launch_nv_weight_bf16(w->sh13, w->packed != 0, w->sh13_scale, w->g13 + d.E, 1, 2 * d.I, d.H, nullptr, sh13b, s);
+    e = launch_nv_weight_bf16(w->sh13, w->packed != 0, w->packed == 2 ? d.I / 128 : 0, w->sh13_scale, w->g13 + d.E, 1, 2 * d.I, d.H, nullptr, sh13b, s);
   if (e == cudaSuccess && d.n_shared)
-    e = launch_nv_weight_bf16(w->sh2, w->packed != 0, w->sh2_scale, w->g2 + d.E, 1, d.H, d.I, nullptr, sh2b, s);
+    e = launch_nv_weight_bf16(w->sh2, w->packed != 0, 0, w->sh2_scale, w->g2 + d.E, 1, d.H, d.I, nullptr, sh2b, s);
   if (e == cudaSuccess) e = launch_amax(x, 0, (int64_t)d.T * d.H, amax, s);
   if (e == cudaSuccess) e = launch_nv_qdq_x_bf16(d, x, route_row, amax, gscale, xb, s);
   if (e == cudaSuccess) e = rec(4);

@@ -531,8 +531,19 @@ __device__ __forceinline__ void nv_quant16(const float* v, float g, uint32_t* pa
 // fp4moe_pack_weights: blocks of 128 rows x 128 bytes (one K tile of 256
 // values), K tiles innermost, rows counted over all matrices (rows per
 // matrix a multiple of 128); ktb = K tiles per row.
-__host__ __device__ __forceinline__ int64_t w_tiled_offset(int64_t r, int64_t cb, int64_t ktb) {
-  return (((r >> 7) * ktb + (cb >> 7)) << 14) + ((r & 127) << 7) + (cb & 127);
+// Block (row tile rt, K tile kt) of the tiled layouts sits at slot
+// rt * KT + kt.  Gate/up-paired (P = I / 128 > 0, matrices of 2P row tiles:
+// gate tiles 0..P-1, up tiles P..2P-1): the gate and up blocks of pair p and
+// K tile kt are adjacent, slot ((m * P + p) * KT + kt) * 2 + h (h: 0 gate,
+// 1 up), so that one copy fetches both.
+__host__ __device__ __forceinline__ int64_t tile_slot(int64_t rt, int64_t kt, int64_t ktiles, int64_t pairs) {
+  if (pairs == 0) return rt * ktiles + kt;
+  const int64_t m = rt / (2 * pairs), lr = rt - m * 2 * pairs, h = lr / pairs, pp = lr - h * pairs;
+  return ((m * pairs + pp) * ktiles + kt) * 2 + h;
+}
+
+__host__ __device__ __forceinline__ int64_t w_tiled_offset(int64_t r, int64_t cb, int64_t ktb, int64_t pairs = 0) {
+  return (tile_slot(r >> 7, cb >> 7, ktb, pairs) << 14) + ((r & 127) << 7) + (cb & 127);
 }
 
 // ---------------------------------------------------------------- tiled scale layout
@@ -541,6 +552,13 @@ __host__ __device__ __forceinline__ int64_t w_tiled_offset(int64_t r, int64_t cb
 //   ((r / 128) * katoms + kb / 4) * 512 + 16 * (r % 32) + 4 * ((r / 32) % 4) + kb % 4.
 __host__ __device__ __forceinline__ int64_t sf_tiled_offset(int64_t r, int64_t kb, int64_t katoms) {
   return ((r >> 7) * katoms + (kb >> 2)) * 512 + 16 * (r & 31) + 4 * ((r >> 5) & 3) + (kb & 3);
+}
+// The same in the gate/up-paired order (tile_slot): `apk` groups per K tile.
+__host__ __device__ __forceinline__ int64_t sf_tiled_offset_gu(int64_t r, int64_t kb, int64_t katoms, int64_t apk,
+                                                               int64_t pairs) {
+  const int64_t atom = kb >> 2, kt = atom / apk;
+  return (tile_slot(r >> 7, kt, katoms / apk, pairs) * apk + (atom - kt * apk)) * 512 + 16 * (r & 31) +
+         4 * ((r >> 5) & 3) + (kb & 3);
 }
 
 // Scale-block groups per 256-value K tile: MXFP4 8 blocks = 2 groups,

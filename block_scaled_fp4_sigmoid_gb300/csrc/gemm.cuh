@@ -69,6 +69,7 @@ struct KParams {
   int E, n_exp, H, I, K, rows_per_expert, m_tiles, katoms_a, katoms_b, katoms_h, has_shared, T;
   int plan_early;  // the plan was written at least two kernels back (see the kernel)
   int w_tiled;     // weights in the tiled layout (tmA / tmA_sh are views of 128-byte rows)
+  int gu_pairs;    // gate/up: weights and scales in the gate/up-paired tiled order (I / 128 pairs), else 0
   int unit_mtiles;  // weight tiles per unit row (128 rows each; 256 on CTA pairs)
   int m_group;      // weight tiles per group of the unit order (divides unit_mtiles)
   uint64_t wait_ns;  // limit of the pipeline waits (drains keep kWaitLimitNs)
@@ -332,6 +333,8 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
     st.two = C::kPairSlots == 2 && cnt > 112;
     st.sfa0 = sfw + ((int64_t)(st.ec * rt_per_e + (st.row0 >> 7)) * p.katoms_a) * 512;
     st.sfa1 = sfw + ((int64_t)(st.ec * rt_per_e + (st.row1 >> 7)) * p.katoms_a) * 512;
+    if (GATEUP && p.gu_pairs)  // paired order: gate then up scale groups of each K tile, kSFBytes apart
+      st.sfa0 = sfw + ((int64_t)(st.ec * p.gu_pairs + mt) * KT) * 2 * C::kSFBytes;
     st.sfb = p.bsf + ((int64_t)st.slot * p.katoms_b) * 512;
     return st;
   };
@@ -345,6 +348,19 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
   auto a_x = [&](int kt) { return p.w_tiled ? 0 : kt * 128; };
   auto a_y = [&](int row, int kt) { return p.w_tiled ? ((row >> 7) * KT + kt) * 128 : row; };
   auto load_weights = [&](const Step& st, int kt, uint32_t base, uint32_t fb) {
+    if constexpr (GATEUP && SF) {
+      if (p.gu_pairs) {  // paired order: one box of the gate and up blocks, one copy of both scale groups
+        const int y = ((st.row0 >> 7) * KT + kt) * 256;
+        if (st.once) {
+          tma_load_3d_hint(base, st.tmA, fb, 0, y, st.ec, pol_once);
+          bulk_load_hint(base + C::kOffSFA0, st.sfa0 + kt * 2 * C::kSFBytes, 2 * C::kSFBytes, fb, pol_once);
+        } else {
+          tma_load_3d(base, st.tmA, fb, 0, y, st.ec);
+          bulk_load(base + C::kOffSFA0, st.sfa0 + kt * 2 * C::kSFBytes, 2 * C::kSFBytes, fb);
+        }
+        return;
+      }
+    }
     if (st.once) {
       tma_load_3d_hint(base, st.tmA, fb, a_x(kt), a_y(st.row0, kt), st.ec, pol_once);
       if constexpr (GATEUP)

@@ -49,16 +49,20 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   const uint64_t a_row = a.w_tiled ? KTb * 128 : Kb;
   const uint64_t a_dim0 = a.w_tiled ? 128 : Kb, a_dim1 = a.w_tiled ? (uint64_t)vis * KTb : (uint64_t)vis;
   const uint64_t a_mat = (uint64_t)rows * a_row;
+  // gate/up-paired tiles (gu_pairs): one box of 256 view rows holds the gate
+  // and the up block of a (pair, K tile)
+  const bool gu_paired = GATEUP && a.w_tiled && a.gu_pairs > 0;
+  const uint32_t box_rows = gu_paired ? 256 : 128;
   {
     const uint64_t dims[3] = {a_dim0, a_dim1, (uint64_t)d.E};
     const uint64_t strides[2] = {a_dim0, a_mat};
-    const uint32_t box[3] = {128, 128, 1};
+    const uint32_t box[3] = {128, box_rows, 1};
     if (!encode_tmap_u8(&p.tmA, a.w + (uint64_t)r0 * a_row, 3, dims, strides, box, true)) return cudaErrorInvalidValue;
   }
   if (a.sh) {
     const uint64_t dims[3] = {a_dim0, a_dim1, 1};
     const uint64_t strides[2] = {a_dim0, a_mat};
-    const uint32_t box[3] = {128, 128, 1};
+    const uint32_t box[3] = {128, box_rows, 1};
     if (!encode_tmap_u8(&p.tmA_sh, a.sh + (uint64_t)r0 * a_row, 3, dims, strides, box, true))
       return cudaErrorInvalidValue;
   }
@@ -111,6 +115,7 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   p.katoms_h = (int)katoms_padded(d.I, a.nv);
   p.has_shared = a.sh != nullptr;
   p.w_tiled = a.w_tiled ? 1 : 0;
+  p.gu_pairs = gu_paired ? a.gu_pairs : 0;
   p.wait_ns = a.wait_ns ? a.wait_ns : kWaitLimitNs;
   p.withhold = (GATEUP && a.withhold) ? 1 : 0;
   p.wrs = a.wrs ? a.wrs + r0 : nullptr;

@@ -107,8 +107,10 @@ cudaError_t launch_h_quant_nv_routes(const fp4moe_dims& d, const float* h32, con
 cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, cudaStream_t s);
 // NVFP4 emulation: weights of touched experts to bf16 (count nullable: all
 // n_mat matrices; tiled: payloads in the layout of fp4moe_pack_weights); x and h through NVFP4 QDQ into bf16 rows
-cudaError_t launch_nv_weight_bf16(const uint8_t* codes, bool tiled, const uint8_t* sf, const float* g, int n_mat,
-                                  int rows, int K, const int32_t* count, uint16_t* out, cudaStream_t s);
+// pairs > 0: gate/up-paired tiled payloads and scales (P = I / 128 pairs per
+// matrix); 0: the plain tiled (or, tiled = false, row-major) payloads
+cudaError_t launch_nv_weight_bf16(const uint8_t* codes, bool tiled, int pairs, const uint8_t* sf, const float* g,
+                                  int n_mat, int rows, int K, const int32_t* count, uint16_t* out, cudaStream_t s);
 cudaError_t launch_nv_qdq_x_bf16(const fp4moe_dims& d, const uint16_t* x, const int32_t* route_row,
                                  const uint32_t* amax_x, float* g_out, uint16_t* xb, cudaStream_t s);
 cudaError_t launch_nv_qdq_h_bf16(const fp4moe_dims& d, const float* h32, const int32_t* route_row,
@@ -123,11 +125,12 @@ cudaError_t launch_fp8_h_quant(const fp4moe_dims& d, const float* h32, const int
 cudaError_t launch_quantize_rows(const void* x, int x_is_fp32, int64_t rows, int cols, bool nv,
                                  const float* global_in, const uint32_t* amax_bits, uint8_t* codes,
                                  uint8_t* scales, float* global_out, cudaStream_t s);
-cudaError_t launch_pack_weights(const uint8_t* src, uint8_t* dst, int64_t rows_total, int kbytes, cudaStream_t s);
+cudaError_t launch_pack_weights(const uint8_t* src, uint8_t* dst, int64_t rows_total, int kbytes, int pairs,
+                                cudaStream_t s);
 // NaN scale bytes (E8M0 255, E4M3 0x7F / 0xFF) of src[n] into the status word
 cudaError_t launch_nan_scales(const uint8_t* src, int64_t n, bool nv, int32_t* status, cudaStream_t s);
 cudaError_t launch_pack_scales(const uint8_t* src, uint8_t* dst, int64_t n_mat, int rows, int kblocks, bool nv,
-                               cudaStream_t s);
+                               int pairs, cudaStream_t s);
 cudaError_t launch_convert(const uint8_t* codes, const uint8_t* scales, int64_t rows, int K, uint8_t* out,
                            float* row_scale, uint8_t* row_status, int32_t* status, cudaStream_t s);
 
@@ -168,6 +171,7 @@ struct GemmArgs {
   uint64_t wait_ns;                // pipeline wait limit; 0: kWaitLimitNs
   bool withhold;                   // gate/up test knob (fp4moe_debug.withhold_first_stage)
   int dn_pair;                     // down, 112-token tiles: 2 = one unit covers two slots (224 tokens)
+  int gu_pairs;                    // gate/up: weights and scales in the gate/up-paired tiled order (I / 128), or 0
   bool dn_cta_pair;                // down, dn_pair 2: run on CTA pairs (units of 256 weight rows)
   // W8A8: channel scales of the weights (routed [E, rows], shared [rows]),
   // scales of the B rows (per permuted row); amax_h is then per permuted row

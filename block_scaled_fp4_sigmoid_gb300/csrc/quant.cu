@@ -273,7 +273,7 @@ __device__ __forceinline__ void nv_block_bf16(uint64_t codes, uint32_t sbyte, fl
 // whose expert has no routes (count[m] == 0) are skipped.  Grid: (.., n_mat).
 constexpr int kDqBlocksPerThread = 4;
 __global__ void nv_weight_bf16_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ sf,
-                                      const float* __restrict__ g, int rows, int K, bool tiled,
+                                      const float* __restrict__ g, int rows, int K, bool tiled, int pairs,
                                       const int32_t* __restrict__ count, uint16_t* __restrict__ out) {
   const int m = blockIdx.y;
   if (count && count[m] == 0) return;
@@ -288,9 +288,10 @@ __global__ void nv_weight_bf16_kernel(const uint8_t* __restrict__ codes, const u
        i += stride, ++j) {
     const int64_t r = (int64_t)m * rows + i / per_row;  // row over all matrices
     const int b = (int)(i % per_row);
-    const int64_t off = tiled ? w_tiled_offset(r, 8 * b, (K + 255) >> 8) : r * (K >> 1) + 8 * b;
+    const int64_t off = tiled ? w_tiled_offset(r, 8 * b, (K + 255) >> 8, pairs) : r * (K >> 1) + 8 * b;
     const uint64_t c = *reinterpret_cast<const uint64_t*>(codes + off);
-    nv_block_bf16(c, sf[sf_tiled_offset(r, b, katoms)], gm, reinterpret_cast<uint4*>(out + r * K + 16 * b));
+    const int64_t so = pairs ? sf_tiled_offset_gu(r, b, katoms, atoms_per_ktile(true), pairs) : sf_tiled_offset(r, b, katoms);
+    nv_block_bf16(c, sf[so], gm, reinterpret_cast<uint4*>(out + r * K + 16 * b));
   }
 }
 
@@ -347,15 +348,23 @@ __global__ void nv_qdq_h_bf16_kernel(const float* __restrict__ h32, int I, int64
 }
 
 __global__ void pack_scales_kernel(const uint8_t* src, uint8_t* dst, int64_t n_mat, int rows, int kblocks,
-                                   int64_t katoms, uint8_t pad) {
+                                   int64_t katoms, int apk, int pairs, uint8_t pad) {
   const int64_t words = n_mat * (rows / 128) * katoms * 128;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (tid >= words) return;
-  const int64_t grp = tid >> 7;  // (matrix, row tile, atom)
+  const int64_t grp = tid >> 7;  // group of the destination: (matrix, row tile, atom) in tile-slot order
   const int w = (int)(tid & 127);
   const int m0 = w >> 2, m1 = w & 3;
-  const int64_t atom = grp % katoms;
-  const int64_t mt = grp / katoms;  // matrix * row tiles + row tile
+  int64_t atom = grp % katoms;
+  int64_t mt = grp / katoms;  // matrix * row tiles + row tile
+  if (pairs) {  // gate/up-paired slots: slot = ((m * P + p) * KT + kt) * 2 + h, apk groups each
+    const int64_t kts = katoms / apk;
+    const int64_t slot = grp / apk, a = grp - slot * apk;
+    const int64_t h = slot & 1, t = slot >> 1, kt = t % kts, mp = t / kts;
+    const int64_t m = mp / pairs, pp = mp - m * pairs;
+    mt = m * 2 * pairs + h * pairs + pp;
+    atom = kt * apk + a;
+  }
   const int64_t row = mt * 128 + 32 * m1 + m0;  // global row over all matrices
   uint32_t word = 0;
 #pragma unroll
@@ -715,12 +724,12 @@ cudaError_t launch_fp8_h_quant(const fp4moe_dims& d, const float* h32, const int
   return cudaGetLastError();
 }
 
-cudaError_t launch_nv_weight_bf16(const uint8_t* codes, bool tiled, const uint8_t* sf, const float* g, int n_mat,
-                                  int rows, int K, const int32_t* count, uint16_t* out, cudaStream_t s) {
+cudaError_t launch_nv_weight_bf16(const uint8_t* codes, bool tiled, int pairs, const uint8_t* sf, const float* g,
+                                  int n_mat, int rows, int K, const int32_t* count, uint16_t* out, cudaStream_t s) {
   if (n_mat <= 0) return cudaSuccess;
   const int64_t n = (int64_t)rows * (K >> 4);
   const dim3 grid((unsigned)blocks_for((n + kDqBlocksPerThread - 1) / kDqBlocksPerThread, 256), (unsigned)n_mat);
-  nv_weight_bf16_kernel<<<grid, 256, 0, s>>>(codes, sf, g, rows, K, tiled, count, out);
+  nv_weight_bf16_kernel<<<grid, 256, 0, s>>>(codes, sf, g, rows, K, tiled, pairs, count, out);
   return cudaGetLastError();
 }
 
@@ -754,23 +763,30 @@ cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, cudaStre
 // 512 contiguous bytes and reads four 128-byte row pieces; bytes past
 // kbytes (K padded to whole K tiles) are zero codes.
 __global__ void pack_weights_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t n16,
-                                    int kbytes, int ktb) {
+                                    int kbytes, int ktb, int pairs) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t blk = i >> 10;          // 1024 pieces of 16 bytes per 128 x 128-byte block
-    const int64_t r = (blk / ktb) * 128 + ((i >> 3) & 127);
-    const int cb = (int)(blk % ktb) * 128 + (int)(i & 7) * 16;
+    const int64_t blk = i >> 10;          // 1024 pieces of 16 bytes per 128 x 128-byte block (tile slot)
+    int64_t rt = blk / ktb, kt = blk % ktb;
+    if (pairs) {  // gate/up-paired slots: slot = ((m * P + p) * KT + kt) * 2 + h
+      const int64_t h = blk & 1, t = blk >> 1, mp = t / ktb, m = mp / pairs, pp = mp - m * pairs;
+      kt = t - mp * ktb;
+      rt = m * 2 * pairs + h * pairs + pp;
+    }
+    const int64_t r = rt * 128 + ((i >> 3) & 127);
+    const int cb = (int)kt * 128 + (int)(i & 7) * 16;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (cb < kbytes) v = *reinterpret_cast<const uint4*>(src + r * kbytes + cb);
     reinterpret_cast<uint4*>(dst)[i] = v;
   }
 }
 
-cudaError_t launch_pack_weights(const uint8_t* src, uint8_t* dst, int64_t rows_total, int kbytes, cudaStream_t s) {
+cudaError_t launch_pack_weights(const uint8_t* src, uint8_t* dst, int64_t rows_total, int kbytes, int pairs,
+                                cudaStream_t s) {
   const int ktb = (kbytes + 127) / 128;
   const int64_t n16 = rows_total * ktb * 8;
   if (n16 == 0) return cudaSuccess;
   const int64_t blocks = std::min<int64_t>(blocks_for(n16, 256), 1 << 20);
-  pack_weights_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, dst, n16, kbytes, ktb);
+  pack_weights_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, dst, n16, kbytes, ktb, pairs);
   return cudaGetLastError();
 }
 
@@ -811,12 +827,12 @@ cudaError_t launch_nan_scales(const uint8_t* src, int64_t n, bool nv, int32_t* s
 }
 
 cudaError_t launch_pack_scales(const uint8_t* src, uint8_t* dst, int64_t n_mat, int rows, int kblocks, bool nv,
-                               cudaStream_t s) {
+                               int pairs, cudaStream_t s) {
   const int64_t katoms = katoms_padded((int64_t)kblocks * (nv ? 16 : 32), nv);
   const int64_t words = n_mat * (rows / 128) * katoms * 128;
   if (words == 0) return cudaSuccess;
   pack_scales_kernel<<<blocks_for(words, 256), 256, 0, s>>>(src, dst, n_mat, rows, kblocks, katoms,
-                                                            nv ? 0x38 : 127);
+                                                            atoms_per_ktile(nv), pairs, nv ? 0x38 : 127);
   return cudaGetLastError();
 }
 

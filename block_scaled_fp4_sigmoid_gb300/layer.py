@@ -19,7 +19,8 @@ import torch
 from . import (FP8, MXFP4, NVFP4, Debug, Fp8Weights, Weights, check_scales, emulation_workspace_size, forward,
                forward_cols,
                forward_nvfp4_emulated, forward_w8a8, get_status, make_dims,
-               mxfp4_to_fp8_rowscale, pack_scales, pack_weights, packed_scales_bytes, packed_weights_bytes,
+               mxfp4_to_fp8_rowscale, pack_gateup_scales, pack_gateup_weights, pack_scales, pack_weights,
+               packed_scales_bytes, packed_weights_bytes,
                quantize_act, workspace_layout, workspace_size)
 
 
@@ -55,27 +56,30 @@ class MoELayer:
         """Tensors on one CUDA device.  Scales are the raw row-major block
         scales ([E, rows, K/32] E8M0 or [E, rows, K/16] E4M3); they are
         repacked here into the layout the GEMMs load.  packed: the forward
-        reads the payloads in the tiled layout (fp4moe_pack_weights), else the
-        row-major tensors themselves; the row-major tensors are kept either
-        way (the FP8 conversion reads them)."""
+        reads the payloads in the tiled layout (fp4moe_pack_weights; gate/up
+        matrices and their scales in the gate/up-paired order of
+        fp4moe_pack_gateup_weights / _scales), else the row-major tensors
+        themselves; the row-major tensors are kept either way (the FP8
+        conversion reads them)."""
         self.dims = dims
         self.fmt = dims.fmt
         self.device = w13.device
         self.raw = dict(w13_scale=w13_scale, w2_scale=w2_scale, sh13_scale=sh13_scale, sh2_scale=sh2_scale)
         blk = 16 if dims.fmt == NVFP4 else 32
         self.w13, self.w2 = w13.contiguous(), w2.contiguous()
-        self.w13_scale = self._pack(w13_scale, dims.E, 2 * dims.I, dims.H // blk)
+        self.w13_scale = self._pack(w13_scale, dims.E, 2 * dims.I, dims.H // blk, gateup=packed)
         self.w2_scale = self._pack(w2_scale, dims.E, dims.H, dims.I // blk)
         self.w_router, self.bias = w_router.contiguous(), bias.contiguous()
         self.g13, self.g2 = g13, g2
         self.sh13, self.sh2 = sh13, sh2
-        self.sh13_scale = self._pack(sh13_scale, 1, 2 * dims.I, dims.H // blk) if sh13 is not None else None
+        self.sh13_scale = (self._pack(sh13_scale, 1, 2 * dims.I, dims.H // blk, gateup=packed) if sh13 is not None
+                           else None)
         self.sh2_scale = self._pack(sh2_scale, 1, dims.H, dims.I // blk) if sh2 is not None else None
         self.packed = packed
-        pw = self._pack_w if packed else (lambda t, *_: t)
-        self.w13_t = pw(self.w13, dims.E, 2 * dims.I, dims.H // 2)
+        pw = self._pack_w if packed else (lambda t, *_, **__: t)
+        self.w13_t = pw(self.w13, dims.E, 2 * dims.I, dims.H // 2, gateup=True)
         self.w2_t = pw(self.w2, dims.E, dims.H, dims.I // 2)
-        self.sh13_t = pw(sh13, 1, 2 * dims.I, dims.H // 2) if sh13 is not None else None
+        self.sh13_t = pw(sh13, 1, 2 * dims.I, dims.H // 2, gateup=True) if sh13 is not None else None
         self.sh2_t = pw(sh2, 1, dims.H, dims.I // 2) if sh2 is not None else None
         self._check_scales()
         self.ws_bytes = workspace_size(dims)
@@ -84,7 +88,7 @@ class MoELayer:
         self.weights = Weights(_ptr(self.w13_t), _ptr(self.w13_scale), _ptr(self.w2_t), _ptr(self.w2_scale),
                                _ptr(self.g13), _ptr(self.g2), _ptr(self.sh13_t), _ptr(self.sh13_scale),
                                _ptr(self.sh2_t), _ptr(self.sh2_scale), _ptr(self.w_router), _ptr(self.bias),
-                               1 if packed else 0)
+                               2 if packed else 0)
 
     def _check_scales(self):
         """Refuses weights with NaN block scales (fp4moe_check_scales): the
@@ -98,17 +102,23 @@ class MoELayer:
         if st != 0:
             raise ValueError(f"{n} NaN block-scale bytes in the expert weights (status {st})")
 
-    def _pack_w(self, codes, n_mat, rows, kbytes):
+    def _pack_w(self, codes, n_mat, rows, kbytes, gateup=False):
         dst = torch.empty(packed_weights_bytes(n_mat, rows, kbytes), dtype=torch.uint8, device=codes.device)
-        pack_weights(codes.data_ptr(), dst.data_ptr(), n_mat, rows, kbytes,
-                     torch.cuda.current_stream(codes.device).cuda_stream)
+        s = torch.cuda.current_stream(codes.device).cuda_stream
+        if gateup:  # rows = 2I: gate/up-paired tiles
+            pack_gateup_weights(codes.data_ptr(), dst.data_ptr(), n_mat, rows // 2, kbytes, s)
+        else:
+            pack_weights(codes.data_ptr(), dst.data_ptr(), n_mat, rows, kbytes, s)
         return dst
 
-    def _pack(self, raw, n_mat, rows, kblocks):
+    def _pack(self, raw, n_mat, rows, kblocks, gateup=False):
         dst = torch.empty(packed_scales_bytes(n_mat, rows, kblocks, self.fmt), dtype=torch.uint8,
                           device=raw.device)
-        pack_scales(raw.data_ptr(), dst.data_ptr(), n_mat, rows, kblocks, self.fmt,
-                    torch.cuda.current_stream(raw.device).cuda_stream)
+        s = torch.cuda.current_stream(raw.device).cuda_stream
+        if gateup:  # rows = 2I: gate/up-paired scale groups
+            pack_gateup_scales(raw.data_ptr(), dst.data_ptr(), n_mat, rows // 2, kblocks, self.fmt, s)
+        else:
+            pack_scales(raw.data_ptr(), dst.data_ptr(), n_mat, rows, kblocks, self.fmt, s)
         return dst
 
     def weight_bytes_per_expert(self) -> int:
@@ -238,7 +248,7 @@ class MoELayer:
         v.emu_ws = None
         v.weights = Weights(_ptr(v.w13_t), _ptr(v.w13_scale), _ptr(v.w2_t), _ptr(v.w2_scale), _ptr(v.g13),
                             _ptr(v.g2), _ptr(v.sh13_t), _ptr(v.sh13_scale), _ptr(v.sh2_t), _ptr(v.sh2_scale),
-                            _ptr(v.w_router), _ptr(v.bias), 1 if v.packed else 0)
+                            _ptr(v.w_router), _ptr(v.bias), 2 if v.packed else 0)
         return v
 
     def synthetic_x(self, t0: int = 0, t1: int | None = None):

@@ -94,7 +94,12 @@ typedef struct {
  *   w_router  bf16 [E, H].   bias  fp32 [E] correction bias.
  *   packed    0: the payloads w13, w2, sh13, sh2 are row-major as above;
  *             1: they hold the tiled layout of fp4moe_pack_weights (the
- *             GEMMs then read each weight tile as one contiguous block). */
+ *             GEMMs then read each weight tile as one contiguous block);
+ *             2: as 1, except that w13 and sh13 hold the gate/up-paired
+ *             layout of fp4moe_pack_gateup_weights and w13_scale and
+ *             sh13_scale that of fp4moe_pack_gateup_scales (the gate/up
+ *             GEMM then reads a K tile's gate and up blocks, and their
+ *             scale groups, with one copy each).  Other values: INVALID_ARG. */
 typedef struct {
   const uint8_t *w13, *w13_scale, *w2, *w2_scale;
   const float *g13, *g2;
@@ -225,6 +230,19 @@ size_t fp4moe_packed_scales_bytes(int64_t n_mat, int32_t rows, int32_t kblocks, 
 fp4moe_status fp4moe_pack_scales(const uint8_t *src, uint8_t *dst, int64_t n_mat, int32_t rows,
                                  int32_t kblocks, int32_t fmt, void *stream);
 
+/* The block scales of gate/up matrices src[n_mat, 2I, kblocks] (rows 0..I-1
+ * gate, I..2I-1 up; I % 128 == 0) in the gate/up-paired order: the same
+ * 512-byte groups as fp4moe_pack_scales, but per matrix ordered by pair p
+ * (row tiles p and p + I/128), K tile kt, then gate before up, so that the
+ * gate and up groups of one K tile are adjacent.  With A groups per K tile
+ * (MXFP4 2, NVFP4 4) and KT K tiles, group a of K tile kt of row tile
+ * h*(I/128) + p (h: 0 gate, 1 up) of matrix m sits at byte
+ *   ((((m*(I/128) + p)*KT + kt)*2 + h)*A + a) * 512.
+ * dst holds fp4moe_packed_scales_bytes(n_mat, 2I, kblocks, fmt) bytes.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE. */
+fp4moe_status fp4moe_pack_gateup_scales(const uint8_t *src, uint8_t *dst, int64_t n_mat, int32_t I,
+                                        int32_t kblocks, int32_t fmt, void *stream);
+
 /* Bytes of the tiled payload layout for n_mat FP4 matrices of `rows` rows
  * and `kbytes` bytes per row (rows % 128 == 0, kbytes % 16 == 0): each row
  * padded to whole K tiles of 128 bytes (256 FP4 values).  0 for an
@@ -245,6 +263,17 @@ size_t fp4moe_packed_weights_bytes(int64_t n_mat, int32_t rows, int32_t kbytes);
  * stream ordered.  Errors: INVALID_ARG (null pointer), UNSUPPORTED_SHAPE. */
 fp4moe_status fp4moe_pack_weights(const uint8_t *src, uint8_t *dst, int64_t n_mat, int32_t rows, int32_t kbytes,
                                   void *stream);
+
+/* The tiled payload layout of gate/up matrices src[n_mat, 2I, kbytes]
+ * (rows 0..I-1 gate, I..2I-1 up; I % 128 == 0) in the gate/up-paired order:
+ * the blocks of fp4moe_pack_weights, per matrix ordered by pair p, K tile kt,
+ * then gate before up.  Byte (r, c) of matrix m, with P = I/128,
+ * rt = r/128 = h*P + p, lands at
+ *   m*2I*KT*128 + (((p*KT + c/128)*2 + h))*16384 + (r%128)*128 + c%128.
+ * Same size as fp4moe_pack_weights(n_mat, 2I, kbytes).  Errors: INVALID_ARG,
+ * UNSUPPORTED_SHAPE. */
+fp4moe_status fp4moe_pack_gateup_weights(const uint8_t *src, uint8_t *dst, int64_t n_mat, int32_t I, int32_t kbytes,
+                                         void *stream);
 
 /* Router: logits, sigmoid + bias, grouped top-k and routing weights
  * ("Kimi-K2.7-Code on Gaudi 2", section "What was built").

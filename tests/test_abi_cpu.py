@@ -119,6 +119,40 @@ def test_tiled_payload_formula_in_the_header_matches_the_layout():
         assert tiled.size == fm.packed_weights_bytes(n_mat, rows, kbytes)
 
 
+def test_gateup_paired_formulas_in_the_header_match_the_layouts():
+    """The byte-offset formulas fp4moe.h prints for fp4moe_pack_gateup_weights
+    and fp4moe_pack_gateup_scales equal their definitions: the blocks (and the
+    scale groups) of the plain tiled layouts, reordered per matrix by (gate/up
+    pair, K tile, gate before up), written as numpy reshapes."""
+    import numpy as np
+    rng = np.random.default_rng(11)
+    for n_mat, I, kbytes in ((2, 128, 192), (1, 384, 512), (3, 256, 16)):
+        P, kt = I // 128, -(-kbytes // 128)
+        src = rng.integers(0, 256, (n_mat, 2 * I, kbytes), dtype=np.uint8)
+        pad = np.zeros((n_mat, 2 * I, kt * 128), dtype=np.uint8)
+        pad[..., :kbytes] = src
+        # [m, h, p, 128 rows, kt, 128 bytes] -> [m, p, kt, h, 128, 128]
+        paired = pad.reshape(n_mat, 2, P, 128, kt, 128).transpose(0, 2, 4, 1, 3, 5).reshape(-1)
+        m, r, c = np.meshgrid(np.arange(n_mat), np.arange(2 * I), np.arange(kbytes), indexing="ij")
+        h, p = (r // 128) // P, (r // 128) % P
+        off = m * 2 * I * kt * 128 + ((p * kt + c // 128) * 2 + h) * 16384 + (r % 128) * 128 + c % 128
+        assert np.array_equal(paired[off], src)
+    for n_mat, I, kblocks, A in ((2, 128, 8, 2), (1, 384, 24, 2), (2, 256, 16, 4)):
+        P = I // 128
+        katoms = -(-kblocks // (4 * A)) * A
+        kt = katoms // A
+        groups = rng.integers(0, 256, (n_mat, 2 * P, katoms, 512), dtype=np.uint8)  # plain tiled groups
+        # [m, h, p, kt, a, 512] -> [m, p, kt, h, a, 512]
+        paired = groups.reshape(n_mat, 2, P, kt, A, 512).transpose(0, 2, 3, 1, 4, 5).reshape(-1)
+        for mm in range(n_mat):
+            for rt in range(2 * P):
+                hh, pp = rt // P, rt % P
+                for k in range(kt):
+                    for a in range(A):
+                        off = ((((mm * P + pp) * kt + k) * 2 + hh) * A + a) * 512
+                        assert np.array_equal(paired[off:off + 512], groups[mm, rt, k * A + a])
+
+
 def _noalloc_scratch_formula(d, route_splits):
     """Scratch bytes of fp4moe_route_noalloc as the header states them: a
     256-byte status word, ceil(T/32) * (E + n_shared) * 4 bytes of counts
