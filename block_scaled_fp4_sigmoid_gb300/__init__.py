@@ -44,7 +44,8 @@ class Dims(ctypes.Structure):
 
 class Weights(ctypes.Structure):
     """fp4moe_weights; packed = 1: payloads in the tiled layout of pack_weights;
-    2: as 1 with w13 / sh13 and their scales in the gate/up-paired layouts."""
+    2: as 1 with w13 / sh13 and their scales in the gate/up-paired layouts;
+    3: as 2 with w2 / sh2 and their scales in the row-tile-paired layouts."""
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("w13", "w13_scale", "w2", "w2_scale", "g13", "g2", "sh13", "sh13_scale", "sh2",
                  "sh2_scale", "w_router", "bias")] + [("packed", ctypes.c_int32)]

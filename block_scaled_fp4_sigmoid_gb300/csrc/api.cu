@@ -60,6 +60,15 @@ bool fp4_down_cta_pair(int dn_pair, int out_rows, const fp4moe_debug* dbg) {
   return dbg && dbg->down_cta_pair && dn_pair == 2 && out_rows % 256 == 0;
 }
 
+// Where paired slots would be chosen and the output range is a multiple of
+// 256 rows, a down unit instead covers two adjacent weight tiles of one
+// 112-token tile: the gate/up GEMM's mainloop (two A operands, one issuer
+// each, one shared B tile), with the same operand bytes per FLOP as the
+// paired slots.  (The CTA-pair opt-in keeps the paired slots.)
+bool fp4_down_w2(int dn_pair, int out_rows, const fp4moe_debug* dbg) {
+  return dn_pair == 2 && out_rows % 256 == 0 && !(dbg && dbg->down_cta_pair);
+}
+
 int pick_n_tile(const fp4moe_dims& d) {
   const double avg = (double)d.T * d.top_k / d.E;
   // Every size keeps two accumulator sets in tensor memory (the epilogue of
@@ -370,12 +379,17 @@ static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights*
   if (d.fmt == FP4MOE_FP8) return FP4MOE_ERR_INVALID_ARG;  // fp4moe_forward_w8a8
   if (ws_bytes < (size_t)L.ws.total_bytes) return FP4MOE_ERR_WORKSPACE;
   const bool nv = d.fmt == FP4MOE_NVFP4;
-  const int dn_pair = fp4_down_pair(L.ws.n_tile, nv, (double)d.T * d.top_k / d.E);
+  int dn_pair = fp4_down_pair(L.ws.n_tile, nv, (double)d.T * d.top_k / d.E);
+  const bool dn_w2 = fp4_down_w2(dn_pair, h_end - h_begin, dbg);
+  if (dn_w2) dn_pair = 1;
   const bool dn_cta = fp4_down_cta_pair(dn_pair, h_end - h_begin, dbg);
-  const int dn_mtiles = (h_end - h_begin) / (dn_cta ? 256 : 128);  // weight-row tiles per down unit row
+  const int dn_mtiles = (h_end - h_begin) / ((dn_cta || dn_w2) ? 256 : 128);  // weight-row tiles per down unit row
   if (!w->w13 || !w->w13_scale || !w->w2 || !w->w2_scale || !w->w_router || !w->bias) return FP4MOE_ERR_INVALID_ARG;
   if (nv && (!w->g13 || !w->g2)) return FP4MOE_ERR_INVALID_ARG;
-  if (w->packed < 0 || w->packed > 2) return FP4MOE_ERR_INVALID_ARG;
+  if (w->packed < 0 || w->packed > 3) return FP4MOE_ERR_INVALID_ARG;
+  // row-tile-paired down weights: whole 256-row slabs of the output
+  if (w->packed == 3 && (d.H % 256 != 0 || h_begin % 256 != 0 || h_end % 256 != 0))
+    return FP4MOE_ERR_UNSUPPORTED_SHAPE;
   if (d.n_shared && (!w->sh13 || !w->sh13_scale || !w->sh2 || !w->sh2_scale)) return FP4MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w->w13) || !aligned16(w->w2) || !aligned16(w->w13_scale) ||
       !aligned16(w->w2_scale) || !aligned16(w->w_router) || !aligned16(ws) || !aligned16(out))
@@ -506,7 +520,7 @@ static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights*
     GemmArgs g = a;
     g.w = w->w13;
     g.w_tiled = w->packed != 0;
-    g.gu_pairs = w->packed == 2 ? d.I / 128 : 0;
+    g.gu_pairs = w->packed >= 2 ? d.I / 128 : 0;
     g.wsf = w->w13_scale;
     g.sh = d.n_shared ? w->sh13 : nullptr;
     g.shsf = d.n_shared ? w->sh13_scale : nullptr;
@@ -546,6 +560,8 @@ static fp4moe_status forward_cols(const fp4moe_dims* dims, const fp4moe_weights*
     g.out_acc = acc;
     g.dn_pair = dn_pair;
     g.dn_cta_pair = dn_cta;
+    g.dn_w2 = dn_w2;
+    g.dn_paired = w->packed == 3;
     e = launch_down(g, s);
   }
   if (e == cudaSuccess) e = rec(6);
@@ -701,7 +717,8 @@ fp4moe_status fp4moe_forward_nvfp4_emulated(const fp4moe_dims* dims, const fp4mo
   if (!w->w13 || !w->w13_scale || !w->w2 || !w->w2_scale || !w->g13 || !w->g2 || !w->w_router || !w->bias)
     return FP4MOE_ERR_INVALID_ARG;
   if (d.n_shared && (!w->sh13 || !w->sh13_scale || !w->sh2 || !w->sh2_scale)) return FP4MOE_ERR_INVALID_ARG;
-  if (w->packed < 0 || w->packed > 2) return FP4MOE_ERR_INVALID_ARG;
+  if (w->packed < 0 || w->packed > 3) return FP4MOE_ERR_INVALID_ARG;
+  if (w->packed == 3 && d.H % 256 != 0) return FP4MOE_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(x) || !aligned16(w->w13) || !aligned16(w->w2) || !aligned16(w->w_router) || !aligned16(ws) ||
       !aligned16(out))
     return FP4MOE_ERR_INVALID_ARG;
@@ -759,12 +776,15 @@ fp4moe_status fp4moe_forward_nvfp4_emulated(const fp4moe_dims* dims, const fp4mo
   if (e == cudaSuccess) e = rec(3);
   // BF16 copies of the dispatched experts' weights (at GEMM time, as the
   // emulation pipeline does) and of the QDQ'd activations
-  if (e == cudaSuccess) e = launch_nv_weight_bf16(w->w13, w->packed != 0, w->packed == 2 ? d.I / 128 : 0, w->w13_scale, w->g13, d.E, 2 * d.I, d.H, ecount, w13b, s);
-  if (e == cudaSuccess) e = launch_nv_weight_bf16(w->w2, w->packed != 0, 0, w->w2_scale, w->g2, d.E, d.H, d.I, ecount, w2b, s);
+  // (paired orders: gate/up pairs of I / 128 tiles; row-tile pairs of the
+  // down matrices, one tile pair per 256-row slab)
+  const int gu_p = w->packed >= 2 ? d.I / 128 : 0, dn_p = w->packed == 3 ? 1 : 0;
+  if (e == cudaSuccess) e = launch_nv_weight_bf16(w->w13, w->packed != 0, gu_p, w->w13_scale, w->g13, d.E, 2 * d.I, d.H, ecount, w13b, s);
+  if (e == cudaSuccess) e = launch_nv_weight_bf16(w->w2, w->packed != 0, dn_p, w->w2_scale, w->g2, d.E, d.H, d.I, ecount, w2b, s);
   if (e == cudaSuccess && d.n_shared)
-    e = launch_nv_weight_bf16(w->sh13, w->packed != 0, w->packed == 2 ? d.I / 128 : 0, w->sh13_scale, w->g13 + d.E, 1, 2 * d.I, d.H, nullptr, sh13b, s);
+    e = launch_nv_weight_bf16(w->sh13, w->packed != 0, gu_p, w->sh13_scale, w->g13 + d.E, 1, 2 * d.I, d.H, nullptr, sh13b, s);
   if (e == cudaSuccess && d.n_shared)
-    e = launch_nv_weight_bf16(w->sh2, w->packed != 0, 0, w->sh2_scale, w->g2 + d.E, 1, d.H, d.I, nullptr, sh2b, s);
+    e = launch_nv_weight_bf16(w->sh2, w->packed != 0, dn_p, w->sh2_scale, w->g2 + d.E, 1, d.H, d.I, nullptr, sh2b, s);
   if (e == cudaSuccess) e = launch_amax(x, 0, (int64_t)d.T * d.H, amax, s);
   if (e == cudaSuccess) e = launch_nv_qdq_x_bf16(d, x, route_row, amax, gscale, xb, s);
   if (e == cudaSuccess) e = rec(4);
@@ -854,13 +874,15 @@ fp4moe_status fp4moe_linear(int32_t fmt, int32_t T, int32_t K, int32_t N, const 
   uint32_t* amax = reinterpret_cast<uint32_t*>(P(L.amax));
   float* acc = reinterpret_cast<float*>(P(L.ws.out_acc));
   const int n_tile = L.ws.n_tile;
-  const int dn_pair = fp4_down_pair(n_tile, nv, T);
+  int dn_pair = fp4_down_pair(n_tile, nv, T);
+  const bool dn_w2 = fp4_down_w2(dn_pair, N, nullptr);
+  if (dn_w2) dn_pair = 1;
   const bool dn_cta = fp4_down_cta_pair(dn_pair, N, nullptr);
 
   cudaError_t e = cudaMemsetAsync(status, 0, kStatusInts * 4, s);
   if (e == cudaSuccess && nv) e = cudaMemsetAsync(amax, 0, 8, s);
   if (e == cudaSuccess)
-    e = launch_linear_plan(T, n_tile, dn_pair, N / (dn_cta ? 256 : 128), ecount, eslot, dn_start, plan, route_row,
+    e = launch_linear_plan(T, n_tile, dn_pair, N / ((dn_cta || dn_w2) ? 256 : 128), ecount, eslot, dn_start, plan, route_row,
                            row_tok, row_w, acc, (int64_t)T * N, s);
   if (e == cudaSuccess && nv) e = launch_amax(x, 0, (int64_t)T * K, amax, s);
   if (e == cudaSuccess) e = launch_gather_quant(dq, x, route_row, xq, xsf, amax, gscale, s);
@@ -888,6 +910,7 @@ fp4moe_status fp4moe_linear(int32_t fmt, int32_t T, int32_t K, int32_t N, const 
     g.status = status;
     g.dn_pair = dn_pair;
     g.dn_cta_pair = dn_cta;
+    g.dn_w2 = dn_w2;
     e = launch_down(g, s);
   }
   if (e == cudaSuccess) e = launch_finalize(acc, out, (int64_t)T * N, s);

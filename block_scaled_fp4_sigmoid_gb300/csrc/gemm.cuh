@@ -22,13 +22,16 @@
 //   warps 1, 6 MMA issuers (warp 1 also owns tensor memory): copy each
 //              stage's scale factors to tensor memory (tcgen05.cp), issue four
 //              K=64 MMAs per 256-wide K tile (gate/up: one A operand each;
-//              down: alternate K tiles into two accumulators), and commit the
-//              stage back to the producer;
+//              down units of two weight tiles: one tile each; other down
+//              units: alternate K tiles into two accumulators, or one issuer
+//              for two token slots), and commit the stage back to the
+//              producer;
 //   warp 7     second TMA producer: the token tile (2-D map over the padded
 //              permuted rows) and its scale groups, once warp 0 has armed
 //              the stage;
 //   warp 8     gate/up only: zeroes the combine buffer when asked;
-//   warps 2-5  epilogue, one per tensor-memory lane quadrant:
+//   warps 2-5  epilogue, one per tensor-memory lane quadrant (down with
+//              64 or more token columns: warps 8-11 as a second set):
 //              gate/up: SwiGLU, then MXFP4 requantisation of h across the
 //              32 lanes of a warp (= one 32-block along I), or (NVFP4) fp32
 //              h plus a per-expert amax;
@@ -88,7 +91,7 @@ constexpr int kOpFp4 = 0, kOpE4M3 = 1, kOpBf16 = 2;
 
 constexpr int kMaxExperts = 520;  // plan arrays cached in shared memory (E + n_shared <= 513)
 
-template <int N, bool GATEUP, bool NV, int OP = kOpFp4, bool PAIR = false>
+template <int N, bool GATEUP, bool NV, int OP = kOpFp4, bool PAIR = false, bool W2 = false>
 struct GemmCfg {
   // N = 240 (MXFP4 down only): a unit covers two slots of the padded layout
   // (two 112-token tiles of one expert), so each pipeline step carries
@@ -107,8 +110,14 @@ struct GemmCfg {
   // slot's scale group).  Both CTAs hold both slots' B scale groups, as each
   // SM's half of the MMA scales all 240 columns.
   static_assert(!PAIR || (N == 240 && !GATEUP && !NV && OP == kOpFp4), "CTA pair: MXFP4 down GEMM with paired slots");
+  // W2 (MXFP4 down, 112-token tiles): a unit covers two adjacent 128-row weight
+  // tiles (256 output rows) of one token tile, the gate/up GEMM's mainloop
+  // shape: issuer i multiplies weight tile i (A operand i) by the shared B
+  // tile into its own accumulator block, and the epilogue adds both blocks
+  // into their output rows.
+  static_assert(!W2 || (N == 112 && !GATEUP && !NV && !PAIR && OP == kOpFp4), "two weight tiles: MXFP4 down, 112 tokens");
   static constexpr int kBRows = PAIR ? N / 2 : N;  // B rows in this CTA's shared memory
-  static constexpr int kA = GATEUP ? 2 : 1;                // A operands per unit (gate and up)
+  static constexpr int kA = (GATEUP || W2) ? 2 : 1;        // A operands per unit (gate and up, or two weight tiles)
   static constexpr int kAtoms = OP != kOpFp4 ? 0 : NV ? 4 : 2;  // scale groups per K tile
   static constexpr int kABytes = 128 * 128;          // 128 rows x 128 bytes
   static constexpr int kBBytes = kBRows * 128;
@@ -128,6 +137,7 @@ struct GemmCfg {
   // chunks between them.  Gate/up transposes through shared memory (one
   // 32 x 33 fp32 tile per epilogue warp); down transposes in registers.
   static constexpr int kEpiWarps = (!GATEUP && N >= 64) ? 8 : 4;
+  static constexpr int kEpiSets = kEpiWarps / 4;  // epilogue warps per lane quadrant
   static constexpr int kEpiTiles = GATEUP ? 4 : 1;
   // 227 KB per CTA = pipeline stages + 1 KB alignment slack + static shared
   // memory (epilogue transpose tiles, plan cache, barriers and flags)
@@ -140,14 +150,15 @@ struct GemmCfg {
   // pipe busy with 112-token MMAs.  Gate/up: issuer i drives A operand i
   // (gate, up).  Down (one A operand): issuer i takes the K tiles kt with
   // kt % 2 == i into its own accumulator; the epilogue adds the two.  Each
-  // issuer copies its own A and B scale factors.
-  // (N = 240: one issuer; its instructions already carry twice the work.)
+  // issuer copies its own A and B scale factors.  (W2: issuer i drives
+  // weight tile i, as gate/up.  N = 240: one issuer; its instructions
+  // already carry twice the work.)
   static constexpr int kIssuers = kPairSlots == 2 ? 1 : 2;  // (CTA pair: in CTA 0 only)
-  static constexpr bool kKSplit = !GATEUP && kIssuers == 2;
+  static constexpr bool kKSplit = !GATEUP && !W2 && kIssuers == 2;
   // warp 7: second producer; gate/up warp 8: combine-buffer zeroing; down
   // with eight epilogue warps: warps 8-11 are the second four
-  static constexpr int kThreads = GATEUP ? 288 : kEpiWarps == 8 ? 384 : 256;
-  static constexpr int kAccCols = (GATEUP || kKSplit) ? 2 * N : N;  // one accumulator set: one N-column block per issuer
+  static constexpr int kThreads = GATEUP ? 288 : 32 * (4 + kEpiWarps);
+  static constexpr int kAccCols = kIssuers * N;  // one accumulator set: one N-column block per issuer
   // scale-factor columns of one K tile: 4 per group of 4 blocks per 128
   // rows (row r of a group at lane r % 32, column r / 32)
   static constexpr int kSfColsA = kAtoms * 4, kSfColsB = kAtoms * 4 * kPairSlots;
@@ -177,48 +188,57 @@ __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) { return smem_desc(s
 // keeps the down GEMM's combine rows of one group (T x G x 128 fp32) in L2
 // while every expert adds into them.
 //
-// The grouped case (two integer divisions) stays out of line: the
-// producers decode every unit on their critical path.
-static __device__ __noinline__ int grouped_unit(const int32_t* s_start, int n_exp, int M, int G, int u, int* e_out) {
-  const int per_group = (s_start[n_exp] / M) * G;  // units of one group
-  const int g = u / per_group;
-  const int r = u - g * per_group;
-  // the last expert whose first unit of the group, s_start / M x G, is <= r
-  // (s_start is a multiple of M)
-  int lo = 0, hi = n_exp;
+// Each role of a CTA decodes its units (u_first, u_first + u_step, ...) in
+// rising order and keeps a UnitPos: the expert and group of its last unit.
+// The next unit's expert is that expert again (one read of shared memory
+// tells) or one after it, found by bisection of the experts that follow.
+// {0, 0} is a valid position for any unit.
+struct UnitPos {
+  int e = 0, g = 0;
+};
+
+// The last i in [lo, n) with key(i) <= x, given key(lo) <= x and key
+// nondecreasing in i.
+template <class Key>
+__device__ __forceinline__ int search_last_le(Key key, int lo, int n, int x) {
+  if (lo + 1 >= n || key(lo + 1) > x) return lo;
+  int hi = n;
+  ++lo;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (s_start[mid] * G <= r * M) lo = mid;
+    if (key(mid) <= x) lo = mid;
     else hi = mid;
   }
-  *e_out = lo;
-  return g * (1 << 20) + (r - (s_start[lo] / M) * G);  // group and local unit (local < 2^20)
+  return lo;
 }
 
 template <int N, bool kGrouped>
 __device__ __forceinline__ void decode_unit(const int32_t* s_start, const int32_t* s_count, const int32_t* s_slot,
-                                            int n_exp, int M, int G, int u, int& e, int& mt, int& slot, int& cnt) {
-  int g = 0, local;
+                                            int n_exp, int M, int G, int u, UnitPos& pos, int& e, int& mt, int& slot,
+                                            int& cnt) {
+  int local;
   if (!kGrouped || G == M) {  // the expert: the last one whose first unit is <= u
-    int lo = 0, hi = n_exp;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_start[mid] <= u) lo = mid;
-      else hi = mid;
-    }
-    e = lo;
-    local = u - s_start[lo];
+    e = search_last_le([&](int i) { return s_start[i]; }, pos.e, n_exp, u);
+    local = u - s_start[e];
   } else {
-    const int gl = grouped_unit(s_start, n_exp, M, G, u, &e);
-    g = gl >> 20;
-    local = gl & ((1 << 20) - 1);
+    const int per_group = (s_start[n_exp] / M) * G;  // units of one group
+    if (u >= (pos.g + 1) * per_group) {  // a later group: search it from the first expert
+      pos.g = u / per_group;
+      pos.e = 0;
+    }
+    const int r = u - pos.g * per_group;
+    // the last expert whose first unit of the group, s_start / M x G, is <= r
+    // (s_start is a multiple of M)
+    e = search_last_le([&](int i) { return s_start[i] * G; }, pos.e, n_exp, r * M);
+    local = r - (s_start[e] / M) * G;
   }
+  pos.e = e;
   const int count = s_count[e];
   constexpr int kCap = GemmCfg<N, false, false>::kUnitRoutes;
   const int nt = (count + kCap - 1) / kCap;
   const int ml = local / nt;
   const int ti = local - ml * nt;
-  mt = g * G + ml;
+  mt = (kGrouped ? pos.g * G : 0) + ml;
   slot = s_slot[e] + ti * GemmCfg<N, false, false>::kPairSlots;
   cnt = min(kCap, count - ti * kCap);
 }
@@ -227,10 +247,12 @@ __device__ __forceinline__ void decode_unit(const int32_t* s_start, const int32_
 // unit_mtiles); the others are compiled with the expert-major order only
 // (measured: the grouped decode merely present cost the decode and NVFP4
 // down GEMMs 2-3%).
-template <int N, bool GATEUP, bool NV, int OP = kOpFp4, bool PAIR = false, bool GROUPED = false>
-__global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
+template <int N, bool GATEUP, bool NV, int OP = kOpFp4, bool PAIR = false, bool GROUPED = false, bool W2 = false,
+          bool DPW = false>
+__global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR, W2>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ KParams p) {
-  using C = GemmCfg<N, GATEUP, NV, OP, PAIR>;
+  using C = GemmCfg<N, GATEUP, NV, OP, PAIR, W2>;
+  static_assert(!DPW || (!GATEUP && OP == kOpFp4), "row-tile-paired weights: block-scaled FP4 down GEMM");
   constexpr bool F8 = OP == kOpE4M3, BF = OP == kOpBf16, SF = OP == kOpFp4;
   static_assert(SF || !NV, "one operand format");
   extern __shared__ uint8_t smem_raw[];
@@ -317,17 +339,18 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
     bool two;   // paired slots: the unit's routes reach into its second slot
     const uint8_t *sfa0, *sfa1, *sfb;
   };
-  auto unit_step = [&](int u) {
+  auto unit_step = [&](int u, UnitPos& pos) {
     int e, mt, slot, cnt;
-    decode_unit<N, GROUPED>(s_start, s_count, s_slot, p.n_exp, p.unit_mtiles, p.m_group, u, e, mt, slot, cnt);
+    decode_unit<N, GROUPED>(s_start, s_count, s_slot, p.n_exp, p.unit_mtiles, p.m_group, u, pos, e, mt, slot, cnt);
     const bool sh = e >= p.E;
     Step st;
     st.tmA = sh ? &p.tmA_sh : &p.tmA;
     st.ec = sh ? e - p.E : e;
     const uint8_t* sfw = sh ? p.shsf : p.wsf;
     const int rt_per_e = p.rows_per_expert >> 7;
-    st.row0 = PAIR ? mt * 256 + (int)crank * 128 : mt * 128;  // (pair: mt counts 256-row tiles)
-    st.row1 = p.I + mt * 128;  // up rows (gate/up only)
+    // (CTA pair and W2: mt counts 256-row tiles)
+    st.row0 = PAIR ? mt * 256 + (int)crank * 128 : W2 ? mt * 256 : mt * 128;
+    st.row1 = W2 ? mt * 256 + 128 : p.I + mt * 128;  // second A operand: up rows, or (W2) the next weight tile
     st.slot = p.tok_mask ? 0 : slot;  // slot of the B rows
     st.once = s_count[e] <= C::kUnitRoutes;
     st.two = C::kPairSlots == 2 && cnt > 112;
@@ -335,6 +358,11 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
     st.sfa1 = sfw + ((int64_t)(st.ec * rt_per_e + (st.row1 >> 7)) * p.katoms_a) * 512;
     if (GATEUP && p.gu_pairs)  // paired order: gate then up scale groups of each K tile, kSFBytes apart
       st.sfa0 = sfw + ((int64_t)(st.ec * p.gu_pairs + mt) * KT) * 2 * C::kSFBytes;
+    if constexpr (DPW) {  // row-tile-paired order: row tile rt's groups of K tile kt at slot
+      // ((slab * KT + kt) * 2 + rt % 2) * kSFBytes, slab = the 256-row slab (2 * kSFBytes per K tile)
+      st.sfa0 = sfw + ((int64_t)(((st.ec * rt_per_e) >> 1) + (st.row0 >> 8)) * KT * 2 + ((st.row0 >> 7) & 1)) * C::kSFBytes;
+      st.sfa1 = sfw + ((int64_t)(((st.ec * rt_per_e) >> 1) + (st.row1 >> 8)) * KT * 2 + ((st.row1 >> 7) & 1)) * C::kSFBytes;
+    }
     st.sfb = p.bsf + ((int64_t)st.slot * p.katoms_b) * 512;
     return st;
   };
@@ -344,13 +372,24 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
   // that those units find them in L2.
   const uint64_t pol_once = l2_evict_first();
   // Coordinates of the (row tile, K tile) box: row-major (byte column, row)
-  // or, in the tiled layout, the block's first 128-byte row of the view.
+  // or, in the tiled layout, the block's first 128-byte row of the view
+  // (DPW, row-tile-paired order: block slot (slab * KT + kt) * 2 + row tile
+  // % 2).  The order is a template parameter: as a run-time branch in these
+  // per-K-tile computations it cost the decode-size down GEMMs 3-6%.
   auto a_x = [&](int kt) { return p.w_tiled ? 0 : kt * 128; };
-  auto a_y = [&](int row, int kt) { return p.w_tiled ? ((row >> 7) * KT + kt) * 128 : row; };
+  auto a_y = [&](int row, int kt) {
+    if (!p.w_tiled) return row;
+    if constexpr (DPW) return (((row >> 8) * KT + kt) * 2 + ((row >> 7) & 1)) * 128;
+    return ((row >> 7) * KT + kt) * 128;
+  };
+  // scale bytes from one K tile of a row tile to the next
+  constexpr int sf_kstep = DPW ? 2 * C::kSFBytes : C::kSFBytes;
   auto load_weights = [&](const Step& st, int kt, uint32_t base, uint32_t fb) {
-    if constexpr (GATEUP && SF) {
-      if (p.gu_pairs) {  // paired order: one box of the gate and up blocks, one copy of both scale groups
-        const int y = ((st.row0 >> 7) * KT + kt) * 256;
+    if constexpr ((GATEUP || W2) && SF) {
+      // paired orders (gate/up pairs; W2 on row-tile pairs): one box of the
+      // unit's two blocks, one copy of both scale groups
+      if (GATEUP ? p.gu_pairs != 0 : DPW) {
+        const int y = ((GATEUP ? st.row0 >> 7 : st.row0 >> 8) * KT + kt) * 256;
         if (st.once) {
           tma_load_3d_hint(base, st.tmA, fb, 0, y, st.ec, pol_once);
           bulk_load_hint(base + C::kOffSFA0, st.sfa0 + kt * 2 * C::kSFBytes, 2 * C::kSFBytes, fb, pol_once);
@@ -363,18 +402,19 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
     }
     if (st.once) {
       tma_load_3d_hint(base, st.tmA, fb, a_x(kt), a_y(st.row0, kt), st.ec, pol_once);
-      if constexpr (GATEUP)
+      if constexpr (C::kA == 2)
         tma_load_3d_hint(base + C::kOffA1, st.tmA, fb, a_x(kt), a_y(st.row1, kt), st.ec, pol_once);
       if constexpr (SF) {
-        bulk_load_hint(base + C::kOffSFA0, st.sfa0 + kt * C::kSFBytes, C::kSFBytes, fb, pol_once);
-        if constexpr (GATEUP) bulk_load_hint(base + C::kOffSFA1, st.sfa1 + kt * C::kSFBytes, C::kSFBytes, fb, pol_once);
+        bulk_load_hint(base + C::kOffSFA0, st.sfa0 + kt * sf_kstep, C::kSFBytes, fb, pol_once);
+        if constexpr (C::kA == 2)
+          bulk_load_hint(base + C::kOffSFA1, st.sfa1 + kt * sf_kstep, C::kSFBytes, fb, pol_once);
       }
     } else {
       tma_load_3d(base, st.tmA, fb, a_x(kt), a_y(st.row0, kt), st.ec);
-      if constexpr (GATEUP) tma_load_3d(base + C::kOffA1, st.tmA, fb, a_x(kt), a_y(st.row1, kt), st.ec);
+      if constexpr (C::kA == 2) tma_load_3d(base + C::kOffA1, st.tmA, fb, a_x(kt), a_y(st.row1, kt), st.ec);
       if constexpr (SF) {
-        bulk_load(base + C::kOffSFA0, st.sfa0 + kt * C::kSFBytes, C::kSFBytes, fb);
-        if constexpr (GATEUP) bulk_load(base + C::kOffSFA1, st.sfa1 + kt * C::kSFBytes, C::kSFBytes, fb);
+        bulk_load(base + C::kOffSFA0, st.sfa0 + kt * sf_kstep, C::kSFBytes, fb);
+        if constexpr (C::kA == 2) bulk_load(base + C::kOffSFA1, st.sfa1 + kt * sf_kstep, C::kSFBytes, fb);
       }
     }
   };
@@ -411,8 +451,9 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
   // they overlap the tail of the previous kernel.
   int pre = 0;
   if (warp == 0 && lane == 0) {
+    UnitPos pos;
     for (int u = u_first; u < total && pre < C::kStages; u += u_step) {
-      const Step st = unit_step(u);
+      const Step st = unit_step(u, pos);
       for (int kt = 0; kt < KT && pre < C::kStages; ++kt, ++pre) {
         if (pre == withheld) continue;
         const uint32_t fb = smem_u32(&bar_full[pre]);
@@ -437,8 +478,9 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
       if constexpr (kSplitProducer) *armed_v = pre;
       int stage = 0, step = 0;
       uint32_t phase = 0, armed = 0, armed_par = 0;
+      UnitPos pos;
       for (int u = u_first; u < total && !*abort_v; u += u_step) {
-        const Step st = unit_step(u);
+        const Step st = unit_step(u, pos);
         bool ok = true;
         for (int kt = 0; kt < KT; ++kt, ++step) {
           const uint32_t fb = smem_u32(&bar_full[stage]);
@@ -486,8 +528,9 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
       // their barriers complete (split: the second producer does it)
       if (!kSplitProducer && step < pre) {
         int s2 = 0;
+        UnitPos pos2;
         for (int u = u_first; u < total && s2 < pre; u += u_step) {
-          const Step st = unit_step(u);
+          const Step st = unit_step(u, pos2);
           for (int kt = 0; kt < KT && s2 < pre; ++kt, ++s2)
             if (s2 >= step && s2 != withheld) {
               load_acts(st, kt, sbase + s2 * C::kStage, smem_u32(&bar_full[s2]));
@@ -520,8 +563,9 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
         };
         int step = 0;
         bool ok = true;
+        UnitPos pos;
         for (int u = u_first; u < total && ok && !*abort_v; u += u_step) {
-          const Step st = unit_step(u);
+          const Step st = unit_step(u, pos);
           for (int kt = 0; kt < KT; ++kt, ++step) {
             if (step == withheld) continue;  // never armed
             if (!wait_armed(step)) { ok = false; break; }
@@ -543,8 +587,9 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
           __threadfence_block();
           const int armed = *armed_v;
           int s2 = 0;
+          UnitPos pos2;
           for (int u = u_first; u < total && s2 < armed; u += u_step) {
-            const Step st = unit_step(u);
+            const Step st = unit_step(u, pos2);
             for (int kt = 0; kt < KT && s2 < armed; ++kt, ++s2)
               if (s2 >= step && s2 != withheld)
                 load_acts(st, kt, sbase + (s2 % C::kStages) * C::kStage, smem_u32(&bar_full[s2 % C::kStages]));
@@ -608,17 +653,20 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
     int stage = 0;
     uint32_t phase = 0, acc_phase = 0;
     int as = 0;  // accumulator set of this unit
+    UnitPos pos;
     for (int u = u_first; u < total && !__any_sync(0xffffffffu, *abort_v); u += u_step) {
-      bool ok = wait_w(smem_u32(&bar_tempty[as]), acc_phase ^ 1u);
-      tc_fence_after();
-      const uint32_t t_acc = tmem + as * C::kAccCols + mi * N;
       // paired slots: a unit within its first slot multiplies 112 columns
+      // (decoded before the accumulator wait, off the MMAs' path)
       bool two = true;
       if constexpr (C::kPairSlots == 2) {
         int e_, mt_, slot_, cnt_;
-        decode_unit<N, GROUPED>(s_start, s_count, s_slot, p.n_exp, p.unit_mtiles, p.m_group, u, e_, mt_, slot_, cnt_);
+        decode_unit<N, GROUPED>(s_start, s_count, s_slot, p.n_exp, p.unit_mtiles, p.m_group, u, pos, e_, mt_, slot_,
+                                cnt_);
         two = cnt_ > 112;
       }
+      bool ok = wait_w(smem_u32(&bar_tempty[as]), acc_phase ^ 1u);
+      tc_fence_after();
+      const uint32_t t_acc = tmem + as * C::kAccCols + mi * N;
       const uint32_t n_mma = two ? N : 112;
       for (int kt = 0; ok && kt < KT; ++kt) {
         if (C::kKSplit && (kt & 1) != mi) {  // the other issuer's K tile
@@ -685,18 +733,21 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
     else tc_commit_elect(smem_u32(&bar_done));
     (void)mbar_wait<PAIR>(smem_u32(&bar_done), 0);
    }
-  } else if (warp < 6 || C::kEpiWarps == 8) {
+  } else if (warp < 6 || C::kEpiWarps > 4) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // tensor-memory lane quadrant of this warp
-    const int half = warp >= 8 ? 1 : 0;  // eight epilogue warps: which chunks of the unit
+    // set of this warp (warps 2-5: set 0, then four warps per set from warp
+    // 8): which part of the unit it takes
+    const int eset = warp < 8 ? 0 : (warp - 4) >> 2;
     const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
     float(*tile)[33] = epi_tile[GATEUP ? warp - 2 : 0];
     uint32_t acc_phase = 0;
     int as = 0;
+    UnitPos pos;
     for (int u = u_first; u < total; u += u_step) {
       if (__any_sync(0xffffffffu, *abort_v)) break;  // warp-uniform: the loop body holds .sync.aligned loads
       int e, mt, slot, cnt;
-      decode_unit<N, GROUPED>(s_start, s_count, s_slot, p.n_exp, p.unit_mtiles, p.m_group, u, e, mt, slot, cnt);
+      decode_unit<N, GROUPED>(s_start, s_count, s_slot, p.n_exp, p.unit_mtiles, p.m_group, u, pos, e, mt, slot, cnt);
       // the unit's accumulator set is complete (bounded; warp-uniform outcome)
       auto wait_acc = [&]() {
         if (!__all_sync(0xffffffffu, mbar_wait_abortable<PAIR>(smem_u32(&bar_tfull[as]), acc_phase, p.wait_ns, abort_v))) {
@@ -799,8 +850,11 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
         // columns of a chunk; a 4 x 4 transpose within each group of four
         // lanes (two shuffle rounds) leaves lane 4 m + r with rows 4 m ..
         // 4 m + 3 of column 4 g + r, which one 16-byte reduction adds.
+        // (W2: the warps of an even set take accumulator block 0, the unit's
+        // first weight tile, those of an odd set block 1.)
         const int m4 = lane >> 2, r4 = lane & 3;
-        const int h0 = (PAIR ? mt * 256 + (int)crank * 128 : mt * 128) + 32 * q + 4 * m4;
+        const int blk = W2 ? (eset & 1) : 0;
+        const int h0 = (PAIR ? mt * 256 + (int)crank * 128 : mt * (128 * C::kA) + 128 * blk) + 32 * q + 4 * m4;
         float sc = 1.f;
         if constexpr (NV) sc = __fmul_rn(__ldg(p.gb + e), __ldg(p.gw + e));
         float rho = 1.f;  // W8A8: channel scale of this lane's output row
@@ -812,9 +866,11 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
         const int cnt1 = cnt - cnt0;
         const int ncol = cnt1 > 0 ? 128 + cnt1 : cnt0;
         auto col_ok = [&](int n) { return n < cnt0 || (n >= 128 && n < ncol); };
-        // this warp's chunks: 32-column chunk ci with ci % halves == half,
-        // skipping chunks of stale columns only
-        constexpr int kHalves = C::kEpiWarps / 4;
+        // this warp's chunks: 32-column chunk ci with ci % kHalves == part
+        // (the sets sharing its accumulator block), skipping chunks of stale
+        // columns only
+        constexpr int kHalves = W2 ? C::kEpiSets / 2 : C::kEpiSets;
+        const int part = W2 ? (eset >> 1) : eset;
         auto chunk_ok = [&](int ci) { return !(C::kPairSlots == 2 && 32 * ci >= cnt0 && 32 * ci < 128); };
         auto next_chunk = [&](int ci) {
           while (32 * ci < ncol && !chunk_ok(ci)) ci += kHalves;
@@ -835,10 +891,10 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
             if constexpr (F8) wk_n = __ldg(p.row_w + rr) * __ldg(p.brs + rr);
           }
         };
-        int ci = next_chunk(half);
+        int ci = next_chunk(part);
         fetch(ci);
         if (!wait_acc()) break;
-        const uint32_t ta = tq + as * C::kAccCols;
+        const uint32_t ta = tq + as * C::kAccCols + blk * N;
         while (32 * ci < ncol) {
           const int c0 = 32 * ci;
           const int tk = tk_n;
@@ -902,10 +958,11 @@ __global__ void __launch_bounds__(GemmCfg<N, GATEUP, NV, OP, PAIR>::kThreads, 1)
   }
 }
 
-template <int N, bool GATEUP, bool NV, int OP = kOpFp4, bool PAIR = false, bool GROUPED = false>
+template <int N, bool GATEUP, bool NV, int OP = kOpFp4, bool PAIR = false, bool GROUPED = false, bool W2 = false,
+          bool DPW = false>
 cudaError_t launch_gemm_t(const KParams& p, int grid, cudaStream_t s) {
-  using C = GemmCfg<N, GATEUP, NV, OP, PAIR>;
-  auto k = moe_gemm_kernel<N, GATEUP, NV, OP, PAIR, GROUPED>;
+  using C = GemmCfg<N, GATEUP, NV, OP, PAIR, W2>;
+  auto k = moe_gemm_kernel<N, GATEUP, NV, OP, PAIR, GROUPED, W2, DPW>;
   static bool attr_set[64] = {};  // once per device and template instance
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

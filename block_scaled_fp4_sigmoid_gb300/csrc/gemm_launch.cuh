@@ -7,23 +7,57 @@
 namespace fp4moe {
 
 // L2 bytes the down GEMM's combine rows of one unit group may take (of the
-// 126 MB): the group's G weight tiles x 128 rows x T tokens x fp32.
+// 126 MB): the group's G weight tiles x their rows x T tokens x fp32.
 constexpr int64_t kCombineL2Bytes = 48ll << 20;
 // Combine buffers up to this size keep the expert-major order: measured, a
 // 4096-token layer (117 MB) gained nothing from groups, a 16384-token layer
 // (470 MB) 19% of its down GEMM.
 constexpr int64_t kCombineGroupAbove = 256ll << 20;
 
-// Weight tiles per group of the down GEMM's unit order: the largest divisor
-// of M whose combine rows fit kCombineL2Bytes; M (expert-major) when the
-// whole buffer is small, or when each token has one route, so that no row
-// is added twice.
-inline int combine_group(int M, int64_t T, int routes_per_token) {
-  if (routes_per_token <= 1 || T * M * 512 <= kCombineGroupAbove) return M;
+// Weight tiles (of tile_rows rows) per group of the down GEMM's unit order:
+// the largest divisor of M whose combine rows fit kCombineL2Bytes; M
+// (expert-major) when the whole buffer is small, or when each token has one
+// route, so that no row is added twice.
+inline int combine_group(int M, int64_t T, int routes_per_token, int tile_rows) {
+  const int64_t row_bytes = (int64_t)tile_rows * 4;  // fp32 combine row slice of one tile
+  if (routes_per_token <= 1 || T * M * row_bytes <= kCombineGroupAbove) return M;
   int g = 1;
   for (int c = 1; c <= M; ++c)
-    if (M % c == 0 && T * c * 512 <= kCombineL2Bytes) g = c;
+    if (M % c == 0 && T * c * row_bytes <= kCombineL2Bytes) g = c;
   return g;
+}
+
+// The block-scaled FP4 instances (MXFP4 / NVFP4); DPW: down weights in the
+// row-tile-paired order.
+template <bool GATEUP, bool DPW>
+cudaError_t launch_fp4(const GemmArgs& a, KParams& p, int vis, int grid, cudaStream_t s) {
+  if constexpr (!GATEUP) {
+    if (a.dn_w2) {  // MXFP4, 112-token tiles: two weight tiles per unit
+      if (a.n_tile != 112 || a.nv || a.dn_pair != 1 || a.dn_cta_pair || vis % 256 != 0) return cudaErrorInvalidValue;
+      if (p.m_group < p.unit_mtiles) return launch_gemm_t<112, false, false, kOpFp4, false, true, true, DPW>(p, grid, s);
+      return launch_gemm_t<112, false, false, kOpFp4, false, false, true, DPW>(p, grid, s);
+    }
+    if (a.dn_pair == 2) {  // MXFP4, 112-token tiles: two slots per unit
+      if (a.n_tile != 112 || a.nv || a.f8 || a.bf) return cudaErrorInvalidValue;
+      if (a.dn_cta_pair) {
+        if (vis % 256 != 0) return cudaErrorInvalidValue;
+        p.m_group = p.unit_mtiles;  // (expert-major order only)
+        return launch_gemm_t<240, false, false, kOpFp4, true, false, false, DPW>(p, grid, s);
+      }
+      if (p.m_group < p.unit_mtiles) return launch_gemm_t<240, false, false, kOpFp4, false, true, false, DPW>(p, grid, s);
+      return launch_gemm_t<240, false, false, kOpFp4, false, false, false, DPW>(p, grid, s);
+    }
+  }
+  switch (a.n_tile * 2 + (a.nv ? 1 : 0)) {
+    case 32: return launch_gemm_t<16, GATEUP, false, kOpFp4, false, false, false, DPW>(p, grid, s);  // few tokens (MXFP4)
+    case 64: return launch_gemm_t<32, GATEUP, false, kOpFp4, false, false, false, DPW>(p, grid, s);
+    case 65: return launch_gemm_t<32, GATEUP, true, kOpFp4, false, false, false, DPW>(p, grid, s);
+    case 128: return launch_gemm_t<64, GATEUP, false, kOpFp4, false, false, false, DPW>(p, grid, s);
+    case 129: return launch_gemm_t<64, GATEUP, true, kOpFp4, false, false, false, DPW>(p, grid, s);
+    case 224: return launch_gemm_t<112, GATEUP, false, kOpFp4, false, false, false, DPW>(p, grid, s);
+    case 225: return launch_gemm_t<112, GATEUP, true, kOpFp4, false, false, false, DPW>(p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <bool GATEUP>
@@ -50,9 +84,13 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   const uint64_t a_dim0 = a.w_tiled ? 128 : Kb, a_dim1 = a.w_tiled ? (uint64_t)vis * KTb : (uint64_t)vis;
   const uint64_t a_mat = (uint64_t)rows * a_row;
   // gate/up-paired tiles (gu_pairs): one box of 256 view rows holds the gate
-  // and the up block of a (pair, K tile)
+  // and the up block of a (pair, K tile); likewise, for the down GEMM's
+  // units of two weight tiles (W2), the two blocks of a row-tile pair
   const bool gu_paired = GATEUP && a.w_tiled && a.gu_pairs > 0;
-  const uint32_t box_rows = gu_paired ? 256 : 128;
+  const bool w2 = !GATEUP && a.dn_w2;
+  const bool dn_paired = !GATEUP && a.w_tiled && a.dn_paired;
+  if (dn_paired && (r0 % 256 != 0 || rows % 256 != 0)) return cudaErrorInvalidValue;  // whole slabs only
+  const uint32_t box_rows = (gu_paired || (w2 && dn_paired)) ? 256 : 128;
   {
     const uint64_t dims[3] = {a_dim0, a_dim1, (uint64_t)d.E};
     const uint64_t strides[2] = {a_dim0, a_mat};
@@ -106,10 +144,12 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
   p.K = K;
   p.rows_per_expert = rows;
   p.m_tiles = GATEUP ? d.I / 128 : vis / 128;
-  p.unit_mtiles = GATEUP ? d.I / 128 : vis / (a.dn_cta_pair ? 256 : 128);
-  // grouped unit order: the paired-slot MXFP4 down instance only (the other
-  // instances take units expert-major)
-  p.m_group = (GATEUP || a.dn_pair != 2) ? p.unit_mtiles : combine_group(p.unit_mtiles, d.T, d.top_k + d.n_shared);
+  p.unit_mtiles = GATEUP ? d.I / 128 : vis / ((a.dn_cta_pair || w2) ? 256 : 128);
+  // grouped unit order: the paired-slot and two-weight-tile down instances
+  // only (the other instances take units expert-major)
+  p.m_group = (GATEUP || (a.dn_pair != 2 && !w2))
+                  ? p.unit_mtiles
+                  : combine_group(p.unit_mtiles, d.T, d.top_k + d.n_shared, w2 ? 256 : 128);
   p.katoms_a = (int)katoms_padded(K, a.nv);
   p.katoms_b = (int)katoms_padded(K, a.nv);
   p.katoms_h = (int)katoms_padded(d.I, a.nv);
@@ -137,28 +177,9 @@ cudaError_t launch_grouped(const GemmArgs& a, cudaStream_t s) {
       default: return cudaErrorInvalidValue;
     }
   }
-  if constexpr (!GATEUP) {
-    if (a.dn_pair == 2) {  // MXFP4, 112-token tiles: two slots per unit
-      if (a.n_tile != 112 || a.nv || a.f8 || a.bf) return cudaErrorInvalidValue;
-      if (a.dn_cta_pair) {
-        if (vis % 256 != 0) return cudaErrorInvalidValue;
-        p.m_group = p.unit_mtiles;  // (expert-major order only)
-        return launch_gemm_t<240, false, false, kOpFp4, true>(p, grid, s);
-      }
-      if (p.m_group < p.unit_mtiles) return launch_gemm_t<240, false, false, kOpFp4, false, true>(p, grid, s);
-      return launch_gemm_t<240, false, false>(p, grid, s);
-    }
-  }
-  switch (a.n_tile * 2 + (a.nv ? 1 : 0)) {
-    case 32: return launch_gemm_t<16, GATEUP, false>(p, grid, s);  // few-token path (MXFP4)
-    case 64: return launch_gemm_t<32, GATEUP, false>(p, grid, s);
-    case 65: return launch_gemm_t<32, GATEUP, true>(p, grid, s);
-    case 128: return launch_gemm_t<64, GATEUP, false>(p, grid, s);
-    case 129: return launch_gemm_t<64, GATEUP, true>(p, grid, s);
-    case 224: return launch_gemm_t<112, GATEUP, false>(p, grid, s);
-    case 225: return launch_gemm_t<112, GATEUP, true>(p, grid, s);
-    default: return cudaErrorInvalidValue;
-  }
+  if constexpr (!GATEUP)
+    if (dn_paired) return launch_fp4<false, true>(a, p, vis, grid, s);
+  return launch_fp4<GATEUP, false>(a, p, vis, grid, s);
 }
 
 }  // namespace fp4moe

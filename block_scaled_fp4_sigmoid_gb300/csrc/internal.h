@@ -173,6 +173,8 @@ struct GemmArgs {
   int dn_pair;                     // down, 112-token tiles: 2 = one unit covers two slots (224 tokens)
   int gu_pairs;                    // gate/up: weights and scales in the gate/up-paired tiled order (I / 128), or 0
   bool dn_cta_pair;                // down, dn_pair 2: run on CTA pairs (units of 256 weight rows)
+  bool dn_w2;                      // down, 112-token tiles, dn_pair 1: units of two weight tiles (256 rows)
+  bool dn_paired;                  // down: w / sh and their scales in the row-tile-paired tiled order
   // W8A8: channel scales of the weights (routed [E, rows], shared [rows]),
   // scales of the B rows (per permuted row); amax_h is then per permuted row
   const float *wrs, *shrs, *brs;

@@ -28,13 +28,14 @@ def _ptr(t):
     return t.data_ptr() if t is not None else None
 
 
-def column_block(H: int, rank: int, world: int) -> tuple[int, int]:
+def column_block(H: int, rank: int, world: int, unit: int = 128) -> tuple[int, int]:
     """Output columns [h0, h1) of rank `rank` of `world` in an
-    output-partitioned layer: whole 128-column tiles, as even as possible."""
-    tiles = H // 128
+    output-partitioned layer: whole tiles of `unit` columns (128, or 256 for
+    down weights in the row-tile-paired layout), as even as possible."""
+    tiles = H // unit
     if not 0 < world <= tiles or not 0 <= rank < world:
-        raise ValueError(f"{world} ranks over {tiles} column tiles")
-    return 128 * (tiles * rank // world), 128 * (tiles * (rank + 1) // world)
+        raise ValueError(f"{world} ranks over {tiles} column tiles of {unit}")
+    return unit * (tiles * rank // world), unit * (tiles * (rank + 1) // world)
 
 
 def tp_forward(layer, x, group=None):
@@ -44,7 +45,7 @@ def tp_forward(layer, x, group=None):
     optimization effort", section "MoE: remove duplicate work across GPUs")."""
     import torch.distributed as dist
     rank, world = dist.get_rank(group), dist.get_world_size(group)
-    h0, h1 = column_block(layer.dims.H, rank, world)
+    h0, h1 = column_block(layer.dims.H, rank, world, layer.column_unit)
     out = layer.forward_cols(x, h0, h1)
     dist.all_reduce(out, group=group)
     return out
@@ -52,35 +53,45 @@ def tp_forward(layer, x, group=None):
 
 class MoELayer:
     def __init__(self, dims, w13, w13_scale, w2, w2_scale, w_router, bias, g13=None, g2=None,
-                 sh13=None, sh13_scale=None, sh2=None, sh2_scale=None, packed: bool = True):
+                 sh13=None, sh13_scale=None, sh2=None, sh2_scale=None, packed: bool | int = True):
         """Tensors on one CUDA device.  Scales are the raw row-major block
         scales ([E, rows, K/32] E8M0 or [E, rows, K/16] E4M3); they are
-        repacked here into the layout the GEMMs load.  packed: the forward
-        reads the payloads in the tiled layout (fp4moe_pack_weights; gate/up
-        matrices and their scales in the gate/up-paired order of
-        fp4moe_pack_gateup_weights / _scales), else the row-major tensors
-        themselves; the row-major tensors are kept either way (the FP8
-        conversion reads them)."""
+        repacked here into the layout the GEMMs load.  packed (the
+        fp4moe_weights level): 0 / False, the forward reads the row-major
+        payloads themselves; 2, the tiled layout of fp4moe_pack_weights, with
+        the gate/up matrices and their scales in the gate/up-paired order of
+        fp4moe_pack_gateup_weights / _scales; 3, as 2 with the down matrices
+        in the row-tile-paired order (each 256-row slab packed as a gate/up
+        pair of I = 128; needs H % 256 == 0, and column blocks of whole
+        slabs); True, 3 where H allows it, else 2.  The row-major tensors
+        are kept either way (the FP8 conversion reads them)."""
         self.dims = dims
         self.fmt = dims.fmt
         self.device = w13.device
         self.raw = dict(w13_scale=w13_scale, w2_scale=w2_scale, sh13_scale=sh13_scale, sh2_scale=sh2_scale)
         blk = 16 if dims.fmt == NVFP4 else 32
+        if packed is True:
+            packed = 3 if dims.H % 256 == 0 else 2
+        packed = int(packed)
+        if packed not in (0, 2, 3) or (packed == 3 and dims.H % 256):
+            raise ValueError(f"packed level {packed} (0, 2, or 3 with H % 256 == 0)")
         self.w13, self.w2 = w13.contiguous(), w2.contiguous()
-        self.w13_scale = self._pack(w13_scale, dims.E, 2 * dims.I, dims.H // blk, gateup=packed)
-        self.w2_scale = self._pack(w2_scale, dims.E, dims.H, dims.I // blk)
+        self.w13_scale = self._pack(w13_scale, dims.E, 2 * dims.I, dims.H // blk, gateup=packed >= 2)
+        self.w2_scale = self._pack(w2_scale, dims.E, dims.H, dims.I // blk, slabs=packed == 3)
         self.w_router, self.bias = w_router.contiguous(), bias.contiguous()
         self.g13, self.g2 = g13, g2
         self.sh13, self.sh2 = sh13, sh2
-        self.sh13_scale = (self._pack(sh13_scale, 1, 2 * dims.I, dims.H // blk, gateup=packed) if sh13 is not None
-                           else None)
-        self.sh2_scale = self._pack(sh2_scale, 1, dims.H, dims.I // blk) if sh2 is not None else None
+        self.sh13_scale = (self._pack(sh13_scale, 1, 2 * dims.I, dims.H // blk, gateup=packed >= 2)
+                           if sh13 is not None else None)
+        self.sh2_scale = (self._pack(sh2_scale, 1, dims.H, dims.I // blk, slabs=packed == 3) if sh2 is not None
+                          else None)
         self.packed = packed
+        self.column_unit = 256 if packed == 3 else 128  # granularity of forward_cols' column blocks
         pw = self._pack_w if packed else (lambda t, *_, **__: t)
         self.w13_t = pw(self.w13, dims.E, 2 * dims.I, dims.H // 2, gateup=True)
-        self.w2_t = pw(self.w2, dims.E, dims.H, dims.I // 2)
+        self.w2_t = pw(self.w2, dims.E, dims.H, dims.I // 2, slabs=packed == 3)
         self.sh13_t = pw(sh13, 1, 2 * dims.I, dims.H // 2, gateup=True) if sh13 is not None else None
-        self.sh2_t = pw(sh2, 1, dims.H, dims.I // 2) if sh2 is not None else None
+        self.sh2_t = pw(sh2, 1, dims.H, dims.I // 2, slabs=packed == 3) if sh2 is not None else None
         self._check_scales()
         self.ws_bytes = workspace_size(dims)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
@@ -88,7 +99,7 @@ class MoELayer:
         self.weights = Weights(_ptr(self.w13_t), _ptr(self.w13_scale), _ptr(self.w2_t), _ptr(self.w2_scale),
                                _ptr(self.g13), _ptr(self.g2), _ptr(self.sh13_t), _ptr(self.sh13_scale),
                                _ptr(self.sh2_t), _ptr(self.sh2_scale), _ptr(self.w_router), _ptr(self.bias),
-                               2 if packed else 0)
+                               packed)
 
     def _check_scales(self):
         """Refuses weights with NaN block scales (fp4moe_check_scales): the
@@ -102,21 +113,25 @@ class MoELayer:
         if st != 0:
             raise ValueError(f"{n} NaN block-scale bytes in the expert weights (status {st})")
 
-    def _pack_w(self, codes, n_mat, rows, kbytes, gateup=False):
+    def _pack_w(self, codes, n_mat, rows, kbytes, gateup=False, slabs=False):
         dst = torch.empty(packed_weights_bytes(n_mat, rows, kbytes), dtype=torch.uint8, device=codes.device)
         s = torch.cuda.current_stream(codes.device).cuda_stream
         if gateup:  # rows = 2I: gate/up-paired tiles
             pack_gateup_weights(codes.data_ptr(), dst.data_ptr(), n_mat, rows // 2, kbytes, s)
+        elif slabs:  # row-tile pairs: each 256-row slab as a gate/up pair of I = 128
+            pack_gateup_weights(codes.data_ptr(), dst.data_ptr(), n_mat * rows // 256, 128, kbytes, s)
         else:
             pack_weights(codes.data_ptr(), dst.data_ptr(), n_mat, rows, kbytes, s)
         return dst
 
-    def _pack(self, raw, n_mat, rows, kblocks, gateup=False):
+    def _pack(self, raw, n_mat, rows, kblocks, gateup=False, slabs=False):
         dst = torch.empty(packed_scales_bytes(n_mat, rows, kblocks, self.fmt), dtype=torch.uint8,
                           device=raw.device)
         s = torch.cuda.current_stream(raw.device).cuda_stream
         if gateup:  # rows = 2I: gate/up-paired scale groups
             pack_gateup_scales(raw.data_ptr(), dst.data_ptr(), n_mat, rows // 2, kblocks, self.fmt, s)
+        elif slabs:  # row-tile pairs (see _pack_w)
+            pack_gateup_scales(raw.data_ptr(), dst.data_ptr(), n_mat * rows // 256, 128, kblocks, self.fmt, s)
         else:
             pack_scales(raw.data_ptr(), dst.data_ptr(), n_mat, rows, kblocks, self.fmt, s)
         return dst
@@ -172,7 +187,7 @@ class MoELayer:
 
     # ------------------------------------------------------------ synthetic layers
     @classmethod
-    def synthetic(cls, cfg, device="cuda", packed: bool = True):
+    def synthetic(cls, cfg, device="cuda", packed: bool | int = True):
         import synth
         fmt = NVFP4 if cfg.fmt == "nvfp4" else MXFP4
         dims = make_dims(cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k, cfg.n_group, cfg.topk_group, cfg.n_shared,
@@ -248,7 +263,7 @@ class MoELayer:
         v.emu_ws = None
         v.weights = Weights(_ptr(v.w13_t), _ptr(v.w13_scale), _ptr(v.w2_t), _ptr(v.w2_scale), _ptr(v.g13),
                             _ptr(v.g2), _ptr(v.sh13_t), _ptr(v.sh13_scale), _ptr(v.sh2_t), _ptr(v.sh2_scale),
-                            _ptr(v.w_router), _ptr(v.bias), 2 if v.packed else 0)
+                            _ptr(v.w_router), _ptr(v.bias), v.packed)
         return v
 
     def synthetic_x(self, t0: int = 0, t1: int | None = None):

@@ -99,7 +99,18 @@ typedef struct {
  *             layout of fp4moe_pack_gateup_weights and w13_scale and
  *             sh13_scale that of fp4moe_pack_gateup_scales (the gate/up
  *             GEMM then reads a K tile's gate and up blocks, and their
- *             scale groups, with one copy each).  Other values: INVALID_ARG. */
+ *             scale groups, with one copy each);
+ *             3: as 2, and w2 and sh2 (and w2_scale, sh2_scale) in the
+ *             row-tile-paired layout: each 256-row slab of a down matrix
+ *             packed as one gate/up pair with I = 128, that is
+ *             fp4moe_pack_gateup_weights(src, dst, n_mat * H / 256, 128,
+ *             I / 2) and fp4moe_pack_gateup_scales(src, dst,
+ *             n_mat * H / 256, 128, kblocks, fmt), so that row tiles 2j
+ *             and 2j + 1 of a K tile are adjacent (the down GEMM's units
+ *             of two weight tiles then read both with one copy each).
+ *             Needs H % 256 == 0 and, for fp4moe_forward_cols, h_begin
+ *             and h_end multiples of 256 (else UNSUPPORTED_SHAPE).  Other
+ *             values: INVALID_ARG. */
 typedef struct {
   const uint8_t *w13, *w13_scale, *w2, *w2_scale;
   const float *g13, *g2;
@@ -360,7 +371,7 @@ fp4moe_status fp4moe_forward(const fp4moe_dims *dims, const fp4moe_weights *w, c
  * writes those columns of out; every other column of out is zero, so the
  * ranks' outputs sum exactly to the layer output.  Arguments as for
  * fp4moe_forward (MXFP4 / NVFP4); 0 <= h_begin < h_end <= H, both multiples
- * of 128, else FP4MOE_ERR_UNSUPPORTED_SHAPE. */
+ * of 128 (of 256 with packed == 3), else FP4MOE_ERR_UNSUPPORTED_SHAPE. */
 fp4moe_status fp4moe_forward_cols(const fp4moe_dims *dims, const fp4moe_weights *w, const uint16_t *x,
                                   uint16_t *out, int32_t h_begin, int32_t h_end, const fp4moe_debug *dbg,
                                   void *ws, size_t ws_bytes, void *stream);

@@ -417,6 +417,15 @@ def test_paired_down_on_cta_pairs(name):
     print(name, full_check(SMALL[name], cta_pair=True))
 
 
+@pytest.mark.parametrize("name", ["front_T16_shared", "paired_padK", "pair_shared", "nv_wide_padK"])
+def test_small_layers_gateup_paired_level(name):
+    """The same parity with the down weights in the plain tiled layout
+    (packed = 2; the other tests use level 3, the row-tile-paired down
+    weights): the down units of two weight tiles then read two 128-row
+    boxes and two scale copies per stage."""
+    print(name, full_check(SMALL[name], packed=2))
+
+
 @pytest.mark.parametrize("name", ["tiny", "wide_padK", "nv_grouped", "nv_wide_padK"])
 def test_small_layers_row_major_weights(name):
     """The same parity with the expert payloads left row-major (packed = 0);
@@ -552,7 +561,7 @@ def _column_slices(cfg, layer, x, world):
     from block_scaled_fp4_sigmoid_gb300.layer import column_block
     total = np.zeros((cfg.T, cfg.H))
     for r in range(world):
-        h0, h1 = column_block(cfg.H, r, world)
+        h0, h1 = column_block(cfg.H, r, world, layer.column_unit)
         out = layer.forward_cols(x, h0, h1)
         torch.cuda.synchronize()
         assert fm.get_status(layer.ws.data_ptr()) == (0, 0)
@@ -578,14 +587,16 @@ def _ambiguous_tokens(cfg, orc, tokens, bias):
 def test_output_column_blocks_sum_to_the_layer(name, world):
     """Output-partitioned layer: the ranks' column blocks, summed, meet the
     layer tolerance against the whole oracle (the few-token front end, the
-    many-token path, a shared expert, NVFP4, K padding, paired down units on
-    CTA pairs (512-column blocks) and on single CTAs (128-column blocks))."""
+    many-token path, a shared expert, NVFP4, K padding; down units of two
+    weight tiles on row-tile-paired weights in 512-column blocks, paired-slot
+    units in 128-column blocks).  Blocks of whole 256-row slabs use the
+    row-tile-paired down weights (packed level 3), 128-column blocks level 2."""
     from types import SimpleNamespace
     torch_cuda()
     ensure_built()
     from block_scaled_fp4_sigmoid_gb300.layer import MoELayer
     cfg = SMALL[name]
-    layer = MoELayer.synthetic(cfg)
+    layer = MoELayer.synthetic(cfg, packed=3 if cfg.H % (256 * world) == 0 else 2)
     total = _column_slices(cfg, layer, layer.synthetic_x(), world)
     x, wr, b = OI.layer_inputs(cfg)
     tokens = np.arange(cfg.T)

@@ -46,6 +46,27 @@ def test_forward_cols_refuses_bad_ranges_without_a_gpu():
                                        None) == 2, (h0, h1)
 
 
+def test_forward_cols_paired_down_weights_need_whole_slabs():
+    """With the down weights in the row-tile-paired layout (packed = 3) a
+    column block must cover whole 256-row slabs; an unknown packing level is
+    an invalid argument.  Both are refused before any device work."""
+    import block_scaled_fp4_sigmoid_gb300 as fm
+    lib = fm.lib()
+    d = fm.make_dims(4, 512, 128, 8, 2)
+    buf = ctypes.create_string_buffer(4096)
+    p = ctypes.addressof(buf)
+    w = fm.Weights(p, p, p, p, None, None, None, None, None, None, p, p, 3)
+    big = 1 << 40  # the workspace size is only compared before any device work
+    for h0, h1 in ((128, 512), (0, 384), (256, 384)):
+        assert lib.fp4moe_forward_cols(ctypes.byref(d), ctypes.byref(w), buf, buf, h0, h1, None, buf, big,
+                                       None) == 2, (h0, h1)
+    w.packed = 4
+    assert lib.fp4moe_forward_cols(ctypes.byref(d), ctypes.byref(w), buf, buf, 0, 512, None, buf, big, None) == 1
+    w.packed = 3
+    d3 = fm.make_dims(4, 384, 128, 8, 2)  # H not a multiple of 256
+    assert lib.fp4moe_forward(ctypes.byref(d3), ctypes.byref(w), buf, buf, None, buf, big, None) == 2
+
+
 class _StandIn:
     """The interface tp_forward uses: dims.H and forward_cols (here on the
     CPU: the block's columns of 2x, zero elsewhere)."""
@@ -53,6 +74,7 @@ class _StandIn:
     def __init__(self, H):
         from types import SimpleNamespace
         self.dims = SimpleNamespace(H=H)
+        self.column_unit = 128
 
     def forward_cols(self, x, h0, h1):
         import torch
